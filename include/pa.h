@@ -1,0 +1,250 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) PagedAttention decode library.
+ *
+ * The library computes softmax attention of ONE new query token per sequence
+ * over a key/value cache that is stored in fixed-size blocks ("pages") of
+ * block_size tokens and addressed through a per-sequence block table.
+ *
+ * Sources of the operations (web pages this library restates):
+ *  - "PagedAttention in mistral.rs" (engine/docs/PAGED_ATTENTION.md), opening
+ *    section and "Using the CLI": the cache is a pool of blocks sized by a GPU
+ *    memory budget; block size = tokens per block, default 32.
+ *  - same page, "KV Cache Quantization": the cache may be stored as FP8 E4M3
+ *    instead of the model's native dtype ("auto"), about half the bytes of FP16.
+ *  - "Optimization plans" (mistral.rs discussion #46), the update that traces
+ *    junk output to reshape_and_cache: the write that scatters each new token's
+ *    K/V into its cache slot.
+ *  - "Rolling buffer cache" (llama.cpp discussion #3581), the opening post
+ *    quoting Mistral 7B: a fixed-size cache of W slots where the K/V of
+ *    timestep i live in slot i mod W and overwrite older entries.
+ *
+ * Conventions for every call below
+ *  - All tensor arguments are DEVICE pointers to dense, row-major (C order)
+ *    arrays owned by the caller. The library never allocates device memory and
+ *    never frees caller memory.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Kernels are
+ *    enqueued asynchronously on it; a call returns as soon as they are queued.
+ *  - Argument errors are detected on the host BEFORE anything is enqueued and
+ *    are returned as a negative pa_status; nothing is written in that case.
+ *  - Data-dependent errors that only the GPU can see (a slot or block id out of
+ *    range, a context length beyond the table) never fault: the offending
+ *    element is skipped, a bit is set in a per-device error word, and
+ *    pa_get_device_error() reports it later.
+ *  - Notation: T = num_tokens, S = num_seqs, Hq = num_heads,
+ *    Hkv = num_kv_heads, G = Hq / Hkv, D = head_dim, bs = block_size,
+ *    NB = num_blocks, MB = max_blocks_per_seq, n_s = context_lens[s]
+ *    (INCLUDING the new token), W = window (0 = no window),
+ *    L_s = n_s if W == 0 else min(n_s, W) (tokens attended by sequence s).
+ *  - Cache layout (both K and V): [NB][Hkv][bs][D]. The page of one
+ *    (block, kv head) is bs*D contiguous elements ("head-major pages").
+ *    Element type: the input dtype for PA_KV_AUTO, one byte (E4M3) for
+ *    PA_KV_FP8_E4M3.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so this header needs no CUDA headers. */
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_NULL = -1,        /* a required pointer is NULL                          */
+    PA_ERR_DTYPE = -2,       /* unsupported element type or combination             */
+    PA_ERR_SHAPE = -3,       /* a size is negative/zero where it may not be, or
+                                num_heads % num_kv_heads != 0, or G > 8            */
+    PA_ERR_HEAD_DIM = -4,    /* head_dim not in {64, 96, 128}                       */
+    PA_ERR_BLOCK_SIZE = -5,  /* block_size not supported                            */
+    PA_ERR_WINDOW = -6,      /* window < 0, window % block_size != 0, or
+                                window / block_size > max_blocks_per_seq           */
+    PA_ERR_WORKSPACE = -7,   /* workspace smaller than the requested split plan     */
+    PA_ERR_CUDA = -8,        /* a CUDA runtime call failed (bad stream, launch)     */
+    PA_ERR_DEVICE = -9,      /* pa_get_device_error(): a kernel flagged bad data    */
+    PA_ERR_ALIGN = -10,      /* a pointer is not 16-byte aligned                    */
+    PA_ERR_SCALE = -11       /* an FP8 scale is not finite and > 0                  */
+} pa_status;
+
+/* Element type of query / key / value / output (and of an AUTO cache). */
+typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype;
+
+/* Cache storage type ("auto" and "f8e4m3" of "KV Cache Quantization"). */
+typedef enum { PA_KV_AUTO = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+
+/* Bits of the per-device error word (see pa_get_device_error). */
+enum {
+    PA_DEVERR_SLOT = 1u,        /* slot_mapping entry >= NB*bs: that token was not written   */
+    PA_DEVERR_BLOCK_ID = 2u,    /* a block-table entry needed by a sequence is outside
+                                   [0, NB): that page was treated as holding no tokens     */
+    PA_DEVERR_CONTEXT_LEN = 4u, /* context_lens[s] < 0 or L_s > MB*bs: clamped to the range */
+    PA_DEVERR_TIMEOUT = 8u,     /* a bounded wait for an asynchronous copy gave up          */
+    PA_DEVERR_SEQ = 16u         /* pa_slot_mapping: seq index out of range or page index
+                                   >= MB: slot set to -1                                   */
+};
+
+/*
+ * pa_slot_mapping -- cache slot of each token to be written (ring-aware).
+ *
+ * Source: "Rolling buffer cache" (opening post): timestep i goes to slot
+ * i mod W of a fixed cache of W entries, overwriting older values; and the
+ * paged store of "PagedAttention in mistral.rs" (block = block_size tokens).
+ *
+ *   r = (window > 0) ? positions[t] mod window : positions[t]
+ *   s = seq_idx ? seq_idx[t] : t
+ *   slot_mapping[t] = block_tables[s][r / bs] * bs + r % bs
+ *
+ * slot_mapping : out, int64 [T].  positions : int32 [T] (absolute position of
+ * the token in its sequence, < 0 = padding -> slot -1).  seq_idx : int32 [T]
+ * or NULL (token t belongs to sequence t).  block_tables : int32 [S][MB].
+ * A seq index outside [0, S) or r/bs >= MB gives slot -1 and sets
+ * PA_DEVERR_SEQ.  T == 0 is a no-op.
+ */
+pa_status pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
+                          const int32_t* seq_idx, const int32_t* positions,
+                          int num_tokens, int num_seqs, int max_blocks_per_seq,
+                          int block_size, int window, pa_stream_t stream);
+
+/*
+ * pa_reshape_and_cache -- scatter the K/V of new tokens into their cache slots.
+ *
+ * Source: "Optimization plans" (reshape_and_cache, the write whose bug gave
+ * junk output) and "KV Cache Quantization" (F8E4M3 cache).
+ *
+ * key, value   : in, [T][Hkv][D] of in_dtype.
+ * k_cache,
+ * v_cache      : in/out, [NB][Hkv][bs][D] of in_dtype (AUTO) or uint8 (FP8).
+ * slot_mapping : in, int64 [T]; slot < 0 = padding (skipped); block
+ *                slot / bs, row slot % bs. Duplicate slots within one call
+ *                leave that slot's value unspecified (one of the writers).
+ * AUTO  : the element bits are copied unchanged.
+ * FP8   : code = E4M3(x / k_scale) (IEEE fp32 divide; bf16/f16 inputs widened
+ *         exactly), round to nearest even, finite overflow and +-inf saturate
+ *         to +-448 (code 0x7E / 0xFE), NaN -> 0x7F | sign, -0 -> 0x80.
+ *         Same for V with v_scale. Scales must be finite and > 0.
+ * Only the rows named by slot_mapping are written; every other byte of the
+ * cache is left untouched. Pointers must be 16-byte aligned.
+ */
+pa_status pa_reshape_and_cache(const void* key, const void* value,
+                               void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping,
+                               int num_tokens, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks,
+                               pa_dtype in_dtype, pa_kv_dtype kv_dtype,
+                               float k_scale, float v_scale, pa_stream_t stream);
+
+/*
+ * pa_decode -- paged decode attention, one query token per sequence.
+ *
+ * Source: "PagedAttention in mistral.rs" (blocked cache read through block
+ * tables; FP8 cache); "Rolling buffer cache" (window W: attend to the last W
+ * positions, held in ring slots 0 .. L_s-1).
+ *
+ * For every sequence s and query head h (kv head g = h / G):
+ *   slot j in [0, L_s) lives at block block_tables[s][j / bs], row j % bs
+ *   logit_j = scale * sum_d q[s][h][d] * K_j[d]          (K_j dequantised)
+ *   out[s][h][:] = sum_j softmax(logit)_j * V_j[:]       (0 when L_s == 0)
+ * With FP8, K_j[d] = E4M3value(byte) * k_scale and V_j likewise with v_scale.
+ * Accumulation is fp32. Bytes of the cache outside the L_s attended slots
+ * (tail rows of the last block, unused blocks) are never used, whatever they
+ * hold (NaN included).
+ *
+ * out          : out, [S][Hq][D] of q_dtype.     query : in, [S][Hq][D] q_dtype.
+ * k_cache,
+ * v_cache      : in, [NB][Hkv][bs][D] (q_dtype for AUTO, uint8 for FP8).
+ * block_tables : in, int32 [S][MB].  context_lens : in, int32 [S].
+ * window       : 0 = none; else W > 0, W % bs == 0, W / bs <= MB (ring of
+ *                W / bs blocks per sequence in block_tables[s][0 .. W/bs-1]).
+ * workspace    : device scratch of workspace_bytes (may be NULL / 0). The
+ *                context of a sequence is split across several CTAs and the
+ *                partial results are combined by a log-sum-exp reduction when
+ *                the workspace holds the plan (pa_decode_workspace_size());
+ *                otherwise one CTA per (sequence, kv head) does the whole
+ *                context. Contents on entry do not matter; on exit undefined.
+ * Supported: D in {64, 96, 128}; bs in {16, 32, 64}; G = Hq/Hkv in 1..8;
+ * q_dtype F32/BF16/F16; AUTO caches hold q_dtype. Pointers 16-byte aligned.
+ */
+pa_status pa_decode(void* out, const void* query,
+                    const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens,
+                    int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                    int block_size, int num_blocks, int max_blocks_per_seq,
+                    float scale, int window, pa_dtype q_dtype, pa_kv_dtype kv_dtype,
+                    float k_scale, float v_scale,
+                    void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_decode_plan -- the split plan pa_decode uses for these sizes.
+ * Writes the number of context splits per (sequence, kv head) and the pages
+ * (blocks) each split covers; split i covers slots
+ * [i*pages_per_split*bs, (i+1)*pages_per_split*bs). num_splits == 1 means the
+ * unsplit kernel (no workspace needed). Host-only; never touches the GPU.
+ */
+pa_status pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                         int block_size, int max_blocks_per_seq, int window,
+                         int* num_splits, int* pages_per_split);
+
+/* Bytes of workspace pa_decode needs for its split plan (0 when unsplit). */
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                int head_dim, int block_size,
+                                int max_blocks_per_seq, int window);
+
+/*
+ * pa_decode_partials -- the split phase of pa_decode with an explicit plan.
+ *
+ * For split i of (s, h) (slots [i*P*bs, (i+1)*P*bs) intersected with
+ * [0, L_s), P = pages_per_split), writes
+ *   max_logits[s][h][i] = m_i = max logit (natural-log units, includes scale)
+ *   exp_sums[s][h][i]   = l_i = sum_j exp(logit_j - m_i)
+ *   tmp_out[s][h][i][:] = sum_j exp(logit_j - m_i) V_j / l_i
+ * A split holding no slot writes m_i = -inf, l_i = 0 and leaves tmp_out[..][i]
+ * untouched. tmp_out fp32 [S][Hq][NS][D]; max_logits, exp_sums fp32 [S][Hq][NS].
+ * Requires num_splits * pages_per_split >= the ring (W / bs) or MB blocks.
+ * Other arguments as pa_decode.
+ */
+pa_status pa_decode_partials(float* tmp_out, float* max_logits, float* exp_sums,
+                             const void* query, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                             int block_size, int num_blocks, int max_blocks_per_seq,
+                             float scale, int window, pa_dtype q_dtype, pa_kv_dtype kv_dtype,
+                             float k_scale, float v_scale,
+                             int num_splits, int pages_per_split, pa_stream_t stream);
+
+/*
+ * pa_reduce -- log-sum-exp combination of split partials.
+ *
+ * For each (s, h): M = max over splits with l_i > 0 of m_i,
+ *   w_i = l_i * exp(m_i - M),  out[s][h][:] = sum_i w_i tmp_out[s][h][i][:] / sum_i w_i,
+ * rounded to out_dtype (round to nearest even). Splits with l_i == 0 are
+ * skipped entirely (their tmp_out rows are not read); if all are empty the
+ * output row is 0. Layouts as pa_decode_partials; out [S][Hq][D] of out_dtype.
+ * Partials of disjoint context segments produced by separate calls may be
+ * combined this way as long as they share one layout.
+ */
+pa_status pa_reduce(void* out, const float* tmp_out, const float* max_logits,
+                    const float* exp_sums, int num_seqs, int num_heads, int head_dim,
+                    int num_splits, pa_dtype out_dtype, pa_stream_t stream);
+
+/*
+ * pa_get_device_error -- synchronise `stream`, then read and clear the error
+ * word of the current device. *error_bits (may be NULL) receives the
+ * PA_DEVERR_* bits. Returns PA_OK when no bit was set, PA_ERR_DEVICE when
+ * some were, PA_ERR_CUDA when the synchronisation itself failed.
+ */
+pa_status pa_get_device_error(pa_stream_t stream, uint32_t* error_bits);
+
+/* Static English text for a pa_status value (never NULL). */
+const char* pa_status_string(int status);
+
+/* Library ABI version, (major << 16) | minor. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */
