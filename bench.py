@@ -1,0 +1,484 @@
+#!/usr/bin/env python
+"""Benchmark: paged decode attention on GB300, one JSON line on stdout.
+
+A step is one pass of the whole decode hot path over one batch: the cache
+write of every sequence's new token (pa_reshape_and_cache), the split decode
+(pa_decode_partials) and the log-sum-exp reduction (pa_reduce) -- exactly the
+kernels pa_decode runs for its split plan. Default workload: the
+Mistral-7B-shaped bf16 batch (32 sequences, 32 query / 8 kv heads, head_dim
+128, block_size 32, context lengths U[512, 4096], shuffled block pool).
+
+value  = algorithmic bytes of a step (K/V of the attended tokens, q, output,
+         block-table entries, context lengths, the new rows written) * steps
+         / device time of the timed region, summed over ranks, in GB/s.
+e2e    = the same metric through pa_decode with host buffers: per step the
+         query, new K/V rows, slot mapping, lengths and tables are copied from
+         pinned host memory, and the output is copied back.
+roofline = the split-decode kernel alone (CUDA events around each launch).
+
+L2: the K/V caches are replicated 4 times (each replica larger than the
+129 MB L2) and consecutive steps use different replicas.
+
+--impl reference times the CPU oracle (fp64 C, all host cores) on a bounded
+sample of the same workload, per step, and prints the same line.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak) and seqs/s"
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ------------------------------------------------------------------ ranks
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def all_reduce(value: float, op: str, device=None) -> float:
+    """max / sum of a float over the ranks of the default process group (the
+    value itself when not distributed)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        window = [l for (t, l) in self.lines if t0 - 0.06 <= t <= t1 + 0.06] or \
+                 [l for (_, l) in self.lines]
+        for line in window:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload bytes
+def step_bytes(case) -> dict:
+    """Algorithmic bytes of one decode step."""
+    S, Hq, Hkv, D, bs = (case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim,
+                         case.block_size)
+    qb = torch.finfo(case.q_dtype).bits // 8
+    cb = 1 if case.kv_dtype == "fp8_e4m3" else qb
+    sb = torch.finfo(case.kv_src_dtype).bits // 8
+    kv = case.kv_bytes()
+    pages = sum(-(-case.attended(s) // bs) for s in range(S))
+    new_rows = int((case.new_pos >= 0).sum())
+    kernel = kv + S * Hq * D * qb + pages * 4 + S * 4  # what the split kernel must read
+    write = new_rows * Hkv * D * (sb + cb) * 2 + S * 8
+    total = kernel + S * Hq * D * qb + write
+    return {"kv": kv, "kernel": kernel, "write": write, "total": total}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_step_time(case, rows_per_step: int, reps: int, build_all: bool = True):
+    """Seconds per oracle step (write of the sample's new rows + decode of the
+    sample's rows) on the host cores; the sample is the first rows_per_step
+    (sequence, head) rows in sequence order."""
+    import oracle  # test infrastructure: only this CPU-baseline leg uses it
+    from paged_kv_cache_context_gb300 import workloads as wl
+    Hq = case.num_heads
+    nseq = min(case.num_seqs, -(-rows_per_step // Hq))
+    kc, vc = wl.empty_caches(case)
+    for s in range(nseq):
+        pos, key, val = case.tokens_of(s)
+        sm, _ = oracle.slot_mapping(case.block_tables, torch.full_like(pos, s), pos,
+                                    case.block_size, case.window)
+        oracle.reshape_and_cache(key[:-1], val[:-1], kc, vc, sm[:-1], case.block_size,
+                                 case.kv_dtype, case.k_scale, case.v_scale)
+    new_sm, _ = oracle.slot_mapping(case.block_tables, None, case.new_pos, case.block_size,
+                                    case.window)
+    new_sm[nseq:] = -1
+    nk, nv = case.new_key.cpu(), case.new_value.cpu()
+    q = case.query.cpu()
+    rows = list(range(min(rows_per_step, case.num_seqs * Hq)))
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.reshape_and_cache(nk, nv, kc, vc, new_sm, case.block_size, case.kv_dtype,
+                                 case.k_scale, case.v_scale)
+        oracle.decode(q, kc, vc, case.block_tables, case.context_lens, case.num_kv_heads,
+                      case.block_size, case.scale, case.window, case.kv_dtype, case.k_scale,
+                      case.v_scale, rows=rows)
+        times.append(time.perf_counter() - t0)
+    sample_bytes = 0
+    for r in rows:
+        s = r // Hq
+        sample_bytes += case.attended(s) * case.head_dim * 2 * (
+            1 if case.kv_dtype == "fp8_e4m3" else torch.finfo(case.q_dtype).bits // 8)
+    return times, sample_bytes, len(rows)
+
+
+def cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, local_rank, world):
+    from paged_kv_cache_context_gb300 import build, pa
+    from paged_kv_cache_context_gb300 import workloads as wl
+    build.build()
+    L = pa.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    sp = ctypes.c_void_p(stream.cuda_stream)
+
+    case = wl.config(args.workload, value_device=str(dev),
+                     seed=None if rank == 0 else 50_000 + rank)
+    S, Hq, Hkv, D, bs = (case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim,
+                         case.block_size)
+    MB, NB = case.max_blocks_per_seq, case.num_blocks
+    bt = case.block_tables.to(dev)
+    cl = case.context_lens.to(dev)
+    q = case.query.to(dev).contiguous()
+
+    # caches: prefill rows written by the library itself
+    kc, vc = wl.empty_caches(case, device=str(dev))
+    for a, b in case.pre_chunks:
+        if b > a:
+            sm = torch.empty(b - a, dtype=torch.int64, device=dev)
+            pa.slot_mapping(sm, bt, case.pre_seq[a:b].to(dev), case.pre_pos[a:b].to(dev), bs,
+                            case.window)
+            pa.reshape_and_cache(case.pre_key[a:b].contiguous(), case.pre_value[a:b].contiguous(),
+                                 kc, vc, sm, case.kv_dtype, case.k_scale, case.v_scale)
+    new_sm = torch.empty(S, dtype=torch.int64, device=dev)
+    pa.slot_mapping(new_sm, bt, None, case.new_pos.to(dev), bs, case.window)
+    new_k = case.new_key.to(dev).contiguous()
+    new_v = case.new_value.to(dev).contiguous()
+    torch.cuda.synchronize()
+    reps = [(kc, vc)] + [(kc.clone(), vc.clone()) for _ in range(args.replicas - 1)]
+
+    ns, pps = pa.decode_plan(S, Hq, Hkv, D, bs, MB, case.window)
+    qd = pa._DTYPE[case.q_dtype]
+    kvd = pa._KV[case.kv_dtype]
+    out = torch.empty(S, Hq, D, dtype=case.q_dtype, device=dev)
+    tmp = torch.empty(S, Hq, max(ns, 1), D, dtype=torch.float32, device=dev)
+    ml = torch.empty(S, Hq, max(ns, 1), dtype=torch.float32, device=dev)
+    es = torch.empty_like(ml)
+
+    # pre-bound C calls (marshalling once, outside the timed loop)
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    def ptr(t):
+        return P(t.data_ptr())
+    write_args, split_args = [], []
+    for (k_, v_) in reps:
+        write_args.append((ptr(new_k), ptr(new_v), ptr(k_), ptr(v_), ptr(new_sm), I(S), I(Hkv),
+                           I(D), I(bs), I(NB), I(pa._DTYPE[new_k.dtype]), I(kvd),
+                           F(case.k_scale), F(case.v_scale), sp))
+        if ns > 1:
+            split_args.append((ptr(tmp), ptr(ml), ptr(es), ptr(q), ptr(k_), ptr(v_), ptr(bt),
+                               ptr(cl), I(S), I(Hq), I(Hkv), I(D), I(bs), I(NB), I(MB),
+                               F(case.scale), I(case.window), I(qd), I(kvd), F(case.k_scale),
+                               F(case.v_scale), I(ns), I(pps), sp))
+        else:
+            split_args.append((ptr(out), ptr(q), ptr(k_), ptr(v_), ptr(bt), ptr(cl), I(S), I(Hq),
+                               I(Hkv), I(D), I(bs), I(NB), I(MB), F(case.scale), I(case.window),
+                               I(qd), I(kvd), F(case.k_scale), F(case.v_scale), None,
+                               ctypes.c_size_t(0), sp))
+    reduce_args = (ptr(out), ptr(tmp), ptr(ml), ptr(es), I(S), I(Hq), I(D), I(ns), I(qd), sp)
+    f_write, f_red = L.pa_reshape_and_cache, L.pa_reduce
+    f_split = L.pa_decode_partials if ns > 1 else L.pa_decode
+    launches_per_step = 3 if ns > 1 else 2
+
+    def step(i, ev_a=None, ev_b=None):
+        r = i % len(reps)
+        rc = f_write(*write_args[r])
+        if ev_a is not None:
+            ev_a.record(stream)
+        rc |= f_split(*split_args[r])
+        if ev_b is not None:
+            ev_b.record(stream)
+        if ns > 1:
+            rc |= f_red(*reduce_args)
+        if rc:
+            raise RuntimeError(f"library call failed: {rc}")
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if pa.get_device_error():
+        raise RuntimeError("device error word set after warm-up")
+
+    K = args.steps
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    phys = int(vis[local_rank]) if local_rank < len(vis) and vis[local_rank].strip().isdigit() \
+        else local_rank
+    clocks = ClockSampler(phys)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for i in range(K):
+        step(i, ev_a[i], ev_b[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    barrier(dev)
+    clk = clocks.stop(t0, t1)
+    if pa.get_device_error():
+        raise RuntimeError("device error word set in the timed region")
+    elapsed = e0.elapsed_time(e1) / 1e3
+    split_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+
+    sb = step_bytes(case)
+    elapsed_max = all_reduce(elapsed, "max", dev)
+    bytes_all = all_reduce(float(sb["total"] * K), "sum", dev)
+    seqs_all = all_reduce(float(S * K), "sum", dev)
+    split_mean = statistics.mean(split_ms) / 1e3
+    peak, peak_kind = peaks()
+    achieved = sb["kernel"] / split_mean / 1e9
+
+    # ---- e2e: the public pa_decode call with host buffers
+    e2e = run_e2e(args, case, pa, L, dev, stream, reps, new_sm, bt, cl, q, new_k, new_v, out,
+                  sb, world)
+
+    result = {
+        "metric": METRIC, "value": round(bytes_all / elapsed_max / 1e9, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(elapsed_max / K * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "impl": "ours",
+        "config": {"workload": args.workload, "num_seqs": S, "num_heads": Hq,
+                   "num_kv_heads": Hkv, "head_dim": D, "block_size": bs,
+                   "window": case.window, "cache_dtype": case.kv_dtype if case.kv_dtype != "auto"
+                   else str(case.q_dtype).replace("torch.", ""),
+                   "storage_dtype": str(case.q_dtype).replace("torch.", ""),
+                   "num_splits": ns, "pages_per_split": pps,
+                   "kv_bytes_per_step": sb["kv"], "bytes_per_step": sb["total"],
+                   "l2": f"{args.replicas} rotating cache replicas of "
+                         f"{kc.numel() * kc.element_size() * 2 / 1e6:.0f} MB (> L2)",
+                   "parallelism": f"replicas x{world} (independent batches, no collective)"},
+        "seqs_per_s": round(seqs_all / elapsed_max, 1),
+        "pct_of_nominal_8tbs": round(100 * bytes_all / elapsed_max / 1e9 / NOMINAL_HBM_GBS, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "kernel": "paged_decode_kernel",
+                     "kernel_bytes_per_launch": sb["kernel"],
+                     "kernel_us_mean": round(split_mean * 1e6, 2),
+                     "kernel_us_median": round(statistics.median(split_ms) * 1e3, 2)},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "wall_s_timed": round(t1 - t0, 4),
+    }
+    if rank == 0:
+        result["cpu_baseline"] = cpu_baseline(case, args)
+        print(json.dumps(result), flush=True)
+
+
+def run_e2e(args, case, pa, L, dev, stream, reps, new_sm, bt, cl, q, new_k, new_v, out, sb,
+            world):
+    """pa_reshape_and_cache + pa_decode from pinned host buffers, output back
+    to pinned host memory, every step."""
+    S, Hq, Hkv, D = case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim
+    host = {n: t.cpu().pin_memory() for n, t in
+            (("q", q), ("k", new_k), ("v", new_v), ("sm", new_sm), ("cl", cl), ("bt", bt))}
+    dev_bufs = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    wsb = pa.decode_workspace_size(S, Hq, Hkv, D, case.block_size, case.max_blocks_per_seq,
+                                   case.window)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    K = args.steps
+
+    def step(i):
+        k_, v_ = reps[i % len(reps)]
+        for n, t in host.items():
+            dev_bufs[n].copy_(t, non_blocking=True)
+        pa.reshape_and_cache(dev_bufs["k"], dev_bufs["v"], k_, v_, dev_bufs["sm"],
+                             case.kv_dtype, case.k_scale, case.v_scale)
+        pa.decode(out, dev_bufs["q"], k_, v_, dev_bufs["bt"], dev_bufs["cl"], Hkv, case.scale,
+                  case.window, case.kv_dtype, case.k_scale, case.v_scale, ws)
+        out_h.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    el = all_reduce(e0.elapsed_time(e1) / 1e3, "max", dev)
+    tot = all_reduce(float(sb["total"] * K), "sum", dev)
+    return {"value": round(tot / el / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(el / K * 1e3, 5)}
+
+
+def cpu_baseline(case, args):
+    """The oracle on the host cores, bounded to ~10-20 s."""
+    rows_total = case.num_seqs * case.num_heads
+    times, sbytes, nrows = oracle_step_time(case, rows_total, 1)
+    per = times[0]
+    reps = max(1, min(20, int(12.0 / max(per, 1e-3))))
+    if reps > 1:
+        times, sbytes, nrows = oracle_step_time(case, rows_total, reps)
+    t = statistics.median(times)
+    return {"value": round(sbytes / t / 1e9, 4), "unit": "GB/s", "cores": cores(),
+            "kind": "oracle", "seconds_per_step": round(t, 4),
+            "sample": f"whole batch ({nrows} sequence-head rows) x {len(times)} reps: oracle "
+                      "write of the new rows + fp64 decode, OpenMP over rows"}
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from paged_kv_cache_context_gb300 import workloads as wl
+    case = wl.config(args.workload)
+    rows_total = case.num_seqs * case.num_heads
+    # calibrate the cost of a row, then size each step's sample to fit the budget
+    t_cal, _, n_cal = oracle_step_time(case, min(rows_total, 64), 1)
+    per_row = t_cal[0] / n_cal
+    budget = 120.0
+    rows = max(1, min(rows_total, int(budget / max(1, args.steps + args.warmup) / per_row)))
+    times, sbytes, nrows = oracle_step_time(case, rows, args.steps + args.warmup)
+    times = times[args.warmup:]
+    el = sum(times)
+    value = sbytes * len(times) / el / 1e9
+    sb = step_bytes(case)
+    out = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / len(times) * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": args.workload, "num_seqs": case.num_seqs,
+                   "num_heads": case.num_heads, "num_kv_heads": case.num_kv_heads,
+                   "head_dim": case.head_dim, "block_size": case.block_size,
+                   "bytes_per_step_full_batch": sb["total"]},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores(),
+                         "kind": "oracle",
+                         "sample": f"{nrows} of {rows_total} sequence-head rows per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="mistral_bf16",
+                    choices=("tiny", "mistral_bf16", "ring_bf16", "fp8_phi3", "prefix_bf16"))
+    ap.add_argument("--replicas", type=int, default=4)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, local_rank, world = rank_info()
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, local_rank, world)
+    finally:
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

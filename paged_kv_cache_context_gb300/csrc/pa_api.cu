@@ -1,0 +1,540 @@
+// pa_api.cu -- the C ABI of include/pa.h: host-side validation and planning,
+// the small kernels (slot mapping, cache write, split reduction) and the
+// per-device error word. The decode kernels live in pa_decode_<q>_<cache>.cu.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "pa_decode.cuh"
+#include "pa_device.cuh"
+
+#define PA_API extern "C" __attribute__((visibility("default")))
+
+namespace pa {
+
+// ================================================================ error word
+// One word per device; kernels OR PA_DEVERR_* bits into it, never trap.
+__device__ unsigned g_error_word;
+
+static std::mutex g_err_mu;
+static unsigned* g_err_ptr[64];
+
+// Device address of the current device's error word (NULL if unavailable).
+static unsigned* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned*>(ptr);
+  }
+  return g_err_ptr[dev];
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int dtype_bytes(int dt) { return dt == PA_F32 ? 4 : 2; }
+
+static bool valid_dtype(int dt) { return dt == PA_F32 || dt == PA_BF16 || dt == PA_F16; }
+
+// GB300: the split plan is sized for its 152 SMs (fixed, so the plan is a
+// pure function of the call's sizes and can be queried without a GPU).
+constexpr int kPlanSMs = 152;
+constexpr int kPlanCtasPerSM = 3;
+constexpr int kPlanWaves = 4;
+constexpr int kMinPagesPerSplit = 4;
+constexpr int kMaxPagesPerSplit = 64;
+
+static int group_bucket(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8; }
+
+// ================================================================ kernels
+// slot = block_tables[s][r / bs] * bs + r % bs, r = pos (mod W for a ring)
+__global__ void slot_mapping_kernel(int64_t* out, const int32_t* block_tables,
+                                    const int32_t* seq_idx, const int32_t* positions, int T,
+                                    int S, int MB, int bs, int window, unsigned* err) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const int pos = positions[t];
+  const int s = seq_idx ? seq_idx[t] : t;
+  if (pos < 0) {
+    out[t] = -1;
+    return;
+  }
+  const int r = window > 0 ? pos % window : pos;
+  const int page = r / bs;
+  if (s < 0 || s >= S || page >= MB) {
+    out[t] = -1;
+    raise_error(err, PA_DEVERR_SEQ);
+    return;
+  }
+  out[t] = (int64_t)block_tables[(size_t)s * MB + page] * bs + r % bs;
+}
+
+// AUTO write: copy 16-byte chunks of each (token, kv head) row to its slot.
+__global__ void cache_copy_kernel(const uint4* key, const uint4* value, uint4* k_cache,
+                                  uint4* v_cache, const int64_t* slots, int T, int Hkv,
+                                  int row_chunks, int bs, int64_t capacity, unsigned* err) {
+  const int64_t total = (int64_t)T * Hkv * row_chunks;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / row_chunks;  // t * Hkv + h
+    const int ch = static_cast<int>(i - row * row_chunks);
+    const int t = static_cast<int>(row / Hkv), h = static_cast<int>(row % Hkv);
+    const int64_t slot = slots[t];
+    if (slot < 0) continue;
+    if (slot >= capacity) {
+      if (h == 0 && ch == 0) raise_error(err, PA_DEVERR_SLOT);
+      continue;
+    }
+    const int64_t blk = slot / bs, off = slot % bs;
+    const int64_t dst = ((blk * Hkv + h) * bs + off) * row_chunks + ch;
+    k_cache[dst] = key[i];
+    v_cache[dst] = value[i];
+  }
+}
+
+// FP8 write: 8 elements per thread, x / scale (IEEE binary32 division) then
+// E4M3 round-to-nearest-even with finite saturation.
+template <typename IT>
+__global__ void cache_fp8_kernel(const IT* key, const IT* value, uint2* k_cache,
+                                 uint2* v_cache, const int64_t* slots, int T, int Hkv,
+                                 int row_chunks, int bs, int64_t capacity, float k_scale,
+                                 float v_scale, unsigned* err) {
+  const int64_t total = (int64_t)T * Hkv * row_chunks;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / row_chunks;
+    const int ch = static_cast<int>(i - row * row_chunks);
+    const int t = static_cast<int>(row / Hkv), h = static_cast<int>(row % Hkv);
+    const int64_t slot = slots[t];
+    if (slot < 0) continue;
+    if (slot >= capacity) {
+      if (h == 0 && ch == 0) raise_error(err, PA_DEVERR_SLOT);
+      continue;
+    }
+    const int64_t blk = slot / bs, off = slot % bs;
+    const int64_t dst = ((blk * Hkv + h) * bs + off) * row_chunks + ch;
+    float xk[8], xv[8];
+    const IT* kp = key + i * 8;
+    const IT* vp = value + i * 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      xk[j] = __fdiv_rn(Elem<IT>::to_f32(kp[j]), k_scale);
+      xv[j] = __fdiv_rn(Elem<IT>::to_f32(vp[j]), v_scale);
+    }
+    uint2 ok, ov;
+    ok.x = e4m3x2_from_float2(xk[0], xk[1]) | e4m3x2_from_float2(xk[2], xk[3]) << 16;
+    ok.y = e4m3x2_from_float2(xk[4], xk[5]) | e4m3x2_from_float2(xk[6], xk[7]) << 16;
+    ov.x = e4m3x2_from_float2(xv[0], xv[1]) | e4m3x2_from_float2(xv[2], xv[3]) << 16;
+    ov.y = e4m3x2_from_float2(xv[4], xv[5]) | e4m3x2_from_float2(xv[6], xv[7]) << 16;
+    k_cache[dst] = ok;
+    v_cache[dst] = ov;
+  }
+}
+
+// LSE combination of split partials: one warp per (sequence, head) row.
+template <typename OT>
+__global__ void __launch_bounds__(128)
+    reduce_kernel(OT* out, const float* tmp_out, const float* max_logits, const float* exp_sums,
+                  int64_t rows, int D, int NS) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = blockIdx.x * 4ll + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const float* ml = max_logits + row * NS;
+  const float* es = exp_sums + row * NS;
+  float M = -INFINITY;
+  for (int j = lane; j < NS; j += 32)
+    if (es[j] > 0.f) M = fmaxf(M, ml[j]);
+#pragma unroll
+  for (int off = 16; off >= 1; off /= 2) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  OT* o = out + row * D;
+  if (M == -INFINITY) {
+    for (int d = lane; d < D; d += 32) o[d] = Elem<OT>::from_f32(0.f);
+    return;
+  }
+  // lane owns 4-float chunks d4 = lane, lane + 32, ... of the row
+  constexpr int MAXC = 4;  // D <= 512
+  float4 a[MAXC];
+#pragma unroll
+  for (int c = 0; c < MAXC; ++c) a[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  const int nchunk = D / 4;
+  for (int j = 0; j < NS; ++j) {
+    const float l = es[j];
+    if (!(l > 0.f)) continue;  // empty split: its tmp_out row is never read
+    const float w = l * expf(ml[j] - M);
+    wsum += w;
+    const float4* src = reinterpret_cast<const float4*>(tmp_out + (row * NS + j) * D);
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c) {
+      const int d4 = lane + 32 * c;
+      if (d4 < nchunk) {
+        const float4 v = src[d4];
+        a[c].x = fmaf(w, v.x, a[c].x);
+        a[c].y = fmaf(w, v.y, a[c].y);
+        a[c].z = fmaf(w, v.z, a[c].z);
+        a[c].w = fmaf(w, v.w, a[c].w);
+      }
+    }
+  }
+  const float inv = 1.f / wsum;
+#pragma unroll
+  for (int c = 0; c < MAXC; ++c) {
+    const int d4 = lane + 32 * c;
+    if (d4 < nchunk) {
+      o[4 * d4 + 0] = Elem<OT>::from_f32(a[c].x * inv);
+      o[4 * d4 + 1] = Elem<OT>::from_f32(a[c].y * inv);
+      o[4 * d4 + 2] = Elem<OT>::from_f32(a[c].z * inv);
+      o[4 * d4 + 3] = Elem<OT>::from_f32(a[c].w * inv);
+    }
+  }
+}
+
+static int grid_for(int64_t work, int threads) {
+  int64_t b = (work + threads - 1) / threads;
+  const int64_t cap = 152 * 16;
+  return static_cast<int>(b < 1 ? 1 : (b > cap ? cap : b));
+}
+
+// ================================================================ validation
+struct DecodeShape {
+  int S, Hq, Hkv, D, bs, NB, MB, window;
+  int q_dtype, kv_dtype;
+  float k_scale, v_scale;
+};
+
+static pa_status check_decode(const DecodeShape& a, const void* out, const void* query,
+                              const void* kc, const void* vc, const int32_t* bt,
+                              const int32_t* cl) {
+  if (a.S < 0 || a.S > 65535) return PA_ERR_SHAPE;
+  if (a.S == 0) return PA_OK;
+  if (!out || !query || !kc || !vc || !bt || !cl) return PA_ERR_NULL;
+  if (!valid_dtype(a.q_dtype) || (a.kv_dtype != PA_KV_AUTO && a.kv_dtype != PA_KV_FP8_E4M3))
+    return PA_ERR_DTYPE;
+  if (a.Hq <= 0 || a.Hkv <= 0 || a.Hkv > 65535 || a.Hq % a.Hkv != 0 || a.Hq / a.Hkv > 8)
+    return PA_ERR_SHAPE;
+  if (a.D != 64 && a.D != 96 && a.D != 128) return PA_ERR_HEAD_DIM;
+  if (a.bs != 16 && a.bs != 32 && a.bs != 64) return PA_ERR_BLOCK_SIZE;
+  if (a.NB <= 0 || a.MB <= 0) return PA_ERR_SHAPE;
+  if (a.window < 0 || (a.window > 0 && (a.window % a.bs != 0 || a.window / a.bs > a.MB)))
+    return PA_ERR_WINDOW;
+  if (a.kv_dtype == PA_KV_FP8_E4M3 &&
+      !(isfinite(a.k_scale) && a.k_scale > 0.f && isfinite(a.v_scale) && a.v_scale > 0.f))
+    return PA_ERR_SCALE;
+  if (!aligned16(out) || !aligned16(query) || !aligned16(kc) || !aligned16(vc)) return PA_ERR_ALIGN;
+  return PA_OK;
+}
+
+static int max_pages(int MB, int bs, int window) { return window > 0 ? window / bs : MB; }
+
+static void plan(int S, int Hkv, int MB, int bs, int window, int* ns, int* pps) {
+  const int64_t mp = max_pages(MB, bs, window);
+  const int64_t units = (int64_t)S * Hkv;
+  const int64_t target = (int64_t)kPlanSMs * kPlanCtasPerSM * kPlanWaves;
+  int64_t p = (units * mp + target - 1) / target;
+  if (p < kMinPagesPerSplit) p = kMinPagesPerSplit;
+  if (p > kMaxPagesPerSplit) p = kMaxPagesPerSplit;
+  int64_t n = (mp + p - 1) / p;
+  if (n <= 1) {
+    *ns = 1;
+    *pps = static_cast<int>(mp);
+    return;
+  }
+  p = (mp + n - 1) / n;  // even out the splits
+  *ns = static_cast<int>(n);
+  *pps = static_cast<int>(p);
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static size_t partials_bytes(int S, int Hq, int D, int ns) {
+  const size_t rows = (size_t)S * Hq * ns;
+  return align256(rows * D * 4) + 2 * align256(rows * 4);
+}
+
+static cudaError_t run_decode(const DecodeParams& prm, const DecodeShape& a, cudaStream_t st) {
+  const int GT = group_bucket(a.Hq / a.Hkv);
+  if (a.kv_dtype == PA_KV_AUTO) {
+    switch (a.q_dtype) {
+      case PA_F32: return pa_dispatch_decode_f32_f32(prm, a.S, a.D, GT, a.bs, st);
+      case PA_BF16: return pa_dispatch_decode_bf16_bf16(prm, a.S, a.D, GT, a.bs, st);
+      default: return pa_dispatch_decode_f16_f16(prm, a.S, a.D, GT, a.bs, st);
+    }
+  }
+  switch (a.q_dtype) {
+    case PA_F32: return pa_dispatch_decode_f32_e4m3(prm, a.S, a.D, GT, a.bs, st);
+    case PA_BF16: return pa_dispatch_decode_bf16_e4m3(prm, a.S, a.D, GT, a.bs, st);
+    default: return pa_dispatch_decode_f16_e4m3(prm, a.S, a.D, GT, a.bs, st);
+  }
+}
+
+static DecodeParams make_params(const DecodeShape& a, const void* query, const void* kc,
+                                const void* vc, const int32_t* bt, const int32_t* cl,
+                                float scale, unsigned* err) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  DecodeParams p{};
+  p.query = query;
+  p.k_cache = static_cast<const uint8_t*>(kc);
+  p.v_cache = static_cast<const uint8_t*>(vc);
+  p.block_tables = bt;
+  p.context_lens = cl;
+  p.err = err;
+  p.num_heads = a.Hq;
+  p.num_kv_heads = a.Hkv;
+  p.group = a.Hq / a.Hkv;
+  p.num_blocks = a.NB;
+  p.max_blocks_per_seq = a.MB;
+  p.window = a.window;
+  const bool fp8 = a.kv_dtype == PA_KV_FP8_E4M3;
+  p.q_scale = scale * kLog2e * (fp8 ? a.k_scale : 1.f);
+  p.v_scale = fp8 ? a.v_scale : 1.f;
+  return p;
+}
+
+static cudaError_t run_reduce(void* out, const float* tmp, const float* ml, const float* es,
+                              int64_t rows, int D, int NS, int dt, cudaStream_t st) {
+  const int grid = static_cast<int>((rows + 3) / 4);
+  switch (dt) {
+    case PA_F32:
+      reduce_kernel<float><<<grid, 128, 0, st>>>(static_cast<float*>(out), tmp, ml, es, rows, D, NS);
+      break;
+    case PA_BF16:
+      reduce_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(static_cast<__nv_bfloat16*>(out), tmp, ml,
+                                                         es, rows, D, NS);
+      break;
+    default:
+      reduce_kernel<__half><<<grid, 128, 0, st>>>(static_cast<__half*>(out), tmp, ml, es, rows, D, NS);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+// ================================================================ C ABI
+PA_API int pa_version(void) { return (1 << 16) | 0; }
+
+PA_API const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_NULL: return "a required pointer is NULL";
+    case PA_ERR_DTYPE: return "unsupported element type or combination";
+    case PA_ERR_SHAPE: return "inconsistent or unsupported sizes";
+    case PA_ERR_HEAD_DIM: return "head_dim must be 64, 96 or 128";
+    case PA_ERR_BLOCK_SIZE: return "block_size must be 16, 32 or 64";
+    case PA_ERR_WINDOW: return "window must be >= 0, a multiple of block_size, and fit the block table";
+    case PA_ERR_WORKSPACE: return "workspace too small for the split plan";
+    case PA_ERR_CUDA: return "a CUDA runtime call failed";
+    case PA_ERR_DEVICE: return "a kernel flagged out-of-range data (see the error bits)";
+    case PA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case PA_ERR_SCALE: return "FP8 scales must be finite and positive";
+    default: return "unknown status";
+  }
+}
+
+PA_API pa_status pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
+                                 const int32_t* seq_idx, const int32_t* positions,
+                                 int num_tokens, int num_seqs, int max_blocks_per_seq,
+                                 int block_size, int window, pa_stream_t stream) {
+  if (num_tokens < 0 || num_seqs < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (!slot_mapping || !block_tables || !positions) return PA_ERR_NULL;
+  if (num_seqs <= 0 || max_blocks_per_seq <= 0) return PA_ERR_SHAPE;
+  if (block_size <= 0) return PA_ERR_BLOCK_SIZE;
+  if (window < 0 || (window > 0 && window % block_size != 0)) return PA_ERR_WINDOW;
+  unsigned* err = error_word();
+  const int threads = 256;
+  slot_mapping_kernel<<<(num_tokens + threads - 1) / threads, threads, 0,
+                        reinterpret_cast<cudaStream_t>(stream)>>>(
+      slot_mapping, block_tables, seq_idx, positions, num_tokens, num_seqs, max_blocks_per_seq,
+      block_size, window, err);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache,
+                                      void* v_cache, const int64_t* slot_mapping, int num_tokens,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int num_blocks, pa_dtype in_dtype, pa_kv_dtype kv_dtype,
+                                      float k_scale, float v_scale, pa_stream_t stream) {
+  if (num_tokens < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_NULL;
+  if (!valid_dtype(in_dtype) || (kv_dtype != PA_KV_AUTO && kv_dtype != PA_KV_FP8_E4M3))
+    return PA_ERR_DTYPE;
+  if (num_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_SHAPE;
+  if (head_dim <= 0 || head_dim % 8 != 0 || head_dim > 1024) return PA_ERR_HEAD_DIM;
+  if (block_size <= 0 || block_size > 1024) return PA_ERR_BLOCK_SIZE;
+  if (kv_dtype == PA_KV_FP8_E4M3 &&
+      !(isfinite(k_scale) && k_scale > 0.f && isfinite(v_scale) && v_scale > 0.f))
+    return PA_ERR_SCALE;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_ALIGN;
+  unsigned* err = error_word();
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t capacity = (int64_t)num_blocks * block_size;
+  const int threads = 256;
+  if (kv_dtype == PA_KV_AUTO) {
+    const int chunks = head_dim * dtype_bytes(in_dtype) / 16;
+    const int64_t work = (int64_t)num_tokens * num_kv_heads * chunks;
+    cache_copy_kernel<<<grid_for(work, threads), threads, 0, st>>>(
+        static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, num_tokens,
+        num_kv_heads, chunks, block_size, capacity, err);
+  } else {
+    const int chunks = head_dim / 8;
+    const int64_t work = (int64_t)num_tokens * num_kv_heads * chunks;
+    const int grid = grid_for(work, threads);
+    uint2* kc = static_cast<uint2*>(k_cache);
+    uint2* vc = static_cast<uint2*>(v_cache);
+    switch (in_dtype) {
+      case PA_F32:
+        cache_fp8_kernel<float><<<grid, threads, 0, st>>>(
+            static_cast<const float*>(key), static_cast<const float*>(value), kc, vc, slot_mapping,
+            num_tokens, num_kv_heads, chunks, block_size, capacity, k_scale, v_scale, err);
+        break;
+      case PA_BF16:
+        cache_fp8_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(key), static_cast<const __nv_bfloat16*>(value), kc,
+            vc, slot_mapping, num_tokens, num_kv_heads, chunks, block_size, capacity, k_scale,
+            v_scale, err);
+        break;
+      default:
+        cache_fp8_kernel<__half><<<grid, threads, 0, st>>>(
+            static_cast<const __half*>(key), static_cast<const __half*>(value), kc, vc,
+            slot_mapping, num_tokens, num_kv_heads, chunks, block_size, capacity, k_scale,
+            v_scale, err);
+    }
+  }
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_blocks_per_seq, int window,
+                                int* num_splits, int* pages_per_split) {
+  (void)head_dim;
+  if (!num_splits || !pages_per_split) return PA_ERR_NULL;
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0)
+    return PA_ERR_SHAPE;
+  if (block_size <= 0) return PA_ERR_BLOCK_SIZE;
+  if (window < 0 || (window > 0 && window % block_size != 0)) return PA_ERR_WINDOW;
+  plan(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, window, num_splits,
+       pages_per_split);
+  return PA_OK;
+}
+
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int max_blocks_per_seq,
+                                       int window) {
+  int ns = 1, pps = 1;
+  if (pa_decode_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                     window, &ns, &pps) != PA_OK || ns <= 1)
+    return 0;
+  return partials_bytes(num_seqs, num_heads, head_dim, ns);
+}
+
+PA_API pa_status pa_decode_partials(float* tmp_out, float* max_logits, float* exp_sums,
+                                    const void* query, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, const int32_t* context_lens,
+                                    int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                    int block_size, int num_blocks, int max_blocks_per_seq,
+                                    float scale, int window, pa_dtype q_dtype,
+                                    pa_kv_dtype kv_dtype, float k_scale, float v_scale,
+                                    int num_splits, int pages_per_split, pa_stream_t stream) {
+  DecodeShape a{num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                max_blocks_per_seq, window, q_dtype, kv_dtype, k_scale, v_scale};
+  pa_status rc = check_decode(a, tmp_out, query, k_cache, v_cache, block_tables, context_lens);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  if (!max_logits || !exp_sums) return PA_ERR_NULL;
+  if (num_splits < 1 || pages_per_split < 1 || num_splits > 65535 ||
+      (int64_t)num_splits * pages_per_split < max_pages(max_blocks_per_seq, block_size, window))
+    return PA_ERR_SHAPE;
+  DecodeParams p = make_params(a, query, k_cache, v_cache, block_tables, context_lens, scale,
+                               error_word());
+  p.tmp_out = tmp_out;
+  p.max_logits = max_logits;
+  p.exp_sums = exp_sums;
+  p.partials = 1;
+  p.num_splits = num_splits;
+  p.pages_per_split = pages_per_split;
+  return run_decode(p, a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_reduce(void* out, const float* tmp_out, const float* max_logits,
+                           const float* exp_sums, int num_seqs, int num_heads, int head_dim,
+                           int num_splits, pa_dtype out_dtype, pa_stream_t stream) {
+  if (num_seqs < 0 || num_heads < 0) return PA_ERR_SHAPE;
+  if (num_seqs == 0 || num_heads == 0) return PA_OK;
+  if (!out || !tmp_out || !max_logits || !exp_sums) return PA_ERR_NULL;
+  if (!valid_dtype(out_dtype)) return PA_ERR_DTYPE;
+  if (head_dim <= 0 || head_dim % 4 != 0 || head_dim > 512) return PA_ERR_HEAD_DIM;
+  if (num_splits < 1) return PA_ERR_SHAPE;
+  if (!aligned16(tmp_out)) return PA_ERR_ALIGN;
+  return run_reduce(out, tmp_out, max_logits, exp_sums, (int64_t)num_seqs * num_heads, head_dim,
+                    num_splits, out_dtype, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_decode(void* out, const void* query, const void* k_cache,
+                           const void* v_cache, const int32_t* block_tables,
+                           const int32_t* context_lens, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           int max_blocks_per_seq, float scale, int window, pa_dtype q_dtype,
+                           pa_kv_dtype kv_dtype, float k_scale, float v_scale, void* workspace,
+                           size_t workspace_bytes, pa_stream_t stream) {
+  DecodeShape a{num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                max_blocks_per_seq, window, q_dtype, kv_dtype, k_scale, v_scale};
+  pa_status rc = check_decode(a, out, query, k_cache, v_cache, block_tables, context_lens);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int ns = 1, pps = 1;
+  plan(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, window, &ns, &pps);
+  const size_t need = ns > 1 ? partials_bytes(num_seqs, num_heads, head_dim, ns) : 0;
+  if (ns > 1 && (!workspace || workspace_bytes < need || !aligned16(workspace))) {
+    ns = 1;  // not enough scratch: one CTA per (sequence, kv head)
+    pps = max_pages(max_blocks_per_seq, block_size, window);
+  }
+  DecodeParams p = make_params(a, query, k_cache, v_cache, block_tables, context_lens, scale,
+                               error_word());
+  p.num_splits = ns;
+  p.pages_per_split = pps;
+  if (ns == 1) {
+    p.out = out;
+    p.partials = 0;
+    return run_decode(p, a, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
+  const size_t rows = (size_t)num_seqs * num_heads * ns;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.tmp_out = reinterpret_cast<float*>(ws);
+  p.max_logits = reinterpret_cast<float*>(ws + align256(rows * head_dim * 4));
+  p.exp_sums = reinterpret_cast<float*>(ws + align256(rows * head_dim * 4) + align256(rows * 4));
+  p.partials = 1;
+  if (run_decode(p, a, st) != cudaSuccess) return PA_ERR_CUDA;
+  return run_reduce(out, p.tmp_out, p.max_logits, p.exp_sums, (int64_t)num_seqs * num_heads,
+                    head_dim, ns, q_dtype, st) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_get_device_error(pa_stream_t stream, uint32_t* error_bits) {
+  if (error_bits) *error_bits = 0;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  unsigned* dev = error_word();
+  if (!dev) return PA_ERR_CUDA;
+  unsigned bits = 0;
+  if (cudaMemcpy(&bits, dev, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (bits) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(dev, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
+  if (error_bits) *error_bits = bits;
+  return bits ? PA_ERR_DEVICE : PA_OK;
+}

@@ -1,0 +1,8 @@
+// Paged decode kernels: query/output __nv_bfloat16, cache pa::E4M3 (all head dims, group sizes
+// and block sizes). One translation unit per dtype pair so they build in parallel.
+#include "pa_decode.cuh"
+
+cudaError_t pa_dispatch_decode_bf16_e4m3(const pa::DecodeParams& prm, int num_seqs, int D, int GT,
+                                  int BS, cudaStream_t stream) {
+  return pa::dispatch_decode<__nv_bfloat16, pa::E4M3>(prm, num_seqs, D, GT, BS, stream);
+}

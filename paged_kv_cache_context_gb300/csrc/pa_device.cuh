@@ -1,0 +1,207 @@
+// pa_device.cuh -- device-side building blocks for the sm_103a paged-attention
+// kernels: mbarrier + 1-D bulk-copy (TMA) wrappers with bounded waits, element
+// loads/conversions, and the per-device error word protocol.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------- error word
+__device__ __forceinline__ void raise_error(unsigned* err, unsigned bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// ---------------------------------------------------------------- timers
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// A bounded wait gives up after this long (normal waits last microseconds).
+constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// 1-D bulk asynchronous copy global -> shared, completion counted in bytes on
+// an mbarrier of this CTA. Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Named barrier over a subset of warps (id 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------- elements
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+  static constexpr int bytes = 4;
+  __device__ __forceinline__ static float to_f32(float x) { return x; }
+  __device__ __forceinline__ static float from_f32(float x) { return x; }
+};
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr int bytes = 2;
+  __device__ __forceinline__ static float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+  __device__ __forceinline__ static __nv_bfloat16 from_f32(float x) { return __float2bfloat16_rn(x); }
+};
+template <>
+struct Elem<__half> {
+  static constexpr int bytes = 2;
+  __device__ __forceinline__ static float to_f32(__half x) { return __half2float(x); }
+  __device__ __forceinline__ static __half from_f32(float x) { return __float2half_rn(x); }
+};
+// FP8 E4M3 cache element (one byte).
+struct E4M3 {};
+template <>
+struct Elem<E4M3> {
+  static constexpr int bytes = 1;
+};
+
+// Two E4M3 codes (low byte first) -> two floats, via the hardware
+// e4m3x2 -> f16x2 conversion (exact: every E4M3 value is an f16 value).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+
+// Widen a 32-bit word holding 32/(8*bytes) elements of CT into floats.
+template <typename CT>
+__device__ __forceinline__ void widen_word(uint32_t w, float* out);
+
+template <>
+__device__ __forceinline__ void widen_word<float>(uint32_t w, float* out) {
+  out[0] = __uint_as_float(w);
+}
+template <>
+__device__ __forceinline__ void widen_word<__nv_bfloat16>(uint32_t w, float* out) {
+  out[0] = __uint_as_float(w << 16);
+  out[1] = __uint_as_float(w & 0xFFFF0000u);
+}
+template <>
+__device__ __forceinline__ void widen_word<__half>(uint32_t w, float* out) {
+  __half2 h = *reinterpret_cast<__half2*>(&w);
+  float2 f = __half22float2(h);
+  out[0] = f.x;
+  out[1] = f.y;
+}
+template <>
+__device__ __forceinline__ void widen_word<E4M3>(uint32_t w, float* out) {
+  float2 a = e4m3x2_to_float2(static_cast<uint16_t>(w & 0xFFFFu));
+  float2 b = e4m3x2_to_float2(static_cast<uint16_t>(w >> 16));
+  out[0] = a.x;
+  out[1] = a.y;
+  out[2] = b.x;
+  out[3] = b.y;
+}
+
+// Load PB bytes (one "piece") from shared memory and widen its PB/bytes(CT)
+// elements into out[]. PB in {1, 2, 4, 8, 16}; the address is PB-aligned.
+template <typename CT, int PB>
+__device__ __forceinline__ void load_piece(const uint8_t* p, float* out) {
+  constexpr int EB = Elem<CT>::bytes;
+  if constexpr (PB == 16) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    constexpr int E = 4 / EB;
+    widen_word<CT>(v.x, out);
+    widen_word<CT>(v.y, out + E);
+    widen_word<CT>(v.z, out + 2 * E);
+    widen_word<CT>(v.w, out + 3 * E);
+  } else if constexpr (PB == 8) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    constexpr int E = 4 / EB;
+    widen_word<CT>(v.x, out);
+    widen_word<CT>(v.y, out + E);
+  } else if constexpr (PB == 4) {
+    widen_word<CT>(*reinterpret_cast<const uint32_t*>(p), out);
+  } else if constexpr (PB == 2) {
+    const uint16_t v = *reinterpret_cast<const uint16_t*>(p);
+    if constexpr (EB == 2) {
+      float tmp[2];
+      widen_word<CT>(static_cast<uint32_t>(v), tmp);
+      out[0] = tmp[0];
+    } else {  // two E4M3 codes
+      float2 f = e4m3x2_to_float2(v);
+      out[0] = f.x;
+      out[1] = f.y;
+    }
+  } else {  // PB == 1: one E4M3 code
+    float2 f = e4m3x2_to_float2(static_cast<uint16_t>(*p));
+    out[0] = f.x;
+  }
+}
+
+// ---------------------------------------------------------------- FP8 encode
+// E4M3 code of x (round to nearest even, finite saturation at +-448; NaN keeps
+// its sign as 0x7F | sign).
+__device__ __forceinline__ uint32_t e4m3x2_from_float2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  uint32_t out = r;
+  if (isnan(lo)) out = (out & 0xFF00u) | 0x7Fu | (__float_as_uint(lo) >> 24 & 0x80u);
+  if (isnan(hi)) out = (out & 0x00FFu) | ((0x7Fu | (__float_as_uint(hi) >> 24 & 0x80u)) << 8);
+  return out;
+}
+
+}  // namespace pa

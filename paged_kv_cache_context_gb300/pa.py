@@ -1,0 +1,181 @@
+"""Python binding of the C ABI in include/pa.h (argument marshalling only).
+
+Every function takes torch CUDA tensors, passes their device pointers and
+sizes to the same-named C entry point of ``libpagedattn.so`` on the current
+torch stream, and raises ``PagedAttentionError`` on a non-zero status. All
+computation runs in the library's CUDA kernels; there is no fallback: if the
+library is missing, loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libpagedattn.so")
+
+# enums of include/pa.h
+PA_F32, PA_BF16, PA_F16 = 0, 1, 2
+PA_KV_AUTO, PA_KV_FP8_E4M3 = 0, 1
+PA_ERR_DEVICE = -9
+DEVERR_BITS = {1: "slot", 2: "block_id", 4: "context_len", 8: "timeout", 16: "seq"}
+
+_DTYPE = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16}
+_KV = {"auto": PA_KV_AUTO, "fp8_e4m3": PA_KV_FP8_E4M3}
+
+_lib = None
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "paged_kv_cache_context_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        sig = {
+            "pa_slot_mapping": [P, P, P, P, I, I, I, I, I, P],
+            "pa_reshape_and_cache": [P, P, P, P, P, I, I, I, I, I, I, I, F, F, P],
+            "pa_decode": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F, F, P, Z, P],
+            "pa_decode_plan": [I, I, I, I, I, I, I, P, P],
+            "pa_decode_workspace_size": [I, I, I, I, I, I, I],
+            "pa_decode_partials": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F,
+                                   F, I, I, P],
+            "pa_reduce": [P, P, P, P, I, I, I, I, I, P],
+            "pa_get_device_error": [P, P],
+            "pa_status_string": [I],
+            "pa_version": [],
+        }
+        for name, args in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = I
+        L.pa_decode_workspace_size.restype = Z
+        L.pa_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pa_status_string(status).decode()
+
+
+def version() -> int:
+    return lib().pa_version()
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise PagedAttentionError(rc, what)
+
+
+def slot_mapping(out: torch.Tensor, block_tables: torch.Tensor, seq_idx: Optional[torch.Tensor],
+                 positions: torch.Tensor, block_size: int, window: int = 0, stream=None):
+    """pa_slot_mapping: out[t] = cache slot of token t (ring-aware)."""
+    S, MB = block_tables.shape
+    _check(lib().pa_slot_mapping(_ptr(out), _ptr(block_tables), _ptr(seq_idx), _ptr(positions),
+                                 positions.numel(), S, MB, block_size, window, _stream(stream)),
+           "pa_slot_mapping")
+
+
+def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, slot_mapping_: torch.Tensor, kv_dtype: str = "auto",
+                      k_scale: float = 1.0, v_scale: float = 1.0, stream=None):
+    """pa_reshape_and_cache: key/value [T, Hkv, D] into caches [NB, Hkv, bs, D]."""
+    T, H, D = key.shape
+    NB, _, bs, _ = k_cache.shape
+    _check(lib().pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(slot_mapping_), T, H, D, bs, NB, _DTYPE[key.dtype],
+                                      _KV[kv_dtype], k_scale, v_scale, _stream(stream)),
+           "pa_reshape_and_cache")
+
+
+def decode_plan(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                block_size: int, max_blocks_per_seq: int, window: int = 0) -> Tuple[int, int]:
+    """pa_decode_plan: (num_splits, pages_per_split)."""
+    ns, pps = ctypes.c_int(), ctypes.c_int()
+    _check(lib().pa_decode_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                max_blocks_per_seq, window, ctypes.addressof(ns),
+                                ctypes.addressof(pps)), "pa_decode_plan")
+    return ns.value, pps.value
+
+
+def decode_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                          block_size: int, max_blocks_per_seq: int, window: int = 0) -> int:
+    return int(lib().pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
+                                              block_size, max_blocks_per_seq, window))
+
+
+def decode(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+           block_tables: torch.Tensor, context_lens: torch.Tensor, num_kv_heads: int,
+           scale: float, window: int = 0, kv_dtype: str = "auto", k_scale: float = 1.0,
+           v_scale: float = 1.0, workspace: Optional[torch.Tensor] = None, stream=None):
+    """pa_decode: out [S, Hq, D] = paged attention of query [S, Hq, D]."""
+    S, Hq, D = query.shape
+    NB, _, bs, _ = k_cache.shape
+    MB = block_tables.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache),
+                           _ptr(block_tables), _ptr(context_lens), S, Hq, num_kv_heads, D, bs, NB,
+                           MB, scale, window, _DTYPE[query.dtype], _KV[kv_dtype], k_scale,
+                           v_scale, _ptr(workspace), ws_bytes, _stream(stream)), "pa_decode")
+
+
+def decode_partials(tmp_out: torch.Tensor, max_logits: torch.Tensor, exp_sums: torch.Tensor,
+                    query: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                    block_tables: torch.Tensor, context_lens: torch.Tensor, num_kv_heads: int,
+                    scale: float, num_splits: int, pages_per_split: int, window: int = 0,
+                    kv_dtype: str = "auto", k_scale: float = 1.0, v_scale: float = 1.0,
+                    stream=None):
+    """pa_decode_partials: split partials tmp_out [S, Hq, NS, D], max_logits and
+    exp_sums [S, Hq, NS]."""
+    S, Hq, D = query.shape
+    NB, _, bs, _ = k_cache.shape
+    MB = block_tables.shape[1]
+    _check(lib().pa_decode_partials(_ptr(tmp_out), _ptr(max_logits), _ptr(exp_sums),
+                                    _ptr(query), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(block_tables), _ptr(context_lens), S, Hq, num_kv_heads,
+                                    D, bs, NB, MB, scale, window, _DTYPE[query.dtype],
+                                    _KV[kv_dtype], k_scale, v_scale, num_splits,
+                                    pages_per_split, _stream(stream)), "pa_decode_partials")
+
+
+def reduce(out: torch.Tensor, tmp_out: torch.Tensor, max_logits: torch.Tensor,
+           exp_sums: torch.Tensor, stream=None):
+    """pa_reduce: LSE combination of [S, Hq, NS, D] partials into out [S, Hq, D]."""
+    S, Hq, NS, D = tmp_out.shape
+    _check(lib().pa_reduce(_ptr(out), _ptr(tmp_out), _ptr(max_logits), _ptr(exp_sums), S, Hq,
+                           D, NS, _DTYPE[out.dtype], _stream(stream)), "pa_reduce")
+
+
+def get_device_error(stream=None) -> int:
+    """pa_get_device_error: synchronise, return and clear the device error bits."""
+    bits = ctypes.c_uint32()
+    rc = lib().pa_get_device_error(_stream(stream), ctypes.addressof(bits))
+    if rc not in (0, PA_ERR_DEVICE):
+        raise PagedAttentionError(rc, "pa_get_device_error")
+    return bits.value

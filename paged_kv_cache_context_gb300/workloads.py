@@ -93,8 +93,9 @@ class DecodeCase:
             sel = sel | ((pre_seq == 0) & (pre_pos < self.shared_prefix_tokens))
         idx = torch.nonzero(sel).flatten()
         pos = pre_pos[idx]
-        key = self.pre_key.cpu()[idx]
-        val = self.pre_value.cpu()[idx]
+        didx = idx.to(self.pre_key.device)
+        key = self.pre_key[didx].cpu()
+        val = self.pre_value[didx].cpu()
         if int(self.new_pos[s]) >= 0:
             pos = torch.cat([pos, self.new_pos.cpu()[s:s + 1]])
             key = torch.cat([key, self.new_key.cpu()[s:s + 1]])

@@ -1,0 +1,123 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/pa.h declares, and rejects bad arguments on the host with the
+documented status codes before touching the device (fake non-NULL pointers
+are never dereferenced on these paths)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from paged_kv_cache_context_gb300 import build, pa
+    build.build()
+    return pa.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(pa_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("pa_reshape_and_cache", "pa_decode", "pa_reduce", "pa_slot_mapping",
+                 "pa_decode_partials", "pa_decode_plan", "pa_decode_workspace_size",
+                 "pa_get_device_error", "pa_status_string", "pa_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    from paged_kv_cache_context_gb300 import pa
+    for code in range(0, -12, -1):
+        assert pa.status_string(code) and pa.status_string(code) != "unknown status"
+    assert pa.status_string(-99) == "unknown status"
+    assert pa.version() >> 16 == 1
+
+
+P = 4096  # a fake, 16-byte aligned, never-dereferenced pointer
+
+
+def decode_call(L, **kw):
+    a = dict(out=P, query=P, k=P, v=P, bt=P, cl=P, S=2, Hq=8, Hkv=2, D=128, bs=32, NB=10, MB=4,
+             scale=0.1, window=0, qd=1, kvd=0, ks=1.0, vs=1.0, ws=None, wsb=0)
+    a.update(kw)
+    return L.pa_decode(a["out"], a["query"], a["k"], a["v"], a["bt"], a["cl"], a["S"], a["Hq"],
+                       a["Hkv"], a["D"], a["bs"], a["NB"], a["MB"], a["scale"], a["window"],
+                       a["qd"], a["kvd"], a["ks"], a["vs"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(query=None), -1), (dict(bt=None), -1), (dict(cl=None), -1),
+    (dict(qd=7), -2), (dict(kvd=5), -2),
+    (dict(Hq=7), -3), (dict(Hq=18, Hkv=2), -3), (dict(S=-1), -3), (dict(NB=0), -3),
+    (dict(MB=0), -3), (dict(S=70000), -3),
+    (dict(D=80), -4), (dict(D=256), -4),
+    (dict(bs=8), -5), (dict(bs=128), -5),
+    (dict(window=-32), -6), (dict(window=48), -6), (dict(window=32 * 5), -6),
+    (dict(kvd=1, ks=0.0), -11), (dict(kvd=1, vs=float("inf")), -11),
+    (dict(kvd=1, ks=float("nan")), -11),
+    (dict(query=P + 8), -10), (dict(k=P + 2), -10),
+])
+def test_decode_rejects_bad_arguments_on_host(L, kw, code):
+    assert decode_call(L, **kw) == code
+
+
+def test_decode_empty_batch_is_a_noop(L):
+    assert decode_call(L, S=0, query=None, out=None) == 0
+
+
+def test_write_rejects_bad_arguments_on_host(L):
+    f = L.pa_reshape_and_cache
+    ok = dict(key=P, value=P, k=P, v=P, sm=P, T=4, H=2, D=64, bs=32, NB=8, ind=1, kvd=0,
+              ks=1.0, vs=1.0)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(a["key"], a["value"], a["k"], a["v"], a["sm"], a["T"], a["H"], a["D"], a["bs"],
+                 a["NB"], a["ind"], a["kvd"], a["ks"], a["vs"], None)
+
+    assert call(T=0, key=None) == 0
+    assert call(key=None) == -1 and call(sm=None) == -1
+    assert call(ind=9) == -2 and call(kvd=3) == -2
+    assert call(T=-1) == -3 and call(H=0) == -3 and call(NB=0) == -3
+    assert call(D=60) == -4 and call(bs=0) == -5
+    assert call(kvd=1, ks=-1.0) == -11
+    assert call(k=P + 4) == -10
+
+
+def test_reduce_and_slot_mapping_reject_bad_arguments(L):
+    assert L.pa_reduce(P, P, P, P, 0, 4, 64, 2, 1, None) == 0
+    assert L.pa_reduce(P, None, P, P, 2, 4, 64, 2, 1, None) == -1
+    assert L.pa_reduce(P, P, P, P, 2, 4, 63, 2, 1, None) == -4
+    assert L.pa_reduce(P, P, P, P, 2, 4, 64, 0, 1, None) == -3
+    assert L.pa_reduce(P, P + 4, P, P, 2, 4, 64, 2, 1, None) == -10
+    assert L.pa_slot_mapping(P, P, None, P, 0, 1, 1, 32, 0, None) == 0
+    assert L.pa_slot_mapping(P, None, None, P, 3, 1, 1, 32, 0, None) == -1
+    assert L.pa_slot_mapping(P, P, None, P, 3, 1, 1, 32, 40, None) == -6
+
+
+def test_split_plan_is_host_only_and_covers_the_context():
+    from paged_kv_cache_context_gb300 import pa
+    for S, Hkv, MB, W in [(32, 8, 128, 0), (8, 8, 128, 4096), (64, 32, 256, 0),
+                          (128, 8, 81, 0), (2, 4, 2, 0), (1, 1, 4096, 0)]:
+        ns, pps = pa.decode_plan(S, 4 * Hkv if Hkv < 32 else Hkv, Hkv, 128, 32, MB, W)
+        pages = W // 32 if W else MB
+        assert ns >= 1 and pps >= 1 and ns * pps >= pages
+        assert (ns - 1) * pps < pages  # no split is entirely past the table
+        ws = pa.decode_workspace_size(S, 32, Hkv, 128, 32, MB, W)
+        assert (ws == 0) == (ns == 1)
+        if ns > 1:
+            assert ws >= S * 32 * ns * (128 + 2) * 4
