@@ -124,7 +124,8 @@ pa_status pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
  * AUTO  : the element bits are copied unchanged.
  * FP8   : code = E4M3(x / k_scale) (IEEE fp32 divide; bf16/f16 inputs widened
  *         exactly), round to nearest even, finite overflow and +-inf saturate
- *         to +-448 (code 0x7E / 0xFE), NaN -> 0x7F | sign, -0 -> 0x80.
+ *         to +-448 (code 0x7E / 0xFE), a NaN input -> 0x7F | (sign of the
+ *         input), -0 -> 0x80.
  *         Same for V with v_scale. Scales must be finite and > 0.
  * Only the rows named by slot_mapping are written; every other byte of the
  * cache is left untouched. Pointers must be 16-byte aligned.

@@ -149,6 +149,21 @@ uint8_t oracle_e4m3_encode(float y)
     return (uint8_t)(sign | ((E + 7) << 3) | mant);
 }
 
+/*
+ * Code stored for input x with per-tensor scale: E4M3(x / scale) with a
+ * binary32 division. A NaN input keeps its own sign (0x7F | sign of x): the
+ * sign of a NaN quotient is not fixed by IEEE 754, so it is not taken from it.
+ */
+static uint8_t or_quantise(float x, float scale)
+{
+    uint32_t u;
+    if (isnan(x)) {
+        memcpy(&u, &x, 4);
+        return (uint8_t)(0x7F | ((u >> 31) ? 0x80 : 0x00));
+    }
+    return oracle_e4m3_encode(x / scale);
+}
+
 /* Bulk helpers so the tests can sweep every binary32 bit pattern. */
 void oracle_e4m3_encode_array(const float* x, uint8_t* out, int64_t n)
 {
@@ -244,10 +259,8 @@ int64_t oracle_reshape_and_cache(const void* key, const void* value, void* k_cac
             }
             for (d = 0; d < head_dim; ++d) {
                 /* binary32 division, correctly rounded (no contraction/fast-math) */
-                float yk = or_load(key, in_code, src + d) / k_scale;
-                float yv = or_load(value, in_code, src + d) / v_scale;
-                ((uint8_t*)k_cache)[dst + d] = oracle_e4m3_encode(yk);
-                ((uint8_t*)v_cache)[dst + d] = oracle_e4m3_encode(yv);
+                ((uint8_t*)k_cache)[dst + d] = or_quantise(or_load(key, in_code, src + d), k_scale);
+                ((uint8_t*)v_cache)[dst + d] = or_quantise(or_load(value, in_code, src + d), v_scale);
             }
         }
     }

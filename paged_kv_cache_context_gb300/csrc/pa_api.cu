@@ -122,8 +122,10 @@ __global__ void cache_fp8_kernel(const IT* key, const IT* value, uint2* k_cache,
     const IT* vp = value + i * 8;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      xk[j] = __fdiv_rn(Elem<IT>::to_f32(kp[j]), k_scale);
-      xv[j] = __fdiv_rn(Elem<IT>::to_f32(vp[j]), v_scale);
+      // a NaN input keeps its own sign (a NaN quotient's sign is unspecified)
+      const float a = Elem<IT>::to_f32(kp[j]), b = Elem<IT>::to_f32(vp[j]);
+      xk[j] = isnan(a) ? a : __fdiv_rn(a, k_scale);
+      xv[j] = isnan(b) ? b : __fdiv_rn(b, v_scale);
     }
     uint2 ok, ov;
     ok.x = e4m3x2_from_float2(xk[0], xk[1]) | e4m3x2_from_float2(xk[2], xk[3]) << 16;

@@ -287,3 +287,16 @@ def test_fp8_write_matches_library_cast():
                 y = x.float() / torch.tensor(sc, dtype=torch.float32)
                 want = torch.clamp(y, -448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
                 assert torch.equal(cache[b, :, r], want)
+
+
+def test_fp8_write_nan_keeps_the_input_sign():
+    """A NaN input is stored as the NaN code with the input's own sign (the
+    sign of a NaN quotient x / scale is not fixed by IEEE 754)."""
+    x = torch.tensor([float("nan"), -float("nan"), 1.0, -0.0]).view(1, 1, 4).repeat(1, 1, 2)
+    x = x.reshape(1, 1, 8).float()
+    kc = torch.zeros(1, 1, 32, 8, dtype=torch.uint8)
+    vc = torch.zeros_like(kc)
+    for scale in (1.0, 0.37, 3.0e5):
+        oracle.reshape_and_cache(x, x, kc, vc, torch.tensor([0]), 32, "fp8_e4m3", scale, scale)
+        assert kc[0, 0, 0, 0] == 0x7F and kc[0, 0, 0, 1] == 0xFF
+        assert kc[0, 0, 0, 3] == 0x80
