@@ -232,6 +232,42 @@ pa_status pa_reduce(void* out, const float* tmp_out, const float* max_logits,
                     int num_splits, pa_dtype out_dtype, pa_stream_t stream);
 
 /*
+ * pa_decode_static_scratch -- pa_decode for callers that cannot allocate.
+ *
+ * The pages have no counterpart of this call; it exists for callers that have
+ * no way to hand pa_decode a workspace: code running inside a host program
+ * that owns every device allocation and offers no allocator, or code that must
+ * never call cudaMalloc (it can synchronise the device and take unbounded
+ * time). It computes exactly what pa_decode computes, with the same kernels
+ * and split plan, but keeps the split partials in an array the library itself
+ * holds in device memory: PA_STATIC_SCRATCH_BYTES (8 MiB) on every GPU where
+ * the library is loaded, kept until the process exits. It allocates nothing.
+ *
+ *  - Limit: when the split plan for these sizes needs more partial storage than
+ *    PA_STATIC_SCRATCH_BYTES (pa_decode_workspace_size() larger than it), the
+ *    call returns PA_ERR_WORKSPACE at once and enqueues nothing. This size
+ *    check comes before the argument checks of pa_decode; every other
+ *    argument rule and error of pa_decode applies unchanged.
+ *  - Set-up: the first call on a device (that device current) looks up the
+ *    array's device address once (cudaGetSymbolAddress); make that first call
+ *    on each device before any stream capture begins.
+ *  - Sharing: all calls on a device share the one array, which keeps whatever
+ *    the last call left in it. Nothing in it needs to start at zero. Calls
+ *    whose kernels may overlap on the GPU (different streams, or different
+ *    host threads, without ordering between them) race on it and must be
+ *    serialised by the caller.
+ */
+#define PA_STATIC_SCRATCH_BYTES (8u << 20)
+pa_status pa_decode_static_scratch(void* out, const void* query,
+                                   const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, const int32_t* context_lens,
+                                   int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int num_blocks, int max_blocks_per_seq,
+                                   float scale, int window, pa_dtype q_dtype,
+                                   pa_kv_dtype kv_dtype, float k_scale, float v_scale,
+                                   pa_stream_t stream);
+
+/*
  * pa_get_device_error -- synchronise `stream`, then read and clear the error
  * word of the current device. *error_bits (may be NULL) receives the
  * PA_DEVERR_* bits. Returns PA_OK when no bit was set, PA_ERR_DEVICE when
