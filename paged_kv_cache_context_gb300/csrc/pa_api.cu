@@ -55,6 +55,8 @@ static int group_bucket(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8
 __global__ void slot_mapping_kernel(int64_t* out, const int32_t* block_tables,
                                     const int32_t* seq_idx, const int32_t* positions, int T,
                                     int S, int MB, int bs, int window, unsigned* err) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   const int pos = positions[t];
@@ -77,6 +79,8 @@ __global__ void slot_mapping_kernel(int64_t* out, const int32_t* block_tables,
 __global__ void cache_copy_kernel(const uint4* key, const uint4* value, uint4* k_cache,
                                   uint4* v_cache, const int64_t* slots, int T, int Hkv,
                                   int row_chunks, int bs, int64_t capacity, unsigned* err) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = (int64_t)T * Hkv * row_chunks;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -103,6 +107,8 @@ __global__ void cache_fp8_kernel(const IT* key, const IT* value, uint2* k_cache,
                                  uint2* v_cache, const int64_t* slots, int T, int Hkv,
                                  int row_chunks, int bs, int64_t capacity, float k_scale,
                                  float v_scale, unsigned* err) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = (int64_t)T * Hkv * row_chunks;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -137,11 +143,15 @@ __global__ void cache_fp8_kernel(const IT* key, const IT* value, uint2* k_cache,
   }
 }
 
-// LSE combination of split partials: one warp per (sequence, head) row.
-template <typename OT>
+// LSE combination of split partials: one warp per (sequence, head) row. Lane j
+// computes the weight of split j; the partial rows of up to 8 splits are
+// loaded before they are accumulated, so their latencies overlap.
+template <typename OT, int MAXC>
 __global__ void __launch_bounds__(128)
     reduce_kernel(OT* out, const float* tmp_out, const float* max_logits, const float* exp_sums,
                   int64_t rows, int D, int NS) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t row = blockIdx.x * 4ll + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -157,31 +167,47 @@ __global__ void __launch_bounds__(128)
     for (int d = lane; d < D; d += 32) o[d] = Elem<OT>::from_f32(0.f);
     return;
   }
-  // lane owns 4-float chunks d4 = lane, lane + 32, ... of the row
-  constexpr int MAXC = 4;  // D <= 512
+  const int nchunk = D / 4;  // lane owns 4-float chunks lane, lane + 32, ...
+  const float4* base = reinterpret_cast<const float4*>(tmp_out + row * NS * (int64_t)D);
   float4 a[MAXC];
 #pragma unroll
   for (int c = 0; c < MAXC; ++c) a[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
-  const int nchunk = D / 4;
-  for (int j = 0; j < NS; ++j) {
-    const float l = es[j];
-    if (!(l > 0.f)) continue;  // empty split: its tmp_out row is never read
-    const float w = l * expf(ml[j] - M);
-    wsum += w;
-    const float4* src = reinterpret_cast<const float4*>(tmp_out + (row * NS + j) * D);
+  for (int j0 = 0; j0 < NS; j0 += 32) {
+    float wl = 0.f;  // weight of split j0 + lane (0 when empty or absent)
+    if (j0 + lane < NS) {
+      const float l = es[j0 + lane];
+      if (l > 0.f) wl = l * expf(ml[j0 + lane] - M);
+    }
+    wsum += wl;
+    const int cnt = min(32, NS - j0);
+    for (int u0 = 0; u0 < cnt; u0 += 8) {
+      float w[8];
+      float4 v[8][MAXC];
 #pragma unroll
-    for (int c = 0; c < MAXC; ++c) {
-      const int d4 = lane + 32 * c;
-      if (d4 < nchunk) {
-        const float4 v = src[d4];
-        a[c].x = fmaf(w, v.x, a[c].x);
-        a[c].y = fmaf(w, v.y, a[c].y);
-        a[c].z = fmaf(w, v.z, a[c].z);
-        a[c].w = fmaf(w, v.w, a[c].w);
+      for (int u = 0; u < 8; ++u) {
+        w[u] = __shfl_sync(0xffffffffu, wl, (u0 + u) & 31);
+        const bool use = u0 + u < cnt && w[u] > 0.f;  // empty splits are never read
+#pragma unroll
+        for (int c = 0; c < MAXC; ++c) {
+          const int d4 = lane + 32 * c;
+          v[u][c] = (use && d4 < nchunk) ? base[(int64_t)(j0 + u0 + u) * nchunk + d4]
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int c = 0; c < MAXC; ++c) {
+          a[c].x = fmaf(w[u], v[u][c].x, a[c].x);
+          a[c].y = fmaf(w[u], v[u][c].y, a[c].y);
+          a[c].z = fmaf(w[u], v[u][c].z, a[c].z);
+          a[c].w = fmaf(w[u], v[u][c].w, a[c].w);
+        }
     }
   }
+#pragma unroll
+  for (int off = 16; off >= 1; off /= 2) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
   const float inv = 1.f / wsum;
 #pragma unroll
   for (int c = 0; c < MAXC; ++c) {
@@ -298,19 +324,25 @@ static DecodeParams make_params(const DecodeShape& a, const void* query, const v
 
 static cudaError_t run_reduce(void* out, const float* tmp, const float* ml, const float* es,
                               int64_t rows, int D, int NS, int dt, cudaStream_t st) {
-  const int grid = static_cast<int>((rows + 3) / 4);
-  switch (dt) {
-    case PA_F32:
-      reduce_kernel<float><<<grid, 128, 0, st>>>(static_cast<float*>(out), tmp, ml, es, rows, D, NS);
-      break;
-    case PA_BF16:
-      reduce_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(static_cast<__nv_bfloat16*>(out), tmp, ml,
-                                                         es, rows, D, NS);
-      break;
-    default:
-      reduce_kernel<__half><<<grid, 128, 0, st>>>(static_cast<__half*>(out), tmp, ml, es, rows, D, NS);
+  const dim3 grid(static_cast<unsigned>((rows + 3) / 4)), block(128);
+  const int mc = (D + 127) / 128;  // float4 chunks per lane
+#define PA_RED(OT, MC)                                                                      \
+  return launch_pdl(reduce_kernel<OT, MC>, grid, block, 0, st, static_cast<OT*>(out), tmp, ml, \
+                    es, rows, D, NS)
+#define PA_RED_MC(OT)      \
+  switch (mc) {            \
+    case 1: PA_RED(OT, 1); \
+    case 2: PA_RED(OT, 2); \
+    case 3: PA_RED(OT, 3); \
+    default: PA_RED(OT, 4); \
   }
-  return cudaGetLastError();
+  switch (dt) {
+    case PA_F32: PA_RED_MC(float)
+    case PA_BF16: PA_RED_MC(__nv_bfloat16)
+    default: PA_RED_MC(__half)
+  }
+#undef PA_RED_MC
+#undef PA_RED
 }
 
 }  // namespace pa
@@ -350,11 +382,11 @@ PA_API pa_status pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tab
   if (window < 0 || (window > 0 && window % block_size != 0)) return PA_ERR_WINDOW;
   unsigned* err = error_word();
   const int threads = 256;
-  slot_mapping_kernel<<<(num_tokens + threads - 1) / threads, threads, 0,
-                        reinterpret_cast<cudaStream_t>(stream)>>>(
-      slot_mapping, block_tables, seq_idx, positions, num_tokens, num_seqs, max_blocks_per_seq,
-      block_size, window, err);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  const cudaError_t e = launch_pdl(
+      slot_mapping_kernel, dim3((num_tokens + threads - 1) / threads), dim3(threads), 0,
+      reinterpret_cast<cudaStream_t>(stream), slot_mapping, block_tables, seq_idx, positions,
+      num_tokens, num_seqs, max_blocks_per_seq, block_size, window, err);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 PA_API pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache,
@@ -379,13 +411,14 @@ PA_API pa_status pa_reshape_and_cache(const void* key, const void* value, void* 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int64_t capacity = (int64_t)num_blocks * block_size;
   const int threads = 256;
+  cudaError_t e = cudaSuccess;
   if (kv_dtype == PA_KV_AUTO) {
     const int chunks = head_dim * dtype_bytes(in_dtype) / 16;
     const int64_t work = (int64_t)num_tokens * num_kv_heads * chunks;
-    cache_copy_kernel<<<grid_for(work, threads), threads, 0, st>>>(
-        static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, num_tokens,
-        num_kv_heads, chunks, block_size, capacity, err);
+    e = launch_pdl(cache_copy_kernel, dim3(grid_for(work, threads)), dim3(threads), 0, st,
+                   static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                   static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping,
+                   num_tokens, num_kv_heads, chunks, block_size, capacity, err);
   } else {
     const int chunks = head_dim / 8;
     const int64_t work = (int64_t)num_tokens * num_kv_heads * chunks;
@@ -394,24 +427,25 @@ PA_API pa_status pa_reshape_and_cache(const void* key, const void* value, void* 
     uint2* vc = static_cast<uint2*>(v_cache);
     switch (in_dtype) {
       case PA_F32:
-        cache_fp8_kernel<float><<<grid, threads, 0, st>>>(
-            static_cast<const float*>(key), static_cast<const float*>(value), kc, vc, slot_mapping,
-            num_tokens, num_kv_heads, chunks, block_size, capacity, k_scale, v_scale, err);
+        e = launch_pdl(cache_fp8_kernel<float>, dim3(grid), dim3(threads), 0, st,
+                       static_cast<const float*>(key), static_cast<const float*>(value), kc, vc,
+                       slot_mapping, num_tokens, num_kv_heads, chunks, block_size, capacity,
+                       k_scale, v_scale, err);
         break;
       case PA_BF16:
-        cache_fp8_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
-            static_cast<const __nv_bfloat16*>(key), static_cast<const __nv_bfloat16*>(value), kc,
-            vc, slot_mapping, num_tokens, num_kv_heads, chunks, block_size, capacity, k_scale,
-            v_scale, err);
+        e = launch_pdl(cache_fp8_kernel<__nv_bfloat16>, dim3(grid), dim3(threads), 0, st,
+                       static_cast<const __nv_bfloat16*>(key),
+                       static_cast<const __nv_bfloat16*>(value), kc, vc, slot_mapping, num_tokens,
+                       num_kv_heads, chunks, block_size, capacity, k_scale, v_scale, err);
         break;
       default:
-        cache_fp8_kernel<__half><<<grid, threads, 0, st>>>(
-            static_cast<const __half*>(key), static_cast<const __half*>(value), kc, vc,
-            slot_mapping, num_tokens, num_kv_heads, chunks, block_size, capacity, k_scale,
-            v_scale, err);
+        e = launch_pdl(cache_fp8_kernel<__half>, dim3(grid), dim3(threads), 0, st,
+                       static_cast<const __half*>(key), static_cast<const __half*>(value), kc, vc,
+                       slot_mapping, num_tokens, num_kv_heads, chunks, block_size, capacity,
+                       k_scale, v_scale, err);
     }
   }
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 PA_API pa_status pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim,

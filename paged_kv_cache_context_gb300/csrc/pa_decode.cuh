@@ -56,11 +56,15 @@ struct DecodeParams {
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
-// Lanes per row: the fewest (>= 4) that keep q and acc at <= 32 fp32 each.
+// Lanes per row: the fewest (>= 4) that keep q and acc at <= 32 fp32 each with
+// an even number of elements per lane (they are processed as fp32 pairs);
+// failing that, the most lanes that still give an even count.
 constexpr int choose_lpr(int D, int GT) {
   for (int l = 4; l <= 32; l *= 2)
-    if (D % l == 0 && (D / l) * GT <= 32) return l;
-  return 32;
+    if (D % l == 0 && (D / l) % 2 == 0 && (D / l) * GT <= 32) return l;
+  for (int l = 32; l >= 4; l /= 2)
+    if (D % l == 0 && (D / l) % 2 == 0) return l;
+  return 4;
 }
 constexpr int choose_pb(int bytes) {
   return bytes % 16 == 0 ? 16 : bytes % 8 == 0 ? 8 : bytes % 4 == 0 ? 4 : bytes % 2 == 0 ? 2 : 1;
@@ -79,13 +83,15 @@ struct Layout {
   static constexpr int PB = choose_pb(EPL * EB);
   static constexpr int EPP = PB / EB;      // elements per piece
   static constexpr int NPL = EPL / EPP;    // pieces per lane
+  static constexpr int EP2 = EPP / 2;      // fp32 pairs per piece
+  static constexpr int EL2 = EPL / 2;      // fp32 pairs per lane
   static constexpr int RPW = 32 / LPR;     // rows a warp covers per step
   static constexpr int NST = TPW / RPW;    // steps per page
   static constexpr int SG = cmin(NST, cmax(1, 16 / GT));  // steps per reduction group
   static constexpr int NV = SG * GT;       // partial dot products per group
   static constexpr int NFIN = cmax(NV / LPR, 1);
   static constexpr int STAGES = cmax(2, cmin(8, 65536 / (2 * PAGE)));
-  static constexpr int SCR = TPW * GT + GT;  // per-warp scratch floats
+  static constexpr int SCR = (TPW * GT + GT + 3) / 4 * 4;  // per-warp scratch floats
   // dynamic shared memory layout
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = STAGES * PAGE;
@@ -98,6 +104,7 @@ struct Layout {
   static_assert(NST >= 1, "lanes per row too small for 8 rows per warp");
   static_assert(NST % SG == 0, "reduction groups must tile the steps");
   static_assert(EPL * LPR == D && NPL * EPP == EPL, "row split");
+  static_assert(EPP % 2 == 0, "pieces hold whole fp32 pairs");
   static_assert(MERGE <= 2 * STAGES * PAGE, "merge area");
   static_assert(PAGE % 16 == 0, "bulk copies move multiples of 16 bytes");
 };
@@ -128,6 +135,49 @@ struct TransposeReduce {
   }
 };
 
+// N consecutive floats from shared memory (vector loads where aligned).
+template <int N>
+__device__ __forceinline__ void load_row(const float* src, float* dst) {
+  if constexpr (N % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src + i);
+      dst[i] = v.x; dst[i + 1] = v.y; dst[i + 2] = v.z; dst[i + 3] = v.w;
+    }
+  } else if constexpr (N == 2) {
+    const float2 v = *reinterpret_cast<const float2*>(src);
+    dst[0] = v.x; dst[1] = v.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) dst[i] = src[i];
+  }
+}
+
+// acc[h][:] += p[h] * V_row[this lane's elements] for one row.
+template <typename CT, typename Ly, int GT, int EL2>
+__device__ __forceinline__ void pv_row_impl(const float* pw_src, const uint8_t* vr, int c,
+                                            float2 (&acc)[GT][EL2]) {
+  float pw[GT];
+  load_row<GT>(pw_src, pw);
+#pragma unroll
+  for (int kk = 0; kk < Ly::NPL; ++kk) {
+    float2 vf[Ly::EP2];
+    load_piece2<CT, Ly::PB>(vr + (kk * Ly::LPR + c) * Ly::PB, vf);
+#pragma unroll
+    for (int h = 0; h < GT; ++h) {
+      const float2 pp = make_float2(pw[h], pw[h]);
+#pragma unroll
+      for (int j2 = 0; j2 < Ly::EP2; ++j2)
+        acc[h][kk * Ly::EP2 + j2] = __ffma2_rn(pp, vf[j2], acc[h][kk * Ly::EP2 + j2]);
+    }
+  }
+}
+template <typename CT, typename Ly, int GT, int EL2>
+__device__ __forceinline__ void pv_row(const float* pw_src, const uint8_t* vr, int c,
+                                       float2 (&acc)[GT][EL2]) {
+  pv_row_impl<CT, Ly, GT, EL2>(pw_src, vr, c, acc);
+}
+
 template <typename QT, typename CT, int D, int GT, int BS>
 __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
     paged_decode_kernel(const __grid_constant__ DecodeParams p) {
@@ -140,6 +190,8 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
   const int split = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = p.num_heads, G = p.group;
+  pdl_wait();
+  pdl_trigger();
 
   // ---- attended slots of this sequence and this split's pages
   int n = p.context_lens[s];
@@ -245,8 +297,9 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
   const int rg = lane / LPR;  // row within a warp step
   float* wscr = reinterpret_cast<float*>(smem + Ly::OFF_SCR) + warp * Ly::SCR;
 
-  float qf[GT][EPL];
-  float acc[GT][EPL];
+  constexpr int EP2 = Ly::EP2, EL2 = Ly::EL2;
+  float2 qf[GT][EL2];   // q (pre-scaled), as consecutive pairs of this lane's elements
+  float2 acc[GT][EL2];  // un-normalised output, same layout
   {
     const QT* q = reinterpret_cast<const QT*>(p.query);
 #pragma unroll
@@ -256,10 +309,13 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
 #pragma unroll
       for (int kk = 0; kk < NPL; ++kk) {
 #pragma unroll
-        for (int jj = 0; jj < EPP; ++jj) {
-          const int d = (kk * LPR + c) * EPP + jj;
-          qf[h][kk * EPP + jj] = live ? Elem<QT>::to_f32(qh[d]) * p.q_scale : 0.f;
-          acc[h][kk * EPP + jj] = 0.f;
+        for (int j2 = 0; j2 < EP2; ++j2) {
+          const int d = (kk * LPR + c) * EPP + 2 * j2;
+          qf[h][kk * EP2 + j2] =
+              live ? make_float2(Elem<QT>::to_f32(qh[d]) * p.q_scale,
+                                 Elem<QT>::to_f32(qh[d + 1]) * p.q_scale)
+                   : make_float2(0.f, 0.f);
+          acc[h][kk * EP2 + j2] = make_float2(0.f, 0.f);
         }
       }
     }
@@ -281,30 +337,36 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
     }
     if (__any_sync(0xffffffffu, aborted)) break;
     const bool ok = stage_ok[slot] != 0;
-    const int base_slot = (pg0 + k) * BS + warp * TPW;  // slot index of this warp's row 0
+    // rows t < lim of this warp's TPW rows hold attended slots
+    const int lim = ok ? L - (pg0 + k) * BS - warp * TPW : 0;
     const uint8_t* Kp = sK + slot * Ly::PAGE;
     const uint8_t* Vp = sV + slot * Ly::PAGE;
 
-    // ---- 1. logits of this warp's 8 rows for the GT heads
+    // ---- 1. logits of this warp's rows for the GT heads (fp32 pair FMAs)
 #pragma unroll
     for (int sg = 0; sg < Ly::NST / Ly::SG; ++sg) {
       float part[Ly::NV];
+      {
+        float2 part2[Ly::NV];
 #pragma unroll
-      for (int i = 0; i < Ly::NV; ++i) part[i] = 0.f;
+        for (int i = 0; i < Ly::NV; ++i) part2[i] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int stl = 0; stl < Ly::SG; ++stl) {
-        const int row = warp * TPW + (sg * Ly::SG + stl) * RPW + rg;
-        const uint8_t* kr = Kp + row * Ly::ROWB;
+        for (int stl = 0; stl < Ly::SG; ++stl) {
+          const int row = warp * TPW + (sg * Ly::SG + stl) * RPW + rg;
+          const uint8_t* kr = Kp + row * Ly::ROWB;
 #pragma unroll
-        for (int kk = 0; kk < NPL; ++kk) {
-          float kf[EPP];
-          load_piece<CT, Ly::PB>(kr + (kk * LPR + c) * Ly::PB, kf);
+          for (int kk = 0; kk < NPL; ++kk) {
+            float2 kf[EP2];
+            load_piece2<CT, Ly::PB>(kr + (kk * LPR + c) * Ly::PB, kf);
 #pragma unroll
-          for (int h = 0; h < GT; ++h)
+            for (int h = 0; h < GT; ++h)
 #pragma unroll
-            for (int jj = 0; jj < EPP; ++jj)
-              part[stl * GT + h] = fmaf(qf[h][kk * EPP + jj], kf[jj], part[stl * GT + h]);
+              for (int j2 = 0; j2 < EP2; ++j2)
+                part2[stl * GT + h] = __ffma2_rn(qf[h][kk * EP2 + j2], kf[j2], part2[stl * GT + h]);
+          }
         }
+#pragma unroll
+        for (int i = 0; i < Ly::NV; ++i) part[i] = part2[i].x + part2[i].y;
       }
       TransposeReduce<Ly::NV, LPR / 2>::run(part, lane);
       constexpr int RED = (Ly::NV < LPR) ? (LPR / Ly::NV) : 1;  // redundant copies
@@ -325,7 +387,7 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
 #pragma unroll
     for (int i = 0; i < TPL; ++i) {
       const int t = j_l + i * JN;
-      const bool valid = ok && j_l < JR && t < TPW && base_slot + t < L;
+      const bool valid = j_l < JR && t < TPW && t < lim;
       sv[i] = valid ? wscr[t * GT + h_l] : -INFINITY;
       tmax = fmaxf(tmax, sv[i]);
     }
@@ -359,40 +421,31 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
     if (j_l == 0) wscr[TPW * GT + h_l] = alpha;
     __syncwarp();
 
-    // ---- 3. rescale and accumulate P.V
+    // ---- 3. rescale and accumulate P.V (fp32 pair FMAs)
     {
       float al[GT];
+      load_row<GT>(wscr + TPW * GT, al);
       bool rescale = false;
 #pragma unroll
-      for (int h = 0; h < GT; ++h) {
-        al[h] = wscr[TPW * GT + h];
-        rescale |= al[h] != 1.f;
-      }
+      for (int h = 0; h < GT; ++h) rescale |= al[h] != 1.f;
       if (rescale) {
 #pragma unroll
         for (int h = 0; h < GT; ++h)
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[h][e] *= al[h];
+          for (int e = 0; e < EL2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], make_float2(al[h], al[h]));
       }
     }
+    if (lim >= TPW) {  // every row of this warp is attended: no per-row test
 #pragma unroll
-    for (int st = 0; st < Ly::NST; ++st) {
-      const int t = st * RPW + rg;
-      if (ok && base_slot + t < L) {
-        float pw[GT];
+      for (int st = 0; st < Ly::NST; ++st) {
+        const int t = st * RPW + rg;
+        pv_row<CT, Ly>(wscr + t * GT, Vp + (warp * TPW + t) * Ly::ROWB, c, acc);
+      }
+    } else {
 #pragma unroll
-        for (int h = 0; h < GT; ++h) pw[h] = wscr[t * GT + h];
-        const uint8_t* vr = Vp + (warp * TPW + t) * Ly::ROWB;
-#pragma unroll
-        for (int kk = 0; kk < NPL; ++kk) {
-          float vf[EPP];
-          load_piece<CT, Ly::PB>(vr + (kk * LPR + c) * Ly::PB, vf);
-#pragma unroll
-          for (int h = 0; h < GT; ++h)
-#pragma unroll
-            for (int jj = 0; jj < EPP; ++jj)
-              acc[h][kk * EPP + jj] = fmaf(pw[h], vf[jj], acc[h][kk * EPP + jj]);
-        }
+      for (int st = 0; st < Ly::NST; ++st) {
+        const int t = st * RPW + rg;
+        if (t < lim) pv_row<CT, Ly>(wscr + t * GT, Vp + (warp * TPW + t) * Ly::ROWB, c, acc);
       }
     }
     __syncwarp();
@@ -405,7 +458,10 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
 #pragma unroll
     for (int h = 0; h < GT; ++h)
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], off);
+      for (int e = 0; e < EL2; ++e) {
+        acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, off);
+        acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, off);
+      }
 
   named_bar_sync(1, NC * 32);  // every consumer is done with the stages
   float* mm = reinterpret_cast<float*>(smem);   // [NC][GT] running max
@@ -421,8 +477,10 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
 #pragma unroll
       for (int kk = 0; kk < NPL; ++kk)
 #pragma unroll
-        for (int jj = 0; jj < EPP; ++jj)
-          ma[(warp * GT + h) * D + (kk * LPR + c) * EPP + jj] = aborted ? 0.f : acc[h][kk * EPP + jj];
+        for (int j2 = 0; j2 < EP2; ++j2) {
+          const float2 a = aborted ? make_float2(0.f, 0.f) : acc[h][kk * EP2 + j2];
+          *reinterpret_cast<float2*>(&ma[(warp * GT + h) * D + (kk * LPR + c) * EPP + 2 * j2]) = a;
+        }
   }
   named_bar_sync(1, NC * 32);
 
@@ -473,8 +531,7 @@ cudaError_t launch_decode(const DecodeParams& prm, int num_seqs, cudaStream_t st
     if (dev < 32) __atomic_fetch_or(&configured_devices, 1 << dev, __ATOMIC_RELEASE);
   }
   dim3 grid(prm.num_splits, prm.num_kv_heads, num_seqs);
-  kern<<<grid, Ly::THREADS, Ly::SMEM, stream>>>(prm);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(Ly::THREADS), Ly::SMEM, stream, prm);
 }
 
 // Dispatch over (head_dim, group bucket, block size) for one (QT, CT) pair.

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/pa.h"
 
 namespace pa {
@@ -82,6 +84,16 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
           smem_u32(smem_dst)),
       "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Programmatic dependent launch. pdl_wait() blocks until the grids this one
+// depends on have completed and their writes are visible (a no-op when the
+// launch had no programmatic dependency); every kernel calls it before its
+// first global-memory access. pdl_trigger() lets the next grid in the stream
+// be scheduled early (its CTAs then wait in their own pdl_wait()).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Named barrier over a subset of warps (id 0 is __syncthreads).
@@ -192,6 +204,57 @@ __device__ __forceinline__ void load_piece(const uint8_t* p, float* out) {
   }
 }
 
+// Load PB bytes (one "piece") from shared memory and widen its PB/bytes(CT)
+// elements into PB/(2*bytes(CT)) float2 pairs (consecutive elements).
+// PB in {2, 4, 8, 16} and PB >= 2*bytes(CT); the address is PB-aligned.
+template <typename CT>
+__device__ __forceinline__ void widen_word2(uint32_t w, float2* out);
+template <>
+__device__ __forceinline__ void widen_word2<__nv_bfloat16>(uint32_t w, float2* out) {
+  out[0] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+template <>
+__device__ __forceinline__ void widen_word2<__half>(uint32_t w, float2* out) {
+  out[0] = __half22float2(*reinterpret_cast<__half2*>(&w));
+}
+template <>
+__device__ __forceinline__ void widen_word2<E4M3>(uint32_t w, float2* out) {
+  out[0] = e4m3x2_to_float2(static_cast<uint16_t>(w & 0xFFFFu));
+  out[1] = e4m3x2_to_float2(static_cast<uint16_t>(w >> 16));
+}
+
+template <typename CT, int PB>
+__device__ __forceinline__ void load_piece2(const uint8_t* p, float2* out) {
+  constexpr int EB = Elem<CT>::bytes;
+  static_assert(PB >= 2 * EB, "a piece must hold whole pairs");
+  if constexpr (EB == 4) {  // float: pairs are already laid out
+    if constexpr (PB == 16) {
+      const float4 v = *reinterpret_cast<const float4*>(p);
+      out[0] = make_float2(v.x, v.y);
+      out[1] = make_float2(v.z, v.w);
+    } else {
+      out[0] = *reinterpret_cast<const float2*>(p);
+    }
+  } else {
+    constexpr int P2W = 4 / (2 * EB);  // pairs per 32-bit word
+    if constexpr (PB == 16) {
+      const uint4 v = *reinterpret_cast<const uint4*>(p);
+      widen_word2<CT>(v.x, out);
+      widen_word2<CT>(v.y, out + P2W);
+      widen_word2<CT>(v.z, out + 2 * P2W);
+      widen_word2<CT>(v.w, out + 3 * P2W);
+    } else if constexpr (PB == 8) {
+      const uint2 v = *reinterpret_cast<const uint2*>(p);
+      widen_word2<CT>(v.x, out);
+      widen_word2<CT>(v.y, out + P2W);
+    } else if constexpr (PB == 4) {
+      widen_word2<CT>(*reinterpret_cast<const uint32_t*>(p), out);
+    } else {  // PB == 2: two E4M3 codes
+      out[0] = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(p));
+    }
+  }
+}
+
 // ---------------------------------------------------------------- FP8 encode
 // E4M3 code of x (round to nearest even, finite saturation at +-448; NaN keeps
 // its sign as 0x7F | sign).
@@ -202,6 +265,24 @@ __device__ __forceinline__ uint32_t e4m3x2_from_float2(float lo, float hi) {
   if (isnan(lo)) out = (out & 0xFF00u) | 0x7Fu | (__float_as_uint(lo) >> 24 & 0x80u);
   if (isnan(hi)) out = (out & 0x00FFu) | ((0x7Fu | (__float_as_uint(hi) >> 24 & 0x80u)) << 8);
   return out;
+}
+
+// Launch `kern` on `stream` with a programmatic dependency on the previous
+// work in the stream (see pdl_wait / pdl_trigger).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 }  // namespace pa
