@@ -54,6 +54,7 @@ struct DecodeParams {
 };
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
+constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 // Lanes per row: the fewest (>= 4) that keep q and acc at <= 32 fp32 each with
@@ -87,11 +88,23 @@ struct Layout {
   static constexpr int EL2 = EPL / 2;      // fp32 pairs per lane
   static constexpr int RPW = 32 / LPR;     // rows a warp covers per step
   static constexpr int NST = TPW / RPW;    // steps per page
-  static constexpr int SG = cmin(NST, cmax(1, 16 / GT));  // steps per reduction group
+  // pages a consumer warp takes per iteration (one softmax round per R pages)
+  static constexpr int R = (2 * PAGE <= 16384) ? 2 : 1;
+  static constexpr int TPI = TPW * R;      // rows per warp per iteration
+  static constexpr int NSTI = NST * R;     // steps per iteration
+  static constexpr int SG = cmin(NSTI, cmax(1, 16 / GT));  // steps per reduction group
   static constexpr int NV = SG * GT;       // partial dot products per group
-  static constexpr int NFIN = cmax(NV / LPR, 1);
-  static constexpr int STAGES = cmax(2, cmin(8, 65536 / (2 * PAGE)));
-  static constexpr int SCR = (TPW * GT + GT + 3) / 4 * 4;  // per-warp scratch floats
+  static constexpr int NFIN = cmax(NV / LPR, 1);   // reduced values a lane holds
+  static constexpr int RED = NV < LPR ? LPR / NV : 1;  // lanes holding the same value
+  static constexpr int NG = NSTI / SG;               // reduction groups per iteration
+  // After the reduction lane c (of a row) holds value index (c*NV)/LPR + kk,
+  // head = index % GT. Lane bits [HB0, HB0 + NHB) of c select the head;
+  // the other lane bits only select tokens (or redundant copies).
+  static constexpr int HB0 = NV >= LPR ? 0 : ilog2(RED);
+  static constexpr int NHB = NV >= LPR ? ilog2(cmax(GT / NFIN, 1)) : ilog2(GT);
+  static constexpr int HEAD_MASK = ((1 << NHB) - 1) << HB0;
+  static constexpr int STAGES = cmax(2 * R, cmin(8, 65536 / (2 * PAGE)));
+  static constexpr int SCR = (TPI * GT + GT + 3) / 4 * 4;  // per-warp scratch floats
   // dynamic shared memory layout
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = STAGES * PAGE;
@@ -100,9 +113,10 @@ struct Layout {
   static constexpr int OFF_SCR = (OFF_OK + STAGES * 4 + 15) / 16 * 16;
   static constexpr int SMEM = OFF_SCR + NC * SCR * 4;
   // end-of-split merge area (reuses the K/V stages)
-  static constexpr int MERGE = NC * GT * (D + 2) * 4;
+  static constexpr int MERGE = NC * GT * (D + 3) * 4;
   static_assert(NST >= 1, "lanes per row too small for 8 rows per warp");
-  static_assert(NST % SG == 0, "reduction groups must tile the steps");
+  static_assert(NSTI % SG == 0, "reduction groups must tile the steps");
+  static_assert(STAGES >= R, "a consumer iteration holds R stages");
   static_assert(EPL * LPR == D && NPL * EPP == EPL, "row split");
   static_assert(EPP % 2 == 0, "pieces hold whole fp32 pairs");
   static_assert(MERGE <= 2 * STAGES * PAGE, "merge area");
@@ -321,39 +335,65 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
     }
   }
 
-  // softmax state of head h_l = lane % GT (identical in lanes of one head)
-  const int h_l = lane % GT, j_l = lane / GT;
-  constexpr int JN = 32 / GT;               // lanes per head
-  constexpr int JR = JN < TPW ? JN : TPW;   // of those, lanes holding tokens
-  constexpr int TPL = (TPW + JN - 1) / JN;  // tokens per lane
-  float m_run = -INFINITY, l_run = 0.f;
+  // Online softmax with a lazy running max (log2 units). For the reduced
+  // values it holds (index kk: head hd[kk]) a lane keeps the running max m of
+  // that head, its own share of the running sum l and the largest logit seen.
+  // Weights are 2^(s - m); m only moves (and acc/l are rescaled) when a logit
+  // exceeds it by more than kLazy, so the weights stay <= 2^kLazy.
+  constexpr float kLazy = 8.f;
+  constexpr int NFIN = Ly::NFIN, RED = Ly::RED, NG = Ly::NG, NV = Ly::NV;
+  constexpr int TPI = Ly::TPI, R = Ly::R;
+  const bool writer = (c % RED) == 0;  // one lane per distinct reduced value
+  int hd[NFIN];
+#pragma unroll
+  for (int kk = 0; kk < NFIN; ++kk) hd[kk] = ((c * NV) / LPR + kk) % GT;
+  float m_run[NFIN], l_run[NFIN], s_top[NFIN];
+#pragma unroll
+  for (int kk = 0; kk < NFIN; ++kk) {
+    m_run[kk] = -INFINITY;
+    l_run[kk] = 0.f;
+    s_top[kk] = -INFINITY;
+  }
 
   bool aborted = false;
-  for (int k = 0; k < npg; ++k) {
-    const int slot = k % STAGES;
-    if (!mbar_wait_bounded(&full[slot], (k / STAGES) & 1)) {
-      raise_error(p.err, PA_DEVERR_TIMEOUT);
-      aborted = true;
+  for (int k0 = 0; k0 < npg; k0 += R) {
+    // this iteration's R pages; token t of the warp's TPI rows is row
+    // warp*TPW + t%TPW of page k0 + t/TPW
+    const uint8_t* Kp[R];
+    const uint8_t* Vp[R];
+    int lim[R];  // rows t%TPW < lim[r] of page r hold attended slots
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int k = k0 + r;
+      const int slot = (k < npg ? k : k0) % STAGES;
+      Kp[r] = sK + slot * Ly::PAGE;
+      Vp[r] = sV + slot * Ly::PAGE;
+      lim[r] = 0;
+      if (k < npg) {
+        if (!mbar_wait_bounded(&full[slot], (k / STAGES) & 1)) {
+          raise_error(p.err, PA_DEVERR_TIMEOUT);
+          aborted = true;
+        }
+        if (stage_ok[slot] != 0) lim[r] = L - (pg0 + k) * BS - warp * TPW;
+      }
     }
     if (__any_sync(0xffffffffu, aborted)) break;
-    const bool ok = stage_ok[slot] != 0;
-    // rows t < lim of this warp's TPW rows hold attended slots
-    const int lim = ok ? L - (pg0 + k) * BS - warp * TPW : 0;
-    const uint8_t* Kp = sK + slot * Ly::PAGE;
-    const uint8_t* Vp = sV + slot * Ly::PAGE;
 
-    // ---- 1. logits of this warp's rows for the GT heads (fp32 pair FMAs)
+    // ---- 1. logits of this warp's rows for the GT heads (fp32 pair FMAs),
+    //         reduced across the row's lanes; invalid rows become -inf
+    float sl[NG][NFIN];
 #pragma unroll
-    for (int sg = 0; sg < Ly::NST / Ly::SG; ++sg) {
-      float part[Ly::NV];
+    for (int sg = 0; sg < NG; ++sg) {
+      float part[NV];
       {
-        float2 part2[Ly::NV];
+        float2 part2[NV];
 #pragma unroll
-        for (int i = 0; i < Ly::NV; ++i) part2[i] = make_float2(0.f, 0.f);
+        for (int i = 0; i < NV; ++i) part2[i] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int stl = 0; stl < Ly::SG; ++stl) {
-          const int row = warp * TPW + (sg * Ly::SG + stl) * RPW + rg;
-          const uint8_t* kr = Kp + row * Ly::ROWB;
+          const int st = sg * Ly::SG + stl;
+          const int row = warp * TPW + (st % Ly::NST) * RPW + rg;
+          const uint8_t* kr = Kp[st / Ly::NST] + row * Ly::ROWB;
 #pragma unroll
           for (int kk = 0; kk < NPL; ++kk) {
             float2 kf[EP2];
@@ -366,93 +406,117 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
           }
         }
 #pragma unroll
-        for (int i = 0; i < Ly::NV; ++i) part[i] = part2[i].x + part2[i].y;
+        for (int i = 0; i < NV; ++i) part[i] = part2[i].x + part2[i].y;
       }
-      TransposeReduce<Ly::NV, LPR / 2>::run(part, lane);
-      constexpr int RED = (Ly::NV < LPR) ? (LPR / Ly::NV) : 1;  // redundant copies
-      if (c % RED == 0) {
+      TransposeReduce<NV, LPR / 2>::run(part, lane);
 #pragma unroll
-        for (int kk = 0; kk < Ly::NFIN; ++kk) {
-          const int idx = (c * Ly::NV) / LPR + kk;
+      for (int kk = 0; kk < NFIN; ++kk) {
+        const int t = (sg * Ly::SG + ((c * NV) / LPR + kk) / GT) * RPW + rg;
+        int lim_t = lim[0];  // lim of token t's page, without dynamic indexing
+#pragma unroll
+        for (int r = 1; r < R; ++r) lim_t = t >= r * TPW ? lim[r] : lim_t;
+        sl[sg][kk] = (writer && (t % TPW) < lim_t) ? part[kk] : -INFINITY;
+      }
+    }
+
+    // ---- 2. lazy max: move m only when a logit clears it by kLazy
+    bool raise = false;
+#pragma unroll
+    for (int kk = 0; kk < NFIN; ++kk) {
+      float top = sl[0][kk];
+#pragma unroll
+      for (int sg = 1; sg < NG; ++sg) top = fmaxf(top, sl[sg][kk]);
+      s_top[kk] = fmaxf(s_top[kk], top);
+      raise |= top > m_run[kk] + kLazy;
+    }
+    if (__any_sync(0xffffffffu, raise)) {
+      float alpha[NFIN];
+#pragma unroll
+      for (int kk = 0; kk < NFIN; ++kk) {
+        float top = sl[0][kk];
+#pragma unroll
+        for (int sg = 1; sg < NG; ++sg) top = fmaxf(top, sl[sg][kk]);
+#pragma unroll
+        for (int off = 1; off < 32; off *= 2)  // over every lane bit but the head bits
+          if ((off & Ly::HEAD_MASK) == 0) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, off));
+        const float m_new = fmaxf(m_run[kk], top);
+        alpha[kk] = m_new == -INFINITY ? 1.f : exp2f(m_run[kk] - m_new);
+        m_run[kk] = m_new;
+        l_run[kk] *= alpha[kk];
+      }
+      float al[GT];  // every head's factor, from a lane that holds that head
+#pragma unroll
+      for (int h = 0; h < GT; ++h)
+        al[h] = __shfl_sync(0xffffffffu, alpha[h % NFIN], Ly::NV >= LPR ? h / NFIN : h * RED);
+#pragma unroll
+      for (int h = 0; h < GT; ++h)
+#pragma unroll
+        for (int e = 0; e < EL2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], make_float2(al[h], al[h]));
+    }
+
+    // ---- 3. weights 2^(s - m) to shared memory, then P.V (fp32 pair FMAs)
+#pragma unroll
+    for (int sg = 0; sg < NG; ++sg)
+#pragma unroll
+      for (int kk = 0; kk < NFIN; ++kk) {
+        const float pw = sl[sg][kk] == -INFINITY ? 0.f : exp2f(sl[sg][kk] - m_run[kk]);
+        l_run[kk] += pw;
+        if (writer) {
+          const int idx = (c * NV) / LPR + kk;
           const int t = (sg * Ly::SG + idx / GT) * RPW + rg;
-          wscr[t * GT + idx % GT] = part[kk];
+          wscr[t * GT + idx % GT] = pw;
+        }
+      }
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (lim[r] >= TPW) {  // every row of this warp in page r is attended
+#pragma unroll
+        for (int st = 0; st < Ly::NST; ++st) {
+          const int tr = st * RPW + rg;
+          pv_row<CT, Ly>(wscr + (r * TPW + tr) * GT, Vp[r] + (warp * TPW + tr) * Ly::ROWB, c, acc);
+        }
+      } else if (lim[r] > 0) {
+#pragma unroll
+        for (int st = 0; st < Ly::NST; ++st) {
+          const int tr = st * RPW + rg;
+          if (tr < lim[r])
+            pv_row<CT, Ly>(wscr + (r * TPW + tr) * GT, Vp[r] + (warp * TPW + tr) * Ly::ROWB, c,
+                           acc);
         }
       }
     }
     __syncwarp();
-
-    // ---- 2. online softmax over the warp's rows, per head (log2 units)
-    float sv[TPL];
-    float tmax = -INFINITY;
+    if (lane == 0) {
 #pragma unroll
-    for (int i = 0; i < TPL; ++i) {
-      const int t = j_l + i * JN;
-      const bool valid = j_l < JR && t < TPW && t < lim;
-      sv[i] = valid ? wscr[t * GT + h_l] : -INFINITY;
-      tmax = fmaxf(tmax, sv[i]);
+      for (int r = 0; r < R; ++r)
+        if (k0 + r < npg) mbar_arrive(&empty[(k0 + r) % STAGES]);
     }
-#pragma unroll
-    for (int off = GT; off < GT * JR; off *= 2)
-      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-    const float m_new = fmaxf(m_run, tmax);
-    float alpha = 1.f, psum = 0.f;
-    float pv[TPL];
-    if (m_new == -INFINITY) {
-#pragma unroll
-      for (int i = 0; i < TPL; ++i) pv[i] = 0.f;
-    } else {
-      alpha = exp2f(m_run - m_new);
-#pragma unroll
-      for (int i = 0; i < TPL; ++i) {
-        pv[i] = exp2f(sv[i] - m_new);
-        psum += pv[i];
-      }
-    }
-#pragma unroll
-    for (int off = GT; off < GT * JR; off *= 2) psum += __shfl_xor_sync(0xffffffffu, psum, off);
-    l_run = l_run * alpha + psum;
-    m_run = m_new;
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < TPL; ++i) {
-      const int t = j_l + i * JN;
-      if (j_l < JR && t < TPW) wscr[t * GT + h_l] = pv[i];
-    }
-    if (j_l == 0) wscr[TPW * GT + h_l] = alpha;
-    __syncwarp();
-
-    // ---- 3. rescale and accumulate P.V (fp32 pair FMAs)
-    {
-      float al[GT];
-      load_row<GT>(wscr + TPW * GT, al);
-      bool rescale = false;
-#pragma unroll
-      for (int h = 0; h < GT; ++h) rescale |= al[h] != 1.f;
-      if (rescale) {
-#pragma unroll
-        for (int h = 0; h < GT; ++h)
-#pragma unroll
-          for (int e = 0; e < EL2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], make_float2(al[h], al[h]));
-      }
-    }
-    if (lim >= TPW) {  // every row of this warp is attended: no per-row test
-#pragma unroll
-      for (int st = 0; st < Ly::NST; ++st) {
-        const int t = st * RPW + rg;
-        pv_row<CT, Ly>(wscr + t * GT, Vp + (warp * TPW + t) * Ly::ROWB, c, acc);
-      }
-    } else {
-#pragma unroll
-      for (int st = 0; st < Ly::NST; ++st) {
-        const int t = st * RPW + rg;
-        if (t < lim) pv_row<CT, Ly>(wscr + t * GT, Vp + (warp * TPW + t) * Ly::ROWB, c, acc);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
   }
 
-  // ---- merge the row groups of the warp, then the NC warps
+  // ---- per-head (m, l, top) of this warp, then merge row groups and warps
+  float mh[GT], lh[GT], th[GT];
+  {
+    float lsum[NFIN], tmax[NFIN];
+#pragma unroll
+    for (int kk = 0; kk < NFIN; ++kk) {
+      lsum[kk] = l_run[kk];
+      tmax[kk] = s_top[kk];
+#pragma unroll
+      for (int off = 1; off < 32; off *= 2)
+        if ((off & Ly::HEAD_MASK) == 0) {
+          lsum[kk] += __shfl_xor_sync(0xffffffffu, lsum[kk], off);
+          tmax[kk] = fmaxf(tmax[kk], __shfl_xor_sync(0xffffffffu, tmax[kk], off));
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < GT; ++h) {
+      const int src = Ly::NV >= LPR ? h / NFIN : h * RED;
+      mh[h] = __shfl_sync(0xffffffffu, m_run[h % NFIN], src);
+      lh[h] = __shfl_sync(0xffffffffu, lsum[h % NFIN], src);
+      th[h] = __shfl_sync(0xffffffffu, tmax[h % NFIN], src);
+    }
+  }
 #pragma unroll
   for (int off = LPR; off < 32; off *= 2)
 #pragma unroll
@@ -465,11 +529,13 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
 
   named_bar_sync(1, NC * 32);  // every consumer is done with the stages
   float* mm = reinterpret_cast<float*>(smem);   // [NC][GT] running max
-  float* ml = mm + NC * GT;                     // [NC][GT] running sum
-  float* ma = ml + NC * GT;                     // [NC][GT][D] accumulators
-  if (j_l == 0) {
-    mm[warp * GT + h_l] = aborted ? -INFINITY : m_run;
-    ml[warp * GT + h_l] = aborted ? 0.f : l_run;
+  float* ml = mm + NC * GT;                     // [NC][GT] running sum (relative to mm)
+  float* mt = ml + NC * GT;                     // [NC][GT] largest logit
+  float* ma = mt + NC * GT;                     // [NC][GT][D] accumulators
+  if (lane < GT) {
+    mm[warp * GT + lane] = aborted ? -INFINITY : mh[lane];
+    ml[warp * GT + lane] = aborted ? 0.f : lh[lane];
+    mt[warp * GT + lane] = aborted ? -INFINITY : th[lane];
   }
   if (rg == 0) {
 #pragma unroll
@@ -486,9 +552,12 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
 
   for (int i = threadIdx.x; i < G * D; i += NC * 32) {
     const int h = i / D, d = i % D;
-    float M = -INFINITY;
+    float M = -INFINITY, T = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NC; ++w) M = fmaxf(M, mm[w * GT + h]);
+    for (int w = 0; w < NC; ++w) {
+      M = fmaxf(M, mm[w * GT + h]);
+      T = fmaxf(T, mt[w * GT + h]);
+    }
     float o = 0.f, lsum = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
@@ -505,10 +574,12 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
     const size_t row = (size_t)s * Hq + (size_t)g * G + h;
     if (p.partials) {
       const size_t pi = row * p.num_splits + split;
-      if (M != -INFINITY) p.tmp_out[pi * D + d] = o;
+      const bool any = M != -INFINITY && lsum > 0.f;
+      if (any) p.tmp_out[pi * D + d] = o;
       if (d == 0) {
-        p.max_logits[pi] = M == -INFINITY ? -INFINITY : M * kLn2;
-        p.exp_sums[pi] = M == -INFINITY ? 0.f : lsum;
+        // report the split's largest logit and the sum relative to it
+        p.max_logits[pi] = any ? T * kLn2 : -INFINITY;
+        p.exp_sums[pi] = any ? lsum * exp2f(M - T) : 0.f;
       }
     } else {
       reinterpret_cast<QT*>(p.out)[row * D + d] = Elem<QT>::from_f32(o);
