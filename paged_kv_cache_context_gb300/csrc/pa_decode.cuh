@@ -53,6 +53,18 @@ struct DecodeParams {
   float v_scale;  // FP8: v_scale, else 1
 };
 
+// Shared-memory budget for one CTA's K/V stages, and the most pages a
+// consumer warp takes per iteration (build-time tunables).
+#ifndef PA_STAGE_BYTES
+#define PA_STAGE_BYTES 65536
+#endif
+#ifndef PA_PAGES_PER_ITER
+#define PA_PAGES_PER_ITER 2
+#endif
+#ifndef PA_MAX_STAGES
+#define PA_MAX_STAGES 8
+#endif
+
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
@@ -89,7 +101,7 @@ struct Layout {
   static constexpr int RPW = 32 / LPR;     // rows a warp covers per step
   static constexpr int NST = TPW / RPW;    // steps per page
   // pages a consumer warp takes per iteration (one softmax round per R pages)
-  static constexpr int R = (2 * PAGE <= 16384) ? 2 : 1;
+  static constexpr int R = (2 * PAGE <= 16384) ? PA_PAGES_PER_ITER : 1;
   static constexpr int TPI = TPW * R;      // rows per warp per iteration
   static constexpr int NSTI = NST * R;     // steps per iteration
   static constexpr int SG = cmin(NSTI, cmax(1, 16 / GT));  // steps per reduction group
@@ -103,7 +115,7 @@ struct Layout {
   static constexpr int HB0 = NV >= LPR ? 0 : ilog2(RED);
   static constexpr int NHB = NV >= LPR ? ilog2(cmax(GT / NFIN, 1)) : ilog2(GT);
   static constexpr int HEAD_MASK = ((1 << NHB) - 1) << HB0;
-  static constexpr int STAGES = cmax(2 * R, cmin(8, 65536 / (2 * PAGE)));
+  static constexpr int STAGES = cmax(2 * R, cmin(PA_MAX_STAGES, PA_STAGE_BYTES / (2 * PAGE)));
   static constexpr int SCR = (TPI * GT + GT + 3) / 4 * 4;  // per-warp scratch floats
   // dynamic shared memory layout
   static constexpr int OFF_K = 0;
