@@ -2,9 +2,10 @@
 """Benchmark: paged decode attention on GB300, one JSON line on stdout.
 
 A step is one pass of the whole decode hot path over one batch: the cache
-write of every sequence's new token (pa_reshape_and_cache), the split decode
-(pa_decode_partials) and the log-sum-exp reduction (pa_reduce) -- exactly the
-kernels pa_decode runs for its split plan. Default workload: the
+write of every sequence's new token (pa_reshape_and_cache), then the two
+launches of pa_decode's balanced path: the persistent decode
+(pa_decode_balanced) and the combine of contexts cut between CTAs
+(pa_decode_combine). Default workload: the
 Mistral-7B-shaped bf16 batch (32 sequences, 32 query / 8 kv heads, head_dim
 128, block_size 32, context lengths U[512, 4096], shuffled block pool).
 
@@ -14,7 +15,7 @@ value  = algorithmic bytes of a step (K/V of the attended tokens, q, output,
 e2e    = the same metric through pa_decode with host buffers: per step the
          query, new K/V rows, slot mapping, lengths and tables are copied from
          pinned host memory, and the output is copied back.
-roofline = the split-decode kernel alone (CUDA events around each launch).
+roofline = the persistent decode kernel alone (CUDA events around each launch).
 
 L2: the K/V caches are replicated 4 times (each replica larger than the
 129 MB L2) and consecutive steps use different replicas.
@@ -237,48 +238,45 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.synchronize()
     reps = [(kc, vc)] + [(kc.clone(), vc.clone()) for _ in range(args.replicas - 1)]
 
-    ns, pps = pa.decode_plan(S, Hq, Hkv, D, bs, MB, case.window)
     qd = pa._DTYPE[case.q_dtype]
     kvd = pa._KV[case.kv_dtype]
     out = torch.empty(S, Hq, D, dtype=case.q_dtype, device=dev)
-    tmp = torch.empty(S, Hq, max(ns, 1), D, dtype=torch.float32, device=dev)
-    ml = torch.empty(S, Hq, max(ns, 1), dtype=torch.float32, device=dev)
-    es = torch.empty_like(ml)
+    ws_bytes = pa.decode_workspace_size(S, Hq, Hkv, D, bs, MB, case.window)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    num_ctas = ctypes.c_int(0)
 
     # pre-bound C calls (marshalling once, outside the timed loop)
-    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     def ptr(t):
         return P(t.data_ptr())
-    write_args, split_args = [], []
+    write_args, dec_args = [], []
     for (k_, v_) in reps:
         write_args.append((ptr(new_k), ptr(new_v), ptr(k_), ptr(v_), ptr(new_sm), I(S), I(Hkv),
                            I(D), I(bs), I(NB), I(pa._DTYPE[new_k.dtype]), I(kvd),
                            F(case.k_scale), F(case.v_scale), sp))
-        if ns > 1:
-            split_args.append((ptr(tmp), ptr(ml), ptr(es), ptr(q), ptr(k_), ptr(v_), ptr(bt),
-                               ptr(cl), I(S), I(Hq), I(Hkv), I(D), I(bs), I(NB), I(MB),
-                               F(case.scale), I(case.window), I(qd), I(kvd), F(case.k_scale),
-                               F(case.v_scale), I(ns), I(pps), sp))
-        else:
-            split_args.append((ptr(out), ptr(q), ptr(k_), ptr(v_), ptr(bt), ptr(cl), I(S), I(Hq),
-                               I(Hkv), I(D), I(bs), I(NB), I(MB), F(case.scale), I(case.window),
-                               I(qd), I(kvd), F(case.k_scale), F(case.v_scale), None,
-                               ctypes.c_size_t(0), sp))
-    reduce_args = (ptr(out), ptr(tmp), ptr(ml), ptr(es), I(S), I(Hq), I(D), I(ns), I(qd), sp)
-    f_write, f_red = L.pa_reshape_and_cache, L.pa_reduce
-    f_split = L.pa_decode_partials if ns > 1 else L.pa_decode
-    launches_per_step = 3 if ns > 1 else 2
+        dec_args.append((ptr(out), ptr(q), ptr(k_), ptr(v_), ptr(bt), ptr(cl), I(S), I(Hq),
+                         I(Hkv), I(D), I(bs), I(NB), I(MB), F(case.scale), I(case.window), I(qd),
+                         I(kvd), F(case.k_scale), F(case.v_scale), ptr(ws), Z(ws_bytes),
+                         P(ctypes.addressof(num_ctas)), sp))
+    f_write, f_dec, f_comb = L.pa_reshape_and_cache, L.pa_decode_balanced, L.pa_decode_combine
+    # the decode grid size is fixed for these sizes: learn it once
+    if f_dec(*dec_args[0]):
+        raise RuntimeError("pa_decode_balanced failed")
+    comb_args = (ptr(out), ptr(cl), I(S), I(Hq), I(Hkv), I(D), I(bs), I(MB), I(case.window),
+                 I(qd), ptr(ws), Z(ws_bytes), I(num_ctas.value), sp)
+    if f_comb(*comb_args):
+        raise RuntimeError("pa_decode_combine failed")
+    launches_per_step = 3
 
     def step(i, ev_a=None, ev_b=None):
         r = i % len(reps)
         rc = f_write(*write_args[r])
         if ev_a is not None:
             ev_a.record(stream)
-        rc |= f_split(*split_args[r])
+        rc |= f_dec(*dec_args[r])
         if ev_b is not None:
             ev_b.record(stream)
-        if ns > 1:
-            rc |= f_red(*reduce_args)
+        rc |= f_comb(*comb_args)
         if rc:
             raise RuntimeError(f"library call failed: {rc}")
 
@@ -337,7 +335,7 @@ def run_ours(args, rank, local_rank, world):
                    "window": case.window, "cache_dtype": case.kv_dtype if case.kv_dtype != "auto"
                    else str(case.q_dtype).replace("torch.", ""),
                    "storage_dtype": str(case.q_dtype).replace("torch.", ""),
-                   "num_splits": ns, "pages_per_split": pps,
+                   "decode_ctas": num_ctas.value, "workspace_bytes": ws_bytes,
                    "kv_bytes_per_step": sb["kv"], "bytes_per_step": sb["total"],
                    "l2": f"{args.replicas} rotating cache replicas of "
                          f"{kc.numel() * kc.element_size() * 2 / 1e6:.0f} MB (> L2)",
@@ -346,7 +344,7 @@ def run_ours(args, rank, local_rank, world):
         "pct_of_nominal_8tbs": round(100 * bytes_all / elapsed_max / 1e9 / NOMINAL_HBM_GBS, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": None, "kernel": "paged_decode_kernel",
+                     "traffic": None, "kernel": "paged_decode_kernel (balanced mode)",
                      "kernel_bytes_per_launch": sb["kernel"],
                      "kernel_us_mean": round(split_mean * 1e6, 2),
                      "kernel_us_median": round(statistics.median(split_ms) * 1e3, 2)},

@@ -160,12 +160,13 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
  * block_tables : in, int32 [S][MB].  context_lens : in, int32 [S].
  * window       : 0 = none; else W > 0, W % bs == 0, W / bs <= MB (ring of
  *                W / bs blocks per sequence in block_tables[s][0 .. W/bs-1]).
- * workspace    : device scratch of workspace_bytes (may be NULL / 0). The
- *                context of a sequence is split across several CTAs and the
- *                partial results are combined by a log-sum-exp reduction when
- *                the workspace holds the plan (pa_decode_workspace_size());
- *                otherwise one CTA per (sequence, kv head) does the whole
- *                context. Contents on entry do not matter; on exit undefined.
+ * workspace    : device scratch of workspace_bytes (may be NULL / 0). With
+ *                at least pa_decode_workspace_size() bytes the call runs the
+ *                balanced path (pa_decode_balanced then pa_decode_combine):
+ *                one persistent CTA per resident slot, each streaming an equal
+ *                share of all sequences' pages; otherwise one CTA per
+ *                (sequence, kv head) does that whole context. Contents on
+ *                entry do not matter; on exit undefined.
  * Supported: D in {64, 96, 128}; bs in {16, 32, 64}; G = Hq/Hkv in 1..8;
  * q_dtype F32/BF16/F16; AUTO caches hold q_dtype. Pointers 16-byte aligned.
  */
@@ -179,20 +180,58 @@ pa_status pa_decode(void* out, const void* query,
                     void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
- * pa_decode_plan -- the split plan pa_decode uses for these sizes.
+ * pa_decode_plan -- a split plan for pa_decode_partials at these sizes.
  * Writes the number of context splits per (sequence, kv head) and the pages
  * (blocks) each split covers; split i covers slots
- * [i*pages_per_split*bs, (i+1)*pages_per_split*bs). num_splits == 1 means the
- * unsplit kernel (no workspace needed). Host-only; never touches the GPU.
+ * [i*pages_per_split*bs, (i+1)*pages_per_split*bs). Sized so the splits of a
+ * batch fill a 152-SM GPU several times over. Host-only; never touches the GPU.
  */
 pa_status pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                          int block_size, int max_blocks_per_seq, int window,
                          int* num_splits, int* pages_per_split);
 
-/* Bytes of workspace pa_decode needs for its split plan (0 when unsplit). */
+/*
+ * Bytes of workspace for pa_decode's balanced path (and for
+ * pa_decode_balanced / pa_decode_combine). It depends only on the query-head
+ * group size and head_dim, not on the batch: partial results of at most two
+ * pieces per persistent CTA (about 2.6 MB for G = 4, D = 128). 0 for invalid
+ * head counts.
+ */
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                 int head_dim, int block_size,
                                 int max_blocks_per_seq, int window);
+
+/*
+ * pa_decode_balanced / pa_decode_combine -- the two launches of pa_decode's
+ * balanced path, exposed so a caller can time or interleave them.
+ *
+ * pa_decode_balanced: the pages of every (sequence, kv head) context, taken
+ * in (sequence, kv head, page) order, are cut into C equal contiguous ranges,
+ * C = the kernel's resident capacity on this device (written to *num_ctas);
+ * persistent CTA c streams range c. A context lying wholly inside one range
+ * is written to `out` by that CTA; a context cut by range boundaries leaves
+ * per-CTA partials (max logit, sum, normalised output) in the workspace.
+ * pa_decode_combine: combines those partials by log-sum-exp weights into
+ * `out`, and writes zeros for sequences with nothing to attend. It must follow
+ * pa_decode_balanced on the same stream with the same workspace, sizes and
+ * num_ctas. Arguments and errors otherwise as pa_decode (workspace required:
+ * PA_ERR_NULL when missing, PA_ERR_WORKSPACE when smaller than
+ * pa_decode_workspace_size()).
+ */
+pa_status pa_decode_balanced(void* out, const void* query,
+                             const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                             int block_size, int num_blocks, int max_blocks_per_seq,
+                             float scale, int window, pa_dtype q_dtype, pa_kv_dtype kv_dtype,
+                             float k_scale, float v_scale,
+                             void* workspace, size_t workspace_bytes, int* num_ctas,
+                             pa_stream_t stream);
+pa_status pa_decode_combine(void* out, const int32_t* context_lens,
+                            int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                            int block_size, int max_blocks_per_seq, int window,
+                            pa_dtype out_dtype, const void* workspace, size_t workspace_bytes,
+                            int num_ctas, pa_stream_t stream);
 
 /*
  * pa_decode_partials -- the split phase of pa_decode with an explicit plan.
@@ -238,16 +277,17 @@ pa_status pa_reduce(void* out, const float* tmp_out, const float* max_logits,
  * no way to hand pa_decode a workspace: code running inside a host program
  * that owns every device allocation and offers no allocator, or code that must
  * never call cudaMalloc (it can synchronise the device and take unbounded
- * time). It computes exactly what pa_decode computes, with the same kernels
- * and split plan, but keeps the split partials in an array the library itself
- * holds in device memory: PA_STATIC_SCRATCH_BYTES (8 MiB) on every GPU where
- * the library is loaded, kept until the process exits. It allocates nothing.
+ * time). It computes exactly what pa_decode computes, with the same kernels,
+ * but keeps the partial results in an array the library itself holds in
+ * device memory: PA_STATIC_SCRATCH_BYTES (8 MiB) on every GPU where the
+ * library is loaded, kept until the process exits. It allocates nothing.
  *
- *  - Limit: when the split plan for these sizes needs more partial storage than
+ *  - Limit: when these sizes need more partial storage than
  *    PA_STATIC_SCRATCH_BYTES (pa_decode_workspace_size() larger than it), the
- *    call returns PA_ERR_WORKSPACE at once and enqueues nothing. This size
- *    check comes before the argument checks of pa_decode; every other
- *    argument rule and error of pa_decode applies unchanged.
+ *    call returns PA_ERR_WORKSPACE at once and enqueues nothing. Every head
+ *    dimension and group size pa_decode supports fits. This size check comes
+ *    before the argument checks of pa_decode; every other argument rule and
+ *    error of pa_decode applies unchanged.
  *  - Set-up: the first call on a device (that device current) looks up the
  *    array's device address once (cudaGetSymbolAddress); make that first call
  *    on each device before any stream capture begins.

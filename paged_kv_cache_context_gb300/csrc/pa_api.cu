@@ -278,24 +278,65 @@ static void plan(int S, int Hkv, int MB, int bs, int window, int* ns, int* pps) 
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-static size_t partials_bytes(int S, int Hq, int D, int ns) {
-  const size_t rows = (size_t)S * Hq * ns;
-  return align256(rows * D * 4) + 2 * align256(rows * 4);
-}
 
-static cudaError_t run_decode(const DecodeParams& prm, const DecodeShape& a, cudaStream_t st) {
+static cudaError_t run_decode(const DecodeParams& prm, const DecodeShape& a, dim3 grid, int mode,
+                              int* ctas, cudaStream_t st) {
   const int GT = group_bucket(a.Hq / a.Hkv);
   if (a.kv_dtype == PA_KV_AUTO) {
     switch (a.q_dtype) {
-      case PA_F32: return pa_dispatch_decode_f32_f32(prm, a.S, a.D, GT, a.bs, st);
-      case PA_BF16: return pa_dispatch_decode_bf16_bf16(prm, a.S, a.D, GT, a.bs, st);
-      default: return pa_dispatch_decode_f16_f16(prm, a.S, a.D, GT, a.bs, st);
+      case PA_F32: return pa_dispatch_decode_f32_f32(prm, grid, a.D, GT, a.bs, mode, ctas, st);
+      case PA_BF16: return pa_dispatch_decode_bf16_bf16(prm, grid, a.D, GT, a.bs, mode, ctas, st);
+      default: return pa_dispatch_decode_f16_f16(prm, grid, a.D, GT, a.bs, mode, ctas, st);
     }
   }
   switch (a.q_dtype) {
-    case PA_F32: return pa_dispatch_decode_f32_e4m3(prm, a.S, a.D, GT, a.bs, st);
-    case PA_BF16: return pa_dispatch_decode_bf16_e4m3(prm, a.S, a.D, GT, a.bs, st);
-    default: return pa_dispatch_decode_f16_e4m3(prm, a.S, a.D, GT, a.bs, st);
+    case PA_F32: return pa_dispatch_decode_f32_e4m3(prm, grid, a.D, GT, a.bs, mode, ctas, st);
+    case PA_BF16: return pa_dispatch_decode_bf16_e4m3(prm, grid, a.D, GT, a.bs, mode, ctas, st);
+    default: return pa_dispatch_decode_f16_e4m3(prm, grid, a.D, GT, a.bs, mode, ctas, st);
+  }
+}
+
+// Balanced-mode workspace: per decode CTA two partial slots of GT rows of D
+// floats, their (max, sum) pairs and four ints of slot record.
+struct BalancedWs {
+  float* piece_o;
+  float* piece_ml;
+  int* piece_info;
+};
+static size_t balanced_bytes(int GT, int D) {
+  const size_t slots = (size_t)kMaxBalancedCtas * kPieceSlots;
+  return align256(slots * GT * D * 4) + align256(slots * GT * 2 * 4) + align256(slots * 4 * 4);
+}
+static BalancedWs balanced_carve(void* ws, int GT, int D) {
+  const size_t slots = (size_t)kMaxBalancedCtas * kPieceSlots;
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  BalancedWs w;
+  w.piece_o = reinterpret_cast<float*>(b);
+  b += align256(slots * GT * D * 4);
+  w.piece_ml = reinterpret_cast<float*>(b);
+  b += align256(slots * GT * 2 * 4);
+  w.piece_info = reinterpret_cast<int*>(b);
+  return w;
+}
+
+static cudaError_t run_combine(void* out, const BalancedWs& w, const int32_t* cl, int S, int Hq,
+                               int Hkv, int D, int GT, int bs, int MB, int window, int ctas,
+                               int dt, unsigned* err, cudaStream_t st) {
+  const dim3 grid(static_cast<unsigned>(ctas > 0 ? ctas : 1)), block(128);
+  switch (dt) {
+    case PA_F32:
+      return launch_pdl(combine_pieces_kernel<float>, grid, block, 0, st, static_cast<float*>(out),
+                        (const float*)w.piece_o, (const float*)w.piece_ml, (const int*)w.piece_info,
+                        cl, S, Hq, Hkv, D, GT, bs, MB, window, ctas, err);
+    case PA_BF16:
+      return launch_pdl(combine_pieces_kernel<__nv_bfloat16>, grid, block, 0, st,
+                        static_cast<__nv_bfloat16*>(out), (const float*)w.piece_o,
+                        (const float*)w.piece_ml, (const int*)w.piece_info, cl, S, Hq, Hkv, D, GT,
+                        bs, MB, window, ctas, err);
+    default:
+      return launch_pdl(combine_pieces_kernel<__half>, grid, block, 0, st, static_cast<__half*>(out),
+                        (const float*)w.piece_o, (const float*)w.piece_ml, (const int*)w.piece_info,
+                        cl, S, Hq, Hkv, D, GT, bs, MB, window, ctas, err);
   }
 }
 
@@ -310,6 +351,7 @@ static DecodeParams make_params(const DecodeShape& a, const void* query, const v
   p.block_tables = bt;
   p.context_lens = cl;
   p.err = err;
+  p.num_seqs = a.S;
   p.num_heads = a.Hq;
   p.num_kv_heads = a.Hkv;
   p.group = a.Hq / a.Hkv;
@@ -465,11 +507,13 @@ PA_API pa_status pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, i
 PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                        int head_dim, int block_size, int max_blocks_per_seq,
                                        int window) {
-  int ns = 1, pps = 1;
-  if (pa_decode_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                     window, &ns, &pps) != PA_OK || ns <= 1)
+  (void)num_seqs;
+  (void)block_size;
+  (void)max_blocks_per_seq;
+  (void)window;
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0)
     return 0;
-  return partials_bytes(num_seqs, num_heads, head_dim, ns);
+  return balanced_bytes(group_bucket(num_heads / num_kv_heads), head_dim);
 }
 
 PA_API pa_status pa_decode_partials(float* tmp_out, float* max_logits, float* exp_sums,
@@ -496,8 +540,11 @@ PA_API pa_status pa_decode_partials(float* tmp_out, float* max_logits, float* ex
   p.partials = 1;
   p.num_splits = num_splits;
   p.pages_per_split = pages_per_split;
-  return run_decode(p, a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
-                                                                                : PA_ERR_CUDA;
+  const dim3 grid(num_splits, num_kv_heads, num_seqs);
+  return run_decode(p, a, grid, kModeSplit, nullptr, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 
 PA_API pa_status pa_reduce(void* out, const float* tmp_out, const float* max_logits,
@@ -516,6 +563,63 @@ PA_API pa_status pa_reduce(void* out, const float* tmp_out, const float* max_log
              : PA_ERR_CUDA;
 }
 
+PA_API pa_status pa_decode_balanced(void* out, const void* query, const void* k_cache,
+                                    const void* v_cache, const int32_t* block_tables,
+                                    const int32_t* context_lens, int num_seqs, int num_heads,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, int max_blocks_per_seq, float scale,
+                                    int window, pa_dtype q_dtype, pa_kv_dtype kv_dtype,
+                                    float k_scale, float v_scale, void* workspace,
+                                    size_t workspace_bytes, int* num_ctas, pa_stream_t stream) {
+  if (num_ctas) *num_ctas = 0;
+  DecodeShape a{num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                max_blocks_per_seq, window, q_dtype, kv_dtype, k_scale, v_scale};
+  pa_status rc = check_decode(a, out, query, k_cache, v_cache, block_tables, context_lens);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  if (!workspace || !num_ctas) return PA_ERR_NULL;
+  const int GT = group_bucket(num_heads / num_kv_heads);
+  if (workspace_bytes < balanced_bytes(GT, head_dim)) return PA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return PA_ERR_ALIGN;
+  DecodeParams p = make_params(a, query, k_cache, v_cache, block_tables, context_lens, scale,
+                               error_word());
+  const BalancedWs w = balanced_carve(workspace, GT, head_dim);
+  p.out = out;
+  p.piece_o = w.piece_o;
+  p.piece_ml = w.piece_ml;
+  p.piece_info = w.piece_info;
+  p.num_splits = 1;
+  p.pages_per_split = 1;
+  int ctas = 0;
+  if (run_decode(p, a, dim3(0, 1, 1), kModeBalanced, &ctas, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return PA_ERR_CUDA;
+  *num_ctas = ctas;
+  return PA_OK;
+}
+
+PA_API pa_status pa_decode_combine(void* out, const int32_t* context_lens, int num_seqs,
+                                   int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                   int max_blocks_per_seq, int window, pa_dtype out_dtype,
+                                   const void* workspace, size_t workspace_bytes, int num_ctas,
+                                   pa_stream_t stream) {
+  if (num_seqs < 0) return PA_ERR_SHAPE;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !context_lens || !workspace) return PA_ERR_NULL;
+  if (!valid_dtype(out_dtype)) return PA_ERR_DTYPE;
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
+      num_heads / num_kv_heads > 8 || num_ctas < 1 || num_ctas > kMaxBalancedCtas)
+    return PA_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 96 && head_dim != 128) return PA_ERR_HEAD_DIM;
+  const int GT = group_bucket(num_heads / num_kv_heads);
+  if (workspace_bytes < balanced_bytes(GT, head_dim)) return PA_ERR_WORKSPACE;
+  const BalancedWs w = balanced_carve(const_cast<void*>(workspace), GT, head_dim);
+  return run_combine(out, w, context_lens, num_seqs, num_heads, num_kv_heads, head_dim, GT,
+                     block_size, max_blocks_per_seq, window, num_ctas, out_dtype, error_word(),
+                     reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
 PA_API pa_status pa_decode(void* out, const void* query, const void* k_cache,
                            const void* v_cache, const int32_t* block_tables,
                            const int32_t* context_lens, int num_seqs, int num_heads,
@@ -527,32 +631,27 @@ PA_API pa_status pa_decode(void* out, const void* query, const void* k_cache,
                 max_blocks_per_seq, window, q_dtype, kv_dtype, k_scale, v_scale};
   pa_status rc = check_decode(a, out, query, k_cache, v_cache, block_tables, context_lens);
   if (rc != PA_OK || num_seqs == 0) return rc;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int ns = 1, pps = 1;
-  plan(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, window, &ns, &pps);
-  const size_t need = ns > 1 ? partials_bytes(num_seqs, num_heads, head_dim, ns) : 0;
-  if (ns > 1 && (!workspace || workspace_bytes < need || !aligned16(workspace))) {
-    ns = 1;  // not enough scratch: one CTA per (sequence, kv head)
-    pps = max_pages(max_blocks_per_seq, block_size, window);
+  const int GT = group_bucket(num_heads / num_kv_heads);
+  if (workspace && workspace_bytes >= balanced_bytes(GT, head_dim) && aligned16(workspace)) {
+    int ctas = 0;
+    rc = pa_decode_balanced(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                            num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                            max_blocks_per_seq, scale, window, q_dtype, kv_dtype, k_scale, v_scale,
+                            workspace, workspace_bytes, &ctas, stream);
+    if (rc != PA_OK) return rc;
+    return pa_decode_combine(out, context_lens, num_seqs, num_heads, num_kv_heads, head_dim,
+                             block_size, max_blocks_per_seq, window, q_dtype, workspace,
+                             workspace_bytes, ctas, stream);
   }
+  // no usable workspace: one CTA per (sequence, kv head), straight to the output
   DecodeParams p = make_params(a, query, k_cache, v_cache, block_tables, context_lens, scale,
                                error_word());
-  p.num_splits = ns;
-  p.pages_per_split = pps;
-  if (ns == 1) {
-    p.out = out;
-    p.partials = 0;
-    return run_decode(p, a, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
-  }
-  const size_t rows = (size_t)num_seqs * num_heads * ns;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.tmp_out = reinterpret_cast<float*>(ws);
-  p.max_logits = reinterpret_cast<float*>(ws + align256(rows * head_dim * 4));
-  p.exp_sums = reinterpret_cast<float*>(ws + align256(rows * head_dim * 4) + align256(rows * 4));
-  p.partials = 1;
-  if (run_decode(p, a, st) != cudaSuccess) return PA_ERR_CUDA;
-  return run_reduce(out, p.tmp_out, p.max_logits, p.exp_sums, (int64_t)num_seqs * num_heads,
-                    head_dim, ns, q_dtype, st) == cudaSuccess
+  p.out = out;
+  p.partials = 0;
+  p.num_splits = 1;
+  p.pages_per_split = max_pages(max_blocks_per_seq, block_size, window);
+  return run_decode(p, a, dim3(1, num_kv_heads, num_seqs), kModeSplit, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }

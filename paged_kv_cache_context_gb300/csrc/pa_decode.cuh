@@ -1,57 +1,51 @@
-// pa_decode.cuh -- split-context paged decode attention kernel for sm_103a.
+// pa_decode.cuh -- paged decode attention kernels for sm_103a.
 //
-// What it computes ("PagedAttention in mistral.rs": blocked K/V pool read
+// What they compute ("PagedAttention in mistral.rs": blocked K/V pool read
 // through per-sequence block tables, optional FP8 E4M3 cache; "Rolling buffer
-// cache": a window of W slots): for sequence s, kv head g and the G query
-// heads sharing it, softmax(q K^T * scale) V over the attended slots
-// [0, L_s), restricted to this CTA's split of pages.
+// cache": a window of W ring slots): for sequence s, kv head g and the G query
+// heads sharing it, softmax(q K^T * scale) V over the attended slots [0, L_s).
 //
-// One CTA = one (split, kv head, sequence). Warp roles:
-//   * producer warp (last warp): reads the split's block-table entries and,
-//     per page, issues two 1-D bulk asynchronous copies (K page, V page; each
-//     bs*D contiguous elements of the head-major layout) into a ring of
-//     STAGES shared-memory stages, completion tracked by "full" mbarriers;
-//     waits on "empty" mbarriers before reusing a stage.
-//   * NC = bs/8 consumer warps: each owns 8 rows (tokens) of every page.
-//     A lane covers LPR-th of a row (EPL elements of D, in PB-byte pieces
-//     interleaved across the LPR lanes of the row, so every shared-memory
-//     load instruction of a row reads contiguous bytes). Per page:
-//       1. partial dot products q.k for (token, head) pairs, then a
-//          transposing butterfly reduction across the LPR lanes (each level
-//          halves the values a lane keeps, so a warp spends ~1 shuffle per
-//          (token, head) instead of log2(LPR));
-//       2. online softmax per head over the warp's 8 tokens (running max and
-//          sum in log2 units; q is pre-scaled by scale*log2(e)*k_scale);
-//       3. P.V accumulation into per-lane fp32 accumulators, skipping rows
-//          past L_s (never multiplying a weight by a stale or NaN value).
-//     At the end the NC warps' (m, l, acc) are merged through shared memory
-//     and written either as the final output (one split) or as a split
-//     partial (m in natural-log units, l, acc / l) for the LSE reduction.
-// Each K/V byte of the split is read from HBM exactly once per kv head.
+// Work is cut into "pieces": a run of consecutive pages of one (sequence,
+// kv head) "segment". Two ways of cutting:
+//  * split mode: grid (splits, kv heads, seqs); CTA (i, g, s) takes pages
+//    [i*P, (i+1)*P) of segment (s, g) and writes the final output (one
+//    split) or the split's partial (m, l, o) for pa_reduce.
+//  * balanced mode: a persistent grid of C CTAs (the resident capacity).
+//    The pages of all segments, in (sequence, kv head, page) order, are cut
+//    into C equal contiguous ranges; each CTA streams its range without a
+//    break, crossing segment boundaries. A segment lying wholly inside one
+//    range is finished by that CTA; a segment cut by range boundaries leaves
+//    a partial in each CTA it touches (at most two per CTA: its first and
+//    its last piece), combined afterwards by combine_pieces_kernel.
+//
+// CTA structure (both modes):
+//  * producer warp (last warp): walks the CTA's pages; per page it issues 1-D
+//    bulk asynchronous copies (K page, V page: bs*D contiguous elements of the
+//    head-major layout; plus the G query rows at the first page of a piece)
+//    into a ring of STAGES shared-memory stages, and writes the stage's
+//    descriptor (attended rows, segment, first/last-of-piece flags). Stage
+//    completion is tracked by "full" mbarriers (expect-tx), reuse by "empty"
+//    mbarriers.
+//  * NC = bs/8 consumer warps, 8 rows of every page each, R pages per
+//    iteration. A lane covers EPL elements of a row in PB-byte pieces
+//    interleaved across the row's LPR lanes (each shared-memory load
+//    instruction of a row reads contiguous bytes). Per iteration:
+//       1. partial q.k dot products as fp32 pairs (packed FMA), reduced
+//          across the row's lanes by a transposing butterfly (each level
+//          halves the values a lane keeps: ~1 shuffle per (token, head));
+//       2. softmax weights 2^(s - m) against a lazy running max m (log2
+//          units; q pre-scaled by scale*log2(e)*k_scale): m moves, with a
+//          rescale, only when a logit clears it by 2^8;
+//       3. P.V into fp32 pair accumulators; rows past L_s are skipped, never
+//          weighted, so stale or NaN cache rows cannot reach the output.
+//     At the end of a piece the warps merge (m, l, acc) through the piece's
+//     last stage (reused as scratch before it is released) and store.
+// Every K/V byte is read from HBM once per kv head. All waits are bounded.
 #pragma once
 
 #include "pa_device.cuh"
 
 namespace pa {
-
-struct DecodeParams {
-  void* out;           // [S][Hq][D] of QT (final mode)
-  float* tmp_out;      // [S][Hq][NS][D]  (partials mode)
-  float* max_logits;   // [S][Hq][NS]
-  float* exp_sums;     // [S][Hq][NS]
-  const void* query;   // [S][Hq][D] of QT
-  const uint8_t* k_cache;
-  const uint8_t* v_cache;
-  const int32_t* block_tables;  // [S][MB]
-  const int32_t* context_lens;  // [S]
-  unsigned* err;
-  int num_heads, num_kv_heads, group;  // group = G (runtime, <= template GT)
-  int num_blocks, max_blocks_per_seq, window;
-  int num_splits, pages_per_split;
-  int partials;   // 1: split partials, 0: final output
-  float q_scale;  // scale * log2(e) (* k_scale for FP8)
-  float v_scale;  // FP8: v_scale, else 1
-};
 
 // Shared-memory budget for one CTA's K/V stages, and the most pages a
 // consumer warp takes per iteration (build-time tunables).
@@ -65,9 +59,51 @@ struct DecodeParams {
 #define PA_MAX_STAGES 8
 #endif
 
+enum : int { kModeSplit = 0, kModeBalanced = 1 };
+
+// Stage-descriptor flags.
+enum : int {
+  kFirst = 1,      // first page of a piece (its stage also carries the q rows)
+  kLast = 2,       // last page of a piece
+  kCtaLast = 4,    // last page of the CTA's work
+  kSegFirst = 8,   // the piece starts at page 0 of its segment
+  kSegLast = 16,   // the piece ends at the segment's last page
+  kSlot1 = 32      // balanced mode: the piece is stored in partial slot 1
+};
+
+// Balanced mode: partial slots per CTA and the most CTAs a workspace is
+// sized for (152 SMs x 4 resident CTAs).
+constexpr int kPieceSlots = 2;
+constexpr int kMaxBalancedCtas = 152 * 4;
+
+struct DecodeParams {
+  // outputs
+  void* out;            // [S][Hq][D] of QT
+  float* tmp_out;       // split mode partials: [S][Hq][NS][D]
+  float* max_logits;    // [S][Hq][NS]
+  float* exp_sums;      // [S][Hq][NS]
+  float* piece_o;       // balanced mode: [C][2][GT][D]
+  float* piece_ml;      // [C][2][GT][2]: max logit (natural log), sum relative to it
+  int* piece_info;      // [C][2][4]: valid, segment, flags, 0
+  // inputs
+  const void* query;    // [S][Hq][D] of QT
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const int32_t* block_tables;  // [S][MB]
+  const int32_t* context_lens;  // [S]
+  unsigned* err;
+  int num_seqs, num_heads, num_kv_heads, group;  // group = G (runtime, <= GT)
+  int num_blocks, max_blocks_per_seq, window;
+  int num_splits, pages_per_split;  // split mode
+  int partials;   // split mode: 1 = write split partials, 0 = final output
+  float q_scale;  // scale * log2(e) (* k_scale for FP8)
+  float v_scale;  // FP8: v_scale, else 1
+};
+
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
-constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
+constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 // Lanes per row: the fewest (>= 4) that keep q and acc at <= 32 fp32 each with
 // an even number of elements per lane (they are processed as fp32 pairs);
@@ -83,9 +119,10 @@ constexpr int choose_pb(int bytes) {
   return bytes % 16 == 0 ? 16 : bytes % 8 == 0 ? 8 : bytes % 4 == 0 ? 4 : bytes % 2 == 0 ? 2 : 1;
 }
 
-template <typename CT, int D, int GT, int BS>
+template <typename QT, typename CT, int D, int GT, int BS>
 struct Layout {
   static constexpr int EB = Elem<CT>::bytes;
+  static constexpr int QB = Elem<QT>::bytes;
   static constexpr int ROWB = D * EB;      // bytes of one cached row
   static constexpr int PAGE = BS * ROWB;   // bytes of one (block, kv head) page
   static constexpr int TPW = 8;            // rows per consumer warp per page
@@ -100,39 +137,52 @@ struct Layout {
   static constexpr int EL2 = EPL / 2;      // fp32 pairs per lane
   static constexpr int RPW = 32 / LPR;     // rows a warp covers per step
   static constexpr int NST = TPW / RPW;    // steps per page
-  // pages a consumer warp takes per iteration (one softmax round per R pages)
+  // pages a consumer warp takes per iteration (one weight round per R pages)
   static constexpr int R = (2 * PAGE <= 16384) ? PA_PAGES_PER_ITER : 1;
   static constexpr int TPI = TPW * R;      // rows per warp per iteration
   static constexpr int NSTI = NST * R;     // steps per iteration
-  static constexpr int SG = cmin(NSTI, cmax(1, 16 / GT));  // steps per reduction group
+  static constexpr int SG = cmin(NSTI, cmax(1, 8 / GT));   // steps per reduction group
   static constexpr int NV = SG * GT;       // partial dot products per group
-  static constexpr int NFIN = cmax(NV / LPR, 1);   // reduced values a lane holds
+  static constexpr int NFIN = cmax(NV / LPR, 1);       // reduced values a lane holds
   static constexpr int RED = NV < LPR ? LPR / NV : 1;  // lanes holding the same value
-  static constexpr int NG = NSTI / SG;               // reduction groups per iteration
+  static constexpr int NG = NSTI / SG;                 // reduction groups per iteration
   // After the reduction lane c (of a row) holds value index (c*NV)/LPR + kk,
-  // head = index % GT. Lane bits [HB0, HB0 + NHB) of c select the head;
-  // the other lane bits only select tokens (or redundant copies).
+  // head = index % GT. Lane bits [HB0, HB0 + NHB) of c select the head; the
+  // other lane bits only select tokens (or redundant copies).
   static constexpr int HB0 = NV >= LPR ? 0 : ilog2(RED);
   static constexpr int NHB = NV >= LPR ? ilog2(cmax(GT / NFIN, 1)) : ilog2(GT);
   static constexpr int HEAD_MASK = ((1 << NHB) - 1) << HB0;
   static constexpr int STAGES = cmax(2 * R, cmin(PA_MAX_STAGES, PA_STAGE_BYTES / (2 * PAGE)));
-  static constexpr int SCR = (TPI * GT + GT + 3) / 4 * 4;  // per-warp scratch floats
+  static constexpr int QSLOT = round_up(GT * D * QB, 16);        // q rows of a piece
+  static constexpr int STAGE = round_up(2 * PAGE + QSLOT, 128);  // K page | V page | q rows
+  static constexpr int SCR = round_up(TPI * GT, 4);              // per-warp weights
+  static constexpr int MACC = NC * GT * D * 4;                   // merge accumulators
+  static constexpr bool MERGE_IN_STAGE = MACC <= STAGE;
   // dynamic shared memory layout
-  static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = STAGES * PAGE;
-  static constexpr int OFF_BAR = 2 * STAGES * PAGE;
-  static constexpr int OFF_OK = OFF_BAR + 2 * STAGES * 8;
-  static constexpr int OFF_SCR = (OFF_OK + STAGES * 4 + 15) / 16 * 16;
-  static constexpr int SMEM = OFF_SCR + NC * SCR * 4;
-  // end-of-split merge area (reuses the K/V stages)
-  static constexpr int MERGE = NC * GT * (D + 3) * 4;
+  static constexpr int OFF_BAR = STAGES * STAGE;
+  static constexpr int OFF_DESC = round_up(OFF_BAR + (2 * STAGES + 1) * 8, 16);
+  static constexpr int OFF_SCR = round_up(OFF_DESC + STAGES * 16, 16);
+  static constexpr int OFF_MSTAT = OFF_SCR + NC * SCR * 4;  // [3][NC][GT]
+  static constexpr int OFF_MACC = round_up(OFF_MSTAT + 3 * NC * GT * 4, 16);
+  static constexpr int OFF_MISC = OFF_MACC + (MERGE_IN_STAGE ? 0 : MACC);
+  static constexpr int SMEM = OFF_MISC + 16;
+  // CTAs per SM to plan registers for: what the shared memory allows (228 KB
+  // per SM, 1 KB reserved per CTA), at most 4, and no more than keeps a
+  // register budget per thread (96 for one or two heads per kv head, else
+  // 128); __launch_bounds__ makes ptxas fit that many.
+  static constexpr int REG_BUDGET = GT <= 2 ? 96 : 128;
+  static constexpr int MIN_CTAS =
+      cmax(1, cmin(cmin(4, (228 * 1024) / (SMEM + 1024)), 65536 / (THREADS * REG_BUDGET)));
   static_assert(NST >= 1, "lanes per row too small for 8 rows per warp");
   static_assert(NSTI % SG == 0, "reduction groups must tile the steps");
   static_assert(STAGES >= R, "a consumer iteration holds R stages");
   static_assert(EPL * LPR == D && NPL * EPP == EPL, "row split");
   static_assert(EPP % 2 == 0, "pieces hold whole fp32 pairs");
-  static_assert(MERGE <= 2 * STAGES * PAGE, "merge area");
   static_assert(PAGE % 16 == 0, "bulk copies move multiples of 16 bytes");
+  static_assert(STAGE % 128 == 0 && OFF_BAR % 8 == 0, "stage and mbarrier alignment");
+  static_assert(OFF_DESC % 16 == 0 && OFF_SCR % 16 == 0 && OFF_MSTAT % 16 == 0 &&
+                    OFF_MACC % 16 == 0 && OFF_MISC % 4 == 0 && (SCR * 4) % 16 == 0,
+                "16-byte vector accesses need 16-byte aligned shared-memory regions");
 };
 
 // Transposing butterfly reduction of N per-lane values over lane offsets
@@ -181,8 +231,8 @@ __device__ __forceinline__ void load_row(const float* src, float* dst) {
 
 // acc[h][:] += p[h] * V_row[this lane's elements] for one row.
 template <typename CT, typename Ly, int GT, int EL2>
-__device__ __forceinline__ void pv_row_impl(const float* pw_src, const uint8_t* vr, int c,
-                                            float2 (&acc)[GT][EL2]) {
+__device__ __forceinline__ void pv_row(const float* pw_src, const uint8_t* vr, int c,
+                                       float2 (&acc)[GT][EL2]) {
   float pw[GT];
   load_row<GT>(pw_src, pw);
 #pragma unroll
@@ -198,322 +248,197 @@ __device__ __forceinline__ void pv_row_impl(const float* pw_src, const uint8_t* 
     }
   }
 }
-template <typename CT, typename Ly, int GT, int EL2>
-__device__ __forceinline__ void pv_row(const float* pw_src, const uint8_t* vr, int c,
-                                       float2 (&acc)[GT][EL2]) {
-  pv_row_impl<CT, Ly, GT, EL2>(pw_src, vr, c, acc);
+
+// Per-lane state of one piece's online softmax.
+template <typename Ly, int GT>
+struct PieceState {
+  float2 qf[GT][Ly::EL2];   // q (pre-scaled), consecutive pairs of this lane's elements
+  float2 acc[GT][Ly::EL2];  // un-normalised output, same layout
+  float m_run[Ly::NFIN];    // running (lazy) max of the head of reduced value kk
+  float l_run[Ly::NFIN];    // this lane's share of the running sum
+  float s_top[Ly::NFIN];    // largest logit seen
+};
+
+// Start a piece: q rows (G of them, row-major [G][D] of QT in shared memory).
+template <typename QT, typename Ly, int GT, int D>
+__device__ __forceinline__ void begin_piece(PieceState<Ly, GT>& st, const uint8_t* qrows, int G,
+                                            int c, float q_scale) {
+  const QT* q = reinterpret_cast<const QT*>(qrows);
+#pragma unroll
+  for (int h = 0; h < GT; ++h) {
+#pragma unroll
+    for (int kk = 0; kk < Ly::NPL; ++kk) {
+#pragma unroll
+      for (int j2 = 0; j2 < Ly::EP2; ++j2) {
+        const int d = (kk * Ly::LPR + c) * Ly::EPP + 2 * j2;
+        st.qf[h][kk * Ly::EP2 + j2] =
+            h < G ? make_float2(Elem<QT>::to_f32(q[h * D + d]) * q_scale,
+                                Elem<QT>::to_f32(q[h * D + d + 1]) * q_scale)
+                  : make_float2(0.f, 0.f);
+        st.acc[h][kk * Ly::EP2 + j2] = make_float2(0.f, 0.f);
+      }
+    }
+  }
+#pragma unroll
+  for (int kk = 0; kk < Ly::NFIN; ++kk) {
+    st.m_run[kk] = -INFINITY;
+    st.l_run[kk] = 0.f;
+    st.s_top[kk] = -INFINITY;
+  }
 }
 
-template <typename QT, typename CT, int D, int GT, int BS>
-__global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
-    paged_decode_kernel(const __grid_constant__ DecodeParams p) {
-  using Ly = Layout<CT, D, GT, BS>;
-  constexpr int NC = Ly::NC, STAGES = Ly::STAGES, LPR = Ly::LPR, EPP = Ly::EPP;
-  constexpr int NPL = Ly::NPL, EPL = Ly::EPL, RPW = Ly::RPW, TPW = Ly::TPW;
-  constexpr float kLn2 = 0.69314718055994530942f;
-  extern __shared__ __align__(128) uint8_t smem[];
-
-  const int split = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Hq = p.num_heads, G = p.group;
-  pdl_wait();
-  pdl_trigger();
-
-  // ---- attended slots of this sequence and this split's pages
-  int n = p.context_lens[s];
-  const int cap = p.max_blocks_per_seq * BS;
-  int L;
-  if (n < 0) {
-    L = 0;
-    if (threadIdx.x == 0 && split == 0 && g == 0) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
-  } else if (p.window > 0) {
-    L = n < p.window ? n : p.window;
-  } else if (n > cap) {
-    L = cap;
-    if (threadIdx.x == 0 && split == 0 && g == 0) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
-  } else {
-    L = n;
-  }
-  const int total_pages = (L + BS - 1) / BS;
-  const int pg0 = split * p.pages_per_split;
-  const int pg1 = min(total_pages, pg0 + p.pages_per_split);
-  const int npg = pg1 - pg0;
-
-  if (npg <= 0) {  // nothing to attend in this split (uniform for the CTA)
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-      const int h = i / D, d = i % D;
-      const size_t row = (size_t)s * Hq + (size_t)g * G + h;
-      if (p.partials) {
-        if (d == 0) {
-          p.max_logits[row * p.num_splits + split] = -INFINITY;
-          p.exp_sums[row * p.num_splits + split] = 0.f;
-        }
-      } else {
-        reinterpret_cast<QT*>(p.out)[row * D + d] = Elem<QT>::from_f32(0.f);
-      }
-    }
-    return;
-  }
-
-  uint8_t* sK = smem + Ly::OFF_K;
-  uint8_t* sV = smem + Ly::OFF_V;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Ly::OFF_BAR);
-  uint64_t* empty = full + STAGES;
-  volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + Ly::OFF_OK);
-
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], NC);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  // ======================================================== producer warp
-  if (warp == NC) {
-    const int32_t* bt = p.block_tables + (size_t)s * p.max_blocks_per_seq + pg0;
-    const size_t head_off = (size_t)g * Ly::PAGE;
-    const size_t blk_stride = (size_t)p.num_kv_heads * Ly::PAGE;
-    int tbl = -1;
-    int issued = 0;
-    bool aborted = false;
-    for (int k = 0; k < npg; ++k) {
-      if ((k & 31) == 0) {
-        const int idx = k + lane;
-        tbl = idx < npg ? __ldg(bt + idx) : -1;
-      }
-      const int bid = __shfl_sync(0xffffffffu, tbl, k & 31);
-      const int slot = k % STAGES;
-      if (lane == 0) {
-        if (k >= STAGES && !mbar_wait_bounded(&empty[slot], ((k / STAGES) - 1) & 1)) {
-          raise_error(p.err, PA_DEVERR_TIMEOUT);
-          aborted = true;
-        }
-        if (!aborted) {
-          const bool ok = bid >= 0 && bid < p.num_blocks;
-          stage_ok[slot] = ok ? 1 : 0;
-          if (ok) {
-            const size_t off = (size_t)bid * blk_stride + head_off;
-            mbar_arrive_expect_tx(&full[slot], 2u * Ly::PAGE);
-            bulk_g2s(sK + slot * Ly::PAGE, p.k_cache + off, Ly::PAGE, &full[slot]);
-            bulk_g2s(sV + slot * Ly::PAGE, p.v_cache + off, Ly::PAGE, &full[slot]);
-          } else {
-            raise_error(p.err, PA_DEVERR_BLOCK_ID);
-            mbar_arrive(&full[slot]);
-          }
-          ++issued;
-        }
-      }
-      if (__shfl_sync(0xffffffffu, aborted ? 1 : 0, 0)) break;
-    }
-    // never leave the CTA with copies in flight: wait for the last fill of
-    // every stage (already complete in the normal case)
-    if (lane == 0) {
-      for (int k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k)
-        if (!mbar_wait_bounded(&full[k % STAGES], (k / STAGES) & 1))
-          raise_error(p.err, PA_DEVERR_TIMEOUT);
-    }
-    return;
-  }
-
-  // ======================================================== consumer warps
-  const int c = lane % LPR;   // piece column of the row
-  const int rg = lane / LPR;  // row within a warp step
-  float* wscr = reinterpret_cast<float*>(smem + Ly::OFF_SCR) + warp * Ly::SCR;
-
-  constexpr int EP2 = Ly::EP2, EL2 = Ly::EL2;
-  float2 qf[GT][EL2];   // q (pre-scaled), as consecutive pairs of this lane's elements
-  float2 acc[GT][EL2];  // un-normalised output, same layout
-  {
-    const QT* q = reinterpret_cast<const QT*>(p.query);
-#pragma unroll
-    for (int h = 0; h < GT; ++h) {
-      const bool live = h < G;
-      const QT* qh = q + ((size_t)s * Hq + (size_t)g * G + (live ? h : 0)) * D;
-#pragma unroll
-      for (int kk = 0; kk < NPL; ++kk) {
-#pragma unroll
-        for (int j2 = 0; j2 < EP2; ++j2) {
-          const int d = (kk * LPR + c) * EPP + 2 * j2;
-          qf[h][kk * EP2 + j2] =
-              live ? make_float2(Elem<QT>::to_f32(qh[d]) * p.q_scale,
-                                 Elem<QT>::to_f32(qh[d + 1]) * p.q_scale)
-                   : make_float2(0.f, 0.f);
-          acc[h][kk * EP2 + j2] = make_float2(0.f, 0.f);
-        }
-      }
-    }
-  }
-
-  // Online softmax with a lazy running max (log2 units). For the reduced
-  // values it holds (index kk: head hd[kk]) a lane keeps the running max m of
-  // that head, its own share of the running sum l and the largest logit seen.
-  // Weights are 2^(s - m); m only moves (and acc/l are rescaled) when a logit
-  // exceeds it by more than kLazy, so the weights stay <= 2^kLazy.
-  constexpr float kLazy = 8.f;
-  constexpr int NFIN = Ly::NFIN, RED = Ly::RED, NG = Ly::NG, NV = Ly::NV;
-  constexpr int TPI = Ly::TPI, R = Ly::R;
+// One consumer iteration over R pages of the current piece (a page with
+// lim[r] <= 0 contributes nothing). Token t of the warp's TPI rows is row
+// warp*TPW + t%TPW of page t/TPW; rows t%TPW < lim[t/TPW] are attended.
+template <typename CT, typename Ly, int GT>
+__device__ __forceinline__ void process_pages(PieceState<Ly, GT>& st,
+                                              const uint8_t* const (&Kp)[Ly::R],
+                                              const uint8_t* const (&Vp)[Ly::R],
+                                              const int (&lim)[Ly::R], float* wscr, int warp,
+                                              int lane, int c, int rg) {
+  constexpr int R = Ly::R, TPW = Ly::TPW, RPW = Ly::RPW, LPR = Ly::LPR, NV = Ly::NV;
+  constexpr int NG = Ly::NG, NFIN = Ly::NFIN, RED = Ly::RED, EP2 = Ly::EP2, EL2 = Ly::EL2;
+  constexpr float kLazy = 8.f;  // weights stay <= 2^kLazy
   const bool writer = (c % RED) == 0;  // one lane per distinct reduced value
-  int hd[NFIN];
+
+  // ---- 1. logits, reduced across the row's lanes; invalid rows become -inf
+  float sl[NG][NFIN];
 #pragma unroll
-  for (int kk = 0; kk < NFIN; ++kk) hd[kk] = ((c * NV) / LPR + kk) % GT;
-  float m_run[NFIN], l_run[NFIN], s_top[NFIN];
+  for (int sg = 0; sg < NG; ++sg) {
+    float part[NV];
+    {
+      float2 part2[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) part2[i] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int stl = 0; stl < Ly::SG; ++stl) {
+        const int stp = sg * Ly::SG + stl;
+        const int row = warp * TPW + (stp % Ly::NST) * RPW + rg;
+        const uint8_t* kr = Kp[stp / Ly::NST] + row * Ly::ROWB;
+#pragma unroll
+        for (int kk = 0; kk < Ly::NPL; ++kk) {
+          float2 kf[EP2];
+          load_piece2<CT, Ly::PB>(kr + (kk * LPR + c) * Ly::PB, kf);
+#pragma unroll
+          for (int h = 0; h < GT; ++h)
+#pragma unroll
+            for (int j2 = 0; j2 < EP2; ++j2)
+              part2[stl * GT + h] = __ffma2_rn(st.qf[h][kk * EP2 + j2], kf[j2], part2[stl * GT + h]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < NV; ++i) part[i] = part2[i].x + part2[i].y;
+    }
+    TransposeReduce<NV, LPR / 2>::run(part, lane);
+#pragma unroll
+    for (int kk = 0; kk < NFIN; ++kk) {
+      const int t = (sg * Ly::SG + ((c * NV) / LPR + kk) / GT) * RPW + rg;
+      int lim_t = lim[0];  // lim of token t's page, without dynamic indexing
+#pragma unroll
+      for (int r = 1; r < R; ++r) lim_t = t >= r * TPW ? lim[r] : lim_t;
+      sl[sg][kk] = (writer && (t % TPW) < lim_t) ? part[kk] : -INFINITY;
+    }
+  }
+
+  // ---- 2. lazy max: move m only when a logit clears it by kLazy
+  bool raise = false;
 #pragma unroll
   for (int kk = 0; kk < NFIN; ++kk) {
-    m_run[kk] = -INFINITY;
-    l_run[kk] = 0.f;
-    s_top[kk] = -INFINITY;
+    float top = sl[0][kk];
+#pragma unroll
+    for (int sg = 1; sg < NG; ++sg) top = fmaxf(top, sl[sg][kk]);
+    st.s_top[kk] = fmaxf(st.s_top[kk], top);
+    raise |= top > st.m_run[kk] + kLazy;
   }
-
-  bool aborted = false;
-  for (int k0 = 0; k0 < npg; k0 += R) {
-    // this iteration's R pages; token t of the warp's TPI rows is row
-    // warp*TPW + t%TPW of page k0 + t/TPW
-    const uint8_t* Kp[R];
-    const uint8_t* Vp[R];
-    int lim[R];  // rows t%TPW < lim[r] of page r hold attended slots
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int k = k0 + r;
-      const int slot = (k < npg ? k : k0) % STAGES;
-      Kp[r] = sK + slot * Ly::PAGE;
-      Vp[r] = sV + slot * Ly::PAGE;
-      lim[r] = 0;
-      if (k < npg) {
-        if (!mbar_wait_bounded(&full[slot], (k / STAGES) & 1)) {
-          raise_error(p.err, PA_DEVERR_TIMEOUT);
-          aborted = true;
-        }
-        if (stage_ok[slot] != 0) lim[r] = L - (pg0 + k) * BS - warp * TPW;
-      }
-    }
-    if (__any_sync(0xffffffffu, aborted)) break;
-
-    // ---- 1. logits of this warp's rows for the GT heads (fp32 pair FMAs),
-    //         reduced across the row's lanes; invalid rows become -inf
-    float sl[NG][NFIN];
-#pragma unroll
-    for (int sg = 0; sg < NG; ++sg) {
-      float part[NV];
-      {
-        float2 part2[NV];
-#pragma unroll
-        for (int i = 0; i < NV; ++i) part2[i] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int stl = 0; stl < Ly::SG; ++stl) {
-          const int st = sg * Ly::SG + stl;
-          const int row = warp * TPW + (st % Ly::NST) * RPW + rg;
-          const uint8_t* kr = Kp[st / Ly::NST] + row * Ly::ROWB;
-#pragma unroll
-          for (int kk = 0; kk < NPL; ++kk) {
-            float2 kf[EP2];
-            load_piece2<CT, Ly::PB>(kr + (kk * LPR + c) * Ly::PB, kf);
-#pragma unroll
-            for (int h = 0; h < GT; ++h)
-#pragma unroll
-              for (int j2 = 0; j2 < EP2; ++j2)
-                part2[stl * GT + h] = __ffma2_rn(qf[h][kk * EP2 + j2], kf[j2], part2[stl * GT + h]);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < NV; ++i) part[i] = part2[i].x + part2[i].y;
-      }
-      TransposeReduce<NV, LPR / 2>::run(part, lane);
-#pragma unroll
-      for (int kk = 0; kk < NFIN; ++kk) {
-        const int t = (sg * Ly::SG + ((c * NV) / LPR + kk) / GT) * RPW + rg;
-        int lim_t = lim[0];  // lim of token t's page, without dynamic indexing
-#pragma unroll
-        for (int r = 1; r < R; ++r) lim_t = t >= r * TPW ? lim[r] : lim_t;
-        sl[sg][kk] = (writer && (t % TPW) < lim_t) ? part[kk] : -INFINITY;
-      }
-    }
-
-    // ---- 2. lazy max: move m only when a logit clears it by kLazy
-    bool raise = false;
+  if (__any_sync(0xffffffffu, raise)) {
+    float alpha[NFIN];
 #pragma unroll
     for (int kk = 0; kk < NFIN; ++kk) {
       float top = sl[0][kk];
 #pragma unroll
       for (int sg = 1; sg < NG; ++sg) top = fmaxf(top, sl[sg][kk]);
-      s_top[kk] = fmaxf(s_top[kk], top);
-      raise |= top > m_run[kk] + kLazy;
+#pragma unroll
+      for (int off = 1; off < 32; off *= 2)  // over every lane bit but the head bits
+        if ((off & Ly::HEAD_MASK) == 0) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, off));
+      const float m_new = fmaxf(st.m_run[kk], top);
+      alpha[kk] = m_new == -INFINITY ? 1.f : exp2f(st.m_run[kk] - m_new);
+      st.m_run[kk] = m_new;
+      st.l_run[kk] *= alpha[kk];
     }
-    if (__any_sync(0xffffffffu, raise)) {
-      float alpha[NFIN];
+    float al[GT];  // every head's factor, from a lane that holds that head
 #pragma unroll
-      for (int kk = 0; kk < NFIN; ++kk) {
-        float top = sl[0][kk];
+    for (int h = 0; h < GT; ++h)
+      al[h] = __shfl_sync(0xffffffffu, alpha[h % NFIN], NV >= LPR ? h / NFIN : h * RED);
 #pragma unroll
-        for (int sg = 1; sg < NG; ++sg) top = fmaxf(top, sl[sg][kk]);
+    for (int h = 0; h < GT; ++h)
 #pragma unroll
-        for (int off = 1; off < 32; off *= 2)  // over every lane bit but the head bits
-          if ((off & Ly::HEAD_MASK) == 0) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, off));
-        const float m_new = fmaxf(m_run[kk], top);
-        alpha[kk] = m_new == -INFINITY ? 1.f : exp2f(m_run[kk] - m_new);
-        m_run[kk] = m_new;
-        l_run[kk] *= alpha[kk];
-      }
-      float al[GT];  // every head's factor, from a lane that holds that head
-#pragma unroll
-      for (int h = 0; h < GT; ++h)
-        al[h] = __shfl_sync(0xffffffffu, alpha[h % NFIN], Ly::NV >= LPR ? h / NFIN : h * RED);
-#pragma unroll
-      for (int h = 0; h < GT; ++h)
-#pragma unroll
-        for (int e = 0; e < EL2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], make_float2(al[h], al[h]));
-    }
-
-    // ---- 3. weights 2^(s - m) to shared memory, then P.V (fp32 pair FMAs)
-#pragma unroll
-    for (int sg = 0; sg < NG; ++sg)
-#pragma unroll
-      for (int kk = 0; kk < NFIN; ++kk) {
-        const float pw = sl[sg][kk] == -INFINITY ? 0.f : exp2f(sl[sg][kk] - m_run[kk]);
-        l_run[kk] += pw;
-        if (writer) {
-          const int idx = (c * NV) / LPR + kk;
-          const int t = (sg * Ly::SG + idx / GT) * RPW + rg;
-          wscr[t * GT + idx % GT] = pw;
-        }
-      }
-    __syncwarp();
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      if (lim[r] >= TPW) {  // every row of this warp in page r is attended
-#pragma unroll
-        for (int st = 0; st < Ly::NST; ++st) {
-          const int tr = st * RPW + rg;
-          pv_row<CT, Ly>(wscr + (r * TPW + tr) * GT, Vp[r] + (warp * TPW + tr) * Ly::ROWB, c, acc);
-        }
-      } else if (lim[r] > 0) {
-#pragma unroll
-        for (int st = 0; st < Ly::NST; ++st) {
-          const int tr = st * RPW + rg;
-          if (tr < lim[r])
-            pv_row<CT, Ly>(wscr + (r * TPW + tr) * GT, Vp[r] + (warp * TPW + tr) * Ly::ROWB, c,
-                           acc);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) {
-#pragma unroll
-      for (int r = 0; r < R; ++r)
-        if (k0 + r < npg) mbar_arrive(&empty[(k0 + r) % STAGES]);
-    }
+      for (int e = 0; e < EL2; ++e) st.acc[h][e] = __fmul2_rn(st.acc[h][e], make_float2(al[h], al[h]));
   }
 
-  // ---- per-head (m, l, top) of this warp, then merge row groups and warps
+  // ---- 3. weights 2^(s - m) to shared memory, then P.V
+#pragma unroll
+  for (int sg = 0; sg < NG; ++sg)
+#pragma unroll
+    for (int kk = 0; kk < NFIN; ++kk) {
+      const float pw = sl[sg][kk] == -INFINITY ? 0.f : exp2f(sl[sg][kk] - st.m_run[kk]);
+      st.l_run[kk] += pw;
+      if (writer) {
+        const int idx = (c * NV) / LPR + kk;
+        const int t = (sg * Ly::SG + idx / GT) * RPW + rg;
+        wscr[t * GT + idx % GT] = pw;
+      }
+    }
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (lim[r] >= TPW) {  // every row of this warp in page r is attended
+#pragma unroll
+      for (int stp = 0; stp < Ly::NST; ++stp) {
+        const int tr = stp * RPW + rg;
+        pv_row<CT, Ly>(wscr + (r * TPW + tr) * GT, Vp[r] + (warp * TPW + tr) * Ly::ROWB, c, st.acc);
+      }
+    } else if (lim[r] > 0) {
+#pragma unroll
+      for (int stp = 0; stp < Ly::NST; ++stp) {
+        const int tr = stp * RPW + rg;
+        if (tr < lim[r])
+          pv_row<CT, Ly>(wscr + (r * TPW + tr) * GT, Vp[r] + (warp * TPW + tr) * Ly::ROWB, c,
+                         st.acc);
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// Bounded barrier among the NC consumer warps (an mbarrier with one arrival
+// per warp), so a consumer that gave up on a wait can never hang the others.
+__device__ __forceinline__ void consumer_sync(uint64_t* bar, uint32_t& phase, int lane,
+                                              unsigned* err) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  if (!mbar_wait_bounded(bar, phase & 1)) raise_error(err, PA_DEVERR_TIMEOUT);
+  ++phase;
+}
+
+// End of a piece: reduce each warp's state, merge the NC warps through shared
+// memory, and hand every (head, element) result to `sink`:
+//   sink(h, d, o, m_nat, l) with o the normalised output (v_scale applied),
+//   m_nat the piece's largest logit in natural-log units and l the sum of
+//   exp(logit - m_nat) (m_nat = -inf, l = 0 when no slot was attended).
+template <typename Ly, int GT, int D, typename Sink>
+__device__ __forceinline__ void finish_piece(PieceState<Ly, GT>& st, float* mstat, float* macc,
+                                             uint64_t* cbar, uint32_t& cphase, int G, int warp,
+                                             int lane, int c, int rg, float v_scale, unsigned* err,
+                                             Sink&& sink) {
+  constexpr int NC = Ly::NC, LPR = Ly::LPR, NFIN = Ly::NFIN, EL2 = Ly::EL2, EP2 = Ly::EP2;
+  constexpr float kLn2 = 0.69314718055994530942f;
   float mh[GT], lh[GT], th[GT];
   {
     float lsum[NFIN], tmax[NFIN];
 #pragma unroll
     for (int kk = 0; kk < NFIN; ++kk) {
-      lsum[kk] = l_run[kk];
-      tmax[kk] = s_top[kk];
+      lsum[kk] = st.l_run[kk];
+      tmax[kk] = st.s_top[kk];
 #pragma unroll
       for (int off = 1; off < 32; off *= 2)
         if ((off & Ly::HEAD_MASK) == 0) {
@@ -523,8 +448,8 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
     }
 #pragma unroll
     for (int h = 0; h < GT; ++h) {
-      const int src = Ly::NV >= LPR ? h / NFIN : h * RED;
-      mh[h] = __shfl_sync(0xffffffffu, m_run[h % NFIN], src);
+      const int src = Ly::NV >= LPR ? h / NFIN : h * Ly::RED;
+      mh[h] = __shfl_sync(0xffffffffu, st.m_run[h % NFIN], src);
       lh[h] = __shfl_sync(0xffffffffu, lsum[h % NFIN], src);
       th[h] = __shfl_sync(0xffffffffu, tmax[h % NFIN], src);
     }
@@ -535,34 +460,33 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
     for (int h = 0; h < GT; ++h)
 #pragma unroll
       for (int e = 0; e < EL2; ++e) {
-        acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, off);
-        acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, off);
+        st.acc[h][e].x += __shfl_xor_sync(0xffffffffu, st.acc[h][e].x, off);
+        st.acc[h][e].y += __shfl_xor_sync(0xffffffffu, st.acc[h][e].y, off);
       }
 
-  named_bar_sync(1, NC * 32);  // every consumer is done with the stages
-  float* mm = reinterpret_cast<float*>(smem);   // [NC][GT] running max
-  float* ml = mm + NC * GT;                     // [NC][GT] running sum (relative to mm)
-  float* mt = ml + NC * GT;                     // [NC][GT] largest logit
-  float* ma = mt + NC * GT;                     // [NC][GT][D] accumulators
-  if (lane < GT) {
-    mm[warp * GT + lane] = aborted ? -INFINITY : mh[lane];
-    ml[warp * GT + lane] = aborted ? 0.f : lh[lane];
-    mt[warp * GT + lane] = aborted ? -INFINITY : th[lane];
-  }
+  consumer_sync(cbar, cphase, lane, err);  // every warp is done with the stage
+  float* mm = mstat;                // [NC][GT] running max (log2 units)
+  float* ml = mstat + NC * GT;      // [NC][GT] running sum relative to mm
+  float* mt = mstat + 2 * NC * GT;  // [NC][GT] largest logit
+#pragma unroll
+  for (int h = 0; h < GT; ++h)  // static indices keep mh/lh/th in registers
+    if (lane == h) {
+      mm[warp * GT + h] = mh[h];
+      ml[warp * GT + h] = lh[h];
+      mt[warp * GT + h] = th[h];
+    }
   if (rg == 0) {
 #pragma unroll
     for (int h = 0; h < GT; ++h)
 #pragma unroll
-      for (int kk = 0; kk < NPL; ++kk)
+      for (int kk = 0; kk < Ly::NPL; ++kk)
 #pragma unroll
-        for (int j2 = 0; j2 < EP2; ++j2) {
-          const float2 a = aborted ? make_float2(0.f, 0.f) : acc[h][kk * EP2 + j2];
-          *reinterpret_cast<float2*>(&ma[(warp * GT + h) * D + (kk * LPR + c) * EPP + 2 * j2]) = a;
-        }
+        for (int j2 = 0; j2 < EP2; ++j2)
+          *reinterpret_cast<float2*>(&macc[(warp * GT + h) * D + (kk * LPR + c) * Ly::EPP + 2 * j2]) =
+              st.acc[h][kk * EP2 + j2];
   }
-  named_bar_sync(1, NC * 32);
-
-  for (int i = threadIdx.x; i < G * D; i += NC * 32) {
+  consumer_sync(cbar, cphase, lane, err);
+  for (int i = warp * 32 + lane; i < G * D; i += NC * 32) {
     const int h = i / D, d = i % D;
     float M = -INFINITY, T = -INFINITY;
 #pragma unroll
@@ -578,62 +502,527 @@ __global__ void __launch_bounds__(Layout<CT, D, GT, BS>::THREADS)
         if (lw > 0.f) {
           const float f = exp2f(mm[w * GT + h] - M);
           lsum += lw * f;
-          o += ma[(w * GT + h) * D + d] * f;
+          o += macc[(w * GT + h) * D + d] * f;
         }
       }
-      o = o / lsum * p.v_scale;
     }
-    const size_t row = (size_t)s * Hq + (size_t)g * G + h;
-    if (p.partials) {
-      const size_t pi = row * p.num_splits + split;
-      const bool any = M != -INFINITY && lsum > 0.f;
-      if (any) p.tmp_out[pi * D + d] = o;
-      if (d == 0) {
-        // report the split's largest logit and the sum relative to it
-        p.max_logits[pi] = any ? T * kLn2 : -INFINITY;
-        p.exp_sums[pi] = any ? lsum * exp2f(M - T) : 0.f;
+    const bool any = M != -INFINITY && lsum > 0.f;
+    sink(h, d, any ? o / lsum * v_scale : 0.f, any ? T * kLn2 : -INFINITY,
+         any ? lsum * exp2f(M - T) : 0.f);
+  }
+  // the merge wrote the stage with ordinary stores; order them before the
+  // bulk copies that will refill it
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  consumer_sync(cbar, cphase, lane, err);
+}
+
+// Attended slots of sequence s (window- and table-limited); flags bad lengths.
+__device__ __forceinline__ int attended_len(const DecodeParams& p, int s, int bs, bool flag) {
+  const int n = p.context_lens[s];
+  const int cap = p.max_blocks_per_seq * bs;
+  if (n < 0) {
+    if (flag) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
+    return 0;
+  }
+  if (p.window > 0) return n < p.window ? n : p.window;
+  if (n > cap) {
+    if (flag) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
+    return cap;
+  }
+  return n;
+}
+
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off /= 2) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+template <typename QT, typename CT, int D, int GT, int BS, int MODE>
+__global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
+                                  Layout<QT, CT, D, GT, BS>::MIN_CTAS)
+    paged_decode_kernel(const __grid_constant__ DecodeParams p) {
+  using Ly = Layout<QT, CT, D, GT, BS>;
+  constexpr int NC = Ly::NC, STAGES = Ly::STAGES, R = Ly::R, TPW = Ly::TPW;
+  extern __shared__ __align__(128) uint8_t smem[];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hq = p.num_heads, Hkv = p.num_kv_heads, G = p.group;
+  const int MB = p.max_blocks_per_seq;
+  pdl_wait();
+  pdl_trigger();
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Ly::OFF_BAR);
+  uint64_t* empty = full + STAGES;
+  uint64_t* cbar = empty + STAGES;  // consumer-to-consumer barrier
+  int4* desc = reinterpret_cast<int4*>(smem + Ly::OFF_DESC);
+  int* misc = reinterpret_cast<int*>(smem + Ly::OFF_MISC);
+
+  // ---------------------------------------------------------- work of this CTA
+  // Both modes end up with: start segment (s0, g0), start page pg0 in it, and
+  // npages pages to stream (crossing segments only in balanced mode).
+  int s0, g0, pg0, npages;
+  if constexpr (MODE == kModeSplit) {
+    const int split = blockIdx.x;
+    g0 = blockIdx.y;
+    s0 = blockIdx.z;
+    const int L = attended_len(p, s0, BS, threadIdx.x == 0 && split == 0 && g0 == 0);
+    const int total = (L + BS - 1) / BS;
+    pg0 = split * p.pages_per_split;
+    npages = min(total, pg0 + p.pages_per_split) - pg0;
+    if (npages <= 0) {  // nothing attended in this split (uniform for the CTA)
+      for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+        const int h = i / D, d = i % D;
+        const size_t row = (size_t)s0 * Hq + (size_t)g0 * G + h;
+        if (p.partials) {
+          if (d == 0) {
+            p.max_logits[row * p.num_splits + split] = -INFINITY;
+            p.exp_sums[row * p.num_splits + split] = 0.f;
+          }
+        } else {
+          reinterpret_cast<QT*>(p.out)[row * D + d] = Elem<QT>::from_f32(0.f);
+        }
       }
-    } else {
-      reinterpret_cast<QT*>(p.out)[row * D + d] = Elem<QT>::from_f32(o);
+      return;
     }
+  } else {
+    const int cta = blockIdx.x, C = gridDim.x, S = p.num_seqs;
+    if (threadIdx.x < kPieceSlots * 4)  // this call's slot records start invalid
+      p.piece_info[(size_t)cta * kPieceSlots * 4 + threadIdx.x] = 0;
+    if (warp == NC) {
+      // total pages, then this CTA's equal share [lo, hi) of the flattened
+      // (sequence, kv head, page) order, then where lo falls
+      long long total = 0;
+      for (int b = 0; b < S; b += 32) {
+        const int s = b + lane;
+        const int pg = s < S ? (attended_len(p, s, BS, false) + BS - 1) / BS : 0;
+        total += warp_sum_int(pg);
+      }
+      const long long P = total * Hkv;
+      const long long lo = (long long)cta * P / C, hi = (long long)(cta + 1) * P / C;
+      int ls0 = 0, lg0 = 0, lpg0 = 0;
+      if (lo < hi) {
+        long long run = 0;  // pages of the sequences before this chunk
+        for (int b = 0; b < S; b += 32) {
+          const int s = b + lane;
+          const int pg = s < S ? (attended_len(p, s, BS, false) + BS - 1) / BS : 0;
+          int incl = pg;  // inclusive prefix within the chunk
+#pragma unroll
+          for (int off = 1; off < 32; off *= 2) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+          }
+          const unsigned hit = __ballot_sync(0xffffffffu, s < S && (run + incl) * Hkv > lo);
+          if (hit) {
+            const int src = __ffs(hit) - 1;
+            const int pgs = __shfl_sync(0xffffffffu, pg, src);
+            const long long before = run + __shfl_sync(0xffffffffu, incl, src) - pgs;
+            const long long rem = lo - before * Hkv;
+            ls0 = b + src;
+            lg0 = static_cast<int>(rem / pgs);
+            lpg0 = static_cast<int>(rem % pgs);
+            break;
+          }
+          run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+      }
+      if (lane == 0) {
+        misc[0] = ls0;
+        misc[1] = lg0;
+        misc[2] = lpg0;
+        misc[3] = static_cast<int>(hi - lo);
+      }
+    }
+    __syncthreads();
+    s0 = misc[0];
+    g0 = misc[1];
+    pg0 = misc[2];
+    npages = misc[3];
+    if (npages <= 0) return;
+  }
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], NC);
+    }
+    mbar_init(cbar, NC);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // ======================================================== producer warp
+  if (warp == NC) {
+    const size_t blk_stride = (size_t)Hkv * Ly::PAGE;
+    const uint32_t qbytes = static_cast<uint32_t>(G) * D * Ly::QB;
+    int s = s0, g = g0, pg = pg0;
+    int L = attended_len(p, s, BS, false);
+    int pages = (L + BS - 1) / BS;
+    int tb_s = -1, tb_base = 0, tbl = -1;  // 32 table entries cached across lanes
+    bool piece_start = true;
+    int piece_flags = 0, piece_end = 0, issued = 0;
+    bool aborted = false;
+    for (int k = 0; k < npages; ++k) {
+      if (s != tb_s || pg < tb_base || pg >= tb_base + 32) {
+        tb_s = s;
+        tb_base = pg;
+        const int idx = pg + lane;
+        tbl = idx < pages ? __ldg(p.block_tables + (size_t)s * MB + idx) : -1;
+      }
+      const int bid = __shfl_sync(0xffffffffu, tbl, pg - tb_base);
+      if (piece_start) {
+        const int len = min(pages - pg, npages - k);
+        piece_end = k + len - 1;
+        piece_flags = (pg == 0 ? kSegFirst : 0) | (pg + len == pages ? kSegLast : 0) |
+                      (k > 0 ? kSlot1 : 0);
+      }
+      const int slot = k % STAGES;
+      if (lane == 0) {
+        if (k >= STAGES && !mbar_wait_bounded(&empty[slot], ((k / STAGES) - 1) & 1)) {
+          raise_error(p.err, PA_DEVERR_TIMEOUT);
+          aborted = true;
+        }
+        if (!aborted) {
+          const bool ok = bid >= 0 && bid < p.num_blocks;
+          if (!ok) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+          const int rows = ok ? min(BS, L - pg * BS) : 0;
+          const int flags = piece_flags | (piece_start ? kFirst : 0) | (k == piece_end ? kLast : 0) |
+                            (k == npages - 1 ? kCtaLast : 0);
+          desc[slot] = make_int4(rows, s * Hkv + g, flags, 0);
+          uint8_t* stage = smem + slot * Ly::STAGE;
+          const uint32_t bytes = (ok ? 2u * Ly::PAGE : 0u) + (piece_start ? qbytes : 0u);
+          if (bytes) {
+            mbar_arrive_expect_tx(&full[slot], bytes);
+            if (ok) {
+              const size_t off = (size_t)bid * blk_stride + (size_t)g * Ly::PAGE;
+              bulk_g2s(stage, p.k_cache + off, Ly::PAGE, &full[slot]);
+              bulk_g2s(stage + Ly::PAGE, p.v_cache + off, Ly::PAGE, &full[slot]);
+            }
+            if (piece_start)
+              bulk_g2s(stage + 2 * Ly::PAGE,
+                       static_cast<const uint8_t*>(p.query) +
+                           ((size_t)s * Hq + (size_t)g * G) * D * Ly::QB,
+                       qbytes, &full[slot]);
+          } else {
+            mbar_arrive(&full[slot]);
+          }
+          ++issued;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, aborted ? 1 : 0, 0)) break;
+      // advance to the next page of the walk
+      piece_start = false;
+      ++pg;
+      if (k == piece_end) {
+        piece_start = true;
+        if constexpr (MODE == kModeBalanced) {
+          if (pg == pages && k + 1 < npages) {
+            pg = 0;
+            if (++g == Hkv) {
+              g = 0;
+              do {
+                ++s;
+                L = attended_len(p, s, BS, false);
+                pages = (L + BS - 1) / BS;
+              } while (pages == 0 && s + 1 < p.num_seqs);
+            }
+          }
+        }
+      }
+    }
+    // never leave the CTA with copies in flight: wait for the last fill of
+    // every stage (already complete in the normal case)
+    if (lane == 0) {
+      for (int k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k)
+        if (!mbar_wait_bounded(&full[k % STAGES], (k / STAGES) & 1))
+          raise_error(p.err, PA_DEVERR_TIMEOUT);
+    }
+    return;
+  }
+
+  // ======================================================== consumer warps
+  const int c = lane % Ly::LPR;   // piece column of the row
+  const int rg = lane / Ly::LPR;  // row within a warp step
+  float* wscr = reinterpret_cast<float*>(smem + Ly::OFF_SCR) + warp * Ly::SCR;
+  float* mstat = reinterpret_cast<float*>(smem + Ly::OFF_MSTAT);
+  uint32_t cphase = 0;
+  PieceState<Ly, GT> st;
+
+  int k = 0;
+  bool aborted = false;
+  while (true) {
+    // up to R pages of the current piece
+    const uint8_t* Kp[R];
+    const uint8_t* Vp[R];
+    int lim[R];
+    int n_here = 0, last_flags = 0, seg = 0, last_slot = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      lim[r] = 0;
+      Kp[r] = smem;
+      Vp[r] = smem;
+      if (aborted || (r > 0 && (last_flags & kLast))) continue;
+      const int slot = (k + r) % STAGES;
+      if (!mbar_wait_bounded(&full[slot], ((k + r) / STAGES) & 1)) {
+        raise_error(p.err, PA_DEVERR_TIMEOUT);
+        aborted = true;
+        continue;
+      }
+      const int4 d = desc[slot];
+      uint8_t* stage = smem + slot * Ly::STAGE;
+      if (r == 0) {
+        seg = d.y;
+        if (d.z & kFirst) begin_piece<QT, Ly, GT, D>(st, stage + 2 * Ly::PAGE, G, c, p.q_scale);
+      }
+      Kp[r] = stage;
+      Vp[r] = stage + Ly::PAGE;
+      lim[r] = d.x - warp * TPW;
+      last_flags = d.z;
+      last_slot = slot;
+      n_here = r + 1;
+    }
+    if (__any_sync(0xffffffffu, aborted)) break;
+
+    process_pages<CT, Ly, GT>(st, Kp, Vp, lim, wscr, warp, lane, c, rg);
+
+    const bool ends_piece = (last_flags & kLast) != 0;
+    if (lane == 0) {
+      for (int r = 0; r < n_here - (ends_piece ? 1 : 0); ++r) mbar_arrive(&empty[(k + r) % STAGES]);
+    }
+    if (ends_piece) {
+      float* macc = Ly::MERGE_IN_STAGE
+                        ? reinterpret_cast<float*>(smem + last_slot * Ly::STAGE)
+                        : reinterpret_cast<float*>(smem + Ly::OFF_MACC);
+      const int s = seg / Hkv, g = seg % Hkv;
+      if constexpr (MODE == kModeSplit) {
+        const int split = blockIdx.x, nsplit = p.num_splits;
+        const bool partials = p.partials != 0;
+        QT* out = reinterpret_cast<QT*>(p.out);
+        float* tmp_out = p.tmp_out;
+        float* max_logits = p.max_logits;
+        float* exp_sums = p.exp_sums;
+        const size_t row0 = (size_t)s * Hq + (size_t)g * G;
+        finish_piece<Ly, GT, D>(
+            st, mstat, macc, cbar, cphase, G, warp, lane, c, rg, p.v_scale, p.err,
+            [=](int h, int d, float o, float m_nat, float l) {
+              const size_t row = row0 + h;
+              if (partials) {
+                const size_t pi = row * nsplit + split;
+                if (l > 0.f) tmp_out[pi * D + d] = o;
+                if (d == 0) {
+                  max_logits[pi] = m_nat;
+                  exp_sums[pi] = l;
+                }
+              } else {
+                out[row * D + d] = Elem<QT>::from_f32(o);
+              }
+            });
+      } else {
+        const bool whole = (last_flags & kSegFirst) && (last_flags & kSegLast);
+        const int pslot = (last_flags & kSlot1) ? 1 : 0;
+        const size_t base = (size_t)blockIdx.x * kPieceSlots + pslot;
+        QT* out = reinterpret_cast<QT*>(p.out) + ((size_t)s * Hq + (size_t)g * G) * D;
+        float* piece_o = p.piece_o + base * GT * D;
+        float* piece_ml = p.piece_ml + base * GT * 2;
+        finish_piece<Ly, GT, D>(
+            st, mstat, macc, cbar, cphase, G, warp, lane, c, rg, p.v_scale, p.err,
+            [=](int h, int d, float o, float m_nat, float l) {
+              if (whole) {
+                out[h * D + d] = Elem<QT>::from_f32(o);
+              } else {
+                piece_o[h * D + d] = o;
+                if (d == 0) {
+                  piece_ml[h * 2 + 0] = m_nat;
+                  piece_ml[h * 2 + 1] = l;
+                }
+              }
+            });
+        if (!whole && warp == 0 && lane == 0) {
+          int* info = p.piece_info + base * 4;
+          info[1] = seg;
+          info[2] = last_flags & (kSegFirst | kSegLast);
+          info[0] = 1;
+        }
+      }
+      if (lane == 0) mbar_arrive(&empty[last_slot]);
+    }
+    k += n_here;
+    if (last_flags & kCtaLast) break;
   }
 }
 
-// Host-side launcher for one instantiation.
-template <typename QT, typename CT, int D, int GT, int BS>
-cudaError_t launch_decode(const DecodeParams& prm, int num_seqs, cudaStream_t stream) {
-  using Ly = Layout<CT, D, GT, BS>;
-  auto kern = paged_decode_kernel<QT, CT, D, GT, BS>;
+// Balanced mode, second kernel: one CTA per decode CTA. The CTA whose piece
+// ends a cut segment combines that segment's pieces by log-sum-exp weights
+// and writes the output; the same CTAs also write zeros for sequences with
+// nothing to attend. The pieces of a segment sit in the consecutive CTAs
+// before the combiner (CTAs with an empty range hold none): warp 0 finds them
+// 32 CTAs at a time with ballots and turns their (max, sum) into weights in
+// shared memory; then every thread sums its output elements over the pieces.
+constexpr int kCombineMaxPieces = kMaxBalancedCtas;
+constexpr int kCombineMaxHeads = 8;
+template <typename OT>
+__global__ void __launch_bounds__(128)
+    combine_pieces_kernel(OT* out, const float* piece_o, const float* piece_ml,
+                          const int* piece_info, const int32_t* context_lens, int num_seqs,
+                          int num_heads, int num_kv_heads, int D, int GT, int bs, int MB,
+                          int window, int num_ctas, unsigned* err) {
+  __shared__ int members[kCombineMaxPieces];    // piece indices (cta * 2 + slot)
+  __shared__ float weights[kCombineMaxHeads * kCombineMaxPieces];  // [head][piece]
+  __shared__ int count;
+  pdl_wait();
+  pdl_trigger();
+  const int c = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int G = num_heads / num_kv_heads;
+  // sequences with no attended slot: zeros (and flag impossible lengths)
+  for (int s = c; s < num_seqs; s += gridDim.x) {
+    const int n = context_lens[s];
+    if (threadIdx.x == 0 && (n < 0 || (window == 0 && n > MB * bs)))
+      raise_error(err, PA_DEVERR_CONTEXT_LEN);
+    if (n <= 0)
+      for (int i = threadIdx.x; i < num_heads * D; i += blockDim.x)
+        out[(size_t)s * num_heads * D + i] = Elem<OT>::from_f32(0.f);
+  }
+  if (c >= num_ctas) return;
+  for (int slot = 0; slot < kPieceSlots; ++slot) {
+    const int* info = piece_info + ((size_t)c * kPieceSlots + slot) * 4;
+    const bool combiner = info[0] == 1 && !(info[2] & kSegFirst) && (info[2] & kSegLast);
+    if (!combiner) continue;  // uniform across the CTA
+    const int seg = info[1];
+    const int s = seg / num_kv_heads, g = seg % num_kv_heads;
+    if (warp == 0) {
+      // walk back in batches of 32 CTAs, collecting the pieces of `seg`
+      int n = 0;
+      if (lane == 0) members[0] = c * kPieceSlots + slot;
+      n = 1;
+      bool done = false;
+      for (int base = c - 1; base >= 0 && !done; base -= 32) {
+        const int cc = base - lane;
+        int pid = -1, first = 0;
+        if (cc >= 0) {
+          const int* i1 = piece_info + ((size_t)cc * kPieceSlots + 1) * 4;
+          const int* i0 = piece_info + ((size_t)cc * kPieceSlots + 0) * 4;
+          if (i1[0] == 1 && i1[1] == seg) {
+            pid = cc * kPieceSlots + 1;
+            first = i1[2] & kSegFirst;
+          } else if (i0[0] == 1 && i0[1] == seg) {
+            pid = cc * kPieceSlots;
+            first = i0[2] & kSegFirst;
+          }
+        }
+        const unsigned firsts = __ballot_sync(0xffffffffu, pid >= 0 && first);
+        // pieces up to and including the segment's first piece (lowest lane
+        // with kSegFirst = nearest to the combiner's side of the walk)
+        const int stop = firsts ? __ffs(firsts) - 1 : 31;
+        const unsigned take = __ballot_sync(0xffffffffu, pid >= 0 && lane <= stop);
+        const int rank = __popc(take & ((1u << lane) - 1));
+        if ((take >> lane) & 1) {
+          if (n + rank < kCombineMaxPieces) members[n + rank] = pid;
+        }
+        n += __popc(take);
+        done = firsts != 0;
+      }
+      if (lane == 0) count = n < kCombineMaxPieces ? n : kCombineMaxPieces;
+      if (lane == 0 && !done && c > 0) raise_error(err, PA_DEVERR_TIMEOUT);  // chain broken
+    }
+    __syncthreads();
+    const int npc = count;
+    // weights of every head at once: warp w takes heads w, w + 4, ...
+    for (int h = warp; h < G; h += blockDim.x / 32) {
+      float M = -INFINITY;
+      for (int i = lane; i < npc; i += 32) {
+        const size_t b = (size_t)members[i] * GT + h;
+        if (piece_ml[b * 2 + 1] > 0.f) M = fmaxf(M, piece_ml[b * 2]);
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off /= 2) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      float wsum = 0.f;
+      for (int i = lane; i < npc; i += 32) {
+        const size_t b = (size_t)members[i] * GT + h;
+        const float l = piece_ml[b * 2 + 1];
+        const float w = (l > 0.f && M != -INFINITY) ? l * expf(piece_ml[b * 2] - M) : 0.f;
+        weights[h * kCombineMaxPieces + i] = w;
+        wsum += w;
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off /= 2) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+      __syncwarp();
+      for (int i = lane; i < npc; i += 32) weights[h * kCombineMaxPieces + i] *= inv;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+      const int h = e / D, d = e % D;
+      float acc = 0.f;
+      for (int i = 0; i < npc; ++i) {
+        const float w = weights[h * kCombineMaxPieces + i];
+        if (w > 0.f) acc = fmaf(w, piece_o[((size_t)members[i] * GT + h) * D + d], acc);
+      }
+      out[((size_t)s * num_heads + (size_t)g * G + h) * D + d] = Elem<OT>::from_f32(acc);
+    }
+    __syncthreads();
+  }
+}
+
+// Host side: launch one instantiation in the given mode. In balanced mode a
+// grid.x of 0 asks for the kernel's resident capacity (SMs x CTAs per SM,
+// at most kMaxBalancedCtas); the grid size used is returned in *ctas.
+template <typename QT, typename CT, int D, int GT, int BS, int MODE>
+cudaError_t launch_decode(const DecodeParams& prm, dim3 grid, int* ctas, cudaStream_t stream) {
+  using Ly = Layout<QT, CT, D, GT, BS>;
+  auto kern = paged_decode_kernel<QT, CT, D, GT, BS, MODE>;
   static int configured_devices = 0;  // bit per device id < 32
+  static int capacity[32] = {};       // resident CTAs per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 32 || !(__atomic_load_n(&configured_devices, __ATOMIC_ACQUIRE) & (1 << dev))) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
     if (e != cudaSuccess) return e;
-    if (dev < 32) __atomic_fetch_or(&configured_devices, 1 << dev, __ATOMIC_RELEASE);
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Ly::THREADS, Ly::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long C = (long long)sms * (per_sm > 0 ? per_sm : 1);
+    if (dev < 32) {
+      capacity[dev] = static_cast<int>(C < kMaxBalancedCtas ? C : kMaxBalancedCtas);
+      __atomic_fetch_or(&configured_devices, 1 << dev, __ATOMIC_RELEASE);
+    }
   }
-  dim3 grid(prm.num_splits, prm.num_kv_heads, num_seqs);
+  if (MODE == kModeBalanced && grid.x == 0)
+    grid.x = dev < 32 && capacity[dev] > 0 ? capacity[dev] : kMaxBalancedCtas;
+  if (ctas) *ctas = static_cast<int>(grid.x);
   return launch_pdl(kern, grid, dim3(Ly::THREADS), Ly::SMEM, stream, prm);
 }
 
 // Dispatch over (head_dim, group bucket, block size) for one (QT, CT) pair.
 template <typename QT, typename CT>
-cudaError_t dispatch_decode(const DecodeParams& prm, int num_seqs, int D, int GT, int BS,
-                            cudaStream_t stream) {
-#define PA_CASE_BS(D_, GT_)                                                               \
-  switch (BS) {                                                                           \
-    case 16: return launch_decode<QT, CT, D_, GT_, 16>(prm, num_seqs, stream);            \
-    case 32: return launch_decode<QT, CT, D_, GT_, 32>(prm, num_seqs, stream);            \
-    case 64: return launch_decode<QT, CT, D_, GT_, 64>(prm, num_seqs, stream);            \
-    default: return cudaErrorInvalidValue;                                                \
+cudaError_t dispatch_decode(const DecodeParams& prm, dim3 grid, int D, int GT, int BS, int mode,
+                            int* ctas, cudaStream_t stream) {
+#define PA_CASE_BS(D_, GT_)                                                                     \
+  switch (BS) {                                                                                 \
+    case 16:                                                                                    \
+      return mode == kModeSplit                                                                 \
+                 ? launch_decode<QT, CT, D_, GT_, 16, kModeSplit>(prm, grid, ctas, stream)      \
+                 : launch_decode<QT, CT, D_, GT_, 16, kModeBalanced>(prm, grid, ctas, stream);  \
+    case 32:                                                                                    \
+      return mode == kModeSplit                                                                 \
+                 ? launch_decode<QT, CT, D_, GT_, 32, kModeSplit>(prm, grid, ctas, stream)      \
+                 : launch_decode<QT, CT, D_, GT_, 32, kModeBalanced>(prm, grid, ctas, stream);  \
+    case 64:                                                                                    \
+      return mode == kModeSplit                                                                 \
+                 ? launch_decode<QT, CT, D_, GT_, 64, kModeSplit>(prm, grid, ctas, stream)      \
+                 : launch_decode<QT, CT, D_, GT_, 64, kModeBalanced>(prm, grid, ctas, stream);  \
+    default:                                                                                    \
+      return cudaErrorInvalidValue;                                                             \
   }
-#define PA_CASE_GT(D_)                  \
-  switch (GT) {                         \
-    case 1: PA_CASE_BS(D_, 1)           \
-    case 2: PA_CASE_BS(D_, 2)           \
-    case 4: PA_CASE_BS(D_, 4)           \
-    case 8: PA_CASE_BS(D_, 8)           \
+#define PA_CASE_GT(D_)                     \
+  switch (GT) {                            \
+    case 1: PA_CASE_BS(D_, 1)              \
+    case 2: PA_CASE_BS(D_, 2)              \
+    case 4: PA_CASE_BS(D_, 4)              \
+    case 8: PA_CASE_BS(D_, 8)              \
     default: return cudaErrorInvalidValue; \
   }
   switch (D) {
@@ -650,8 +1039,8 @@ cudaError_t dispatch_decode(const DecodeParams& prm, int num_seqs, int D, int GT
 
 // One translation unit per (query dtype, cache dtype) pair defines these.
 #define PA_DECLARE_DISPATCH(NAME)                                                       \
-  cudaError_t NAME(const pa::DecodeParams& prm, int num_seqs, int D, int GT, int BS,   \
-                   cudaStream_t stream)
+  cudaError_t NAME(const pa::DecodeParams& prm, dim3 grid, int D, int GT, int BS,      \
+                   int mode, int* ctas, cudaStream_t stream)
 PA_DECLARE_DISPATCH(pa_dispatch_decode_f32_f32);
 PA_DECLARE_DISPATCH(pa_dispatch_decode_bf16_bf16);
 PA_DECLARE_DISPATCH(pa_dispatch_decode_f16_f16);

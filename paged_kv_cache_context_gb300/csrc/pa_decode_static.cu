@@ -1,13 +1,14 @@
 // pa_decode_static.cu -- pa_decode_static_scratch: paged decode for callers that
 // cannot allocate device memory.
 //
-// pa_decode needs a caller-provided workspace for the partial results of its
-// context splits. Some callers have no way to provide one: code embedded in a
-// host application that owns every device allocation and exposes no allocator,
-// or code that must not call cudaMalloc at all (its implicit synchronisation and
-// unbounded latency are not acceptable where it runs). For them this entry point
-// keeps the split partials in a fixed array that the library itself carries in
-// device memory, and otherwise runs exactly the kernels pa_decode runs.
+// pa_decode needs a caller-provided workspace for the partial results of the
+// contexts its persistent CTAs share. Some callers have no way to provide one:
+// code embedded in a host application that owns every device allocation and
+// exposes no allocator, or code that must not call cudaMalloc at all (its
+// implicit synchronisation and unbounded latency are not acceptable where it
+// runs). For them this entry point keeps those partials in a fixed array that
+// the library itself carries in device memory, and otherwise runs exactly the
+// kernels pa_decode runs.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -62,9 +63,9 @@ PA_API pa_status pa_decode_static_scratch(void* out, const void* query, const vo
     if (scratch_on_current_device(&scratch) != cudaSuccess) return PA_ERR_CUDA;
     scratch_bytes = PA_STATIC_SCRATCH_BYTES;
   }
-  // Nothing in the array has to start at zero: every split writes its own
-  // max/sum entries (and, when it holds tokens, its partial row) before the
-  // reduction of the same call reads them.
+  // Nothing in the array has to start at zero: every decode CTA first marks
+  // its partial slots empty, then fills the ones it uses, before the combine
+  // launch of the same call reads them.
   return pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads,
                    num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale,
                    window, q_dtype, kv_dtype, k_scale, v_scale, scratch, scratch_bytes, stream);

@@ -53,6 +53,11 @@ def lib() -> ctypes.CDLL:
             "pa_decode_partials": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F,
                                    F, I, I, P],
             "pa_reduce": [P, P, P, P, I, I, I, I, I, P],
+            "pa_decode_balanced": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F, F, P,
+                                   Z, P, P],
+            "pa_decode_combine": [P, P, I, I, I, I, I, I, I, I, P, Z, I, P],
+            "pa_decode_static_scratch": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F,
+                                         F, P],
             "pa_get_device_error": [P, P],
             "pa_status_string": [I],
             "pa_version": [],
@@ -143,6 +148,36 @@ def decode(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor, v_cach
                            _ptr(block_tables), _ptr(context_lens), S, Hq, num_kv_heads, D, bs, NB,
                            MB, scale, window, _DTYPE[query.dtype], _KV[kv_dtype], k_scale,
                            v_scale, _ptr(workspace), ws_bytes, _stream(stream)), "pa_decode")
+
+
+def decode_balanced(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+                    v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                    num_kv_heads: int, scale: float, workspace: torch.Tensor, window: int = 0,
+                    kv_dtype: str = "auto", k_scale: float = 1.0, v_scale: float = 1.0,
+                    stream=None) -> int:
+    """pa_decode_balanced: first launch of the balanced path; returns num_ctas."""
+    S, Hq, D = query.shape
+    NB, _, bs, _ = k_cache.shape
+    MB = block_tables.shape[1]
+    n = ctypes.c_int()
+    _check(lib().pa_decode_balanced(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(block_tables), _ptr(context_lens), S, Hq, num_kv_heads,
+                                    D, bs, NB, MB, scale, window, _DTYPE[query.dtype],
+                                    _KV[kv_dtype], k_scale, v_scale, _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    ctypes.addressof(n), _stream(stream)), "pa_decode_balanced")
+    return n.value
+
+
+def decode_combine(out: torch.Tensor, context_lens: torch.Tensor, num_kv_heads: int,
+                   block_size: int, max_blocks_per_seq: int, workspace: torch.Tensor,
+                   num_ctas: int, window: int = 0, stream=None):
+    """pa_decode_combine: second launch of the balanced path."""
+    S, Hq, D = out.shape
+    _check(lib().pa_decode_combine(_ptr(out), _ptr(context_lens), S, Hq, num_kv_heads, D,
+                                   block_size, max_blocks_per_seq, window, _DTYPE[out.dtype],
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   num_ctas, _stream(stream)), "pa_decode_combine")
 
 
 def decode_partials(tmp_out: torch.Tensor, max_logits: torch.Tensor, exp_sums: torch.Tensor,

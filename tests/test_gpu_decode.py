@@ -199,3 +199,38 @@ def test_bad_block_id_and_context_len_are_flagged_not_faulted():
     gpu_decode(case, kg, vg, context_lens=cl)
     assert device_errors() & 4
     assert torch.isfinite(out.float()).all()
+
+
+# ------------------------------------------------------------ balanced path cuts
+def test_balanced_one_context_cut_across_every_cta():
+    """A single 98k-token context: every persistent CTA holds a piece of it,
+    and the combine walks the whole chain of partials."""
+    case = wl.make_case("long", 96, 1, 4, 1, 128, lens=[98_000], q_dtype=torch.float32,
+                        max_blocks_per_seq=-(-98_000 // 32))
+    check_case(case, splits=(True,))
+
+
+def test_balanced_thousands_of_tiny_contexts_with_empty_ones():
+    g = torch.Generator().manual_seed(97)
+    lens = torch.randint(0, 41, (3000,), generator=g)
+    lens[::7] = 0  # empty sequences interleaved
+    case = wl.make_case("tiny_many", 98, 3000, 8, 2, 64, lens=lens.tolist(),
+                        q_dtype=torch.bfloat16, max_blocks_per_seq=2)
+    check_case(case)
+
+
+def test_balanced_two_launch_form_equals_pa_decode():
+    case = wl.make_case("two", 99, 9, 32, 8, 128, len_range=(1, 3000), max_blocks_per_seq=94)
+    kg, vg = gpu_caches(case)
+    ref = gpu_decode(case, kg, vg, split=True)
+    nbytes = pa.decode_workspace_size(case.num_seqs, case.num_heads, case.num_kv_heads,
+                                      case.head_dim, case.block_size, case.max_blocks_per_seq)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    out = torch.full_like(ref, float("nan"))
+    n = pa.decode_balanced(out, to_dev(case.query), kg, vg, to_dev(case.block_tables),
+                           to_dev(case.context_lens), case.num_kv_heads, case.scale, ws)
+    assert n > 0
+    pa.decode_combine(out, to_dev(case.context_lens), case.num_kv_heads, case.block_size,
+                      case.max_blocks_per_seq, ws, n)
+    assert torch.equal(bits(out), bits(ref))
+    assert device_errors() == 0

@@ -65,14 +65,16 @@ def test_static_scratch_matches_pa_decode_on_two_calls_in_a_row():
     assert device_errors() == 0
 
 
-def test_static_scratch_refuses_plans_beyond_its_size():
-    """512 sequences of up to 131072 tokens on one kv head need ~134 MB of
-    partials: refused with PA_ERR_WORKSPACE before anything is enqueued (the
-    pointers below are never dereferenced)."""
+def test_static_scratch_refuses_sizes_beyond_its_array():
+    """Partial storage grows with the head dimension: head_dim 2048 with 8
+    query heads per kv head would need ~80 MB, more than the fixed array, so
+    the call is refused with PA_ERR_WORKSPACE before anything is enqueued (the
+    pointers below are never dereferenced). Every supported shape fits."""
     f = _fn()
-    need = pa.decode_workspace_size(512, 8, 1, 128, 32, 4096, 0)
+    need = pa.decode_workspace_size(4, 64, 8, 2048, 32, 16, 0)
     assert need > STATIC_SCRATCH_BYTES
+    for Hq, Hkv, D in [(64, 8, 128), (32, 32, 96), (16, 16, 64)]:
+        assert pa.decode_workspace_size(4, Hq, Hkv, D, 32, 16, 0) <= STATIC_SCRATCH_BYTES
     P = 4096
-    rc = f(P, P, P, P, P, P, 512, 8, 1, 128, 32, 100000, 4096, 0.1, 0, pa.PA_BF16, 0, 1.0,
-           1.0, None)
+    rc = f(P, P, P, P, P, P, 4, 64, 8, 2048, 32, 100, 16, 0.1, 0, pa.PA_BF16, 0, 1.0, 1.0, None)
     assert rc == -7 and "workspace" in pa.status_string(rc)
