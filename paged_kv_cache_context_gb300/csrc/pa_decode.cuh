@@ -138,7 +138,9 @@ struct Layout {
   static constexpr int RPW = 32 / LPR;     // rows a warp covers per step
   static constexpr int NST = TPW / RPW;    // steps per page
   // pages a consumer warp takes per iteration (one weight round per R pages)
-  static constexpr int R = (2 * PAGE <= 16384) ? PA_PAGES_PER_ITER : 1;
+  static constexpr int R = (2 * PAGE <= 8192)    ? 2 * PA_PAGES_PER_ITER
+                           : (2 * PAGE <= 16384) ? PA_PAGES_PER_ITER
+                                                 : 1;
   static constexpr int TPI = TPW * R;      // rows per warp per iteration
   static constexpr int NSTI = NST * R;     // steps per iteration
   static constexpr int SG = cmin(NSTI, cmax(1, 8 / GT));   // steps per reduction group
