@@ -45,6 +45,35 @@ METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak) and seqs/s
 NOMINAL_HBM_GBS = 8000.0
 
 
+# ------------------------------------------------------------------ traffic
+def csrc_digest() -> str:
+    """First 16 hex digits of sha256 over the library's CUDA sources."""
+    import glob
+    import hashlib
+    m = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_context_gb300", "csrc", "*"))):
+        m.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu capture of this
+    workload, or None when there is none or the sources changed since."""
+    path = os.path.join(ROOT, "profiles", "paged_decode_kernel_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = csrc_digest()
+    with open(path) as fh:
+        for line in fh:
+            parts = line.split()
+            if len(parts) == 3 and not line.startswith("#") and parts[0] == workload \
+                    and parts[1] == digest:
+                return int(parts[2])
+    return None
+
+
 # ------------------------------------------------------------------ ranks
 def rank_info():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
@@ -344,7 +373,8 @@ def run_ours(args, rank, local_rank, world):
         "pct_of_nominal_8tbs": round(100 * bytes_all / elapsed_max / 1e9 / NOMINAL_HBM_GBS, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": None, "kernel": "paged_decode_kernel (balanced mode)",
+                     "traffic": measured_traffic(args.workload),
+                     "kernel": "paged_decode_kernel (balanced mode)",
                      "kernel_bytes_per_launch": sb["kernel"],
                      "kernel_us_mean": round(split_mean * 1e6, 2),
                      "kernel_us_median": round(statistics.median(split_ms) * 1e3, 2)},
