@@ -3,9 +3,10 @@
 
 A step is one pass of the whole decode hot path over one batch: the cache
 write of every sequence's new token (pa_reshape_and_cache), then the two
-launches of pa_decode's balanced path: the persistent decode
-(pa_decode_balanced) and the combine of contexts cut between CTAs
-(pa_decode_combine). Default workload: the
+stream operations of pa_decode's balanced path: the zero fill of the arrival
+counters (pa_decode_workspace_clear) and the persistent decode launch
+(pa_decode_balanced), whose CTAs also combine the contexts cut between them.
+Default workload: the
 Mistral-7B-shaped bf16 batch (32 sequences, 32 query / 8 kv heads, head_dim
 128, block_size 32, context lengths U[512, 4096], shuffled block pool).
 
@@ -287,25 +288,22 @@ def run_ours(args, rank, local_rank, world):
                          I(Hkv), I(D), I(bs), I(NB), I(MB), F(case.scale), I(case.window), I(qd),
                          I(kvd), F(case.k_scale), F(case.v_scale), ptr(ws), Z(ws_bytes),
                          P(ctypes.addressof(num_ctas)), sp))
-    f_write, f_dec, f_comb = L.pa_reshape_and_cache, L.pa_decode_balanced, L.pa_decode_combine
-    # the decode grid size is fixed for these sizes: learn it once
-    if f_dec(*dec_args[0]):
+    f_write, f_clear, f_dec = (L.pa_reshape_and_cache, L.pa_decode_workspace_clear,
+                               L.pa_decode_balanced)
+    clear_args = (ptr(ws), Z(ws_bytes), sp)
+    if f_clear(*clear_args) or f_dec(*dec_args[0]):
         raise RuntimeError("pa_decode_balanced failed")
-    comb_args = (ptr(out), ptr(cl), I(S), I(Hq), I(Hkv), I(D), I(bs), I(MB), I(case.window),
-                 I(qd), ptr(ws), Z(ws_bytes), I(num_ctas.value), sp)
-    if f_comb(*comb_args):
-        raise RuntimeError("pa_decode_combine failed")
-    launches_per_step = 3
+    launches_per_step = 3  # cache write, counter clear, decode
 
     def step(i, ev_a=None, ev_b=None):
         r = i % len(reps)
         rc = f_write(*write_args[r])
+        rc |= f_clear(*clear_args)
         if ev_a is not None:
             ev_a.record(stream)
         rc |= f_dec(*dec_args[r])
         if ev_b is not None:
             ev_b.record(stream)
-        rc |= f_comb(*comb_args)
         if rc:
             raise RuntimeError(f"library call failed: {rc}")
 

@@ -162,11 +162,11 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
  *                W / bs blocks per sequence in block_tables[s][0 .. W/bs-1]).
  * workspace    : device scratch of workspace_bytes (may be NULL / 0). With
  *                at least pa_decode_workspace_size() bytes the call runs the
- *                balanced path (pa_decode_balanced then pa_decode_combine):
- *                one persistent CTA per resident slot, each streaming an equal
- *                share of all sequences' pages; otherwise one CTA per
- *                (sequence, kv head) does that whole context. Contents on
- *                entry do not matter; on exit undefined.
+ *                balanced path (pa_decode_workspace_clear, then one launch of
+ *                pa_decode_balanced): one persistent CTA per resident slot,
+ *                each streaming an equal share of all sequences' pages;
+ *                otherwise one CTA per (sequence, kv head) does that whole
+ *                context. Contents on entry do not matter; on exit undefined.
  * Supported: D in {64, 96, 128}; bs in {16, 32, 64}; G = Hq/Hkv in 1..8;
  * q_dtype F32/BF16/F16; AUTO caches hold q_dtype. Pointers 16-byte aligned.
  */
@@ -192,32 +192,41 @@ pa_status pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head
 
 /*
  * Bytes of workspace for pa_decode's balanced path (and for
- * pa_decode_balanced / pa_decode_combine). It depends only on the query-head
- * group size and head_dim, not on the batch: partial results of at most two
- * pieces per persistent CTA (about 2.6 MB for G = 4, D = 128). 0 for invalid
- * head counts.
+ * pa_decode_balanced). It depends only on the query-head group size and
+ * head_dim, not on the batch: one arrival counter per persistent CTA, then
+ * the partial results of at most two pieces per persistent CTA (about 2.5 MB
+ * for G = 4, D = 128). 0 for invalid head counts.
  */
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                 int head_dim, int block_size,
                                 int max_blocks_per_seq, int window);
 
 /*
- * pa_decode_balanced / pa_decode_combine -- the two launches of pa_decode's
- * balanced path, exposed so a caller can time or interleave them.
+ * pa_decode_workspace_clear / pa_decode_balanced -- pa_decode's balanced path
+ * as its two stream operations, exposed so a caller can time the decode
+ * kernel alone or clear the workspace once for several decodes.
  *
- * pa_decode_balanced: the pages of every (sequence, kv head) context, taken
- * in (sequence, kv head, page) order, are cut into C equal contiguous ranges,
- * C = the kernel's resident capacity on this device (written to *num_ctas);
- * persistent CTA c streams range c. A context lying wholly inside one range
- * is written to `out` by that CTA; a context cut by range boundaries leaves
- * per-CTA partials (max logit, sum, normalised output) in the workspace.
- * pa_decode_combine: combines those partials by log-sum-exp weights into
- * `out`, and writes zeros for sequences with nothing to attend. It must follow
- * pa_decode_balanced on the same stream with the same workspace, sizes and
- * num_ctas. Arguments and errors otherwise as pa_decode (workspace required:
- * PA_ERR_NULL when missing, PA_ERR_WORKSPACE when smaller than
- * pa_decode_workspace_size()).
+ * pa_decode_workspace_clear: enqueues a zero fill of the workspace's arrival
+ * counters (its first 2560 bytes). Errors: PA_ERR_NULL, PA_ERR_WORKSPACE
+ * (fewer bytes), PA_ERR_ALIGN, PA_ERR_CUDA.
+ *
+ * pa_decode_balanced: one launch. The pages of every (sequence, kv head)
+ * context, taken in (sequence, kv head, page) order, are cut into C equal
+ * contiguous ranges, C = the kernel's resident capacity on this device
+ * (written to *num_ctas); persistent CTA c streams range c. A context lying
+ * wholly inside one range is written to `out` by that CTA. A context cut by
+ * range boundaries leaves per-CTA partials (max logit, sum, normalised
+ * output) in the workspace; each CTA then adds the pages of its partial to the
+ * context's arrival counter, and the CTA whose addition completes the context
+ * combines the partials by log-sum-exp weights into `out` and sets the
+ * counter back to zero. Sequences with nothing to attend get zero rows.
+ * Precondition: the arrival counters are zero when the kernel starts, as
+ * pa_decode_workspace_clear leaves them and as every launch that raised no
+ * device error leaves them. Arguments and errors otherwise as pa_decode
+ * (workspace required: PA_ERR_NULL when missing, PA_ERR_WORKSPACE when smaller
+ * than pa_decode_workspace_size()).
  */
+pa_status pa_decode_workspace_clear(void* workspace, size_t workspace_bytes, pa_stream_t stream);
 pa_status pa_decode_balanced(void* out, const void* query,
                              const void* k_cache, const void* v_cache,
                              const int32_t* block_tables, const int32_t* context_lens,
@@ -227,11 +236,6 @@ pa_status pa_decode_balanced(void* out, const void* query,
                              float k_scale, float v_scale,
                              void* workspace, size_t workspace_bytes, int* num_ctas,
                              pa_stream_t stream);
-pa_status pa_decode_combine(void* out, const int32_t* context_lens,
-                            int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-                            int block_size, int max_blocks_per_seq, int window,
-                            pa_dtype out_dtype, const void* workspace, size_t workspace_bytes,
-                            int num_ctas, pa_stream_t stream);
 
 /*
  * pa_decode_partials -- the split phase of pa_decode with an explicit plan.
@@ -292,7 +296,8 @@ pa_status pa_reduce(void* out, const float* tmp_out, const float* max_logits,
  *    array's device address once (cudaGetSymbolAddress); make that first call
  *    on each device before any stream capture begins.
  *  - Sharing: all calls on a device share the one array, which keeps whatever
- *    the last call left in it. Nothing in it needs to start at zero. Calls
+ *    the last call left in it. Nothing in it needs to start at zero (each call
+ *    clears the counters it relies on). Calls
  *    whose kernels may overlap on the GPU (different streams, or different
  *    host threads, without ordering between them) race on it and must be
  *    serialised by the caller.

@@ -51,6 +51,15 @@ constexpr int kMaxPagesPerSplit = 64;
 static int group_bucket(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8; }
 
 // ================================================================ kernels
+// Zero fill of the balanced path's arrival counters. It waits for the
+// previous kernel on the stream (which may be a decode still counting into
+// them) and lets the next one launch early.
+__global__ void clear_counters_kernel(int* counters, int n) {
+  pdl_wait();
+  pdl_trigger();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) counters[i] = 0;
+}
+
 // slot = block_tables[s][r / bs] * bs + r % bs, r = pos (mod W for a ring)
 __global__ void slot_mapping_kernel(int64_t* out, const int32_t* block_tables,
                                     const int32_t* seq_idx, const int32_t* positions, int T,
@@ -296,48 +305,31 @@ static cudaError_t run_decode(const DecodeParams& prm, const DecodeShape& a, dim
   }
 }
 
-// Balanced-mode workspace: per decode CTA two partial slots of GT rows of D
-// floats, their (max, sum) pairs and four ints of slot record.
+// Balanced-mode workspace: first the arrival counters (one int per possible
+// decode CTA), then per decode CTA two partial slots of GT rows of D floats
+// and their (max, sum) pairs. Only the counters need a known value (zero) at
+// launch; pa_decode_workspace_clear sets them.
 struct BalancedWs {
+  int* arrived;
   float* piece_o;
   float* piece_ml;
-  int* piece_info;
 };
+static constexpr size_t kCounterBytes = (kMaxBalancedCtas * 4 + 255) / 256 * 256;
+static_assert(kCounterBytes == 2560, "the header documents 2560 bytes of counters");
 static size_t balanced_bytes(int GT, int D) {
   const size_t slots = (size_t)kMaxBalancedCtas * kPieceSlots;
-  return align256(slots * GT * D * 4) + align256(slots * GT * 2 * 4) + align256(slots * 4 * 4);
+  return kCounterBytes + align256(slots * GT * D * 4) + align256(slots * GT * 2 * 4);
 }
 static BalancedWs balanced_carve(void* ws, int GT, int D) {
   const size_t slots = (size_t)kMaxBalancedCtas * kPieceSlots;
   uint8_t* b = static_cast<uint8_t*>(ws);
   BalancedWs w;
+  w.arrived = reinterpret_cast<int*>(b);
+  b += kCounterBytes;
   w.piece_o = reinterpret_cast<float*>(b);
   b += align256(slots * GT * D * 4);
   w.piece_ml = reinterpret_cast<float*>(b);
-  b += align256(slots * GT * 2 * 4);
-  w.piece_info = reinterpret_cast<int*>(b);
   return w;
-}
-
-static cudaError_t run_combine(void* out, const BalancedWs& w, const int32_t* cl, int S, int Hq,
-                               int Hkv, int D, int GT, int bs, int MB, int window, int ctas,
-                               int dt, unsigned* err, cudaStream_t st) {
-  const dim3 grid(static_cast<unsigned>(ctas > 0 ? ctas : 1)), block(128);
-  switch (dt) {
-    case PA_F32:
-      return launch_pdl(combine_pieces_kernel<float>, grid, block, 0, st, static_cast<float*>(out),
-                        (const float*)w.piece_o, (const float*)w.piece_ml, (const int*)w.piece_info,
-                        cl, S, Hq, Hkv, D, GT, bs, MB, window, ctas, err);
-    case PA_BF16:
-      return launch_pdl(combine_pieces_kernel<__nv_bfloat16>, grid, block, 0, st,
-                        static_cast<__nv_bfloat16*>(out), (const float*)w.piece_o,
-                        (const float*)w.piece_ml, (const int*)w.piece_info, cl, S, Hq, Hkv, D, GT,
-                        bs, MB, window, ctas, err);
-    default:
-      return launch_pdl(combine_pieces_kernel<__half>, grid, block, 0, st, static_cast<__half*>(out),
-                        (const float*)w.piece_o, (const float*)w.piece_ml, (const int*)w.piece_info,
-                        cl, S, Hq, Hkv, D, GT, bs, MB, window, ctas, err);
-  }
 }
 
 static DecodeParams make_params(const DecodeShape& a, const void* query, const void* kc,
@@ -586,7 +578,7 @@ PA_API pa_status pa_decode_balanced(void* out, const void* query, const void* k_
   p.out = out;
   p.piece_o = w.piece_o;
   p.piece_ml = w.piece_ml;
-  p.piece_info = w.piece_info;
+  p.arrived = w.arrived;
   p.num_splits = 1;
   p.pages_per_split = 1;
   int ctas = 0;
@@ -597,25 +589,14 @@ PA_API pa_status pa_decode_balanced(void* out, const void* query, const void* k_
   return PA_OK;
 }
 
-PA_API pa_status pa_decode_combine(void* out, const int32_t* context_lens, int num_seqs,
-                                   int num_heads, int num_kv_heads, int head_dim, int block_size,
-                                   int max_blocks_per_seq, int window, pa_dtype out_dtype,
-                                   const void* workspace, size_t workspace_bytes, int num_ctas,
-                                   pa_stream_t stream) {
-  if (num_seqs < 0) return PA_ERR_SHAPE;
-  if (num_seqs == 0) return PA_OK;
-  if (!out || !context_lens || !workspace) return PA_ERR_NULL;
-  if (!valid_dtype(out_dtype)) return PA_ERR_DTYPE;
-  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
-      num_heads / num_kv_heads > 8 || num_ctas < 1 || num_ctas > kMaxBalancedCtas)
-    return PA_ERR_SHAPE;
-  if (head_dim != 64 && head_dim != 96 && head_dim != 128) return PA_ERR_HEAD_DIM;
-  const int GT = group_bucket(num_heads / num_kv_heads);
-  if (workspace_bytes < balanced_bytes(GT, head_dim)) return PA_ERR_WORKSPACE;
-  const BalancedWs w = balanced_carve(const_cast<void*>(workspace), GT, head_dim);
-  return run_combine(out, w, context_lens, num_seqs, num_heads, num_kv_heads, head_dim, GT,
-                     block_size, max_blocks_per_seq, window, num_ctas, out_dtype, error_word(),
-                     reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+PA_API pa_status pa_decode_workspace_clear(void* workspace, size_t workspace_bytes,
+                                           pa_stream_t stream) {
+  if (!workspace) return PA_ERR_NULL;
+  if (workspace_bytes < kCounterBytes) return PA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return PA_ERR_ALIGN;
+  return launch_pdl(clear_counters_kernel, dim3(1), dim3(256), 0,
+                    reinterpret_cast<cudaStream_t>(stream), static_cast<int*>(workspace),
+                    static_cast<int>(kCounterBytes / 4)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }
@@ -634,14 +615,12 @@ PA_API pa_status pa_decode(void* out, const void* query, const void* k_cache,
   const int GT = group_bucket(num_heads / num_kv_heads);
   if (workspace && workspace_bytes >= balanced_bytes(GT, head_dim) && aligned16(workspace)) {
     int ctas = 0;
-    rc = pa_decode_balanced(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs,
-                            num_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                            max_blocks_per_seq, scale, window, q_dtype, kv_dtype, k_scale, v_scale,
-                            workspace, workspace_bytes, &ctas, stream);
+    rc = pa_decode_workspace_clear(workspace, workspace_bytes, stream);
     if (rc != PA_OK) return rc;
-    return pa_decode_combine(out, context_lens, num_seqs, num_heads, num_kv_heads, head_dim,
-                             block_size, max_blocks_per_seq, window, q_dtype, workspace,
-                             workspace_bytes, ctas, stream);
+    return pa_decode_balanced(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                              num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                              max_blocks_per_seq, scale, window, q_dtype, kv_dtype, k_scale,
+                              v_scale, workspace, workspace_bytes, &ctas, stream);
   }
   // no usable workspace: one CTA per (sequence, kv head), straight to the output
   DecodeParams p = make_params(a, query, k_cache, v_cache, block_tables, context_lens, scale,

@@ -16,7 +16,10 @@
 //    break, crossing segment boundaries. A segment lying wholly inside one
 //    range is finished by that CTA; a segment cut by range boundaries leaves
 //    a partial in each CTA it touches (at most two per CTA: its first and
-//    its last piece), combined afterwards by combine_pieces_kernel.
+//    its last piece). A CTA publishes such a partial, then adds its page
+//    count to the segment's arrival counter; the CTA that completes the
+//    count combines the segment's partials and writes the output. No CTA
+//    waits for another, so nothing depends on the CTAs being co-resident.
 //
 // CTA structure (both modes):
 //  * producer warp (last warp): walks the CTA's pages; per page it issues 1-D
@@ -84,7 +87,8 @@ struct DecodeParams {
   float* exp_sums;      // [S][Hq][NS]
   float* piece_o;       // balanced mode: [C][2][GT][D]
   float* piece_ml;      // [C][2][GT][2]: max logit (natural log), sum relative to it
-  int* piece_info;      // [C][2][4]: valid, segment, flags, 0
+  int* arrived;         // [C]: pages of a cut segment whose pieces are published,
+                        // at the CTA holding the segment's last page (zero at launch)
   // inputs
   const void* query;    // [S][Hq][D] of QT
   const uint8_t* k_cache;
@@ -167,7 +171,8 @@ struct Layout {
   static constexpr int OFF_MSTAT = OFF_SCR + NC * SCR * 4;  // [3][NC][GT]
   static constexpr int OFF_MACC = round_up(OFF_MSTAT + 3 * NC * GT * 4, 16);
   static constexpr int OFF_MISC = OFF_MACC + (MERGE_IN_STAGE ? 0 : MACC);
-  static constexpr int SMEM = OFF_MISC + 16;
+  // misc: 4 ints, 2 int64 (range start, total pages), 2 cut-piece records
+  static constexpr int SMEM = OFF_MISC + 32 + 2 * 24;
   // CTAs per SM to plan registers for: what the shared memory allows (228 KB
   // per SM, 1 KB reserved per CTA), at most 4, and no more than keeps a
   // register budget per thread (96 for one or two heads per kv head, else
@@ -183,7 +188,7 @@ struct Layout {
   static_assert(PAGE % 16 == 0, "bulk copies move multiples of 16 bytes");
   static_assert(STAGE % 128 == 0 && OFF_BAR % 8 == 0, "stage and mbarrier alignment");
   static_assert(OFF_DESC % 16 == 0 && OFF_SCR % 16 == 0 && OFF_MSTAT % 16 == 0 &&
-                    OFF_MACC % 16 == 0 && OFF_MISC % 4 == 0 && (SCR * 4) % 16 == 0,
+                    OFF_MACC % 16 == 0 && OFF_MISC % 16 == 0 && (SCR * 4) % 16 == 0,
                 "16-byte vector accesses need 16-byte aligned shared-memory regions");
 };
 
@@ -540,6 +545,131 @@ __device__ __forceinline__ int warp_sum_int(int v) {
   return v;
 }
 
+// Balanced mode. The work is the flattened (sequence, kv head, page) order of
+// P pages; CTA c of C streams pages [lo(c), lo(c+1)) with lo(c) = c*P/C.
+// cta_of(x) is the CTA whose range holds flattened page x.
+__device__ __forceinline__ long long range_lo(int c, long long P, int C) {
+  return (long long)c * P / C;
+}
+__device__ __forceinline__ int cta_of(long long x, long long P, int C) {
+  return static_cast<int>(((x + 1) * C - 1) / P);
+}
+
+// Partial slot (cta * 2 + slot) of the j-th piece of the cut segment that
+// covers flattened pages [seg0, seg0 + pages); c_first = cta_of(seg0). With
+// P >= C every CTA holds at least one page, so the pieces sit in CTAs
+// c_first, c_first + 1, ...; with P < C every CTA holds at most one page and
+// piece j sits in cta_of(seg0 + j). Only the first piece can be a CTA's
+// second piece (its range began with the end of another segment).
+__device__ __forceinline__ int piece_index(int j, long long seg0, long long P, int C,
+                                           int c_first, bool first_in_slot1) {
+  const int cc = P >= C ? c_first + j : cta_of(seg0 + j, P, C);
+  return cc * kPieceSlots + ((j == 0 && first_in_slot1) ? 1 : 0);
+}
+
+// Log-sum-exp combination of a cut segment's pieces into its G output rows,
+// run by `nwarps` warps of the CTA whose piece arrived last (warp w takes
+// heads w, w + nwarps, ...; a lane takes D / 32 elements of the row). Each
+// piece holds its normalised output o_j, its largest logit m_j and the sum
+// l_j of exp(logit - m_j); the segment's output is
+//   sum_j l_j exp(m_j - M) o_j / sum_j l_j exp(m_j - M),  M = max_j m_j,
+// accumulated here with a running maximum, four pieces per round of loads.
+// The pieces were written by other CTAs of this launch: they are read
+// through L2 (ld.global.cg), after the acquire of the caller.
+template <typename QT, typename Ly, int GT, int D>
+__device__ __forceinline__ void combine_segment(const DecodeParams& p, QT* out, long long seg0,
+                                                int pages, long long P, int C, int G, int warp,
+                                                int nwarps, int lane) {
+  constexpr int DPL = D / 32, U = 4;
+  static_assert(D % 32 == 0, "a lane takes D / 32 elements of a row");
+  const int c_first = cta_of(seg0, P, C);
+  const bool first_in_slot1 = seg0 != range_lo(c_first, P, C);
+  const int n = P >= C ? cta_of(seg0 + pages - 1, P, C) - c_first + 1 : pages;
+  const float2* mlp = reinterpret_cast<const float2*>(p.piece_ml);
+  for (int h = warp; h < G; h += nwarps) {
+    float M = -INFINITY, lsum = 0.f, acc[DPL];
+#pragma unroll
+    for (int t = 0; t < DPL; ++t) acc[t] = 0.f;
+    for (int j0 = 0; j0 < n; j0 += U) {
+      float2 ml[U];
+      float o[U][DPL];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        ml[u] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) o[u][t] = 0.f;
+        if (j0 + u < n) {
+          const size_t b =
+              (size_t)piece_index(j0 + u, seg0, P, C, c_first, first_in_slot1) * GT + h;
+          ml[u] = __ldcg(mlp + b);
+#pragma unroll
+          for (int t = 0; t < DPL; ++t) o[u][t] = __ldcg(p.piece_o + b * D + lane + 32 * t);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (ml[u].y > 0.f) {
+          if (ml[u].x > M) {
+            const float f = expf(M - ml[u].x);
+            lsum *= f;
+#pragma unroll
+            for (int t = 0; t < DPL; ++t) acc[t] *= f;
+            M = ml[u].x;
+          }
+          const float w = ml[u].y * expf(ml[u].x - M);
+          lsum += w;
+#pragma unroll
+          for (int t = 0; t < DPL; ++t) acc[t] = fmaf(w, o[u][t], acc[t]);
+        }
+      }
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+    for (int t = 0; t < DPL; ++t) out[h * D + lane + 32 * t] = Elem<QT>::from_f32(acc[t] * inv);
+  }
+}
+
+// A cut piece the producer still has to count (balanced mode), kept in
+// shared memory while the CTA streams on.
+struct CutPiece {
+  long long seg0;  // flattened index of its segment's first page
+  int pages;       // pages of the segment
+  int len;         // pages of the piece
+  int row;         // first output row of the segment (s * Hq + g * G)
+  int pad;
+};
+static_assert(sizeof(CutPiece) == 24, "two records fit the misc area");
+
+// Balanced mode, producer warp: count a finished cut piece (cp.len pages of
+// the segment at flattened pages [cp.seg0, cp.seg0 + cp.pages), output rows
+// from cp.row) and combine the segment if this piece completes it. The consumers' stores
+// of the piece are ordered before this through the stage's empty barrier
+// (release/acquire, CTA scope); lane 0's fence then makes them visible at
+// device scope before the count, and after a completing count orders the
+// other pieces' stores before the combine's loads.
+template <typename QT, typename Ly, int GT, int D>
+__device__ __forceinline__ void publish_piece(const DecodeParams& p, const CutPiece& cp,
+                                              long long P, int C, int G, int lane) {
+  const long long seg0 = cp.seg0;
+  const int pages = cp.pages, len = cp.len, row = cp.row;
+  int last = 0;
+  if (lane == 0) {
+    int* cnt = p.arrived + cta_of(seg0 + pages - 1, P, C);
+    fence_acq_rel_gpu();
+    const int before = atomicAdd(cnt, len);
+    last = before + len == pages ? 1 : 0;
+    if (last) {
+      *cnt = 0;  // nobody else touches it in this launch: leave it zero
+      fence_acq_rel_gpu();
+    }
+  }
+  __syncwarp();
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (last)
+    combine_segment<QT, Ly, GT, D>(p, reinterpret_cast<QT*>(p.out) + (size_t)row * D, seg0, pages,
+                                   P, C, G, 0, 1, lane);
+}
+
 template <typename QT, typename CT, int D, int GT, int BS, int MODE>
 __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
                                   Layout<QT, CT, D, GT, BS>::MIN_CTAS)
@@ -559,6 +689,7 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
   uint64_t* cbar = empty + STAGES;  // consumer-to-consumer barrier
   int4* desc = reinterpret_cast<int4*>(smem + Ly::OFF_DESC);
   int* misc = reinterpret_cast<int*>(smem + Ly::OFF_MISC);
+  long long* misc64 = reinterpret_cast<long long*>(smem + Ly::OFF_MISC + 16);
 
   // ---------------------------------------------------------- work of this CTA
   // Both modes end up with: start segment (s0, g0), start page pg0 in it, and
@@ -589,9 +720,15 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
     }
   } else {
     const int cta = blockIdx.x, C = gridDim.x, S = p.num_seqs;
-    if (threadIdx.x < kPieceSlots * 4)  // this call's slot records start invalid
-      p.piece_info[(size_t)cta * kPieceSlots * 4 + threadIdx.x] = 0;
-    if (warp == NC) {
+    if (warp < NC) {
+      // sequences with nothing to attend get zero rows (CTA c takes c, c + C,
+      // ...); impossible lengths are flagged here, once per sequence
+      for (int s = cta; s < S; s += C)
+        if (attended_len(p, s, BS, threadIdx.x == 0) == 0) {
+          QT* o = reinterpret_cast<QT*>(p.out) + (size_t)s * Hq * D;
+          for (int i = threadIdx.x; i < Hq * D; i += NC * 32) o[i] = Elem<QT>::from_f32(0.f);
+        }
+    } else {
       // total pages, then this CTA's equal share [lo, hi) of the flattened
       // (sequence, kv head, page) order, then where lo falls
       long long total = 0;
@@ -633,6 +770,8 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
         misc[1] = lg0;
         misc[2] = lpg0;
         misc[3] = static_cast<int>(hi - lo);
+        misc64[0] = lo;
+        misc64[1] = P;
       }
     }
     __syncthreads();
@@ -665,6 +804,19 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
     bool piece_start = true;
     int piece_flags = 0, piece_end = 0, issued = 0;
     bool aborted = false;
+    // balanced mode: the CTA's range start and the total page count, and the
+    // CTA's cut pieces: the head piece (the range starts inside its segment
+    // and goes on past it), counted here once the consumers have finished
+    // it, and the tail piece (the range ends inside its segment), recorded
+    // for the consumers, who count it themselves at the end
+    long long lo = 0, P = 1;
+    if constexpr (MODE == kModeBalanced) {
+      lo = misc64[0];
+      P = misc64[1];
+    }
+    CutPiece* cut = reinterpret_cast<CutPiece*>(smem + Ly::OFF_MISC + 32);  // head, tail
+    bool h_on = false;
+    int h_k = 0;
     for (int k = 0; k < npages; ++k) {
       if (s != tb_s || pg < tb_base || pg >= tb_base + 32) {
         tb_s = s;
@@ -678,6 +830,19 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
         piece_end = k + len - 1;
         piece_flags = (pg == 0 ? kSegFirst : 0) | (pg + len == pages ? kSegLast : 0) |
                       (k > 0 ? kSlot1 : 0);
+        if constexpr (MODE == kModeBalanced) {
+          if (pg != 0 || pg + len != pages) {  // cut
+            const bool tail = k + len == npages;
+            if (!tail) {
+              h_on = true;
+              h_k = len - 1;
+            }
+            // the consumers read the tail record after the piece's full
+            // barriers, which this write precedes
+            if (lane == 0) cut[tail ? 1 : 0] = CutPiece{lo + k - pg, pages, len, s * Hq + g * G, 0};
+            __syncwarp();
+          }
+        }
       }
       const int slot = k % STAGES;
       if (lane == 0) {
@@ -713,6 +878,14 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
         }
       }
       if (__shfl_sync(0xffffffffu, aborted ? 1 : 0, 0)) break;
+      if constexpr (MODE == kModeBalanced) {
+        // the wait above saw the head piece's last stage released: count it
+        // now, with this iteration's copies already in flight
+        if (h_on && k == h_k + STAGES) {
+          publish_piece<QT, Ly, GT, D>(p, cut[0], P, gridDim.x, G, lane);
+          h_on = false;
+        }
+      }
       // advance to the next page of the walk
       piece_start = false;
       ++pg;
@@ -740,6 +913,19 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
         if (!mbar_wait_bounded(&full[k % STAGES], (k / STAGES) & 1))
           raise_error(p.err, PA_DEVERR_TIMEOUT);
     }
+    if constexpr (MODE == kModeBalanced) {
+      // a head piece whose last stage was not reused: wait for the consumers
+      // to release it, then count it (skipped after any timeout)
+      if (h_on && __shfl_sync(0xffffffffu, aborted ? 0 : 1, 0)) {
+        int got = 1;
+        if (lane == 0 && !mbar_wait_bounded(&empty[h_k % STAGES], (h_k / STAGES) & 1)) {
+          raise_error(p.err, PA_DEVERR_TIMEOUT);
+          got = 0;
+        }
+        if (__shfl_sync(0xffffffffu, got, 0))
+          publish_piece<QT, Ly, GT, D>(p, cut[0], P, gridDim.x, G, lane);
+      }
+    }
     return;
   }
 
@@ -752,7 +938,7 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
   PieceState<Ly, GT> st;
 
   int k = 0;
-  bool aborted = false;
+  bool aborted = false, tail_cut = false;
   while (true) {
     // up to R pages of the current piece
     const uint8_t* Kp[R];
@@ -820,6 +1006,7 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
                 out[row * D + d] = Elem<QT>::from_f32(o);
               }
             });
+        if (lane == 0) mbar_arrive(&empty[last_slot]);
       } else {
         const bool whole = (last_flags & kSegFirst) && (last_flags & kSegLast);
         const int pslot = (last_flags & kSlot1) ? 1 : 0;
@@ -840,129 +1027,40 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
                 }
               }
             });
-        if (!whole && warp == 0 && lane == 0) {
-          int* info = p.piece_info + base * 4;
-          info[1] = seg;
-          info[2] = last_flags & (kSegFirst | kSegLast);
-          info[0] = 1;
-        }
+        // the merge is done with the stage; for a head piece this release also
+        // tells the producer that the piece's rows are stored
+        if (lane == 0) mbar_arrive(&empty[last_slot]);
+        tail_cut = !whole && (last_flags & kCtaLast);
       }
-      if (lane == 0) mbar_arrive(&empty[last_slot]);
     }
     k += n_here;
     if (last_flags & kCtaLast) break;
   }
-}
-
-// Balanced mode, second kernel: one CTA per decode CTA. The CTA whose piece
-// ends a cut segment combines that segment's pieces by log-sum-exp weights
-// and writes the output; the same CTAs also write zeros for sequences with
-// nothing to attend. The pieces of a segment sit in the consecutive CTAs
-// before the combiner (CTAs with an empty range hold none): warp 0 finds them
-// 32 CTAs at a time with ballots and turns their (max, sum) into weights in
-// shared memory; then every thread sums its output elements over the pieces.
-constexpr int kCombineMaxPieces = kMaxBalancedCtas;
-constexpr int kCombineMaxHeads = 8;
-template <typename OT>
-__global__ void __launch_bounds__(128)
-    combine_pieces_kernel(OT* out, const float* piece_o, const float* piece_ml,
-                          const int* piece_info, const int32_t* context_lens, int num_seqs,
-                          int num_heads, int num_kv_heads, int D, int GT, int bs, int MB,
-                          int window, int num_ctas, unsigned* err) {
-  __shared__ int members[kCombineMaxPieces];    // piece indices (cta * 2 + slot)
-  __shared__ float weights[kCombineMaxHeads * kCombineMaxPieces];  // [head][piece]
-  __shared__ int count;
-  pdl_wait();
-  pdl_trigger();
-  const int c = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int G = num_heads / num_kv_heads;
-  // sequences with no attended slot: zeros (and flag impossible lengths)
-  for (int s = c; s < num_seqs; s += gridDim.x) {
-    const int n = context_lens[s];
-    if (threadIdx.x == 0 && (n < 0 || (window == 0 && n > MB * bs)))
-      raise_error(err, PA_DEVERR_CONTEXT_LEN);
-    if (n <= 0)
-      for (int i = threadIdx.x; i < num_heads * D; i += blockDim.x)
-        out[(size_t)s * num_heads * D + i] = Elem<OT>::from_f32(0.f);
-  }
-  if (c >= num_ctas) return;
-  for (int slot = 0; slot < kPieceSlots; ++slot) {
-    const int* info = piece_info + ((size_t)c * kPieceSlots + slot) * 4;
-    const bool combiner = info[0] == 1 && !(info[2] & kSegFirst) && (info[2] & kSegLast);
-    if (!combiner) continue;  // uniform across the CTA
-    const int seg = info[1];
-    const int s = seg / num_kv_heads, g = seg % num_kv_heads;
-    if (warp == 0) {
-      // walk back in batches of 32 CTAs, collecting the pieces of `seg`
-      int n = 0;
-      if (lane == 0) members[0] = c * kPieceSlots + slot;
-      n = 1;
-      bool done = false;
-      for (int base = c - 1; base >= 0 && !done; base -= 32) {
-        const int cc = base - lane;
-        int pid = -1, first = 0;
-        if (cc >= 0) {
-          const int* i1 = piece_info + ((size_t)cc * kPieceSlots + 1) * 4;
-          const int* i0 = piece_info + ((size_t)cc * kPieceSlots + 0) * 4;
-          if (i1[0] == 1 && i1[1] == seg) {
-            pid = cc * kPieceSlots + 1;
-            first = i1[2] & kSegFirst;
-          } else if (i0[0] == 1 && i0[1] == seg) {
-            pid = cc * kPieceSlots;
-            first = i0[2] & kSegFirst;
-          }
+  if constexpr (MODE == kModeBalanced) {
+    if (tail_cut) {
+      // The tail piece, counted here. If every other piece of its segment
+      // has been counted already, it completes the segment and needs no
+      // publishing; otherwise publish it (the consumer barrier that ended
+      // finish_piece ordered every thread's rows before lane 0's fence) and
+      // count it.
+      const CutPiece cp = *reinterpret_cast<const CutPiece*>(smem + Ly::OFF_MISC + 32 + 24);
+      const long long P = misc64[1];
+      if (warp == 0 && lane == 0) {
+        int* cnt = p.arrived + cta_of(cp.seg0 + cp.pages - 1, P, gridDim.x);
+        int last = ld_acquire_gpu(cnt) + cp.len == cp.pages ? 1 : 0;
+        if (!last) {
+          fence_acq_rel_gpu();
+          last = atomicAdd(cnt, cp.len) + cp.len == cp.pages ? 1 : 0;
+          if (last) fence_acq_rel_gpu();
         }
-        const unsigned firsts = __ballot_sync(0xffffffffu, pid >= 0 && first);
-        // pieces up to and including the segment's first piece (lowest lane
-        // with kSegFirst = nearest to the combiner's side of the walk)
-        const int stop = firsts ? __ffs(firsts) - 1 : 31;
-        const unsigned take = __ballot_sync(0xffffffffu, pid >= 0 && lane <= stop);
-        const int rank = __popc(take & ((1u << lane) - 1));
-        if ((take >> lane) & 1) {
-          if (n + rank < kCombineMaxPieces) members[n + rank] = pid;
-        }
-        n += __popc(take);
-        done = firsts != 0;
+        if (last) *cnt = 0;  // leave it zero for the next launch
+        misc[8] = last;
       }
-      if (lane == 0) count = n < kCombineMaxPieces ? n : kCombineMaxPieces;
-      if (lane == 0 && !done && c > 0) raise_error(err, PA_DEVERR_TIMEOUT);  // chain broken
+      consumer_sync(cbar, cphase, lane, p.err);
+      if (misc[8])
+        combine_segment<QT, Ly, GT, D>(p, reinterpret_cast<QT*>(p.out) + (size_t)cp.row * D,
+                                       cp.seg0, cp.pages, P, gridDim.x, G, warp, NC, lane);
     }
-    __syncthreads();
-    const int npc = count;
-    // weights of every head at once: warp w takes heads w, w + 4, ...
-    for (int h = warp; h < G; h += blockDim.x / 32) {
-      float M = -INFINITY;
-      for (int i = lane; i < npc; i += 32) {
-        const size_t b = (size_t)members[i] * GT + h;
-        if (piece_ml[b * 2 + 1] > 0.f) M = fmaxf(M, piece_ml[b * 2]);
-      }
-#pragma unroll
-      for (int off = 16; off >= 1; off /= 2) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-      float wsum = 0.f;
-      for (int i = lane; i < npc; i += 32) {
-        const size_t b = (size_t)members[i] * GT + h;
-        const float l = piece_ml[b * 2 + 1];
-        const float w = (l > 0.f && M != -INFINITY) ? l * expf(piece_ml[b * 2] - M) : 0.f;
-        weights[h * kCombineMaxPieces + i] = w;
-        wsum += w;
-      }
-#pragma unroll
-      for (int off = 16; off >= 1; off /= 2) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
-      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-      __syncwarp();
-      for (int i = lane; i < npc; i += 32) weights[h * kCombineMaxPieces + i] *= inv;
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-      const int h = e / D, d = e % D;
-      float acc = 0.f;
-      for (int i = 0; i < npc; ++i) {
-        const float w = weights[h * kCombineMaxPieces + i];
-        if (w > 0.f) acc = fmaf(w, piece_o[((size_t)members[i] * GT + h) * D + d], acc);
-      }
-      out[((size_t)s * num_heads + (size_t)g * G + h) * D + d] = Elem<OT>::from_f32(acc);
-    }
-    __syncthreads();
   }
 }
 

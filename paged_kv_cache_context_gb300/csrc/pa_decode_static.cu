@@ -63,9 +63,9 @@ PA_API pa_status pa_decode_static_scratch(void* out, const void* query, const vo
     if (scratch_on_current_device(&scratch) != cudaSuccess) return PA_ERR_CUDA;
     scratch_bytes = PA_STATIC_SCRATCH_BYTES;
   }
-  // Nothing in the array has to start at zero: every decode CTA first marks
-  // its partial slots empty, then fills the ones it uses, before the combine
-  // launch of the same call reads them.
+  // Nothing in the array has to start at zero: pa_decode clears the arrival
+  // counters before its decode launch, and a partial slot is only read after
+  // the launch that reads it has written it.
   return pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads,
                    num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale,
                    window, q_dtype, kv_dtype, k_scale, v_scale, scratch, scratch_bytes, stream);

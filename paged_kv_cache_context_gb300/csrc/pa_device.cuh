@@ -19,6 +19,19 @@ __device__ __forceinline__ void raise_error(unsigned* err, unsigned bit) {
   if (err) atomicOr(err, bit);
 }
 
+// ------------------------------------------------- device-scope ordering
+// Release/acquire fence at GPU scope: before a relaxed atomic it publishes
+// the stores ordered before it (also other threads' stores this thread has
+// synchronised with); after one it orders later loads after what it saw.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------- timers
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;

@@ -55,7 +55,7 @@ def lib() -> ctypes.CDLL:
             "pa_reduce": [P, P, P, P, I, I, I, I, I, P],
             "pa_decode_balanced": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F, F, P,
                                    Z, P, P],
-            "pa_decode_combine": [P, P, I, I, I, I, I, I, I, I, P, Z, I, P],
+            "pa_decode_workspace_clear": [P, Z, P],
             "pa_decode_static_scratch": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F,
                                          F, P],
             "pa_get_device_error": [P, P],
@@ -155,7 +155,8 @@ def decode_balanced(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tenso
                     num_kv_heads: int, scale: float, workspace: torch.Tensor, window: int = 0,
                     kv_dtype: str = "auto", k_scale: float = 1.0, v_scale: float = 1.0,
                     stream=None) -> int:
-    """pa_decode_balanced: first launch of the balanced path; returns num_ctas."""
+    """pa_decode_balanced: the balanced path's decode launch (arrival counters
+    must be zero: see decode_workspace_clear); returns num_ctas."""
     S, Hq, D = query.shape
     NB, _, bs, _ = k_cache.shape
     MB = block_tables.shape[1]
@@ -169,15 +170,11 @@ def decode_balanced(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tenso
     return n.value
 
 
-def decode_combine(out: torch.Tensor, context_lens: torch.Tensor, num_kv_heads: int,
-                   block_size: int, max_blocks_per_seq: int, workspace: torch.Tensor,
-                   num_ctas: int, window: int = 0, stream=None):
-    """pa_decode_combine: second launch of the balanced path."""
-    S, Hq, D = out.shape
-    _check(lib().pa_decode_combine(_ptr(out), _ptr(context_lens), S, Hq, num_kv_heads, D,
-                                   block_size, max_blocks_per_seq, window, _DTYPE[out.dtype],
-                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                   num_ctas, _stream(stream)), "pa_decode_combine")
+def decode_workspace_clear(workspace: torch.Tensor, stream=None):
+    """pa_decode_workspace_clear: zero the balanced path's arrival counters."""
+    _check(lib().pa_decode_workspace_clear(_ptr(workspace),
+                                           workspace.numel() * workspace.element_size(),
+                                           _stream(stream)), "pa_decode_workspace_clear")
 
 
 def decode_partials(tmp_out: torch.Tensor, max_logits: torch.Tensor, exp_sums: torch.Tensor,

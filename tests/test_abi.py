@@ -120,8 +120,9 @@ def test_split_plan_is_host_only_and_covers_the_context():
 
 
 def test_balanced_workspace_depends_only_on_group_and_head_dim():
-    """Two partial slots of G' x D floats (G' = group rounded up to 1, 2, 4 or 8)
-    plus their (max, sum) and a 4-int record, for 152 x 4 persistent CTAs."""
+    """An arrival counter per persistent CTA (2560 bytes for 152 x 4 CTAs), then
+    two partial slots of G' x D floats (G' = group rounded up to 1, 2, 4 or 8)
+    plus their (max, sum) per CTA."""
     from paged_kv_cache_context_gb300 import pa
     for Hq, Hkv, D, gt in [(32, 8, 128, 4), (32, 32, 96, 1), (12, 4, 64, 4), (56, 8, 128, 8)]:
         sizes = {pa.decode_workspace_size(S, Hq, Hkv, D, 32, MB, 0)
@@ -129,8 +130,8 @@ def test_balanced_workspace_depends_only_on_group_and_head_dim():
         assert len(sizes) == 1
         ws = sizes.pop()
         slots = 152 * 4 * 2
-        assert ws >= slots * (gt * D * 4 + gt * 2 * 4 + 16)
-        assert ws <= slots * (gt * D * 4 + gt * 2 * 4 + 16) + 3 * 256
+        assert ws >= 2560 + slots * (gt * D * 4 + gt * 2 * 4)
+        assert ws <= 2560 + slots * (gt * D * 4 + gt * 2 * 4) + 2 * 256
     assert pa.decode_workspace_size(2, 6, 4, 128, 32, 8, 0) == 0  # 6 % 4 != 0
     assert pa.decode_workspace_size(2, 32, 4, 128, 32, 8, 0) <= 8 << 20  # G = 8, D = 128
 
@@ -142,7 +143,6 @@ def test_balanced_entry_points_reject_bad_arguments_on_host(L):
     assert n.value == 0
     assert L.pa_decode_balanced(*args, P, 1024, ctypes.addressof(n), None) == -7
     assert L.pa_decode_balanced(*args, P, 1 << 30, None, None) == -1
-    assert L.pa_decode_combine(P, P, 2, 8, 2, 128, 32, 4, 0, 1, P, 1024, 100, None) == -7
-    assert L.pa_decode_combine(P, P, 2, 8, 2, 128, 32, 4, 0, 1, P, 1 << 30, 0, None) == -3
-    assert L.pa_decode_combine(P, P, 2, 8, 2, 100, 32, 4, 0, 1, P, 1 << 30, 10, None) == -4
-    assert L.pa_decode_combine(P, None, 2, 8, 2, 128, 32, 4, 0, 1, P, 1 << 30, 10, None) == -1
+    assert L.pa_decode_workspace_clear(None, 4096, None) == -1
+    assert L.pa_decode_workspace_clear(P, 2559, None) == -7
+    assert L.pa_decode_workspace_clear(P + 4, 4096, None) == -10

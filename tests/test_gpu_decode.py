@@ -204,7 +204,7 @@ def test_bad_block_id_and_context_len_are_flagged_not_faulted():
 # ------------------------------------------------------------ balanced path cuts
 def test_balanced_one_context_cut_across_every_cta():
     """A single 98k-token context: every persistent CTA holds a piece of it,
-    and the combine walks the whole chain of partials."""
+    and the CTA whose piece arrives last combines all of them."""
     case = wl.make_case("long", 96, 1, 4, 1, 128, lens=[98_000], q_dtype=torch.float32,
                         max_blocks_per_seq=-(-98_000 // 32))
     check_case(case, splits=(True,))
@@ -219,18 +219,33 @@ def test_balanced_thousands_of_tiny_contexts_with_empty_ones():
     check_case(case)
 
 
-def test_balanced_two_launch_form_equals_pa_decode():
+@pytest.mark.parametrize("lens,Hkv", [([1, 70, 0, 129, 64], 2),  # fewer pages than CTAs
+                                      ([17, 200, 33], 1), ([0, 0, 0], 4), ([300], 8)])
+def test_balanced_fewer_pages_than_ctas(lens, Hkv):
+    """With fewer pages than persistent CTAs a CTA holds one page or none:
+    a cut context's pieces sit in every CTA its pages map to, with empty CTAs
+    between them; all-empty batches write zero rows only."""
+    case = wl.make_case(f"thin{Hkv}", 100 + Hkv, len(lens), 2 * Hkv, Hkv, 96, lens=lens,
+                        q_dtype=torch.float16, max_blocks_per_seq=10, extra_blocks=2)
+    check_case(case, splits=(True,))
+
+
+def test_balanced_launch_without_clear_after_a_clean_launch():
+    """A launch that raised no device error leaves the arrival counters zero,
+    so pa_decode_balanced may follow it without a clear; and clear + balanced
+    gives bit-for-bit what pa_decode gives."""
     case = wl.make_case("two", 99, 9, 32, 8, 128, len_range=(1, 3000), max_blocks_per_seq=94)
     kg, vg = gpu_caches(case)
     ref = gpu_decode(case, kg, vg, split=True)
     nbytes = pa.decode_workspace_size(case.num_seqs, case.num_heads, case.num_kv_heads,
                                       case.head_dim, case.block_size, case.max_blocks_per_seq)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
-    out = torch.full_like(ref, float("nan"))
-    n = pa.decode_balanced(out, to_dev(case.query), kg, vg, to_dev(case.block_tables),
-                           to_dev(case.context_lens), case.num_kv_heads, case.scale, ws)
-    assert n > 0
-    pa.decode_combine(out, to_dev(case.context_lens), case.num_kv_heads, case.block_size,
-                      case.max_blocks_per_seq, ws, n)
-    assert torch.equal(bits(out), bits(ref))
+    pa.decode_workspace_clear(ws)
+    for _ in range(3):
+        out = torch.full_like(ref, float("nan"))
+        n = pa.decode_balanced(out, to_dev(case.query), kg, vg, to_dev(case.block_tables),
+                               to_dev(case.context_lens), case.num_kv_heads, case.scale, ws)
+        assert n > 0
+        assert torch.equal(bits(out), bits(ref))
+    assert torch.all(ws[:2560] == 0)
     assert device_errors() == 0
