@@ -61,6 +61,15 @@ namespace pa {
 #ifndef PA_MAX_STAGES
 #define PA_MAX_STAGES 8
 #endif
+// Fewest lanes a cached row is spread over, and the register budget per
+// thread planned for more than two query heads per kv head (build-time
+// tunables).
+#ifndef PA_LPR_MIN
+#define PA_LPR_MIN 4
+#endif
+#ifndef PA_REG_BUDGET_WIDE
+#define PA_REG_BUDGET_WIDE 128
+#endif
 
 enum : int { kModeSplit = 0, kModeBalanced = 1 };
 
@@ -120,11 +129,11 @@ constexpr int cmax(int a, int b) { return a > b ? a : b; }
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-// Lanes per row: the fewest (>= 4) that keep q and acc at <= 32 fp32 each with
+// Lanes per row: the fewest (>= PA_LPR_MIN) that keep q and acc at <= 32 fp32 each with
 // an even number of elements per lane (they are processed as fp32 pairs);
 // failing that, the most lanes that still give an even count.
 constexpr int choose_lpr(int D, int GT) {
-  for (int l = 4; l <= 32; l *= 2)
+  for (int l = PA_LPR_MIN; l <= 32; l *= 2)
     if (D % l == 0 && (D / l) % 2 == 0 && (D / l) * GT <= 32) return l;
   for (int l = 32; l >= 4; l /= 2)
     if (D % l == 0 && (D / l) % 2 == 0) return l;
@@ -188,7 +197,7 @@ struct Layout {
   // per SM, 1 KB reserved per CTA), at most 4, and no more than keeps a
   // register budget per thread (96 for one or two heads per kv head, else
   // 128); __launch_bounds__ makes ptxas fit that many.
-  static constexpr int REG_BUDGET = GT <= 2 ? 96 : 128;
+  static constexpr int REG_BUDGET = GT <= 2 ? 96 : PA_REG_BUDGET_WIDE;
   static constexpr int MIN_CTAS =
       cmax(1, cmin(cmin(4, (228 * 1024) / (SMEM + 1024)), 65536 / (THREADS * REG_BUDGET)));
   static_assert(NST >= 1, "lanes per row too small for 8 rows per warp");
