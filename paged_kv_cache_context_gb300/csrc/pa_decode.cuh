@@ -88,13 +88,6 @@ enum : int {
 constexpr int kPieceSlots = 2;
 constexpr int kMaxBalancedCtas = 152 * 4;
 
-// Balanced mode: how much smaller, in thousandths, the last launch rank's
-// share of the pages is than the first's (build-time tunable; at most 500).
-#ifndef PA_RANK_SLOPE
-#define PA_RANK_SLOPE 130
-#endif
-static_assert(PA_RANK_SLOPE >= 0 && PA_RANK_SLOPE <= 500, "every share stays >= 1/2 of the first");
-
 struct DecodeParams {
   // outputs
   void* out;            // [S][Hq][D] of QT
@@ -118,10 +111,6 @@ struct DecodeParams {
   int partials;   // split mode: 1 = write split partials, 0 = final output
   float q_scale;  // scale * log2(e) (* k_scale for FP8)
   float v_scale;  // FP8: v_scale, else 1
-  // balanced mode: CTAs per launch rank (the SM count; CTA b is in rank
-  // b / rank_size) and how much smaller, in thousandths, each rank's share is
-  // than the one before (0: equal shares)
-  int rank_size, rank_step;
 };
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
@@ -566,53 +555,24 @@ __device__ __forceinline__ int warp_sum_int(int v) {
 }
 
 // Balanced mode. The work is the flattened (sequence, kv head, page) order of
-// P pages, cut into C contiguous ranges, one per CTA. CTA b gets a share
-// proportional to w(b) = 1000 - step * (b / rank_size): the hardware starts
-// the CTAs of a launch rank by rank, one per SM, and on an SM shared by
-// several of them the earlier ones get more issue slots, so later ranks are
-// given slightly less (the shares only change speed, never the result). With
-// P < 2C the shares are equal (step 0); otherwise every CTA gets at least one
-// page, since every w >= 500.
-struct Ranges {
-  long long P, T;  // pages in all; sum of the weights of all C CTAs
-  int C, rs, step;
-  __device__ __forceinline__ long long w(int r) const { return 1000 - (long long)step * r; }
-  // sum of the weights of CTAs 0 .. c-1
-  __device__ __forceinline__ long long cum(int c) const {
-    const long long R = c / rs;
-    return rs * (R * 1000 - (long long)step * (R * (R - 1) / 2)) + (c - R * rs) * w((int)R);
-  }
-  __device__ __forceinline__ long long lo(int c) const { return P * cum(c) / T; }
-  // the CTA whose range holds flattened page x < P: the largest c with
-  // lo(c) <= x, i.e. with cum(c) <= ((x + 1) T - 1) / P
-  __device__ __forceinline__ int of(long long x) const {
-    const long long y = ((x + 1) * T - 1) / P;
-    for (int b0 = 0;; b0 += rs) {
-      const int b1 = b0 + rs < C ? b0 + rs : C;
-      if (b1 == C || cum(b1) > y) return b0 + (int)((y - cum(b0)) / w(b0 / rs));
-    }
-  }
-};
-
-__device__ __forceinline__ Ranges make_ranges(long long P, int C, int rank_size, int rank_step) {
-  Ranges q;
-  q.P = P;
-  q.C = C;
-  q.rs = rank_size > 0 ? rank_size : C;
-  q.step = P >= 2LL * C ? rank_step : 0;
-  q.T = q.cum(C);
-  return q;
+// P pages; CTA c of C streams pages [lo(c), lo(c+1)) with lo(c) = c*P/C.
+// cta_of(x) is the CTA whose range holds flattened page x.
+__device__ __forceinline__ long long range_lo(int c, long long P, int C) {
+  return (long long)c * P / C;
+}
+__device__ __forceinline__ int cta_of(long long x, long long P, int C) {
+  return static_cast<int>(((x + 1) * C - 1) / P);
 }
 
 // Partial slot (cta * 2 + slot) of the j-th piece of the cut segment that
-// covers flattened pages [seg0, seg0 + pages); c_first = of(seg0). With
+// covers flattened pages [seg0, seg0 + pages); c_first = cta_of(seg0). With
 // P >= C every CTA holds at least one page, so the pieces sit in CTAs
-// c_first, c_first + 1, ...; with P < C (equal shares) every CTA holds at
-// most one page and piece j sits in of(seg0 + j). Only the first piece can be
-// a CTA's second piece (its range began with the end of another segment).
-__device__ __forceinline__ int piece_index(int j, long long seg0, const Ranges& rg, int c_first,
-                                           bool first_in_slot1) {
-  const int cc = rg.P >= rg.C ? c_first + j : rg.of(seg0 + j);
+// c_first, c_first + 1, ...; with P < C every CTA holds at most one page and
+// piece j sits in cta_of(seg0 + j). Only the first piece can be a CTA's
+// second piece (its range began with the end of another segment).
+__device__ __forceinline__ int piece_index(int j, long long seg0, long long P, int C,
+                                           int c_first, bool first_in_slot1) {
+  const int cc = P >= C ? c_first + j : cta_of(seg0 + j, P, C);
   return cc * kPieceSlots + ((j == 0 && first_in_slot1) ? 1 : 0);
 }
 
@@ -627,13 +587,13 @@ __device__ __forceinline__ int piece_index(int j, long long seg0, const Ranges& 
 // through L2 (ld.global.cg), after the acquire of the caller.
 template <typename QT, typename Ly, int GT, int D>
 __device__ __forceinline__ void combine_segment(const DecodeParams& p, QT* out, long long seg0,
-                                                int pages, const Ranges& rg, int G, int warp,
+                                                int pages, long long P, int C, int G, int warp,
                                                 int nwarps, int lane) {
   constexpr int DPL = D / 32, U = 4;
   static_assert(D % 32 == 0, "a lane takes D / 32 elements of a row");
-  const int c_first = rg.of(seg0);
-  const bool first_in_slot1 = seg0 != rg.lo(c_first);
-  const int n = rg.P >= rg.C ? rg.of(seg0 + pages - 1) - c_first + 1 : pages;
+  const int c_first = cta_of(seg0, P, C);
+  const bool first_in_slot1 = seg0 != range_lo(c_first, P, C);
+  const int n = P >= C ? cta_of(seg0 + pages - 1, P, C) - c_first + 1 : pages;
   const float2* mlp = reinterpret_cast<const float2*>(p.piece_ml);
   for (int h = warp; h < G; h += nwarps) {
     float M = -INFINITY, lsum = 0.f, acc[DPL];
@@ -649,7 +609,7 @@ __device__ __forceinline__ void combine_segment(const DecodeParams& p, QT* out, 
         for (int t = 0; t < DPL; ++t) o[u][t] = 0.f;
         if (j0 + u < n) {
           const size_t b =
-              (size_t)piece_index(j0 + u, seg0, rg, c_first, first_in_slot1) * GT + h;
+              (size_t)piece_index(j0 + u, seg0, P, C, c_first, first_in_slot1) * GT + h;
           ml[u] = __ldcg(mlp + b);
 #pragma unroll
           for (int t = 0; t < DPL; ++t) o[u][t] = __ldcg(p.piece_o + b * D + lane + 32 * t);
@@ -698,12 +658,12 @@ static_assert(sizeof(CutPiece) == 24, "two records fit the misc area");
 // other pieces' stores before the combine's loads.
 template <typename QT, typename Ly, int GT, int D>
 __device__ __forceinline__ void publish_piece(const DecodeParams& p, const CutPiece& cp,
-                                              const Ranges& rg, int G, int lane) {
+                                              long long P, int C, int G, int lane) {
   const long long seg0 = cp.seg0;
   const int pages = cp.pages, len = cp.len, row = cp.row;
   int last = 0;
   if (lane == 0) {
-    int* cnt = p.arrived + rg.of(seg0 + pages - 1);
+    int* cnt = p.arrived + cta_of(seg0 + pages - 1, P, C);
     fence_acq_rel_gpu();
     const int before = atomicAdd(cnt, len);
     last = before + len == pages ? 1 : 0;
@@ -716,7 +676,7 @@ __device__ __forceinline__ void publish_piece(const DecodeParams& p, const CutPi
   last = __shfl_sync(0xffffffffu, last, 0);
   if (last)
     combine_segment<QT, Ly, GT, D>(p, reinterpret_cast<QT*>(p.out) + (size_t)row * D, seg0, pages,
-                                   rg, G, 0, 1, lane);
+                                   P, C, G, 0, 1, lane);
 }
 
 template <typename QT, typename CT, int D, int GT, int BS, int MODE>
@@ -787,8 +747,7 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
         total += warp_sum_int(pg);
       }
       const long long P = total * Hkv;
-      const Ranges rg = make_ranges(P, C, p.rank_size, p.rank_step);
-      const long long lo = rg.lo(cta), hi = cta + 1 < C ? rg.lo(cta + 1) : P;
+      const long long lo = (long long)cta * P / C, hi = (long long)(cta + 1) * P / C;
       int ls0 = 0, lg0 = 0, lpg0 = 0;
       if (lo < hi) {
         long long run = 0;  // pages of the sequences before this chunk
@@ -859,11 +818,10 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
     // and goes on past it), counted here once the consumers have finished
     // it, and the tail piece (the range ends inside its segment), recorded
     // for the consumers, who count it themselves at the end
-    long long lo = 0;
-    Ranges rg{};
+    long long lo = 0, P = 1;
     if constexpr (MODE == kModeBalanced) {
       lo = misc64[0];
-      rg = make_ranges(misc64[1], gridDim.x, p.rank_size, p.rank_step);
+      P = misc64[1];
     }
     CutPiece* cut = reinterpret_cast<CutPiece*>(smem + Ly::OFF_MISC + 32);  // head, tail
     bool h_on = false;
@@ -933,7 +891,7 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
         // the wait above saw the head piece's last stage released: count it
         // now, with this iteration's copies already in flight
         if (h_on && k == h_k + STAGES) {
-          publish_piece<QT, Ly, GT, D>(p, cut[0], rg, G, lane);
+          publish_piece<QT, Ly, GT, D>(p, cut[0], P, gridDim.x, G, lane);
           h_on = false;
         }
       }
@@ -974,7 +932,7 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
           got = 0;
         }
         if (__shfl_sync(0xffffffffu, got, 0))
-          publish_piece<QT, Ly, GT, D>(p, cut[0], rg, G, lane);
+          publish_piece<QT, Ly, GT, D>(p, cut[0], P, gridDim.x, G, lane);
       }
     }
     return;
@@ -1095,9 +1053,9 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
       // finish_piece ordered every thread's rows before lane 0's fence) and
       // count it.
       const CutPiece cp = *reinterpret_cast<const CutPiece*>(smem + Ly::OFF_MISC + 32 + 24);
-      const Ranges rg = make_ranges(misc64[1], gridDim.x, p.rank_size, p.rank_step);
+      const long long P = misc64[1];
       if (warp == 0 && lane == 0) {
-        int* cnt = p.arrived + rg.of(cp.seg0 + cp.pages - 1);
+        int* cnt = p.arrived + cta_of(cp.seg0 + cp.pages - 1, P, gridDim.x);
         int last = ld_acquire_gpu(cnt) + cp.len == cp.pages ? 1 : 0;
         if (!last) {
           fence_acq_rel_gpu();
@@ -1110,7 +1068,7 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
       consumer_sync(cbar, cphase, lane, p.err);
       if (misc[8])
         combine_segment<QT, Ly, GT, D>(p, reinterpret_cast<QT*>(p.out) + (size_t)cp.row * D,
-                                       cp.seg0, cp.pages, rg, G, warp, NC, lane);
+                                       cp.seg0, cp.pages, P, gridDim.x, G, warp, NC, lane);
     }
   }
 }
@@ -1124,7 +1082,6 @@ cudaError_t launch_decode(const DecodeParams& prm, dim3 grid, int* ctas, cudaStr
   auto kern = paged_decode_kernel<QT, CT, D, GT, BS, MODE>;
   static int configured_devices = 0;  // bit per device id < 32
   static int capacity[32] = {};       // resident CTAs per device
-  static int rank_size[32] = {};      // SMs per device (CTAs per launch rank)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1139,22 +1096,13 @@ cudaError_t launch_decode(const DecodeParams& prm, dim3 grid, int* ctas, cudaStr
     const long long C = (long long)sms * (per_sm > 0 ? per_sm : 1);
     if (dev < 32) {
       capacity[dev] = static_cast<int>(C < kMaxBalancedCtas ? C : kMaxBalancedCtas);
-      rank_size[dev] = sms;
       __atomic_fetch_or(&configured_devices, 1 << dev, __ATOMIC_RELEASE);
     }
   }
-  DecodeParams q = prm;
-  if (MODE == kModeBalanced) {
-    if (grid.x == 0) grid.x = dev < 32 && capacity[dev] > 0 ? capacity[dev] : kMaxBalancedCtas;
-    // launch ranks of rank_size CTAs; the shares fall linearly by
-    // PA_RANK_SLOPE thousandths from the first rank to the last
-    const int rs = dev < 32 && rank_size[dev] > 0 ? rank_size[dev] : static_cast<int>(grid.x);
-    const int ranks = (static_cast<int>(grid.x) + rs - 1) / rs;
-    q.rank_size = rs;
-    q.rank_step = ranks > 1 ? PA_RANK_SLOPE / (ranks - 1) : 0;
-  }
+  if (MODE == kModeBalanced && grid.x == 0)
+    grid.x = dev < 32 && capacity[dev] > 0 ? capacity[dev] : kMaxBalancedCtas;
   if (ctas) *ctas = static_cast<int>(grid.x);
-  return launch_pdl(kern, grid, dim3(Ly::THREADS), Ly::SMEM, stream, q);
+  return launch_pdl(kern, grid, dim3(Ly::THREADS), Ly::SMEM, stream, prm);
 }
 
 // Dispatch over (head_dim, group bucket, block size) for one (QT, CT) pair.
