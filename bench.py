@@ -217,12 +217,15 @@ def oracle_step_time(case, rows_per_step: int, reps: int, build_all: bool = True
                       case.block_size, case.scale, case.window, case.kv_dtype, case.k_scale,
                       case.v_scale, rows=rows)
         times.append(time.perf_counter() - t0)
+    # the same algorithmic bytes as the GPU step: the K/V rows a (sequence,
+    # kv head) attends count once for the G query-head rows that share them
+    G = Hq // case.num_kv_heads
     sample_bytes = 0
     for r in rows:
         s = r // Hq
         sample_bytes += case.attended(s) * case.head_dim * 2 * (
             1 if case.kv_dtype == "fp8_e4m3" else torch.finfo(case.q_dtype).bits // 8)
-    return times, sample_bytes, len(rows)
+    return times, sample_bytes / G, len(rows)
 
 
 def cores() -> int:
