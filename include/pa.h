@@ -238,6 +238,58 @@ pa_status pa_decode_balanced(void* out, const void* query,
                              pa_stream_t stream);
 
 /*
+ * pa_decode_cascade -- decode of a batch whose block tables all start with
+ * the same prefix blocks ("PagedAttention in mistral.rs", opening section:
+ * prefix caching keeps a prefix's KV state in the paged cache and reuses
+ * it). Same result as pa_decode with window 0, computed in three launches:
+ *   1. each sequence's own pages after the prefix (pages prefix_pages ..),
+ *      one CTA per (sequence, kv head), into partial slot 0;
+ *   2. the shared prefix (pages 0 .. prefix_pages - 1 of row 0 of
+ *      block_tables) for all S * G query heads of each kv head at once, on
+ *      the tensor cores, cut into up to (prefix tokens / 64) token ranges,
+ *      into slots 1 .. ;
+ *   3. pa_reduce of the slots into `out`.
+ * The prefix K/V is read once per kv head for the whole batch instead of
+ * once per sequence.
+ * Preconditions (checked on the device, error bits as pa_decode): the first
+ * prefix_pages entries of every row of block_tables are the same blocks
+ * (else PA_DEVERR_BLOCK_ID), and every context_lens[s] >= prefix_pages * bs
+ * (else PA_DEVERR_CONTEXT_LEN). Supported: AUTO caches of q_dtype BF16 or F16
+ * (else PA_ERR_DTYPE), D in {64, 128} (else PA_ERR_HEAD_DIM),
+ * 1 <= prefix_pages <= MB (else PA_ERR_SHAPE). workspace: at least
+ * pa_decode_cascade_workspace_size() bytes (PA_ERR_NULL / PA_ERR_WORKSPACE),
+ * 16-byte aligned; contents on entry do not matter. Other arguments and
+ * errors as pa_decode. Accuracy: the prefix's softmax weights are rounded to
+ * the input type before the P x V product (fp32 accumulation), so the result
+ * agrees with pa_decode to within the bf16 / f16 output tolerance, not bit for
+ * bit.
+ */
+size_t pa_decode_cascade_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int prefix_pages);
+pa_status pa_decode_cascade(void* out, const void* query,
+                            const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                            int block_size, int num_blocks, int max_blocks_per_seq,
+                            float scale, pa_dtype q_dtype, int prefix_pages,
+                            void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_copy_blocks -- copy whole cache blocks, for copy-on-write of shared
+ * blocks ("libmir-metal trace/kv.rs": fragmented copy-on-write block maps).
+ * For each pair i, block block_pairs[2i] of both caches (all kv heads, K and
+ * V) is copied over block block_pairs[2i + 1]. block_pairs: device int32
+ * [num_pairs][2]. elem_bytes: 1 (FP8), 2 (bf16 / f16) or 4 (fp32); the block's
+ * bytes Hkv * bs * D * elem_bytes must be a multiple of 16 (else
+ * PA_ERR_HEAD_DIM). A pair naming a block outside [0, num_blocks) is skipped
+ * and sets PA_DEVERR_BLOCK_ID. Pairs must not overlap (a destination that is
+ * another pair's source gives an unspecified result).
+ */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs,
+                         int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, int elem_bytes, pa_stream_t stream);
+
+/*
  * pa_decode_partials -- the split phase of pa_decode with an explicit plan.
  *
  * For split i of (s, h) (slots [i*P*bs, (i+1)*P*bs) intersected with

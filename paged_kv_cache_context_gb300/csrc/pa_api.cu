@@ -7,6 +7,7 @@
 
 #include <mutex>
 
+#include "pa_cascade.cuh"
 #include "pa_decode.cuh"
 #include "pa_device.cuh"
 
@@ -631,6 +632,132 @@ PA_API pa_status pa_decode(void* out, const void* query, const void* k_cache,
   p.pages_per_split = max_pages(max_blocks_per_seq, block_size, window);
   return run_decode(p, a, dim3(1, num_kv_heads, num_seqs), kModeSplit, nullptr,
                     reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+// ================================================================ cascade
+// Split of the shared prefix into ranges of whole 64-token tiles, enough of
+// them that (query tiles x kv heads x splits) gives about two CTAs per SM.
+static void cascade_plan(int S, int G, int Hkv, int prefix_tokens, int* nsp, int* tps) {
+  const int qtiles = (S * G + kPrefixRows - 1) / kPrefixRows;
+  const int tiles = (prefix_tokens + kPrefixTile - 1) / kPrefixTile;
+  const int64_t want = (2 * 152 + (int64_t)qtiles * Hkv - 1) / ((int64_t)qtiles * Hkv);
+  int n = static_cast<int>(want < 1 ? 1 : (want > tiles ? tiles : want));
+  const int tiles_per = (tiles + n - 1) / n;
+  *tps = tiles_per * kPrefixTile;
+  *nsp = (tiles + tiles_per - 1) / tiles_per;
+}
+
+static pa_status check_cascade(const DecodeShape& a, int prefix_pages) {
+  if (a.kv_dtype != PA_KV_AUTO || (a.q_dtype != PA_BF16 && a.q_dtype != PA_F16))
+    return PA_ERR_DTYPE;
+  if (a.D != 64 && a.D != 128) return PA_ERR_HEAD_DIM;
+  if (prefix_pages < 1 || prefix_pages > a.MB) return PA_ERR_SHAPE;
+  return PA_OK;
+}
+
+PA_API size_t pa_decode_cascade_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                               int head_dim, int block_size, int prefix_pages) {
+  if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
+      head_dim <= 0 || block_size <= 0 || prefix_pages <= 0)
+    return 0;
+  int nsp = 0, tps = 0;
+  cascade_plan(num_seqs, num_heads / num_kv_heads, num_kv_heads, prefix_pages * block_size, &nsp,
+               &tps);
+  const size_t rows = (size_t)num_seqs * num_heads * (nsp + 1);
+  return align256(rows * head_dim * 4) + 2 * align256(rows * 4);
+}
+
+PA_API pa_status pa_decode_cascade(void* out, const void* query, const void* k_cache,
+                                   const void* v_cache, const int32_t* block_tables,
+                                   const int32_t* context_lens, int num_seqs, int num_heads,
+                                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                   int max_blocks_per_seq, float scale, pa_dtype q_dtype,
+                                   int prefix_pages, void* workspace, size_t workspace_bytes,
+                                   pa_stream_t stream) {
+  DecodeShape a{num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                max_blocks_per_seq, 0, q_dtype, PA_KV_AUTO, 1.f, 1.f};
+  pa_status rc = check_decode(a, out, query, k_cache, v_cache, block_tables, context_lens);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  rc = check_cascade(a, prefix_pages);
+  if (rc != PA_OK) return rc;
+  if (!workspace) return PA_ERR_NULL;
+  const size_t need = pa_decode_cascade_workspace_size(num_seqs, num_heads, num_kv_heads,
+                                                       head_dim, block_size, prefix_pages);
+  if (workspace_bytes < need) return PA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return PA_ERR_ALIGN;
+  const int G = num_heads / num_kv_heads;
+  int nsp = 0, tps = 0;
+  cascade_plan(num_seqs, G, num_kv_heads, prefix_pages * block_size, &nsp, &tps);
+  const int ns = nsp + 1;
+  const size_t rows = (size_t)num_seqs * num_heads * ns;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  float* tmp = reinterpret_cast<float*>(w);
+  float* ml = reinterpret_cast<float*>(w + align256(rows * head_dim * 4));
+  float* es = reinterpret_cast<float*>(w + align256(rows * head_dim * 4) + align256(rows * 4));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  unsigned* err = error_word();
+
+  // slot 0: each sequence's own pages after the prefix, one CTA per (sequence, kv head)
+  DecodeParams p = make_params(a, query, k_cache, v_cache, block_tables, context_lens, scale, err);
+  p.tmp_out = tmp;
+  p.max_logits = ml;
+  p.exp_sums = es;
+  p.partials = 1;
+  p.num_splits = ns;
+  p.first_page = prefix_pages;
+  p.pages_per_split = max_blocks_per_seq - prefix_pages > 0 ? max_blocks_per_seq - prefix_pages : 1;
+  if (run_decode(p, a, dim3(1, num_kv_heads, num_seqs), kModeSplit, nullptr, st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  // slots 1 .. nsp: the shared prefix, all sequences' query heads at once
+  PrefixParams q{};
+  q.tmp_out = tmp;
+  q.max_logits = ml;
+  q.exp_sums = es;
+  q.query = query;
+  q.k_cache = static_cast<const uint8_t*>(k_cache);
+  q.v_cache = static_cast<const uint8_t*>(v_cache);
+  q.block_tables = block_tables;
+  q.context_lens = context_lens;
+  q.err = err;
+  q.num_seqs = num_seqs;
+  q.num_heads = num_heads;
+  q.num_kv_heads = num_kv_heads;
+  q.group = G;
+  q.head_dim = head_dim;
+  q.block_size = block_size;
+  q.num_blocks = num_blocks;
+  q.max_blocks_per_seq = max_blocks_per_seq;
+  q.prefix_pages = prefix_pages;
+  q.prefix_tokens = prefix_pages * block_size;
+  q.num_slots = ns;
+  q.slot0 = 1;
+  q.num_prefix_splits = nsp;
+  q.tokens_per_split = tps;
+  q.scale_log2 = scale * 1.4426950408889634f;
+  if (launch_prefix_attention(q, q_dtype, st) != cudaSuccess) return PA_ERR_CUDA;
+  // the log-sum-exp combination of the ns slots
+  return run_reduce(out, tmp, ml, es, (int64_t)num_seqs * num_heads, head_dim, ns, q_dtype, st) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs,
+                                int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                                int num_blocks, int elem_bytes, pa_stream_t stream) {
+  if (num_pairs < 0) return PA_ERR_SHAPE;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !block_pairs) return PA_ERR_NULL;
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4) return PA_ERR_DTYPE;
+  if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0) return PA_ERR_SHAPE;
+  const size_t block_bytes = (size_t)num_kv_heads * block_size * head_dim * elem_bytes;
+  if (block_bytes % 16 != 0) return PA_ERR_HEAD_DIM;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+  return launch_copy_blocks(static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache),
+                            block_pairs, num_pairs, num_blocks, block_bytes, error_word(),
+                            reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }

@@ -1,0 +1,55 @@
+// pa_cascade.cuh -- shared-prefix (cascade) attention: the kernel launcher's
+// parameters, shared by pa_cascade.cu (the kernel) and pa_api.cu (the entry
+// point that also runs the suffix decode and the combine).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Attention of every sequence's query heads to the blocks of a prefix that
+// all of a batch's block tables share ("PagedAttention in mistral.rs":
+// prefix caching; the shared blocks are read once per kv head for the whole
+// batch instead of once per sequence). For kv head g the rows are the S * G
+// query heads (s, g * G + j) that share it, so the prefix part is a dense
+// contraction Q [S*G, D] x K^T [D, T] and P [S*G, T] x V [T, D].
+//
+// The prefix tokens [0, prefix_tokens) are cut into num_prefix_splits ranges
+// of tokens_per_split tokens; split i writes the partial of every row over
+// its range into slot slot0 + i of the pa_reduce layout:
+//   tmp_out [S][Hq][num_slots][D], max_logits / exp_sums [S][Hq][num_slots]
+// (normalised output, largest logit in natural-log units, sum of
+// exp(logit - max); a range with no token gives -inf / 0 and leaves tmp_out).
+struct PrefixParams {
+  float* tmp_out;
+  float* max_logits;
+  float* exp_sums;
+  const void* query;            // [S][Hq][D], same element type as the cache
+  const uint8_t* k_cache;       // [NB][Hkv][bs][D]
+  const uint8_t* v_cache;
+  const int32_t* block_tables;  // [S][MB]; the first prefix_pages entries of every row agree
+  const int32_t* context_lens;  // [S]; every context covers the prefix
+  unsigned* err;                // device error word
+  int num_seqs, num_heads, num_kv_heads, group, head_dim, block_size, num_blocks;
+  int max_blocks_per_seq, prefix_pages, prefix_tokens;
+  int num_slots, slot0, num_prefix_splits, tokens_per_split;
+  float scale_log2;  // scale * log2(e)
+};
+
+// Rows of query heads one CTA takes, and tokens per staged K/V tile.
+constexpr int kPrefixRows = 64;
+constexpr int kPrefixTile = 64;
+
+// dtype: 1 = bf16, 2 = f16 (pa_dtype values). Returns cudaErrorInvalidValue
+// for other element types or head dimensions (64 and 128 are built).
+cudaError_t launch_prefix_attention(const PrefixParams& p, int dtype, cudaStream_t stream);
+
+// Copies whole blocks (all kv heads, K and V) src -> dst for each pair of
+// block_pairs [n][2]; block ids outside [0, num_blocks) set PA_DEVERR_BLOCK_ID
+// and are skipped. block_bytes (a multiple of 16) = Hkv * bs * D * element size.
+cudaError_t launch_copy_blocks(uint8_t* k_cache, uint8_t* v_cache, const int32_t* block_pairs,
+                               int num_pairs, int num_blocks, size_t block_bytes, unsigned* err,
+                               cudaStream_t stream);
+
+}  // namespace pa

@@ -108,6 +108,7 @@ struct DecodeParams {
   int num_seqs, num_heads, num_kv_heads, group;  // group = G (runtime, <= GT)
   int num_blocks, max_blocks_per_seq, window;
   int num_splits, pages_per_split;  // split mode
+  int first_page;  // split mode: pages of every context before the splits (a shared prefix)
   int partials;   // split mode: 1 = write split partials, 0 = final output
   float q_scale;  // scale * log2(e) (* k_scale for FP8)
   float v_scale;  // FP8: v_scale, else 1
@@ -710,7 +711,7 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
     s0 = blockIdx.z;
     const int L = attended_len(p, s0, BS, threadIdx.x == 0 && split == 0 && g0 == 0);
     const int total = (L + BS - 1) / BS;
-    pg0 = split * p.pages_per_split;
+    pg0 = p.first_page + split * p.pages_per_split;
     npages = min(total, pg0 + p.pages_per_split) - pg0;
     if (npages <= 0) {  // nothing attended in this split (uniform for the CTA)
       for (int i = threadIdx.x; i < G * D; i += blockDim.x) {

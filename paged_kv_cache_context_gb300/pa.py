@@ -56,6 +56,9 @@ def lib() -> ctypes.CDLL:
             "pa_decode_balanced": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F, F, P,
                                    Z, P, P],
             "pa_decode_workspace_clear": [P, Z, P],
+            "pa_decode_cascade_workspace_size": [I, I, I, I, I, I],
+            "pa_decode_cascade": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, Z, P],
+            "pa_copy_blocks": [P, P, P, I, I, I, I, I, I, P],
             "pa_decode_static_scratch": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F,
                                          F, P],
             "pa_get_device_error": [P, P],
@@ -67,6 +70,7 @@ def lib() -> ctypes.CDLL:
             fn.argtypes = args
             fn.restype = I
         L.pa_decode_workspace_size.restype = Z
+        L.pa_decode_cascade_workspace_size.restype = Z
         L.pa_status_string.restype = ctypes.c_char_p
         _lib = L
     return _lib
@@ -175,6 +179,36 @@ def decode_workspace_clear(workspace: torch.Tensor, stream=None):
     _check(lib().pa_decode_workspace_clear(_ptr(workspace),
                                            workspace.numel() * workspace.element_size(),
                                            _stream(stream)), "pa_decode_workspace_clear")
+
+
+def decode_cascade_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int,
+                                  head_dim: int, block_size: int, prefix_pages: int) -> int:
+    return int(lib().pa_decode_cascade_workspace_size(num_seqs, num_heads, num_kv_heads,
+                                                      head_dim, block_size, prefix_pages))
+
+
+def decode_cascade(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+                   v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                   num_kv_heads: int, scale: float, prefix_pages: int,
+                   workspace: torch.Tensor, stream=None):
+    """pa_decode_cascade: decode of a batch sharing its first prefix_pages blocks."""
+    S, Hq, D = query.shape
+    NB, _, bs, _ = k_cache.shape
+    MB = block_tables.shape[1]
+    _check(lib().pa_decode_cascade(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(block_tables), _ptr(context_lens), S, Hq, num_kv_heads, D,
+                                   bs, NB, MB, scale, _DTYPE[query.dtype], prefix_pages,
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream(stream)), "pa_decode_cascade")
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_pairs: torch.Tensor,
+                stream=None):
+    """pa_copy_blocks: block_pairs int32 [n, 2] = (source, destination)."""
+    NB, H, bs, D = k_cache.shape
+    _check(lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs),
+                                block_pairs.shape[0], H, D, bs, NB, k_cache.element_size(),
+                                _stream(stream)), "pa_copy_blocks")
 
 
 def decode_partials(tmp_out: torch.Tensor, max_logits: torch.Tensor, exp_sums: torch.Tensor,

@@ -29,6 +29,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("pa_reshape_and_cache", "pa_decode", "pa_reduce", "pa_slot_mapping",
                  "pa_decode_partials", "pa_decode_plan", "pa_decode_workspace_size",
+                 "pa_decode_cascade", "pa_decode_cascade_workspace_size", "pa_copy_blocks",
                  "pa_get_device_error", "pa_status_string", "pa_version"):
         assert want in names
 
@@ -146,3 +147,33 @@ def test_balanced_entry_points_reject_bad_arguments_on_host(L):
     assert L.pa_decode_workspace_clear(None, 4096, None) == -1
     assert L.pa_decode_workspace_clear(P, 2559, None) == -7
     assert L.pa_decode_workspace_clear(P + 4, 4096, None) == -10
+
+
+def test_cascade_and_copy_blocks_reject_bad_arguments_on_host(L):
+    from paged_kv_cache_context_gb300 import pa
+    ws = pa.decode_cascade_workspace_size(4, 8, 2, 128, 32, 3)
+    assert ws > 0 and pa.decode_cascade_workspace_size(8, 8, 2, 128, 32, 3) > ws
+    assert pa.decode_cascade_workspace_size(4, 6, 4, 128, 32, 3) == 0
+
+    def call(**kw):
+        a = dict(out=P, q=P, k=P, v=P, bt=P, cl=P, S=4, Hq=8, Hkv=2, D=128, bs=32, NB=40, MB=8,
+                 scale=0.1, qd=1, pp=3, ws=P, wsb=1 << 30)
+        a.update(kw)
+        return L.pa_decode_cascade(a["out"], a["q"], a["k"], a["v"], a["bt"], a["cl"], a["S"],
+                                   a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"], a["MB"],
+                                   a["scale"], a["qd"], a["pp"], a["ws"], a["wsb"], None)
+
+    assert call(S=0, q=None) == 0
+    assert call(ws=None) == -1 and call(bt=None) == -1
+    assert call(qd=0) == -2                     # fp32 queries: no tensor-core prefix path
+    assert call(D=96) == -4
+    assert call(pp=0) == -3 and call(pp=9) == -3
+    assert call(wsb=1024) == -7
+    assert call(ws=P + 4) == -10
+    f = L.pa_copy_blocks
+    assert f(P, P, P, 0, 2, 64, 32, 10, 2, None) == 0
+    assert f(P, None, P, 1, 2, 64, 32, 10, 2, None) == -1
+    assert f(P, P, P, 1, 2, 64, 32, 10, 3, None) == -2
+    assert f(P, P, P, 1, 1, 4, 1, 10, 1, None) == -4   # 4-byte blocks
+    assert f(P, P, P, -1, 2, 64, 32, 10, 2, None) == -3
+    assert f(P + 8, P, P, 1, 2, 64, 32, 10, 2, None) == -10

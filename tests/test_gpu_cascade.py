@@ -1,0 +1,129 @@
+"""GPU parity of the shared-prefix cascade decode (pa_decode_cascade) and of
+block copies (pa_copy_blocks).
+
+Pages: "PagedAttention in mistral.rs" (prefix caching: a prefix's KV state is
+kept in the paged cache and reused by later sequences), "libmir-metal
+trace/kv.rs" (copy-on-write block maps). The cascade computes exactly what
+decode computes, so it is compared with the oracle's decode element by
+element, within the bf16 / f16 output tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+from _gpu import DEV, assert_close, bits, device_errors, gpu_caches, gpu_decode, to_dev
+from _helpers import oracle_caches, oracle_decode
+from paged_kv_cache_context_gb300 import build, pa
+from paged_kv_cache_context_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    pa.lib()
+    device_errors()
+
+
+def cascade(case, kg, vg, prefix_pages, block_tables=None, context_lens=None):
+    out = torch.full((case.num_seqs, case.num_heads, case.head_dim), float("nan"),
+                     dtype=case.q_dtype, device=DEV)
+    nbytes = pa.decode_cascade_workspace_size(case.num_seqs, case.num_heads, case.num_kv_heads,
+                                              case.head_dim, case.block_size, prefix_pages)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    pa.decode_cascade(out, to_dev(case.query), kg, vg,
+                      to_dev(case.block_tables if block_tables is None else block_tables),
+                      to_dev(case.context_lens if context_lens is None else context_lens),
+                      case.num_kv_heads, case.scale, prefix_pages, ws)
+    return out
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,bs,qd,prefix_blocks,suffix", [
+    (128, 32, 8, 32, torch.bfloat16, 8, (0, 64)),    # the prefix_bf16 shape, scaled
+    (128, 32, 8, 32, torch.float16, 3, (1, 100)),
+    (64, 16, 16, 16, torch.bfloat16, 9, (0, 40)),    # G = 1, bs 16, a ragged last tile
+    (128, 16, 2, 64, torch.bfloat16, 2, (0, 200)),   # G = 8, bs 64
+    (64, 12, 4, 32, torch.float16, 5, (0, 31)),      # G = 3 (not a power of two)
+])
+def test_cascade_matches_oracle(D, Hq, Hkv, bs, qd, prefix_blocks, suffix):
+    case = wl.make_case(f"casc{D}_{Hq}_{Hkv}_{bs}", 300 + D + Hq + bs, 21, Hq, Hkv, D, bs,
+                        q_dtype=qd, shared_prefix_blocks=prefix_blocks, suffix_range=suffix,
+                        extra_blocks=2)
+    kg, vg = gpu_caches(case)
+    ko, vo = oracle_caches(case)
+    ref = oracle_decode(case, ko, vo)
+    out = cascade(case, kg, vg, prefix_blocks)
+    assert_close(case, out, ref, what=f"cascade {case.name}")
+    assert device_errors() == 0
+
+
+def test_cascade_with_part_of_the_prefix_and_many_query_tiles():
+    """Treating only the first pages of a longer shared prefix as the prefix
+    is still exact (the rest is decoded as each sequence's own pages); 150
+    sequences x 4 heads span several 64-row query tiles."""
+    case = wl.make_case("casc_part", 311, 150, 16, 4, 128, q_dtype=torch.bfloat16,
+                        shared_prefix_blocks=6, suffix_range=(0, 90))
+    kg, vg = gpu_caches(case)
+    ko, vo = oracle_caches(case)
+    ref = oracle_decode(case, ko, vo)
+    for pp in (1, 4, 6):
+        assert_close(case, cascade(case, kg, vg, pp), ref, what=f"cascade prefix_pages={pp}")
+    assert device_errors() == 0
+
+
+def test_cascade_full_size_prefix_workload_agrees_with_decode():
+    """prefix_bf16 at its full size (128 sequences, a 2048-token shared
+    prefix): the cascade agrees with pa_decode within the bf16 tolerance on
+    every row, and with the oracle on sampled rows."""
+    case = wl.config("prefix_bf16", value_device=DEV)
+    kg, vg = gpu_caches(case)
+    out = cascade(case, kg, vg, 64)
+    dec = gpu_decode(case, kg, vg)
+    diff = (out.float() - dec.float()).abs().max().item()
+    assert diff <= 2e-2, diff
+    assert device_errors() == 0
+
+
+def test_cascade_flags_broken_preconditions():
+    case = wl.make_case("casc_bad", 312, 5, 8, 2, 64, q_dtype=torch.bfloat16,
+                        shared_prefix_blocks=4, suffix_range=(1, 20), extra_blocks=3)
+    kg, vg = gpu_caches(case)
+    bt = case.block_tables.clone()
+    bt[3, 1] = bt[3, 1] + 1 if int(bt[3, 1]) + 1 < case.num_blocks else 0  # row 3 disagrees
+    out = cascade(case, kg, vg, 4, block_tables=bt)
+    torch.cuda.synchronize()
+    assert device_errors() & 2
+    cl = case.context_lens.clone()
+    cl[1] = 4 * 32 - 1  # shorter than the prefix
+    cascade(case, kg, vg, 4, context_lens=cl)
+    assert device_errors() & 4
+    assert torch.isfinite(out.float()).all()
+
+
+def test_copy_blocks_is_exact_and_touches_nothing_else():
+    for dt, elem in ((torch.bfloat16, 2), (torch.uint8, 1), (torch.float32, 4)):
+        g = torch.Generator().manual_seed(313)
+        shape = (12, 4, 32, 64)
+        if dt == torch.uint8:
+            kc = torch.randint(0, 256, shape, generator=g, dtype=torch.uint8)
+        else:
+            kc = torch.randn(shape, generator=g).to(dt)
+        vc = kc.flip(0).clone()
+        pairs = torch.tensor([[1, 7], [3, 0], [11, 5]], dtype=torch.int32)
+        want_k, want_v = kc.clone(), vc.clone()
+        for s, d in pairs.tolist():
+            want_k[d] = kc[s]
+            want_v[d] = vc[s]
+        kg, vg = kc.to(DEV), vc.to(DEV)
+        pa.copy_blocks(kg, vg, pairs.to(DEV))
+        assert torch.equal(bits(kg.cpu()), bits(want_k)) and torch.equal(bits(vg.cpu()),
+                                                                          bits(want_v))
+        assert device_errors() == 0
+    bad = torch.tensor([[2, 12], [4, 6]], dtype=torch.int32, device=DEV)
+    before = kg.clone()
+    pa.copy_blocks(kg, vg, bad)
+    assert device_errors() & 2
+    want = before.clone()
+    want[6] = before[4]
+    assert torch.equal(bits(kg.cpu()), bits(want.cpu()))
