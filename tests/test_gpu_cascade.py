@@ -127,3 +127,19 @@ def test_copy_blocks_is_exact_and_touches_nothing_else():
     want = before.clone()
     want[6] = before[4]
     assert torch.equal(bits(kg.cpu()), bits(want.cpu()))
+
+
+def test_cascade_when_some_contexts_end_at_the_prefix():
+    """A context exactly as long as the prefix has no page of its own: its
+    output is the prefix's attention alone."""
+    import dataclasses
+    case = wl.make_case("casc_end", 314, 7, 8, 2, 128, q_dtype=torch.bfloat16,
+                        shared_prefix_blocks=3, suffix_range=(0, 50))
+    kg, vg = gpu_caches(case)
+    cl = case.context_lens.clone()
+    cl[::2] = 3 * 32
+    short = dataclasses.replace(case, context_lens=cl)
+    ko, vo = oracle_caches(case)
+    ref = oracle_decode(short, ko, vo)
+    assert_close(short, cascade(short, kg, vg, 3), ref, what="cascade, empty suffixes")
+    assert device_errors() == 0
