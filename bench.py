@@ -6,6 +6,9 @@ write of every sequence's new token (pa_reshape_and_cache), then the two
 stream operations of pa_decode's balanced path: the zero fill of the arrival
 counters (pa_decode_workspace_clear) and the persistent decode launch
 (pa_decode_balanced), whose CTAs also combine the contexts cut between them.
+With --path cascade (workloads whose block tables share prefix blocks) the
+decode is pa_decode_cascade instead: the shared prefix for all query heads at
+once, each sequence's own pages, and the combine.
 Default workload: the
 Mistral-7B-shaped bf16 batch (32 sequences, 32 query / 8 kv heads, head_dim
 128, block_size 32, context lengths U[512, 4096], shuffled block pool).
@@ -297,11 +300,26 @@ def run_ours(args, rank, local_rank, world):
     if f_clear(*clear_args) or f_dec(*dec_args[0]):
         raise RuntimeError("pa_decode_balanced failed")
     launches_per_step = 3  # cache write, counter clear, decode
+    prefix_pages = case.shared_prefix_tokens // bs
+    if args.path == "cascade":
+        # pa_decode_cascade: prefix attention + suffix decode + reduce
+        if prefix_pages < 1:
+            raise SystemExit("--path cascade needs a workload with a shared prefix")
+        ws_bytes = pa.decode_cascade_workspace_size(S, Hq, Hkv, D, bs, prefix_pages)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        dec_args = [(ptr(out), ptr(q), ptr(k_), ptr(v_), ptr(bt), ptr(cl), I(S), I(Hq), I(Hkv),
+                     I(D), I(bs), I(NB), I(MB), F(case.scale), I(qd), I(prefix_pages), ptr(ws),
+                     Z(ws_bytes), sp) for (k_, v_) in reps]
+        f_dec = L.pa_decode_cascade
+        if f_dec(*dec_args[0]):
+            raise RuntimeError("pa_decode_cascade failed")
+        launches_per_step = 4  # cache write, prefix attention, suffix decode, reduce
 
     def step(i, ev_a=None, ev_b=None):
         r = i % len(reps)
         rc = f_write(*write_args[r])
-        rc |= f_clear(*clear_args)
+        if args.path != "cascade":
+            rc |= f_clear(*clear_args)
         if ev_a is not None:
             ev_a.record(stream)
         rc |= f_dec(*dec_args[r])
@@ -343,6 +361,17 @@ def run_ours(args, rank, local_rank, world):
     split_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
 
     sb = step_bytes(case)
+    if args.path == "cascade":
+        # HBM bytes the cascade must move: the prefix K/V once per kv head for
+        # the whole batch, each sequence's own K/V, q and out, and the
+        # partials (fp32, written and read once) of the prefix ranges and the
+        # suffix
+        nslots = ws_bytes // (4 * S * Hq * (D + 2))
+        elem = torch.finfo(case.q_dtype).bits // 8
+        unique_kv = (case.shared_prefix_tokens + sum(
+            case.attended(s) - case.shared_prefix_tokens for s in range(S))) * Hkv * D * 2 * elem
+        sb["kernel"] = (unique_kv + S * Hq * D * 2 * elem + 2 * S * Hq * nslots * (D + 2) * 4 +
+                        S * MB * 4 + S * 4)
     elapsed_max = all_reduce(elapsed, "max", dev)
     bytes_all = all_reduce(float(sb["total"] * K), "sum", dev)
     seqs_all = all_reduce(float(S * K), "sum", dev)
@@ -365,7 +394,8 @@ def run_ours(args, rank, local_rank, world):
                    "window": case.window, "cache_dtype": case.kv_dtype if case.kv_dtype != "auto"
                    else str(case.q_dtype).replace("torch.", ""),
                    "storage_dtype": str(case.q_dtype).replace("torch.", ""),
-                   "decode_ctas": num_ctas.value, "workspace_bytes": ws_bytes,
+                   "decode_path": args.path, "decode_ctas": num_ctas.value,
+                   "workspace_bytes": ws_bytes,
                    "kv_bytes_per_step": sb["kv"], "bytes_per_step": sb["total"],
                    "l2": f"{args.replicas} rotating cache replicas of "
                          f"{kc.numel() * kc.element_size() * 2 / 1e6:.0f} MB (> L2)",
@@ -374,8 +404,11 @@ def run_ours(args, rank, local_rank, world):
         "pct_of_nominal_8tbs": round(100 * bytes_all / elapsed_max / 1e9 / NOMINAL_HBM_GBS, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": measured_traffic(args.workload),
-                     "kernel": "paged_decode_kernel (balanced mode)",
+                     "traffic": (measured_traffic(args.workload)
+                                 if args.path != "cascade" else None),
+                     "kernel": ("pa_decode_cascade: prefix attention + suffix decode + reduce"
+                                if args.path == "cascade" else
+                                "paged_decode_kernel (balanced mode)"),
                      "kernel_bytes_per_launch": sb["kernel"],
                      "kernel_us_mean": round(split_mean * 1e6, 2),
                      "kernel_us_median": round(statistics.median(split_ms) * 1e3, 2)},
@@ -398,8 +431,12 @@ def run_e2e(args, case, pa, L, dev, stream, reps, new_sm, bt, cl, q, new_k, new_
             (("q", q), ("k", new_k), ("v", new_v), ("sm", new_sm), ("cl", cl), ("bt", bt))}
     dev_bufs = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    wsb = pa.decode_workspace_size(S, Hq, Hkv, D, case.block_size, case.max_blocks_per_seq,
-                                   case.window)
+    prefix_pages = case.shared_prefix_tokens // case.block_size
+    if args.path == "cascade":
+        wsb = pa.decode_cascade_workspace_size(S, Hq, Hkv, D, case.block_size, prefix_pages)
+    else:
+        wsb = pa.decode_workspace_size(S, Hq, Hkv, D, case.block_size, case.max_blocks_per_seq,
+                                       case.window)
     ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size()
@@ -411,8 +448,12 @@ def run_e2e(args, case, pa, L, dev, stream, reps, new_sm, bt, cl, q, new_k, new_
             dev_bufs[n].copy_(t, non_blocking=True)
         pa.reshape_and_cache(dev_bufs["k"], dev_bufs["v"], k_, v_, dev_bufs["sm"],
                              case.kv_dtype, case.k_scale, case.v_scale)
-        pa.decode(out, dev_bufs["q"], k_, v_, dev_bufs["bt"], dev_bufs["cl"], Hkv, case.scale,
-                  case.window, case.kv_dtype, case.k_scale, case.v_scale, ws)
+        if args.path == "cascade":
+            pa.decode_cascade(out, dev_bufs["q"], k_, v_, dev_bufs["bt"], dev_bufs["cl"], Hkv,
+                              case.scale, prefix_pages, ws)
+        else:
+            pa.decode(out, dev_bufs["q"], k_, v_, dev_bufs["bt"], dev_bufs["cl"], Hkv,
+                      case.scale, case.window, case.kv_dtype, case.k_scale, case.v_scale, ws)
         out_h.copy_(out, non_blocking=True)
 
     for i in range(args.warmup):
@@ -490,6 +531,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="mistral_bf16",
                     choices=("tiny", "mistral_bf16", "ring_bf16", "fp8_phi3", "prefix_bf16"))
     ap.add_argument("--replicas", type=int, default=4)
+    ap.add_argument("--path", choices=("balanced", "cascade"), default="balanced",
+                    help="decode entry point timed: pa_decode's balanced path, or "
+                         "pa_decode_cascade (workloads with a shared prefix)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
