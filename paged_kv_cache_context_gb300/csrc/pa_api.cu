@@ -699,17 +699,9 @@ PA_API pa_status pa_decode_cascade(void* out, const void* query, const void* k_c
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   unsigned* err = error_word();
 
-  // slot 0: each sequence's own pages after the prefix, one CTA per (sequence, kv head)
-  DecodeParams p = make_params(a, query, k_cache, v_cache, block_tables, context_lens, scale, err);
-  p.tmp_out = tmp;
-  p.max_logits = ml;
-  p.exp_sums = es;
-  p.partials = 1;
-  p.num_splits = ns;
-  p.first_page = prefix_pages;
-  p.pages_per_split = max_blocks_per_seq - prefix_pages > 0 ? max_blocks_per_seq - prefix_pages : 1;
-  if (run_decode(p, a, dim3(1, num_kv_heads, num_seqs), kModeSplit, nullptr, st) != cudaSuccess)
-    return PA_ERR_CUDA;
+  // The prefix launch goes first and waits for the launches before it; the
+  // suffix launch then starts at once and runs beside it (they share only
+  // inputs), and waits for it at its end, so the combine sees both.
   // slots 1 .. nsp: the shared prefix, all sequences' query heads at once
   PrefixParams q{};
   q.tmp_out = tmp;
@@ -737,6 +729,18 @@ PA_API pa_status pa_decode_cascade(void* out, const void* query, const void* k_c
   q.tokens_per_split = tps;
   q.scale_log2 = scale * 1.4426950408889634f;
   if (launch_prefix_attention(q, q_dtype, st) != cudaSuccess) return PA_ERR_CUDA;
+  // slot 0: each sequence's own pages after the prefix, one CTA per (sequence, kv head)
+  DecodeParams p = make_params(a, query, k_cache, v_cache, block_tables, context_lens, scale, err);
+  p.tmp_out = tmp;
+  p.max_logits = ml;
+  p.exp_sums = es;
+  p.partials = 1;
+  p.num_splits = ns;
+  p.first_page = prefix_pages;
+  p.pages_per_split = max_blocks_per_seq - prefix_pages > 0 ? max_blocks_per_seq - prefix_pages : 1;
+  p.join_at_end = 1;  // runs beside the prefix launch, which it waits for at its end
+  if (run_decode(p, a, dim3(1, num_kv_heads, num_seqs), kModeSplit, nullptr, st) != cudaSuccess)
+    return PA_ERR_CUDA;
   // the log-sum-exp combination of the ns slots
   return run_reduce(out, tmp, ml, es, (int64_t)num_seqs * num_heads, head_dim, ns, q_dtype, st) ==
                  cudaSuccess

@@ -109,6 +109,10 @@ struct DecodeParams {
   int num_blocks, max_blocks_per_seq, window;
   int num_splits, pages_per_split;  // split mode
   int first_page;  // split mode: pages of every context before the splits (a shared prefix)
+  // split mode: start without waiting for the previous launch on the stream
+  // and wait for it at the end instead (the previous launch reads nothing
+  // this one writes and has itself waited for everything before it)
+  int join_at_end;
   int partials;   // split mode: 1 = write split partials, 0 = final output
   float q_scale;  // scale * log2(e) (* k_scale for FP8)
   float v_scale;  // FP8: v_scale, else 1
@@ -681,9 +685,7 @@ __device__ __forceinline__ void publish_piece(const DecodeParams& p, const CutPi
 }
 
 template <typename QT, typename CT, int D, int GT, int BS, int MODE>
-__global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
-                                  Layout<QT, CT, D, GT, BS>::MIN_CTAS)
-    paged_decode_kernel(const __grid_constant__ DecodeParams p) {
+__device__ __forceinline__ void decode_body(const DecodeParams& p) {
   using Ly = Layout<QT, CT, D, GT, BS>;
   constexpr int NC = Ly::NC, STAGES = Ly::STAGES, R = Ly::R, TPW = Ly::TPW;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -691,8 +693,6 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = p.num_heads, Hkv = p.num_kv_heads, G = p.group;
   const int MB = p.max_blocks_per_seq;
-  pdl_wait();
-  pdl_trigger();
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Ly::OFF_BAR);
   uint64_t* empty = full + STAGES;
@@ -1071,6 +1071,22 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
         combine_segment<QT, Ly, GT, D>(p, reinterpret_cast<QT*>(p.out) + (size_t)cp.row * D,
                                        cp.seg0, cp.pages, P, gridDim.x, G, warp, NC, lane);
     }
+  }
+}
+
+template <typename QT, typename CT, int D, int GT, int BS, int MODE>
+__global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
+                                  Layout<QT, CT, D, GT, BS>::MIN_CTAS)
+    paged_decode_kernel(const __grid_constant__ DecodeParams p) {
+  if constexpr (MODE == kModeSplit) {
+    if (!p.join_at_end) pdl_wait();
+    pdl_trigger();
+    decode_body<QT, CT, D, GT, BS, MODE>(p);
+    if (p.join_at_end) pdl_wait();
+  } else {
+    pdl_wait();
+    pdl_trigger();
+    decode_body<QT, CT, D, GT, BS, MODE>(p);
   }
 }
 
