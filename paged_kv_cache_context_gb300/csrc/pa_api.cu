@@ -637,12 +637,13 @@ PA_API pa_status pa_decode(void* out, const void* query, const void* k_cache,
 }
 
 // ================================================================ cascade
-// Split of the shared prefix into ranges of whole 64-token tiles, enough of
-// them that (query tiles x kv heads x splits) gives about two CTAs per SM.
+// Split of the shared prefix into ranges of whole 64-token tiles: as many as
+// keep (query tiles x kv heads x splits) within one wave of two CTAs per SM
+// (a second, partial wave would double the time), at least one.
 static void cascade_plan(int S, int G, int Hkv, int prefix_tokens, int* nsp, int* tps) {
   const int qtiles = (S * G + kPrefixRows - 1) / kPrefixRows;
   const int tiles = (prefix_tokens + kPrefixTile - 1) / kPrefixTile;
-  const int64_t want = (2 * 152 + (int64_t)qtiles * Hkv - 1) / ((int64_t)qtiles * Hkv);
+  const int64_t want = (2 * 152) / ((int64_t)qtiles * Hkv);
   int n = static_cast<int>(want < 1 ? 1 : (want > tiles ? tiles : want));
   const int tiles_per = (tiles + n - 1) / n;
   *tps = tiles_per * kPrefixTile;

@@ -203,18 +203,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     const uint32_t kb = sk_u + buf * TBYTES, vb = sv_u + buf * TBYTES;
 
-    // S = Q K^T for 16 rows x 64 tokens
+    // S = Q K^T for 16 rows x 64 tokens; the 8 token tiles are independent
+    // accumulators, so each k-step issues 8 MMAs that do not wait on each
+    // other
     float s[NT][4];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+    for (int j = 0; j < NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < KS; kk += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb + swz<CPR>(8 * j + (lane & 7), 2 * kk + (lane >> 3)), b0, b1, b2, b3);
+    for (int kk = 0; kk < KS; kk += 2) {
+      uint32_t b2[NT], b3[NT];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        uint32_t b0, b1;
+        ldsm_x4(kb + swz<CPR>(8 * j + (lane & 7), 2 * kk + (lane >> 3)), b0, b1, b2[j], b3[j]);
         Mma<T>::run(s[j], qa[kk], b0, b1);
-        Mma<T>::run(s[j], qa[kk + 1], b2, b3);
       }
+#pragma unroll
+      for (int j = 0; j < NT; ++j) Mma<T>::run(s[j], qa[kk + 1], b2[j], b3[j]);
     }
     // scale to log2 units, mask tokens past the range, running maximum
     const int t0 = t_begin + tile * TILE;
