@@ -1050,14 +1050,17 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
     if (tail_cut) {
       // The tail piece, counted here. If every other piece of its segment
       // has been counted already, it completes the segment and needs no
-      // publishing; otherwise publish it (the consumer barrier that ended
-      // finish_piece ordered every thread's rows before lane 0's fence) and
-      // count it.
+      // counting; otherwise count it (the consumer barrier that ended
+      // finish_piece ordered every thread's rows before lane 0's fence).
       const CutPiece cp = *reinterpret_cast<const CutPiece*>(smem + Ly::OFF_MISC + 32 + 24);
       const long long P = misc64[1];
       if (warp == 0 && lane == 0) {
         int* cnt = p.arrived + cta_of(cp.seg0 + cp.pages - 1, P, gridDim.x);
         int last = ld_acquire_gpu(cnt) + cp.len == cp.pages ? 1 : 0;
+        // completing without counting: this CTA's own rows of the piece still
+        // have to reach device scope, since the combine reads them (like every
+        // other piece) through L2
+        if (last) fence_acq_rel_gpu();
         if (!last) {
           fence_acq_rel_gpu();
           last = atomicAdd(cnt, cp.len) + cp.len == cp.pages ? 1 : 0;
