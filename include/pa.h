@@ -365,6 +365,37 @@ pa_status pa_decode_static_scratch(void* out, const void* query,
                                    pa_stream_t stream);
 
 /*
+ * pa_block_budget -- how many cache blocks a KV memory budget buys
+ * ("PagedAttention in mistral.rs", "Using the CLI" and the Rust API
+ * example: the pool is sized by a GPU memory amount in MB, by a fraction of
+ * the GPU's memory, or by a context size in tokens; the block size is the
+ * number of tokens per block). Host only; never touches the GPU.
+ *
+ * One block holds block_size tokens of K and V for every kv head of every
+ * layer:  block_bytes = num_layers * 2 * num_kv_heads * block_size * head_dim
+ *                       * element size (4 for F32, 2 for BF16/F16, 1 for an
+ *                       FP8 E4M3 cache).
+ *   PA_BUDGET_MB:       amount = MB (2^20 bytes) for the cache;
+ *                       blocks = floor(amount * 2^20 / block_bytes).
+ *   PA_BUDGET_FRACTION: amount in (0, 1] of available_bytes (the caller's
+ *                       figure, e.g. free device memory);
+ *                       blocks = floor(amount * available_bytes / block_bytes).
+ *   PA_BUDGET_CONTEXT:  amount = tokens of context to hold;
+ *                       blocks = ceil(amount / block_size).
+ * Returns the number of blocks (>= 0), or a negative pa_status: PA_ERR_SHAPE
+ * for a non-positive layer / head / block count or an amount out of range,
+ * PA_ERR_DTYPE for unknown types, PA_ERR_HEAD_DIM for head_dim <= 0.
+ */
+typedef enum {
+    PA_BUDGET_MB = 0,
+    PA_BUDGET_FRACTION = 1,
+    PA_BUDGET_CONTEXT = 2
+} pa_budget_kind;
+int64_t pa_block_budget(pa_budget_kind kind, double amount, size_t available_bytes,
+                        int num_layers, int num_kv_heads, int head_dim, int block_size,
+                        pa_dtype dtype, pa_kv_dtype kv_dtype);
+
+/*
  * pa_get_device_error -- synchronise `stream`, then read and clear the error
  * word of the current device. *error_bits (may be NULL) receives the
  * PA_DEVERR_* bits. Returns PA_OK when no bit was set, PA_ERR_DEVICE when

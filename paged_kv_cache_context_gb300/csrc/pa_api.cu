@@ -5,6 +5,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "pa_cascade.cuh"
@@ -765,6 +766,37 @@ PA_API pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* blo
                             reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
+}
+
+// ================================================================ pool sizing
+PA_API int64_t pa_block_budget(pa_budget_kind kind, double amount, size_t available_bytes,
+                               int num_layers, int num_kv_heads, int head_dim, int block_size,
+                               pa_dtype dtype, pa_kv_dtype kv_dtype) {
+  if (num_layers <= 0 || num_kv_heads <= 0 || block_size <= 0) return PA_ERR_SHAPE;
+  if (head_dim <= 0) return PA_ERR_HEAD_DIM;
+  if (!valid_dtype(dtype) || (kv_dtype != PA_KV_AUTO && kv_dtype != PA_KV_FP8_E4M3))
+    return PA_ERR_DTYPE;
+  if (!(amount >= 0.0) || !isfinite(amount)) return PA_ERR_SHAPE;
+  const int64_t elem = kv_dtype == PA_KV_FP8_E4M3 ? 1 : (dtype == PA_F32 ? 4 : 2);
+  const double block_bytes =
+      (double)num_layers * 2.0 * num_kv_heads * block_size * head_dim * (double)elem;
+  double blocks = 0.0;
+  switch (kind) {
+    case PA_BUDGET_MB:
+      blocks = std::floor(amount * 1048576.0 / block_bytes);
+      break;
+    case PA_BUDGET_FRACTION:
+      if (amount > 1.0) return PA_ERR_SHAPE;
+      blocks = std::floor(amount * (double)available_bytes / block_bytes);
+      break;
+    case PA_BUDGET_CONTEXT:
+      blocks = std::ceil(amount / block_size);
+      break;
+    default:
+      return PA_ERR_SHAPE;
+  }
+  if (blocks > 9.0e18) return PA_ERR_SHAPE;
+  return static_cast<int64_t>(blocks);
 }
 
 PA_API pa_status pa_get_device_error(pa_stream_t stream, uint32_t* error_bits) {

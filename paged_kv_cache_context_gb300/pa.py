@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
             "pa_decode_cascade_workspace_size": [I, I, I, I, I, I],
             "pa_decode_cascade": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, Z, P],
             "pa_copy_blocks": [P, P, P, I, I, I, I, I, I, P],
+            "pa_block_budget": [I, ctypes.c_double, Z, I, I, I, I, I, I],
             "pa_decode_static_scratch": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F,
                                          F, P],
             "pa_get_device_error": [P, P],
@@ -71,6 +72,7 @@ def lib() -> ctypes.CDLL:
             fn.restype = I
         L.pa_decode_workspace_size.restype = Z
         L.pa_decode_cascade_workspace_size.restype = Z
+        L.pa_block_budget.restype = ctypes.c_int64
         L.pa_status_string.restype = ctypes.c_char_p
         _lib = L
     return _lib
@@ -209,6 +211,31 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_pairs: torch
     _check(lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs),
                                 block_pairs.shape[0], H, D, bs, NB, k_cache.element_size(),
                                 _stream(stream)), "pa_copy_blocks")
+
+
+PA_BUDGET_MB, PA_BUDGET_FRACTION, PA_BUDGET_CONTEXT = 0, 1, 2
+
+
+def block_budget(num_layers: int, num_kv_heads: int, head_dim: int, block_size: int,
+                 dtype: torch.dtype, kv_dtype: str = "auto", *, mb: Optional[float] = None,
+                 fraction: Optional[float] = None, context_tokens: Optional[int] = None,
+                 available_bytes: Optional[int] = None) -> int:
+    """pa_block_budget: cache blocks for a budget given as exactly one of mb,
+    fraction (of available_bytes, by default the device's free memory) or
+    context_tokens."""
+    given = [x is not None for x in (mb, fraction, context_tokens)]
+    if sum(given) != 1:
+        raise ValueError("give exactly one of mb, fraction, context_tokens")
+    if fraction is not None and available_bytes is None:
+        available_bytes = torch.cuda.mem_get_info()[0]
+    kind, amount = ((PA_BUDGET_MB, mb) if mb is not None else
+                    (PA_BUDGET_FRACTION, fraction) if fraction is not None else
+                    (PA_BUDGET_CONTEXT, context_tokens))
+    n = lib().pa_block_budget(kind, float(amount), int(available_bytes or 0), num_layers,
+                              num_kv_heads, head_dim, block_size, _DTYPE[dtype], _KV[kv_dtype])
+    if n < 0:
+        raise PagedAttentionError(int(n), "pa_block_budget")
+    return int(n)
 
 
 def decode_partials(tmp_out: torch.Tensor, max_logits: torch.Tensor, exp_sums: torch.Tensor,

@@ -30,6 +30,7 @@ def test_header_declares_the_boundary():
     for want in ("pa_reshape_and_cache", "pa_decode", "pa_reduce", "pa_slot_mapping",
                  "pa_decode_partials", "pa_decode_plan", "pa_decode_workspace_size",
                  "pa_decode_cascade", "pa_decode_cascade_workspace_size", "pa_copy_blocks",
+                 "pa_block_budget",
                  "pa_get_device_error", "pa_status_string", "pa_version"):
         assert want in names
 
@@ -177,3 +178,47 @@ def test_cascade_and_copy_blocks_reject_bad_arguments_on_host(L):
     assert f(P, P, P, 1, 1, 4, 1, 10, 1, None) == -4   # 4-byte blocks
     assert f(P, P, P, -1, 2, 64, 32, 10, 2, None) == -3
     assert f(P + 8, P, P, 1, 2, 64, 32, 10, 2, None) == -10
+
+
+def test_block_budget_closed_forms(L):
+    """Pool sizing by a memory amount in MB, a fraction of memory, or a context
+    size ("PagedAttention in mistral.rs", Using the CLI and the Rust API): one
+    block is block_size tokens of K and V for every kv head of every layer."""
+    import torch
+    from paged_kv_cache_context_gb300 import pa
+    bf, f32 = torch.bfloat16, torch.float32
+    # 32 layers x K,V x 8 kv heads x 32 tokens x 128 dims x 2 bytes = 4 MiB a block
+    assert pa.block_budget(32, 8, 128, 32, bf, mb=4096) == 1024
+    assert pa.block_budget(32, 8, 128, 32, bf, mb=4095.99) == 1023
+    assert pa.block_budget(32, 8, 128, 32, bf, mb=3.99) == 0
+    # an FP8 cache holds twice the blocks of a 16-bit one, fp32 half
+    for mb in (1, 100, 777.5, 40_000):
+        n16 = pa.block_budget(4, 2, 64, 16, bf, mb=mb)
+        assert pa.block_budget(4, 2, 64, 16, bf, "fp8_e4m3", mb=mb) in (2 * n16, 2 * n16 + 1)
+        assert pa.block_budget(4, 2, 64, 16, f32, mb=mb) == n16 // 2
+        # the FP8 cache's size does not depend on the query type
+        assert (pa.block_budget(4, 2, 64, 16, f32, "fp8_e4m3", mb=mb)
+                == pa.block_budget(4, 2, 64, 16, bf, "fp8_e4m3", mb=mb))
+    # 0.95 of memory, the CLI's example fraction
+    blk = 32 * 2 * 8 * 32 * 128 * 2
+    assert pa.block_budget(32, 8, 128, 32, bf, fraction=1.0, available_bytes=100 * blk) == 100
+    assert pa.block_budget(32, 8, 128, 32, bf, fraction=0.95, available_bytes=100 * blk) == 95
+    assert pa.block_budget(32, 8, 128, 32, bf, fraction=0.95, available_bytes=100 * blk - 1) == 94
+    # a 1024-token context in 32-token blocks, the Rust API's example
+    assert pa.block_budget(32, 8, 128, 32, bf, context_tokens=1024) == 32
+    assert pa.block_budget(32, 8, 128, 32, bf, context_tokens=1025) == 33
+    assert pa.block_budget(32, 8, 128, 32, bf, context_tokens=0) == 0
+    # rejected on the host
+    f = L.pa_block_budget
+    assert f(0, 1.0, 0, 0, 8, 128, 32, 1, 0) == -3
+    assert f(0, 1.0, 0, 32, 0, 128, 32, 1, 0) == -3
+    assert f(0, 1.0, 0, 32, 8, 0, 32, 1, 0) == -4
+    assert f(0, 1.0, 0, 32, 8, 128, 0, 1, 0) == -3
+    assert f(0, 1.0, 0, 32, 8, 128, 32, 5, 0) == -2
+    assert f(0, 1.0, 0, 32, 8, 128, 32, 1, 2) == -2
+    assert f(0, -1.0, 0, 32, 8, 128, 32, 1, 0) == -3
+    assert f(0, float("nan"), 0, 32, 8, 128, 32, 1, 0) == -3
+    assert f(1, 1.5, 1 << 30, 32, 8, 128, 32, 1, 0) == -3
+    assert f(3, 1.0, 0, 32, 8, 128, 32, 1, 0) == -3
+    with pytest.raises(ValueError):
+        pa.block_budget(32, 8, 128, 32, bf, mb=1, context_tokens=1)
