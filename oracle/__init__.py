@@ -10,6 +10,8 @@ Functions follow the web pages on the subject:
     block, FP8 E4M3 cache ("KV Cache Quantization").
   * "Optimization plans" (mistral.rs discussion #46) -- reshape_and_cache.
   * "Rolling buffer cache" (llama.cpp discussion #3581) -- slot i mod W.
+  * "libmir-metal trace/kv.rs" -- INT8 pages with one FP32 scale per token
+    and head.
 """
 from __future__ import annotations
 
@@ -23,6 +25,7 @@ from . import build as _build
 # element codes of the oracle's own C interface
 _CODE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 _E4M3 = 3
+_I8 = 4
 
 _lib = None
 _i64 = ctypes.c_int64
@@ -52,11 +55,16 @@ def lib():
         L.oracle_decode_partial.restype = _int
         L.oracle_decode_partial.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
                                             _int, _int, _int, _int, _int, _int, _i64, _int,
-                                            _dbl, _int, _int, _int, _flt, _flt, _i64, _i64]
+                                            _dbl, _int, _int, _int, _flt, _flt, _ptr, _ptr,
+                                            _i64, _i64]
         L.oracle_decode_rows.restype = _i64
         L.oracle_decode_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _int, _int, _int,
                                          _int, _int, _i64, _int, _dbl, _int, _int, _int, _flt,
-                                         _flt, _ptr, _i64]
+                                         _flt, _ptr, _ptr, _ptr, _i64]
+        L.oracle_int8_quantise_row.argtypes = [_ptr, _int, _ptr, _ptr]
+        L.oracle_reshape_and_cache_int8.restype = _i64
+        L.oracle_reshape_and_cache_int8.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
+                                                    _i64, _int, _int, _int, _i64, _int]
         L.oracle_reduce.argtypes = [_ptr, _ptr, _ptr, _ptr, _i64, _int, _int]
         _lib = L
     return _lib
@@ -75,6 +83,9 @@ def _p(t) -> int:
 
 
 def _cache_code(cache: torch.Tensor, kv_dtype: str) -> int:
+    if kv_dtype == "int8":
+        assert cache.dtype == torch.int8
+        return _I8
     if kv_dtype == "fp8_e4m3":
         assert cache.dtype == torch.uint8
         return _E4M3
@@ -96,6 +107,19 @@ def e4m3_decode(b: np.ndarray) -> np.ndarray:
     out = np.empty(b.shape, dtype=np.float32)
     lib().oracle_e4m3_decode_array(_p(b), _p(out), b.size)
     return out
+
+
+# ---------------------------------------------------------------- INT8 rows
+def int8_quantise_rows(x: np.ndarray):
+    """INT8 per-row quantisation of a [rows, n] binary32 array: (codes int8
+    [rows, n], scales float32 [rows])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, n = x.shape
+    codes = np.empty((rows, n), dtype=np.int8)
+    scales = np.empty(rows, dtype=np.float32)
+    for r in range(rows):
+        lib().oracle_int8_quantise_row(_p(x[r]), n, _p(codes[r]), _p(scales[r:r + 1]))
+    return codes, scales
 
 
 # ---------------------------------------------------------------- slot mapping
@@ -131,14 +155,42 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping_, block_size: i
     return int(bad)
 
 
+def reshape_and_cache_int8(key, value, k_cache, v_cache, k_scales, v_scales, slot_mapping_,
+                           block_size: int) -> int:
+    """INT8 write of key/value [T, Hkv, D] into int8 caches [NB, Hkv, bs, D] and
+    fp32 scales [NB, Hkv, bs] (CPU tensors, in place). Returns the number of
+    tokens whose slot was beyond the pool."""
+    key, value = _cpu(key), _cpu(value)
+    sm = _cpu(slot_mapping_).to(torch.int64)
+    for t, dt in ((k_cache, torch.int8), (v_cache, torch.int8), (k_scales, torch.float32),
+                  (v_scales, torch.float32)):
+        assert t.device.type == "cpu" and t.is_contiguous() and t.dtype == dt
+    T, H, D = key.shape
+    bad = lib().oracle_reshape_and_cache_int8(_p(key), _p(value), _p(k_cache), _p(v_cache),
+                                              _p(k_scales), _p(v_scales), _p(sm), T, H, D,
+                                              block_size, k_cache.shape[0], _CODE[key.dtype])
+    return int(bad)
+
+
 # ---------------------------------------------------------------- decode
+def _row_scales(kv_dtype, k_scales, v_scales):
+    if kv_dtype != "int8":
+        return None, None
+    ks, vs = _cpu(k_scales), _cpu(v_scales)
+    assert ks.dtype == torch.float32 and vs.dtype == torch.float32
+    return ks, vs
+
+
 def decode(query, k_cache, v_cache, block_tables, context_lens, num_kv_heads: int,
            block_size: int, scale: float, window: int = 0, kv_dtype: str = "auto",
-           k_scale: float = 1.0, v_scale: float = 1.0, rows=None) -> np.ndarray:
+           k_scale: float = 1.0, v_scale: float = 1.0, rows=None, k_scales=None,
+           v_scales=None) -> np.ndarray:
     """fp64 attention output [S, Hq, D]; with ``rows`` (s*Hq+h indices) only those
-    rows are computed (the others stay NaN)."""
+    rows are computed (the others stay NaN). An "int8" cache takes its per-row
+    scales k_scales / v_scales [NB, Hkv, bs]."""
     q = _cpu(query)
     kc, vc = _cpu(k_cache), _cpu(v_cache)
+    ks, vs = _row_scales(kv_dtype, k_scales, v_scales)
     bt = _cpu(block_tables).to(torch.int32)
     cl = _cpu(context_lens).to(torch.int32)
     S, Hq, D = q.shape
@@ -150,6 +202,7 @@ def decode(query, k_cache, v_cache, block_tables, context_lens, num_kv_heads: in
                                    num_kv_heads, D, block_size, kc.shape[0], bt.shape[1],
                                    float(np.float32(scale)), window, _CODE[q.dtype],
                                    _cache_code(kc, kv_dtype), k_scale, v_scale,
+                                   None if ks is None else _p(ks), None if vs is None else _p(vs),
                                    None if r is None else _p(r), 0 if r is None else r.size)
     if bad:
         raise ValueError(f"oracle decode: {bad} rows met a block id outside the pool")
@@ -159,10 +212,11 @@ def decode(query, k_cache, v_cache, block_tables, context_lens, num_kv_heads: in
 def decode_partial(query, k_cache, v_cache, block_tables, context_lens, s: int, h: int,
                    num_kv_heads: int, block_size: int, scale: float, tok_begin: int,
                    tok_end: int, window: int = 0, kv_dtype: str = "auto",
-                   k_scale: float = 1.0, v_scale: float = 1.0):
+                   k_scale: float = 1.0, v_scale: float = 1.0, k_scales=None, v_scales=None):
     """(o [D] fp64, m, l) of head h of sequence s over slots [tok_begin, tok_end)."""
     q = _cpu(query)
     kc, vc = _cpu(k_cache), _cpu(v_cache)
+    ks, vs = _row_scales(kv_dtype, k_scales, v_scales)
     bt = _cpu(block_tables).to(torch.int32)
     cl = _cpu(context_lens).to(torch.int32)
     S, Hq, D = q.shape
@@ -173,8 +227,9 @@ def decode_partial(query, k_cache, v_cache, block_tables, context_lens, s: int, 
                                      _p(kc), _p(vc), _p(bt), _p(cl), s, h, Hq, num_kv_heads, D,
                                      block_size, kc.shape[0], bt.shape[1],
                                      float(np.float32(scale)), window, _CODE[q.dtype],
-                                     _cache_code(kc, kv_dtype), k_scale, v_scale, tok_begin,
-                                     tok_end)
+                                     _cache_code(kc, kv_dtype), k_scale, v_scale,
+                                     None if ks is None else _p(ks),
+                                     None if vs is None else _p(vs), tok_begin, tok_end)
     if rc:
         raise ValueError("oracle decode_partial: block id outside the pool")
     return o, m.value, l.value

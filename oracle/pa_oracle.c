@@ -20,6 +20,9 @@
  *  - "Rolling buffer cache" (llama.cpp discussion #3581), opening post: with a
  *    fixed span W, timestep i is stored in slot i mod W and overwrites the
  *    older value there.
+ *  - "libmir-metal trace/kv.rs", model summary strings: a KV cache of type
+ *    "INT8 per token/head" keeps packed INT8 pages with one FP32 scale per
+ *    token and head, dequantised inside the paged attention.
  * Readings where the pages are silent (layout [NB][Hkv][bs][D], kv head
  * h / G, FP8 divide-then-round-to-nearest-even with saturation at 448, NaN to
  * 0x7F|sign, attending exactly the last W positions, context_len including the
@@ -39,6 +42,7 @@
 #define OR_BF16 1
 #define OR_F16 2
 #define OR_E4M3 3 /* only as a cache element type */
+#define OR_I8 4   /* only as a cache element type: INT8 with per-row scales */
 
 /* ------------------------------------------------------------------ */
 /* scalar formats                                                      */
@@ -80,7 +84,7 @@ static float or_load(const void* base, int code, size_t i)
 
 static size_t or_elem_bytes(int code)
 {
-    return code == OR_F32 ? 4 : code == OR_E4M3 ? 1 : 2;
+    return code == OR_F32 ? 4 : (code == OR_E4M3 || code == OR_I8) ? 1 : 2;
 }
 
 /*
@@ -180,6 +184,37 @@ void oracle_e4m3_decode_array(const uint8_t* b, float* out, int64_t n)
         out[i] = oracle_e4m3_decode(b[i]);
 }
 
+/*
+ * INT8 per token/head ("libmir-metal trace/kv.rs": packed INT8 pages, one
+ * FP32 scale per token and head). Symmetric quantisation of one row of n
+ * values (one token of one kv head, K or V separately), all in binary32:
+ *   amax  = max |x_i|
+ *   scale = amax / 127
+ *   q_i   = round-to-nearest-even(x_i / scale), clamped to [-127, 127]
+ * and q_i = 0 for every i when scale is 0 (an all-zero row, or one so small
+ * that amax / 127 underflows). The stored value is q_i * scale (one binary32
+ * multiply). Inputs are finite; NaN or infinity give codes with no meaning.
+ */
+void oracle_int8_quantise_row(const float* x, int n, int8_t* codes, float* scale_out)
+{
+    float amax = 0.0f, scale;
+    int i;
+    for (i = 0; i < n; ++i)
+        amax = fmaxf(amax, fabsf(x[i]));
+    scale = amax / 127.0f;
+    *scale_out = scale;
+    for (i = 0; i < n; ++i) {
+        float r;
+        if (scale == 0.0f) {
+            codes[i] = 0;
+            continue;
+        }
+        r = rintf(x[i] / scale);
+        r = fminf(fmaxf(r, -127.0f), 127.0f);
+        codes[i] = (int8_t)r;
+    }
+}
+
 /* ------------------------------------------------------------------ */
 /* slot mapping (ring-aware)                                           */
 /* ------------------------------------------------------------------ */
@@ -267,14 +302,63 @@ int64_t oracle_reshape_and_cache(const void* key, const void* value, void* k_cac
     return bad;
 }
 
+/*
+ * INT8 write: row [t][h][:] of key (and of value) quantised as one row, codes
+ * to cache[slot / bs][h][slot % bs][:], its scale to
+ * scales[slot / bs][h][slot % bs]. Negative slots are padding. Returns the
+ * number of tokens whose slot was beyond the pool (not written).
+ */
+int64_t oracle_reshape_and_cache_int8(const void* key, const void* value, int8_t* k_cache,
+                                      int8_t* v_cache, float* k_scales, float* v_scales,
+                                      const int64_t* slot_mapping, int64_t num_tokens,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int64_t num_blocks, int in_code)
+{
+    int64_t t, bad = 0;
+    float* row = (float*)malloc(sizeof(float) * (size_t)head_dim);
+    for (t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        int64_t blk, off;
+        int h, d, pass;
+        if (slot < 0)
+            continue;
+        if (slot >= num_blocks * (int64_t)block_size) {
+            ++bad;
+            continue;
+        }
+        blk = slot / block_size;
+        off = slot % block_size;
+        for (h = 0; h < num_kv_heads; ++h) {
+            size_t src = ((size_t)t * num_kv_heads + h) * head_dim;
+            size_t dst_row = ((size_t)blk * num_kv_heads + h) * block_size + off;
+            for (pass = 0; pass < 2; ++pass) {
+                const void* in = pass ? value : key;
+                for (d = 0; d < head_dim; ++d)
+                    row[d] = or_load(in, in_code, src + d);
+                oracle_int8_quantise_row(row, head_dim,
+                                         (pass ? v_cache : k_cache) + dst_row * head_dim,
+                                         (pass ? v_scales : k_scales) + dst_row);
+            }
+        }
+    }
+    free(row);
+    return bad;
+}
+
 /* ------------------------------------------------------------------ */
 /* decode: gather through the block table, then dense softmax attention */
 /* ------------------------------------------------------------------ */
 
-/* Cache element as the method defines it: native value, or E4M3 value times
-   the per-tensor scale (one binary32 multiply). */
-static double or_cache_value(const void* cache, int cache_code, size_t i, float cscale)
+/* Cache element as the method defines it: native value, E4M3 value times the
+   per-tensor scale, or INT8 code times its row's scale (row = i / head_dim);
+   each a single binary32 multiply. */
+static double or_cache_value(const void* cache, int cache_code, size_t i, float cscale,
+                             const float* row_scales, int head_dim)
 {
+    if (cache_code == OR_I8) {
+        float q = (float)((const int8_t*)cache)[i] * row_scales[i / (size_t)head_dim];
+        return (double)q;
+    }
     if (cache_code == OR_E4M3) {
         float q = oracle_e4m3_decode(((const uint8_t*)cache)[i]) * cscale;
         return (double)q;
@@ -287,7 +371,8 @@ static double or_cache_value(const void* cache, int cache_code, size_t i, float 
  * [tok_begin, tok_end) intersected with [0, L_s):
  *   m = max logit, l = sum exp(logit - m), o = sum exp(logit - m) V / l.
  * Empty range: m = -inf, l = 0, o = 0. Returns -1 if a needed block id is
- * outside [0, num_blocks), else 0.
+ * outside [0, num_blocks), else 0. k_scales / v_scales ([NB][Hkv][bs] fp32)
+ * are read only for an INT8 cache (cache_code OR_I8).
  */
 int oracle_decode_partial(double* o, double* m_out, double* l_out, const void* query,
                           const void* k_cache, const void* v_cache,
@@ -295,7 +380,8 @@ int oracle_decode_partial(double* o, double* m_out, double* l_out, const void* q
                           int s, int h, int num_heads, int num_kv_heads, int head_dim,
                           int block_size, int64_t num_blocks, int max_blocks_per_seq,
                           double scale, int window, int q_code, int cache_code,
-                          float k_scale, float v_scale, int64_t tok_begin, int64_t tok_end)
+                          float k_scale, float v_scale, const float* k_scales,
+                          const float* v_scales, int64_t tok_begin, int64_t tok_end)
 {
     int G = num_heads / num_kv_heads;
     int g = h / G; /* contiguous groups of query heads share one kv head */
@@ -336,8 +422,10 @@ int oracle_decode_partial(double* o, double* m_out, double* l_out, const void* q
             continue;
         }
         for (d = 0; d < head_dim; ++d) {
-            K[j * head_dim + d] = or_cache_value(k_cache, cache_code, base + d, k_scale);
-            V[j * head_dim + d] = or_cache_value(v_cache, cache_code, base + d, v_scale);
+            K[j * head_dim + d] =
+                or_cache_value(k_cache, cache_code, base + d, k_scale, k_scales, head_dim);
+            V[j * head_dim + d] =
+                or_cache_value(v_cache, cache_code, base + d, v_scale, v_scales, head_dim);
         }
     }
 
@@ -383,6 +471,7 @@ int64_t oracle_decode_rows(double* out, const void* query, const void* k_cache,
                            int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                            int max_blocks_per_seq, double scale, int window, int q_code,
                            int cache_code, float k_scale, float v_scale,
+                           const float* k_scales, const float* v_scales,
                            const int64_t* rows, int64_t nrows)
 {
     int64_t i, bad = 0;
@@ -395,8 +484,8 @@ int64_t oracle_decode_rows(double* out, const void* query, const void* k_cache,
         if (oracle_decode_partial(out + (size_t)r * head_dim, &m, &l, query, k_cache, v_cache,
                                   block_tables, context_lens, s, h, num_heads, num_kv_heads,
                                   head_dim, block_size, num_blocks, max_blocks_per_seq, scale,
-                                  window, q_code, cache_code, k_scale, v_scale, 0,
-                                  (int64_t)1 << 62) != 0)
+                                  window, q_code, cache_code, k_scale, v_scale, k_scales,
+                                  v_scales, 0, (int64_t)1 << 62) != 0)
             ++bad;
     }
     return bad;

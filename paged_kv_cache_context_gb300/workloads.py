@@ -44,7 +44,7 @@ class DecodeCase:
     block_size: int
     window: int
     q_dtype: torch.dtype
-    kv_dtype: str  # "auto" or "fp8_e4m3"
+    kv_dtype: str  # "auto", "fp8_e4m3" or "int8" (per-token/head scales)
     kv_src_dtype: torch.dtype  # dtype of the key/value rows before the cache write
     scale: float
     context_lens: torch.Tensor  # int32 [S], including the new token
@@ -71,6 +71,8 @@ class DecodeCase:
 
     @property
     def cache_dtype(self) -> torch.dtype:
+        if self.kv_dtype == "int8":
+            return torch.int8
         return torch.uint8 if self.kv_dtype == "fp8_e4m3" else self.q_dtype
 
     @property
@@ -103,10 +105,13 @@ class DecodeCase:
         return pos, key, val
 
     def kv_bytes(self) -> int:
-        """Key+value cache bytes the decode must read (attended tokens only)."""
-        elem = 1 if self.kv_dtype == "fp8_e4m3" else torch.finfo(self.q_dtype).bits // 8
+        """Key+value cache bytes the decode must read (attended tokens only;
+        an INT8 cache adds each row's 4-byte scale)."""
+        elem = (1 if self.kv_dtype in ("fp8_e4m3", "int8")
+                else torch.finfo(self.q_dtype).bits // 8)
+        row = self.head_dim * elem + (4 if self.kv_dtype == "int8" else 0)
         tokens = sum(self.attended(s) for s in range(self.num_seqs))
-        return tokens * self.num_kv_heads * self.head_dim * 2 * elem
+        return tokens * self.num_kv_heads * 2 * row
 
 
 def _normal(g: torch.Generator, shape, dtype, device) -> torch.Tensor:
@@ -257,6 +262,8 @@ def cache_poison(case: DecodeCase) -> int:
     element type), so that a stray read of an unwritten row shows up."""
     if case.kv_dtype == "fp8_e4m3":
         return 0x7F
+    if case.kv_dtype == "int8":
+        return -128  # a code the INT8 quantiser never writes
     return {torch.float32: 0x7FC00000, torch.bfloat16: 0x7FC0, torch.float16: 0x7E00}[case.q_dtype]
 
 
@@ -264,12 +271,19 @@ def empty_caches(case: DecodeCase, device: str = "cpu"):
     """Key and value caches [NB, Hkv, bs, D] filled with the poison pattern."""
     dt = case.cache_dtype
     pat = cache_poison(case)
-    if dt == torch.uint8:
-        k = torch.full(case.cache_shape, pat, dtype=torch.uint8, device=device)
+    if dt in (torch.uint8, torch.int8):
+        k = torch.full(case.cache_shape, pat, dtype=dt, device=device)
     else:
         itype = {torch.float32: torch.int32, torch.bfloat16: torch.int16,
                  torch.float16: torch.int16}[dt]
         k = torch.full(case.cache_shape, pat, dtype=itype, device=device).view(dt)
+    return k, k.clone()
+
+
+def empty_scales(case: DecodeCase, device: str = "cpu"):
+    """Per-row fp32 scales [NB, Hkv, bs] of an INT8 cache, K and V, filled with
+    NaN before any write."""
+    k = torch.full(case.cache_shape[:3], float("nan"), dtype=torch.float32, device=device)
     return k, k.clone()
 
 

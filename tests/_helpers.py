@@ -37,11 +37,28 @@ def oracle_caches(case: wl.DecodeCase, with_new: bool = True):
     return kc, vc
 
 
-def oracle_decode(case: wl.DecodeCase, kc, vc, rows=None, context_lens=None):
+def oracle_int8_caches(case: wl.DecodeCase):
+    """INT8 caches and their per-row scales (kc, vc, ks, vs), written by the
+    oracle's slot mapping and INT8 write in the same order as oracle_caches."""
+    kc, vc = wl.empty_caches(case)
+    ks, vs = wl.empty_scales(case)
+    steps = [(case.pre_seq[a:b], case.pre_pos[a:b], case.pre_key[a:b], case.pre_value[a:b])
+             for a, b in case.pre_chunks if b > a]
+    steps.append((None, case.new_pos, case.new_key, case.new_value))
+    for seq, pos, key, val in steps:
+        sm, bad = oracle.slot_mapping(case.block_tables, seq, pos, case.block_size, case.window)
+        assert bad == 0
+        assert oracle.reshape_and_cache_int8(key, val, kc, vc, ks, vs, sm, case.block_size) == 0
+    return kc, vc, ks, vs
+
+
+def oracle_decode(case: wl.DecodeCase, kc, vc, rows=None, context_lens=None, k_scales=None,
+                  v_scales=None):
     return oracle.decode(case.query, kc, vc, case.block_tables,
                          case.context_lens if context_lens is None else context_lens,
                          case.num_kv_heads, case.block_size, case.scale, case.window,
-                         case.kv_dtype, case.k_scale, case.v_scale, rows=rows)
+                         case.kv_dtype, case.k_scale, case.v_scale, rows=rows,
+                         k_scales=k_scales, v_scales=v_scales)
 
 
 def torch_dequant(x: torch.Tensor, scale: float) -> torch.Tensor:
@@ -50,6 +67,18 @@ def torch_dequant(x: torch.Tensor, scale: float) -> torch.Tensor:
     y = x.float() / torch.tensor(scale, dtype=torch.float32)
     q = torch.clamp(y, -448.0, 448.0).to(torch.float8_e4m3fn).float()
     return q * torch.tensor(scale, dtype=torch.float32)
+
+
+def torch_int8_dequant(x: torch.Tensor) -> torch.Tensor:
+    """Library-routine INT8 per-row round trip over the last dimension, fp32:
+    scale = max|x| / 127, round(x / scale) (ties to even) clamped to +-127,
+    times the scale; a zero scale gives zeros."""
+    x = x.float()
+    scale = x.abs().amax(dim=-1, keepdim=True) / torch.tensor(127.0)
+    safe = torch.where(scale == 0, torch.ones_like(scale), scale)
+    q = torch.clamp(torch.round(x / safe), -127, 127)
+    q = torch.where(scale == 0, torch.zeros_like(q), q)
+    return q * scale
 
 
 def attended_rows(case: wl.DecodeCase, s: int):
@@ -77,6 +106,9 @@ def dense_reference(case: wl.DecodeCase, s: int, h: int) -> np.ndarray:
     if case.kv_dtype == "fp8_e4m3":
         K = torch_dequant(K, case.k_scale)
         V = torch_dequant(V, case.v_scale)
+    if case.kv_dtype == "int8":
+        K = torch_int8_dequant(K)
+        V = torch_int8_dequant(V)
     q = case.query[s, h].cpu().float().double()
     logits = (K.double() @ q) * float(np.float32(case.scale))
     p = torch.softmax(logits, dim=0)
