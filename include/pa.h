@@ -38,7 +38,8 @@
  *  - Cache layout (both K and V): [NB][Hkv][bs][D]. The page of one
  *    (block, kv head) is bs*D contiguous elements ("head-major pages").
  *    Element type: the input dtype for PA_KV_AUTO, one byte (E4M3) for
- *    PA_KV_FP8_E4M3.
+ *    PA_KV_FP8_E4M3, one signed byte for PA_KV_INT8 (whose calls take, beside
+ *    each cache, fp32 row scales [NB][Hkv][bs]: one per token and kv head).
  */
 #ifndef PA_H
 #define PA_H
@@ -74,7 +75,7 @@ typedef enum {
 typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype;
 
 /* Cache storage type ("auto" and "f8e4m3" of "KV Cache Quantization"). */
-typedef enum { PA_KV_AUTO = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+typedef enum { PA_KV_AUTO = 0, PA_KV_FP8_E4M3 = 1, PA_KV_INT8 = 2 } pa_kv_dtype;
 
 /* Bits of the per-device error word (see pa_get_device_error). */
 enum {
@@ -178,6 +179,62 @@ pa_status pa_decode(void* out, const void* query,
                     float scale, int window, pa_dtype q_dtype, pa_kv_dtype kv_dtype,
                     float k_scale, float v_scale,
                     void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_reshape_and_cache_int8 -- scatter the K/V of new tokens into an INT8
+ * cache with one fp32 scale per token and kv head.
+ *
+ * Source: "libmir-metal trace/kv.rs" (model summary strings: packed INT8 pages
+ * with per-token/head FP32 scales, dequantised inside the paged attention).
+ * Each row x = key[t][h][:] (and value[t][h][:]) is quantised on its own, in
+ * binary32 (bf16/f16 inputs widened exactly):
+ *   scale = max_d |x[d]| / 127 (IEEE divide)
+ *   code[d] = round-to-nearest-even(x[d] / scale) clamped to [-127, 127]
+ *   (every code 0 when scale == 0)
+ * and stored as k_cache[blk][h][off][:] = code, k_scales[blk][h][off] = scale
+ * (blk = slot / bs, off = slot % bs). Inputs are expected finite; a NaN or an
+ * infinity gives codes with no meaning but is never a fault.
+ *
+ * key, value   : in, [T][Hkv][D] of in_dtype (F32, BF16 or F16).
+ * k_cache,
+ * v_cache      : in/out, int8 [NB][Hkv][bs][D].
+ * k_scales,
+ * v_scales     : in/out, fp32 [NB][Hkv][bs].
+ * slot_mapping : in, int64 [T]; < 0 = padding (skipped); a slot >= NB*bs is
+ *                skipped and sets PA_DEVERR_SLOT.
+ * Supported: D a multiple of 8 up to 256 (else PA_ERR_HEAD_DIM); bs 1..1024
+ * (else PA_ERR_BLOCK_SIZE). Pointers 16-byte aligned (PA_ERR_ALIGN); NULL ->
+ * PA_ERR_NULL; T == 0 is a no-op.
+ */
+pa_status pa_reshape_and_cache_int8(const void* key, const void* value,
+                                    int8_t* k_cache, int8_t* v_cache,
+                                    float* k_scales, float* v_scales,
+                                    const int64_t* slot_mapping, int num_tokens,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, pa_dtype in_dtype, pa_stream_t stream);
+
+/*
+ * pa_decode_int8 -- pa_decode over an INT8 cache with per-row scales.
+ *
+ * Source: "libmir-metal trace/kv.rs" (INT8 per-token/head pages, fused
+ * dequantisation in the paged attention) on top of the decode of
+ * "PagedAttention in mistral.rs". Same computation, arguments, workspace and
+ * error behaviour as pa_decode, with
+ *   K_j[d] = k_cache[blk][g][row][d] * k_scales[blk][g][row]
+ * and V_j likewise (one binary32 multiply each; the kernel applies the K scale
+ * to the dot product and the V scale to the softmax weight, which is the same
+ * value up to fp32 rounding). k_scales / v_scales : in, fp32 [NB][Hkv][bs].
+ * Supported: q_dtype BF16 or F16 (else PA_ERR_DTYPE); D, bs, G and window as
+ * pa_decode. Pointers 16-byte aligned.
+ */
+pa_status pa_decode_int8(void* out, const void* query,
+                         const int8_t* k_cache, const int8_t* v_cache,
+                         const float* k_scales, const float* v_scales,
+                         const int32_t* block_tables, const int32_t* context_lens,
+                         int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                         int block_size, int num_blocks, int max_blocks_per_seq,
+                         float scale, int window, pa_dtype q_dtype,
+                         void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
  * pa_decode_plan -- a split plan for pa_decode_partials at these sizes.
@@ -372,9 +429,10 @@ pa_status pa_decode_static_scratch(void* out, const void* query,
  * number of tokens per block). Host only; never touches the GPU.
  *
  * One block holds block_size tokens of K and V for every kv head of every
- * layer:  block_bytes = num_layers * 2 * num_kv_heads * block_size * head_dim
- *                       * element size (4 for F32, 2 for BF16/F16, 1 for an
- *                       FP8 E4M3 cache).
+ * layer:  block_bytes = num_layers * 2 * num_kv_heads * block_size * row_bytes,
+ *         row_bytes = head_dim * element size (4 for F32, 2 for BF16/F16, 1
+ *                     for an FP8 E4M3 or INT8 cache), plus 4 for the fp32
+ *                     row scale of an INT8 cache.
  *   PA_BUDGET_MB:       amount = MB (2^20 bytes) for the cache;
  *                       blocks = floor(amount * 2^20 / block_bytes).
  *   PA_BUDGET_FRACTION: amount in (0, 1] of available_bytes (the caller's

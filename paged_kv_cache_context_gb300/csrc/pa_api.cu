@@ -154,6 +154,60 @@ __global__ void cache_fp8_kernel(const IT* key, const IT* value, uint2* k_cache,
   }
 }
 
+// INT8 write: one warp per (token, kv head); lane i holds elements i, i + 32,
+// ... of the row (at most E each). The row's max |x| is reduced across the
+// warp, scale = max / 127 and code = rint(x / scale) clamped to +-127, both
+// IEEE binary32 divisions; a zero scale stores zero codes.
+template <typename IT, int E>
+__device__ __forceinline__ void quantise_row_int8(const IT* x, int8_t* codes, float* scale_out,
+                                                  int D, int lane) {
+  float v[E];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int d = lane + 32 * i;
+    v[i] = d < D ? Elem<IT>::to_f32(x[d]) : 0.f;
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off /= 2) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float scale = __fdiv_rn(amax, 127.f);
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int d = lane + 32 * i;
+    if (d < D) {
+      const float r = scale == 0.f ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(v[i], scale)), -127.f), 127.f);
+      codes[d] = static_cast<int8_t>(__float2int_rz(r));
+    }
+  }
+  if (lane == 0) *scale_out = scale;
+}
+
+template <typename IT, int E>
+__global__ void cache_int8_kernel(const IT* key, const IT* value, int8_t* k_cache,
+                                  int8_t* v_cache, float* k_scales, float* v_scales,
+                                  const int64_t* slots, int T, int Hkv, int D, int bs,
+                                  int64_t capacity, unsigned* err) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int64_t wpb = blockDim.x >> 5;
+  const int64_t total = (int64_t)T * Hkv;
+  for (int64_t row = blockIdx.x * wpb + (threadIdx.x >> 5); row < total;
+       row += (int64_t)gridDim.x * wpb) {
+    const int t = static_cast<int>(row / Hkv), h = static_cast<int>(row % Hkv);
+    const int64_t slot = slots[t];
+    if (slot < 0) continue;
+    if (slot >= capacity) {
+      if (h == 0 && lane == 0) raise_error(err, PA_DEVERR_SLOT);
+      continue;
+    }
+    const int64_t dst = (slot / bs * Hkv + h) * bs + slot % bs;  // row of the cache
+    quantise_row_int8<IT, E>(key + row * D, k_cache + dst * D, k_scales + dst, D, lane);
+    quantise_row_int8<IT, E>(value + row * D, v_cache + dst * D, v_scales + dst, D, lane);
+  }
+}
+
 // LSE combination of split partials: one warp per (sequence, head) row. Lane j
 // computes the weight of split j; the partial rows of up to 8 splits are
 // loaded before they are accumulated, so their latencies overlap.
@@ -299,6 +353,11 @@ static cudaError_t run_decode(const DecodeParams& prm, const DecodeShape& a, dim
       case PA_BF16: return pa_dispatch_decode_bf16_bf16(prm, grid, a.D, GT, a.bs, mode, ctas, st);
       default: return pa_dispatch_decode_f16_f16(prm, grid, a.D, GT, a.bs, mode, ctas, st);
     }
+  }
+  if (a.kv_dtype == PA_KV_INT8) {
+    return a.q_dtype == PA_BF16
+               ? pa_dispatch_decode_bf16_i8(prm, grid, a.D, GT, a.bs, mode, ctas, st)
+               : pa_dispatch_decode_f16_i8(prm, grid, a.D, GT, a.bs, mode, ctas, st);
   }
   switch (a.q_dtype) {
     case PA_F32: return pa_dispatch_decode_f32_e4m3(prm, grid, a.D, GT, a.bs, mode, ctas, st);
@@ -637,6 +696,94 @@ PA_API pa_status pa_decode(void* out, const void* query, const void* k_cache,
              : PA_ERR_CUDA;
 }
 
+// ================================================================ INT8 cache
+PA_API pa_status pa_reshape_and_cache_int8(const void* key, const void* value, int8_t* k_cache,
+                                           int8_t* v_cache, float* k_scales, float* v_scales,
+                                           const int64_t* slot_mapping, int num_tokens,
+                                           int num_kv_heads, int head_dim, int block_size,
+                                           int num_blocks, pa_dtype in_dtype, pa_stream_t stream) {
+  if (num_tokens < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !k_scales || !v_scales || !slot_mapping)
+    return PA_ERR_NULL;
+  if (!valid_dtype(in_dtype)) return PA_ERR_DTYPE;
+  if (num_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_SHAPE;
+  if (head_dim <= 0 || head_dim % 8 != 0 || head_dim > 256) return PA_ERR_HEAD_DIM;
+  if (block_size <= 0 || block_size > 1024) return PA_ERR_BLOCK_SIZE;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(k_scales) || !aligned16(v_scales))
+    return PA_ERR_ALIGN;
+  unsigned* err = error_word();
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t capacity = (int64_t)num_blocks * block_size;
+  const int threads = 256;
+  const int grid = grid_for((int64_t)num_tokens * num_kv_heads * 32, threads);
+#define PA_I8W(IT, E)                                                                         \
+  launch_pdl(cache_int8_kernel<IT, E>, dim3(grid), dim3(threads), 0, st,                      \
+             static_cast<const IT*>(key), static_cast<const IT*>(value), k_cache, v_cache,     \
+             k_scales, v_scales, slot_mapping, num_tokens, num_kv_heads, head_dim, block_size, \
+             capacity, err)
+#define PA_I8W_E(IT) \
+  (head_dim <= 64 ? PA_I8W(IT, 2) : head_dim <= 128 ? PA_I8W(IT, 4) : PA_I8W(IT, 8))
+  cudaError_t e;
+  switch (in_dtype) {
+    case PA_F32: e = PA_I8W_E(float); break;
+    case PA_BF16: e = PA_I8W_E(__nv_bfloat16); break;
+    default: e = PA_I8W_E(__half);
+  }
+#undef PA_I8W_E
+#undef PA_I8W
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_decode_int8(void* out, const void* query, const int8_t* k_cache,
+                                const int8_t* v_cache, const float* k_scales,
+                                const float* v_scales, const int32_t* block_tables,
+                                const int32_t* context_lens, int num_seqs, int num_heads,
+                                int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                int max_blocks_per_seq, float scale, int window,
+                                pa_dtype q_dtype, void* workspace, size_t workspace_bytes,
+                                pa_stream_t stream) {
+  // the shared checks, on the shape with a native cache
+  DecodeShape a{num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                max_blocks_per_seq, window, q_dtype, PA_KV_AUTO, 1.f, 1.f};
+  pa_status rc = check_decode(a, out, query, k_cache, v_cache, block_tables, context_lens);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  if (q_dtype != PA_BF16 && q_dtype != PA_F16) return PA_ERR_DTYPE;
+  if (!k_scales || !v_scales) return PA_ERR_NULL;
+  if (!aligned16(k_scales) || !aligned16(v_scales)) return PA_ERR_ALIGN;
+  a.kv_dtype = PA_KV_INT8;
+  DecodeParams p = make_params(a, query, k_cache, v_cache, block_tables, context_lens, scale,
+                               error_word());
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  p.out = out;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int GT = group_bucket(num_heads / num_kv_heads);
+  if (workspace && workspace_bytes >= balanced_bytes(GT, head_dim) && aligned16(workspace)) {
+    rc = pa_decode_workspace_clear(workspace, workspace_bytes, stream);
+    if (rc != PA_OK) return rc;
+    const BalancedWs w = balanced_carve(workspace, GT, head_dim);
+    p.piece_o = w.piece_o;
+    p.piece_ml = w.piece_ml;
+    p.arrived = w.arrived;
+    p.num_splits = 1;
+    p.pages_per_split = 1;
+    int ctas = 0;
+    return run_decode(p, a, dim3(0, 1, 1), kModeBalanced, &ctas, st) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+  }
+  // no usable workspace: one CTA per (sequence, kv head), straight to the output
+  p.partials = 0;
+  p.num_splits = 1;
+  p.pages_per_split = max_pages(max_blocks_per_seq, block_size, window);
+  return run_decode(p, a, dim3(1, num_kv_heads, num_seqs), kModeSplit, nullptr, st) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
 // ================================================================ cascade
 // Split of the shared prefix into ranges of whole 64-token tiles: as many as
 // keep (query tiles x kv heads x splits) within one wave of two CTAs per SM
@@ -774,12 +921,14 @@ PA_API int64_t pa_block_budget(pa_budget_kind kind, double amount, size_t availa
                                pa_dtype dtype, pa_kv_dtype kv_dtype) {
   if (num_layers <= 0 || num_kv_heads <= 0 || block_size <= 0) return PA_ERR_SHAPE;
   if (head_dim <= 0) return PA_ERR_HEAD_DIM;
-  if (!valid_dtype(dtype) || (kv_dtype != PA_KV_AUTO && kv_dtype != PA_KV_FP8_E4M3))
+  if (!valid_dtype(dtype) ||
+      (kv_dtype != PA_KV_AUTO && kv_dtype != PA_KV_FP8_E4M3 && kv_dtype != PA_KV_INT8))
     return PA_ERR_DTYPE;
   if (!(amount >= 0.0) || !isfinite(amount)) return PA_ERR_SHAPE;
-  const int64_t elem = kv_dtype == PA_KV_FP8_E4M3 ? 1 : (dtype == PA_F32 ? 4 : 2);
-  const double block_bytes =
-      (double)num_layers * 2.0 * num_kv_heads * block_size * head_dim * (double)elem;
+  const int64_t elem = kv_dtype != PA_KV_AUTO ? 1 : (dtype == PA_F32 ? 4 : 2);
+  // bytes of one cached row: its elements, plus its fp32 scale for INT8
+  const double row_bytes = (double)head_dim * elem + (kv_dtype == PA_KV_INT8 ? 4.0 : 0.0);
+  const double block_bytes = (double)num_layers * 2.0 * num_kv_heads * block_size * row_bytes;
   double blocks = 0.0;
   switch (kind) {
     case PA_BUDGET_MB:

@@ -102,6 +102,8 @@ struct DecodeParams {
   const void* query;    // [S][Hq][D] of QT
   const uint8_t* k_cache;
   const uint8_t* v_cache;
+  const float* k_scales;        // INT8 cache: one scale per cached row, [NB][Hkv][bs]
+  const float* v_scales;
   const int32_t* block_tables;  // [S][MB]
   const int32_t* context_lens;  // [S]
   unsigned* err;
@@ -115,7 +117,7 @@ struct DecodeParams {
   int join_at_end;
   int partials;   // split mode: 1 = write split partials, 0 = final output
   float q_scale;  // scale * log2(e) (* k_scale for FP8)
-  float v_scale;  // FP8: v_scale, else 1
+  float v_scale;  // FP8: v_scale, else 1 (an INT8 cache scales each row instead)
 };
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
@@ -174,7 +176,12 @@ struct Layout {
   static constexpr int HEAD_MASK = ((1 << NHB) - 1) << HB0;
   static constexpr int STAGES = cmax(2 * R, cmin(PA_MAX_STAGES, PA_STAGE_BYTES / (2 * PAGE)));
   static constexpr int QSLOT = round_up(GT * D * QB, 16);        // q rows of a piece
-  static constexpr int STAGE = round_up(2 * PAGE + QSLOT, 128);  // K page | V page | q rows
+  // an INT8 cache stages its pages' row scales too (BS floats each for K and V)
+  static constexpr bool ROW_SCALES = std::is_same<CT, I8>::value;
+  static constexpr int SCB = ROW_SCALES ? BS * 4 : 0;
+  static constexpr int OFF_Q = 2 * PAGE + 2 * SCB;
+  // K page | V page | (K row scales | V row scales) | q rows
+  static constexpr int STAGE = round_up(OFF_Q + QSLOT, 128);
   static constexpr int SCR = round_up(TPI * GT, 4);              // per-warp weights
   static constexpr int MACC = NC * GT * D * 4;                   // merge accumulators
   static constexpr bool MERGE_IN_STAGE = MACC <= STAGE;
@@ -199,7 +206,7 @@ struct Layout {
   static_assert(STAGES >= R, "a consumer iteration holds R stages");
   static_assert(EPL * LPR == D && NPL * EPP == EPL, "row split");
   static_assert(EPP % 2 == 0, "pieces hold whole fp32 pairs");
-  static_assert(PAGE % 16 == 0, "bulk copies move multiples of 16 bytes");
+  static_assert(PAGE % 16 == 0 && SCB % 16 == 0, "bulk copies move multiples of 16 bytes");
   static_assert(STAGE % 128 == 0 && OFF_BAR % 8 == 0, "stage and mbarrier alignment");
   static_assert(OFF_DESC % 16 == 0 && OFF_SCR % 16 == 0 && OFF_MSTAT % 16 == 0 &&
                     OFF_MACC % 16 == 0 && OFF_MISC % 16 == 0 && (SCR * 4) % 16 == 0,
@@ -311,10 +318,15 @@ __device__ __forceinline__ void begin_piece(PieceState<Ly, GT>& st, const uint8_
 // One consumer iteration over R pages of the current piece (a page with
 // lim[r] <= 0 contributes nothing). Token t of the warp's TPI rows is row
 // warp*TPW + t%TPW of page t/TPW; rows t%TPW < lim[t/TPW] are attended.
+// With an INT8 cache, Ks / Vs point at the pages' staged row scales: a
+// token's logit is multiplied by its K row's scale, and its softmax weight
+// by its V row's scale before P.V (the running sum takes the bare weight).
 template <typename CT, typename Ly, int GT>
 __device__ __forceinline__ void process_pages(PieceState<Ly, GT>& st,
                                               const uint8_t* const (&Kp)[Ly::R],
                                               const uint8_t* const (&Vp)[Ly::R],
+                                              const float* const (&Ks)[Ly::R],
+                                              const float* const (&Vs)[Ly::R],
                                               const int (&lim)[Ly::R], float* wscr, int warp,
                                               int lane, int c, int rg) {
   constexpr int R = Ly::R, TPW = Ly::TPW, RPW = Ly::RPW, LPR = Ly::LPR, NV = Ly::NV;
@@ -357,7 +369,14 @@ __device__ __forceinline__ void process_pages(PieceState<Ly, GT>& st,
       int lim_t = lim[0];  // lim of token t's page, without dynamic indexing
 #pragma unroll
       for (int r = 1; r < R; ++r) lim_t = t >= r * TPW ? lim[r] : lim_t;
-      sl[sg][kk] = (writer && (t % TPW) < lim_t) ? part[kk] : -INFINITY;
+      float logit = part[kk];
+      if constexpr (Ly::ROW_SCALES) {
+        const float* ks = Ks[0];
+#pragma unroll
+        for (int r = 1; r < R; ++r) ks = t >= r * TPW ? Ks[r] : ks;
+        logit *= ks[warp * TPW + t % TPW];
+      }
+      sl[sg][kk] = (writer && (t % TPW) < lim_t) ? logit : -INFINITY;
     }
   }
 
@@ -406,7 +425,15 @@ __device__ __forceinline__ void process_pages(PieceState<Ly, GT>& st,
       if (writer) {
         const int idx = (c * NV) / LPR + kk;
         const int t = (sg * Ly::SG + idx / GT) * RPW + rg;
-        wscr[t * GT + idx % GT] = pw;
+        float w = pw;
+        if constexpr (Ly::ROW_SCALES) {
+          const float* vs = Vs[0];
+#pragma unroll
+          for (int r = 1; r < R; ++r) vs = t >= r * TPW ? Vs[r] : vs;
+          // rows past the context have weight 0 and may hold any scale
+          w = pw == 0.f ? 0.f : pw * vs[warp * TPW + t % TPW];
+        }
+        wscr[t * GT + idx % GT] = w;
       }
     }
   __syncwarp();
@@ -868,16 +895,22 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
                             (k == npages - 1 ? kCtaLast : 0);
           desc[slot] = make_int4(rows, s * Hkv + g, flags, 0);
           uint8_t* stage = smem + slot * Ly::STAGE;
-          const uint32_t bytes = (ok ? 2u * Ly::PAGE : 0u) + (piece_start ? qbytes : 0u);
+          const uint32_t bytes =
+              (ok ? 2u * (Ly::PAGE + Ly::SCB) : 0u) + (piece_start ? qbytes : 0u);
           if (bytes) {
             mbar_arrive_expect_tx(&full[slot], bytes);
             if (ok) {
               const size_t off = (size_t)bid * blk_stride + (size_t)g * Ly::PAGE;
               bulk_g2s(stage, p.k_cache + off, Ly::PAGE, &full[slot]);
               bulk_g2s(stage + Ly::PAGE, p.v_cache + off, Ly::PAGE, &full[slot]);
+              if constexpr (Ly::ROW_SCALES) {
+                const size_t so = ((size_t)bid * Hkv + g) * BS;
+                bulk_g2s(stage + 2 * Ly::PAGE, p.k_scales + so, Ly::SCB, &full[slot]);
+                bulk_g2s(stage + 2 * Ly::PAGE + Ly::SCB, p.v_scales + so, Ly::SCB, &full[slot]);
+              }
             }
             if (piece_start)
-              bulk_g2s(stage + 2 * Ly::PAGE,
+              bulk_g2s(stage + Ly::OFF_Q,
                        static_cast<const uint8_t*>(p.query) +
                            ((size_t)s * Hq + (size_t)g * G) * D * Ly::QB,
                        qbytes, &full[slot]);
@@ -953,6 +986,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
     // up to R pages of the current piece
     const uint8_t* Kp[R];
     const uint8_t* Vp[R];
+    const float* Ks[R];
+    const float* Vs[R];
     int lim[R];
     int n_here = 0, last_flags = 0, seg = 0, last_slot = 0;
 #pragma unroll
@@ -960,6 +995,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
       lim[r] = 0;
       Kp[r] = smem;
       Vp[r] = smem;
+      Ks[r] = reinterpret_cast<const float*>(smem);
+      Vs[r] = reinterpret_cast<const float*>(smem);
       if (aborted || (r > 0 && (last_flags & kLast))) continue;
       const int slot = (k + r) % STAGES;
       if (!mbar_wait_bounded(&full[slot], ((k + r) / STAGES) & 1)) {
@@ -971,10 +1008,12 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
       uint8_t* stage = smem + slot * Ly::STAGE;
       if (r == 0) {
         seg = d.y;
-        if (d.z & kFirst) begin_piece<QT, Ly, GT, D>(st, stage + 2 * Ly::PAGE, G, c, p.q_scale);
+        if (d.z & kFirst) begin_piece<QT, Ly, GT, D>(st, stage + Ly::OFF_Q, G, c, p.q_scale);
       }
       Kp[r] = stage;
       Vp[r] = stage + Ly::PAGE;
+      Ks[r] = reinterpret_cast<const float*>(stage + 2 * Ly::PAGE);
+      Vs[r] = reinterpret_cast<const float*>(stage + 2 * Ly::PAGE + Ly::SCB);
       lim[r] = d.x - warp * TPW;
       last_flags = d.z;
       last_slot = slot;
@@ -982,7 +1021,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
     }
     if (__any_sync(0xffffffffu, aborted)) break;
 
-    process_pages<CT, Ly, GT>(st, Kp, Vp, lim, wscr, warp, lane, c, rg);
+    process_pages<CT, Ly, GT>(st, Kp, Vp, Ks, Vs, lim, wscr, warp, lane, c, rg);
 
     const bool ends_piece = (last_flags & kLast) != 0;
     if (lane == 0) {
@@ -1176,3 +1215,5 @@ PA_DECLARE_DISPATCH(pa_dispatch_decode_f16_f16);
 PA_DECLARE_DISPATCH(pa_dispatch_decode_f32_e4m3);
 PA_DECLARE_DISPATCH(pa_dispatch_decode_bf16_e4m3);
 PA_DECLARE_DISPATCH(pa_dispatch_decode_f16_e4m3);
+PA_DECLARE_DISPATCH(pa_dispatch_decode_bf16_i8);
+PA_DECLARE_DISPATCH(pa_dispatch_decode_f16_i8);

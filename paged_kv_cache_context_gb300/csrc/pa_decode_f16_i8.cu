@@ -1,0 +1,9 @@
+// Paged decode kernels: query/output __half, cache pa::I8 (INT8 codes with one
+// fp32 scale per cached row; all head dims, group sizes, block sizes and both
+// work modes). One translation unit per dtype pair so they build in parallel.
+#include "pa_decode.cuh"
+
+cudaError_t pa_dispatch_decode_f16_i8(const pa::DecodeParams& prm, dim3 grid, int D, int GT,
+                                      int BS, int mode, int* ctas, cudaStream_t stream) {
+  return pa::dispatch_decode<__half, pa::I8>(prm, grid, D, GT, BS, mode, ctas, stream);
+}

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <type_traits>
 #include <stdint.h>
 
 #include <utility>
@@ -142,6 +144,28 @@ struct Elem<E4M3> {
   static constexpr int bytes = 1;
 };
 
+// INT8 cache element (one two's-complement byte) with one fp32 scale per
+// cached row, held beside the pages.
+struct I8 {};
+template <>
+struct Elem<I8> {
+  static constexpr int bytes = 1;
+};
+
+// Four INT8 codes (low byte first) -> two float pairs, exactly. Flipping a
+// code's sign bit gives u = c + 128 in [0, 255]; the binary32 with bit
+// pattern 0x4B0000uu is 2^23 + u, and subtracting 2^23 + 128 leaves c.
+__device__ __forceinline__ void i8x4_to_float2x2(uint32_t w, float2* out) {
+  const uint32_t u = w ^ 0x80808080u;
+  const float2 bias = make_float2(-8388736.f, -8388736.f);
+  out[0] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
+                                  __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541))),
+                      bias);
+  out[1] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
+                                  __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543))),
+                      bias);
+}
+
 // Two E4M3 codes (low byte first) -> two floats, via the hardware
 // e4m3x2 -> f16x2 conversion (exact: every E4M3 value is an f16 value).
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
@@ -235,6 +259,10 @@ __device__ __forceinline__ void widen_word2<E4M3>(uint32_t w, float2* out) {
   out[0] = e4m3x2_to_float2(static_cast<uint16_t>(w & 0xFFFFu));
   out[1] = e4m3x2_to_float2(static_cast<uint16_t>(w >> 16));
 }
+template <>
+__device__ __forceinline__ void widen_word2<I8>(uint32_t w, float2* out) {
+  i8x4_to_float2x2(w, out);
+}
 
 template <typename CT, int PB>
 __device__ __forceinline__ void load_piece2(const uint8_t* p, float2* out) {
@@ -262,6 +290,10 @@ __device__ __forceinline__ void load_piece2(const uint8_t* p, float2* out) {
       widen_word2<CT>(v.y, out + P2W);
     } else if constexpr (PB == 4) {
       widen_word2<CT>(*reinterpret_cast<const uint32_t*>(p), out);
+    } else if constexpr (std::is_same<CT, I8>::value) {  // PB == 2: two INT8 codes
+      float2 both[2];
+      i8x4_to_float2x2(*reinterpret_cast<const uint16_t*>(p), both);
+      out[0] = both[0];
     } else {  // PB == 2: two E4M3 codes
       out[0] = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(p));
     }

@@ -19,12 +19,12 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libpagedattn.so")
 
 # enums of include/pa.h
 PA_F32, PA_BF16, PA_F16 = 0, 1, 2
-PA_KV_AUTO, PA_KV_FP8_E4M3 = 0, 1
+PA_KV_AUTO, PA_KV_FP8_E4M3, PA_KV_INT8 = 0, 1, 2
 PA_ERR_DEVICE = -9
 DEVERR_BITS = {1: "slot", 2: "block_id", 4: "context_len", 8: "timeout", 16: "seq"}
 
 _DTYPE = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16}
-_KV = {"auto": PA_KV_AUTO, "fp8_e4m3": PA_KV_FP8_E4M3}
+_KV = {"auto": PA_KV_AUTO, "fp8_e4m3": PA_KV_FP8_E4M3, "int8": PA_KV_INT8}
 
 _lib = None
 
@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
             "pa_decode_cascade": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, Z, P],
             "pa_copy_blocks": [P, P, P, I, I, I, I, I, I, P],
             "pa_block_budget": [I, ctypes.c_double, Z, I, I, I, I, I, I],
+            "pa_reshape_and_cache_int8": [P, P, P, P, P, P, P, I, I, I, I, I, I, P],
+            "pa_decode_int8": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, Z, P],
             "pa_decode_static_scratch": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F,
                                          F, P],
             "pa_get_device_error": [P, P],
@@ -123,6 +125,36 @@ def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Ten
                                       _ptr(slot_mapping_), T, H, D, bs, NB, _DTYPE[key.dtype],
                                       _KV[kv_dtype], k_scale, v_scale, _stream(stream)),
            "pa_reshape_and_cache")
+
+
+def reshape_and_cache_int8(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                           v_cache: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor,
+                           slot_mapping_: torch.Tensor, stream=None):
+    """pa_reshape_and_cache_int8: key/value [T, Hkv, D] into int8 caches
+    [NB, Hkv, bs, D] and fp32 row scales [NB, Hkv, bs]."""
+    T, H, D = key.shape
+    NB, _, bs, _ = k_cache.shape
+    _check(lib().pa_reshape_and_cache_int8(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                           _ptr(k_scales), _ptr(v_scales), _ptr(slot_mapping_),
+                                           T, H, D, bs, NB, _DTYPE[key.dtype], _stream(stream)),
+           "pa_reshape_and_cache_int8")
+
+
+def decode_int8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+                v_cache: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor,
+                block_tables: torch.Tensor, context_lens: torch.Tensor, num_kv_heads: int,
+                scale: float, window: int = 0, workspace: Optional[torch.Tensor] = None,
+                stream=None):
+    """pa_decode_int8: pa_decode over an INT8 cache with per-row scales."""
+    S, Hq, D = query.shape
+    NB, _, bs, _ = k_cache.shape
+    MB = block_tables.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode_int8(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(k_scales), _ptr(v_scales), _ptr(block_tables),
+                                _ptr(context_lens), S, Hq, num_kv_heads, D, bs, NB, MB, scale,
+                                window, _DTYPE[query.dtype], _ptr(workspace), ws_bytes,
+                                _stream(stream)), "pa_decode_int8")
 
 
 def decode_plan(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,

@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     for want in ("pa_reshape_and_cache", "pa_decode", "pa_reduce", "pa_slot_mapping",
                  "pa_decode_partials", "pa_decode_plan", "pa_decode_workspace_size",
                  "pa_decode_cascade", "pa_decode_cascade_workspace_size", "pa_copy_blocks",
-                 "pa_block_budget",
+                 "pa_block_budget", "pa_reshape_and_cache_int8", "pa_decode_int8",
                  "pa_get_device_error", "pa_status_string", "pa_version"):
         assert want in names
 
@@ -215,10 +215,46 @@ def test_block_budget_closed_forms(L):
     assert f(0, 1.0, 0, 32, 8, 0, 32, 1, 0) == -4
     assert f(0, 1.0, 0, 32, 8, 128, 0, 1, 0) == -3
     assert f(0, 1.0, 0, 32, 8, 128, 32, 5, 0) == -2
-    assert f(0, 1.0, 0, 32, 8, 128, 32, 1, 2) == -2
+    assert f(0, 1.0, 0, 32, 8, 128, 32, 1, 3) == -2
     assert f(0, -1.0, 0, 32, 8, 128, 32, 1, 0) == -3
     assert f(0, float("nan"), 0, 32, 8, 128, 32, 1, 0) == -3
     assert f(1, 1.5, 1 << 30, 32, 8, 128, 32, 1, 0) == -3
     assert f(3, 1.0, 0, 32, 8, 128, 32, 1, 0) == -3
     with pytest.raises(ValueError):
         pa.block_budget(32, 8, 128, 32, bf, mb=1, context_tokens=1)
+    # an INT8 row is D bytes plus its 4-byte scale: 32*2*8*32*(128+4) bytes a block
+    assert pa.block_budget(32, 8, 128, 32, bf, "int8", mb=4096) == (4096 << 20) // (
+        32 * 2 * 8 * 32 * 132)
+    assert pa.block_budget(1, 1, 64, 16, bf, "int8", mb=2 * 16 * 68 / 2 ** 20 * 5) == 5
+
+
+def test_int8_entry_points_reject_bad_arguments_on_host(L):
+    d = L.pa_decode_int8
+
+    def dec(**kw):
+        a = dict(out=P, q=P, k=P, v=P, ks=P, vs=P, bt=P, cl=P, S=4, Hq=8, Hkv=2, D=128, bs=32,
+                 NB=10, MB=8, scale=0.1, W=0, qd=1, ws=None, wsb=0)
+        a.update(kw)
+        return d(a["out"], a["q"], a["k"], a["v"], a["ks"], a["vs"], a["bt"], a["cl"], a["S"],
+                 a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"], a["MB"], a["scale"], a["W"],
+                 a["qd"], a["ws"], a["wsb"], None)
+
+    assert dec(S=0, q=None) == 0
+    assert dec(ks=None) == -1 and dec(vs=None) == -1 and dec(k=None) == -1
+    assert dec(qd=0) == -2 and dec(qd=7) == -2        # fp32 queries are not built for INT8
+    assert dec(D=80) == -4 and dec(bs=8) == -5 and dec(Hq=7) == -3
+    assert dec(W=48) == -6
+    assert dec(ks=P + 4) == -10 and dec(vs=P + 8) == -10
+    w = L.pa_reshape_and_cache_int8
+    assert w(P, P, P, P, P, P, P, 0, 2, 128, 32, 10, 1, None) == 0
+    assert w(P, P, P, P, None, P, P, 4, 2, 128, 32, 10, 1, None) == -1
+    assert w(P, P, P, P, P, P, P, 4, 2, 128, 32, 10, 5, None) == -2
+    assert w(P, P, P, P, P, P, P, 4, 2, 264, 32, 10, 1, None) == -4
+    assert w(P, P, P, P, P, P, P, 4, 2, 100, 32, 10, 1, None) == -4
+    assert w(P, P, P, P, P, P, P, 4, 2, 128, 0, 10, 1, None) == -5
+    assert w(P, P, P, P, P, P, P, -1, 2, 128, 32, 10, 1, None) == -3
+    assert w(P, P, P, P, P + 4, P, P, 4, 2, 128, 32, 10, 1, None) == -10
+    # the native-cache entry points take no row scales, so they refuse INT8
+    assert L.pa_decode(P, P, P, P, P, P, 4, 8, 2, 128, 32, 10, 8, 0.1, 0, 1, 2, 1.0, 1.0, None,
+                       0, None) == -2
+    assert L.pa_reshape_and_cache(P, P, P, P, P, 4, 2, 128, 32, 10, 1, 2, 1.0, 1.0, None) == -2
