@@ -8,7 +8,10 @@ counters (pa_decode_workspace_clear) and the persistent decode launch
 (pa_decode_balanced), whose CTAs also combine the contexts cut between them.
 With --path cascade (workloads whose block tables share prefix blocks) the
 decode is pa_decode_cascade instead: the shared prefix for all query heads at
-once, each sequence's own pages, and the combine.
+once, each sequence's own pages, and the combine. With --path int8 the same
+batch is held as an INT8 cache with one fp32 scale per token and kv head: the
+write is pa_reshape_and_cache_int8 and the decode pa_decode_int8 (counter
+clear + the balanced decode launch).
 Default workload: the
 Mistral-7B-shaped bf16 batch (32 sequences, 32 query / 8 kv heads, head_dim
 128, block_size 32, context lengths U[512, 4096], shuffled block pool).
@@ -31,6 +34,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 import json
 import math
 import os
@@ -169,13 +173,14 @@ def step_bytes(case) -> dict:
     S, Hq, Hkv, D, bs = (case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim,
                          case.block_size)
     qb = torch.finfo(case.q_dtype).bits // 8
-    cb = 1 if case.kv_dtype == "fp8_e4m3" else qb
+    cb = 1 if case.kv_dtype in ("fp8_e4m3", "int8") else qb
     sb = torch.finfo(case.kv_src_dtype).bits // 8
-    kv = case.kv_bytes()
+    kv = case.kv_bytes()  # with an INT8 cache, the rows' scales too
     pages = sum(-(-case.attended(s) // bs) for s in range(S))
     new_rows = int((case.new_pos >= 0).sum())
     kernel = kv + S * Hq * D * qb + pages * 4 + S * 4  # what the split kernel must read
-    write = new_rows * Hkv * D * (sb + cb) * 2 + S * 8
+    row_scale = 4 if case.kv_dtype == "int8" else 0
+    write = new_rows * Hkv * (D * (sb + cb) + row_scale) * 2 + S * 8
     total = kernel + S * Hq * D * qb + write
     return {"kv": kv, "kernel": kernel, "write": write, "total": total}
 
@@ -199,12 +204,21 @@ def oracle_step_time(case, rows_per_step: int, reps: int, build_all: bool = True
     Hq = case.num_heads
     nseq = min(case.num_seqs, -(-rows_per_step // Hq))
     kc, vc = wl.empty_caches(case)
+    int8 = case.kv_dtype == "int8"
+    ks, vs = wl.empty_scales(case) if int8 else (None, None)
+
+    def write(key, val, sm):
+        if int8:
+            oracle.reshape_and_cache_int8(key, val, kc, vc, ks, vs, sm, case.block_size)
+        else:
+            oracle.reshape_and_cache(key, val, kc, vc, sm, case.block_size, case.kv_dtype,
+                                     case.k_scale, case.v_scale)
+
     for s in range(nseq):
         pos, key, val = case.tokens_of(s)
         sm, _ = oracle.slot_mapping(case.block_tables, torch.full_like(pos, s), pos,
                                     case.block_size, case.window)
-        oracle.reshape_and_cache(key[:-1], val[:-1], kc, vc, sm[:-1], case.block_size,
-                                 case.kv_dtype, case.k_scale, case.v_scale)
+        write(key[:-1], val[:-1], sm[:-1])
     new_sm, _ = oracle.slot_mapping(case.block_tables, None, case.new_pos, case.block_size,
                                     case.window)
     new_sm[nseq:] = -1
@@ -214,11 +228,10 @@ def oracle_step_time(case, rows_per_step: int, reps: int, build_all: bool = True
     times = []
     for _ in range(reps):
         t0 = time.perf_counter()
-        oracle.reshape_and_cache(nk, nv, kc, vc, new_sm, case.block_size, case.kv_dtype,
-                                 case.k_scale, case.v_scale)
+        write(nk, nv, new_sm)
         oracle.decode(q, kc, vc, case.block_tables, case.context_lens, case.num_kv_heads,
                       case.block_size, case.scale, case.window, case.kv_dtype, case.k_scale,
-                      case.v_scale, rows=rows)
+                      case.v_scale, rows=rows, k_scales=ks, v_scales=vs)
         times.append(time.perf_counter() - t0)
     # the same algorithmic bytes as the GPU step: the K/V rows a (sequence,
     # kv head) attends count once for the G query-head rows that share them
@@ -226,8 +239,9 @@ def oracle_step_time(case, rows_per_step: int, reps: int, build_all: bool = True
     sample_bytes = 0
     for r in rows:
         s = r // Hq
-        sample_bytes += case.attended(s) * case.head_dim * 2 * (
-            1 if case.kv_dtype == "fp8_e4m3" else torch.finfo(case.q_dtype).bits // 8)
+        elem = (1 if case.kv_dtype in ("fp8_e4m3", "int8")
+                else torch.finfo(case.q_dtype).bits // 8)
+        sample_bytes += case.attended(s) * 2 * (case.head_dim * elem + (4 if int8 else 0))
     return times, sample_bytes / G, len(rows)
 
 
@@ -251,6 +265,11 @@ def run_ours(args, rank, local_rank, world):
 
     case = wl.config(args.workload, value_device=str(dev),
                      seed=None if rank == 0 else 50_000 + rank)
+    int8 = args.path == "int8"
+    if int8:
+        if case.kv_dtype != "auto" or case.q_dtype == torch.float32:
+            raise SystemExit("--path int8 needs a workload with a bf16/f16 native cache")
+        case = dataclasses.replace(case, kv_dtype="int8")
     S, Hq, Hkv, D, bs = (case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim,
                          case.block_size)
     MB, NB = case.max_blocks_per_seq, case.num_blocks
@@ -260,19 +279,28 @@ def run_ours(args, rank, local_rank, world):
 
     # caches: prefill rows written by the library itself
     kc, vc = wl.empty_caches(case, device=str(dev))
+    ks, vs = wl.empty_scales(case, device=str(dev)) if int8 else (None, None)
     for a, b in case.pre_chunks:
         if b > a:
             sm = torch.empty(b - a, dtype=torch.int64, device=dev)
             pa.slot_mapping(sm, bt, case.pre_seq[a:b].to(dev), case.pre_pos[a:b].to(dev), bs,
                             case.window)
-            pa.reshape_and_cache(case.pre_key[a:b].contiguous(), case.pre_value[a:b].contiguous(),
-                                 kc, vc, sm, case.kv_dtype, case.k_scale, case.v_scale)
+            if int8:
+                pa.reshape_and_cache_int8(case.pre_key[a:b].contiguous(),
+                                          case.pre_value[a:b].contiguous(), kc, vc, ks, vs, sm)
+            else:
+                pa.reshape_and_cache(case.pre_key[a:b].contiguous(),
+                                     case.pre_value[a:b].contiguous(), kc, vc, sm, case.kv_dtype,
+                                     case.k_scale, case.v_scale)
     new_sm = torch.empty(S, dtype=torch.int64, device=dev)
     pa.slot_mapping(new_sm, bt, None, case.new_pos.to(dev), bs, case.window)
     new_k = case.new_key.to(dev).contiguous()
     new_v = case.new_value.to(dev).contiguous()
     torch.cuda.synchronize()
-    reps = [(kc, vc)] + [(kc.clone(), vc.clone()) for _ in range(args.replicas - 1)]
+    def clone(t):
+        return None if t is None else t.clone()
+    reps = [(kc, vc, ks, vs)] + [tuple(clone(t) for t in (kc, vc, ks, vs))
+                                 for _ in range(args.replicas - 1)]
 
     qd = pa._DTYPE[case.q_dtype]
     kvd = pa._KV[case.kv_dtype]
@@ -286,7 +314,7 @@ def run_ours(args, rank, local_rank, world):
     def ptr(t):
         return P(t.data_ptr())
     write_args, dec_args = [], []
-    for (k_, v_) in reps:
+    for (k_, v_, _, _) in reps:
         write_args.append((ptr(new_k), ptr(new_v), ptr(k_), ptr(v_), ptr(new_sm), I(S), I(Hkv),
                            I(D), I(bs), I(NB), I(pa._DTYPE[new_k.dtype]), I(kvd),
                            F(case.k_scale), F(case.v_scale), sp))
@@ -297,7 +325,7 @@ def run_ours(args, rank, local_rank, world):
     f_write, f_clear, f_dec = (L.pa_reshape_and_cache, L.pa_decode_workspace_clear,
                                L.pa_decode_balanced)
     clear_args = (ptr(ws), Z(ws_bytes), sp)
-    if f_clear(*clear_args) or f_dec(*dec_args[0]):
+    if not int8 and (f_clear(*clear_args) or f_dec(*dec_args[0])):
         raise RuntimeError("pa_decode_balanced failed")
     launches_per_step = 3  # cache write, counter clear, decode
     prefix_pages = case.shared_prefix_tokens // bs
@@ -309,16 +337,29 @@ def run_ours(args, rank, local_rank, world):
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         dec_args = [(ptr(out), ptr(q), ptr(k_), ptr(v_), ptr(bt), ptr(cl), I(S), I(Hq), I(Hkv),
                      I(D), I(bs), I(NB), I(MB), F(case.scale), I(qd), I(prefix_pages), ptr(ws),
-                     Z(ws_bytes), sp) for (k_, v_) in reps]
+                     Z(ws_bytes), sp) for (k_, v_, _, _) in reps]
         f_dec = L.pa_decode_cascade
         if f_dec(*dec_args[0]):
             raise RuntimeError("pa_decode_cascade failed")
         launches_per_step = 4  # cache write, prefix attention, suffix decode, reduce
+    if int8:
+        # pa_reshape_and_cache_int8, then pa_decode_int8 (counter clear + balanced decode)
+        write_args = [(ptr(new_k), ptr(new_v), ptr(k_), ptr(v_), ptr(ks_), ptr(vs_),
+                       ptr(new_sm), I(S), I(Hkv), I(D), I(bs), I(NB),
+                       I(pa._DTYPE[new_k.dtype]), sp) for (k_, v_, ks_, vs_) in reps]
+        dec_args = [(ptr(out), ptr(q), ptr(k_), ptr(v_), ptr(ks_), ptr(vs_), ptr(bt), ptr(cl),
+                     I(S), I(Hq), I(Hkv), I(D), I(bs), I(NB), I(MB), F(case.scale),
+                     I(case.window), I(qd), ptr(ws), Z(ws_bytes), sp)
+                    for (k_, v_, ks_, vs_) in reps]
+        f_write, f_dec = L.pa_reshape_and_cache_int8, L.pa_decode_int8
+        if f_write(*write_args[0]) or f_dec(*dec_args[0]):
+            raise RuntimeError("pa_decode_int8 failed")
+        launches_per_step = 3  # cache write, counter clear, decode
 
     def step(i, ev_a=None, ev_b=None):
         r = i % len(reps)
         rc = f_write(*write_args[r])
-        if args.path != "cascade":
+        if args.path == "balanced":
             rc |= f_clear(*clear_args)
         if ev_a is not None:
             ev_a.record(stream)
@@ -394,7 +435,7 @@ def run_ours(args, rank, local_rank, world):
                    "window": case.window, "cache_dtype": case.kv_dtype if case.kv_dtype != "auto"
                    else str(case.q_dtype).replace("torch.", ""),
                    "storage_dtype": str(case.q_dtype).replace("torch.", ""),
-                   "decode_path": args.path, "decode_ctas": num_ctas.value,
+                   "decode_path": args.path, "decode_ctas": num_ctas.value if not int8 else None,
                    "workspace_bytes": ws_bytes,
                    "kv_bytes_per_step": sb["kv"], "bytes_per_step": sb["total"],
                    "l2": f"{args.replicas} rotating cache replicas of "
@@ -405,10 +446,12 @@ def run_ours(args, rank, local_rank, world):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": (measured_traffic(args.workload)
-                                 if args.path != "cascade" else None),
-                     "kernel": ("pa_decode_cascade: prefix attention + suffix decode + reduce"
-                                if args.path == "cascade" else
-                                "paged_decode_kernel (balanced mode)"),
+                                 if args.path == "balanced" else None),
+                     "kernel": {"cascade": "pa_decode_cascade: prefix attention + suffix "
+                                           "decode + reduce",
+                                "int8": "pa_decode_int8: counter clear + paged_decode_kernel "
+                                        "(balanced mode, INT8 rows and row scales)",
+                                "balanced": "paged_decode_kernel (balanced mode)"}[args.path],
                      "kernel_bytes_per_launch": sb["kernel"],
                      "kernel_us_mean": round(split_mean * 1e6, 2),
                      "kernel_us_median": round(statistics.median(split_ms) * 1e3, 2)},
@@ -443,9 +486,16 @@ def run_e2e(args, case, pa, L, dev, stream, reps, new_sm, bt, cl, q, new_k, new_
     K = args.steps
 
     def step(i):
-        k_, v_ = reps[i % len(reps)]
+        k_, v_, ks_, vs_ = reps[i % len(reps)]
         for n, t in host.items():
             dev_bufs[n].copy_(t, non_blocking=True)
+        if args.path == "int8":
+            pa.reshape_and_cache_int8(dev_bufs["k"], dev_bufs["v"], k_, v_, ks_, vs_,
+                                      dev_bufs["sm"])
+            pa.decode_int8(out, dev_bufs["q"], k_, v_, ks_, vs_, dev_bufs["bt"], dev_bufs["cl"],
+                           Hkv, case.scale, case.window, ws)
+            out_h.copy_(out, non_blocking=True)
+            return
         pa.reshape_and_cache(dev_bufs["k"], dev_bufs["v"], k_, v_, dev_bufs["sm"],
                              case.kv_dtype, case.k_scale, case.v_scale)
         if args.path == "cascade":
@@ -531,9 +581,10 @@ def main(argv=None):
     ap.add_argument("--workload", default="mistral_bf16",
                     choices=("tiny", "mistral_bf16", "ring_bf16", "fp8_phi3", "prefix_bf16"))
     ap.add_argument("--replicas", type=int, default=4)
-    ap.add_argument("--path", choices=("balanced", "cascade"), default="balanced",
-                    help="decode entry point timed: pa_decode's balanced path, or "
-                         "pa_decode_cascade (workloads with a shared prefix)")
+    ap.add_argument("--path", choices=("balanced", "cascade", "int8"), default="balanced",
+                    help="decode entry point timed: pa_decode's balanced path, "
+                         "pa_decode_cascade (workloads with a shared prefix), or "
+                         "pa_decode_int8 over the workload held as an INT8 cache")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
