@@ -62,6 +62,10 @@ def lib():
                                          _int, _int, _i64, _int, _dbl, _int, _int, _int, _flt,
                                          _flt, _ptr, _ptr, _ptr, _i64]
         L.oracle_int8_quantise_row.argtypes = [_ptr, _int, _ptr, _ptr]
+        L.oracle_prefill_rows.restype = _i64
+        L.oracle_prefill_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _i64, _ptr, _ptr, _ptr, _int,
+                                          _int, _int, _int, _int, _i64, _int, _dbl, _int, _int,
+                                          _flt, _flt, _ptr, _ptr]
         L.oracle_reshape_and_cache_int8.restype = _i64
         L.oracle_reshape_and_cache_int8.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
                                                     _i64, _int, _int, _int, _i64, _int]
@@ -233,6 +237,30 @@ def decode_partial(query, k_cache, v_cache, block_tables, context_lens, s: int, 
     if rc:
         raise ValueError("oracle decode_partial: block id outside the pool")
     return o, m.value, l.value
+
+
+# ---------------------------------------------------------------- prefill
+def prefill(query, q_seq, q_pos, k_cache, v_cache, block_tables, num_kv_heads: int,
+            block_size: int, scale: float, kv_dtype: str = "auto", k_scale: float = 1.0,
+            v_scale: float = 1.0, k_scales=None, v_scales=None):
+    """Causal multi-query attention over the paged cache: query [T, Hq, D], token
+    t of sequence q_seq[t] at position q_pos[t] attends to positions
+    0..q_pos[t]. Returns (out [T, Hq, D] fp64, number of bad rows)."""
+    q = _cpu(query)
+    qs = _cpu(q_seq).to(torch.int32)
+    qp = _cpu(q_pos).to(torch.int32)
+    kc, vc = _cpu(k_cache), _cpu(v_cache)
+    bt = _cpu(block_tables).to(torch.int32)
+    ks, vs = _row_scales(kv_dtype, k_scales, v_scales)
+    T, Hq, D = q.shape
+    out = np.empty((T, Hq, D), dtype=np.float64)
+    bad = lib().oracle_prefill_rows(_p(out), _p(q), _p(qs), _p(qp), T, _p(kc), _p(vc), _p(bt),
+                                    bt.shape[0], Hq, num_kv_heads, D, block_size, kc.shape[0],
+                                    bt.shape[1], float(np.float32(scale)), _CODE[q.dtype],
+                                    _cache_code(kc, kv_dtype), k_scale, v_scale,
+                                    None if ks is None else _p(ks),
+                                    None if vs is None else _p(vs))
+    return out, int(bad)
 
 
 # ---------------------------------------------------------------- reduce

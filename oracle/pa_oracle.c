@@ -20,6 +20,9 @@
  *  - "Rolling buffer cache" (llama.cpp discussion #3581), opening post: with a
  *    fixed span W, timestep i is stored in slot i mod W and overwrites the
  *    older value there.
+ *  - same page, "FlashAttention V2/V3 + PagedAttention" and its feature list
+ *    (speculative decoding): a prefill phase runs several query tokens of a
+ *    sequence against the paged cache at once; each attends causally.
  *  - "libmir-metal trace/kv.rs", model summary strings: a KV cache of type
  *    "INT8 per token/head" keeps packed INT8 pages with one FP32 scale per
  *    token and head, dequantised inside the paged attention.
@@ -367,34 +370,25 @@ static double or_cache_value(const void* cache, int cache_code, size_t i, float 
 }
 
 /*
- * Partial attention of query head h of sequence s over its slots
- * [tok_begin, tok_end) intersected with [0, L_s):
- *   m = max logit, l = sum exp(logit - m), o = sum exp(logit - m) V / l.
+ * Attention of one query row q[D] (fp64) of sequence s, kv head g, over the
+ * slots [b0, b1) of its block table (0 <= b0, b1 <= MB * bs):
+ *   m = max logit, l = sum exp(logit - m), o = sum exp(logit - m) V / l,
+ *   logit_j = scale * q . K_j.
  * Empty range: m = -inf, l = 0, o = 0. Returns -1 if a needed block id is
  * outside [0, num_blocks), else 0. k_scales / v_scales ([NB][Hkv][bs] fp32)
  * are read only for an INT8 cache (cache_code OR_I8).
  */
-int oracle_decode_partial(double* o, double* m_out, double* l_out, const void* query,
-                          const void* k_cache, const void* v_cache,
-                          const int32_t* block_tables, const int32_t* context_lens,
-                          int s, int h, int num_heads, int num_kv_heads, int head_dim,
-                          int block_size, int64_t num_blocks, int max_blocks_per_seq,
-                          double scale, int window, int q_code, int cache_code,
-                          float k_scale, float v_scale, const float* k_scales,
-                          const float* v_scales, int64_t tok_begin, int64_t tok_end)
+static int or_attend(double* o, double* m_out, double* l_out, const double* q, int s, int g,
+                     const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                     int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                     int max_blocks_per_seq, double scale, int cache_code, float k_scale,
+                     float v_scale, const float* k_scales, const float* v_scales, int64_t b0,
+                     int64_t b1)
 {
-    int G = num_heads / num_kv_heads;
-    int g = h / G; /* contiguous groups of query heads share one kv head */
-    int64_t n = context_lens[s];
-    int64_t L = (window > 0 && n > window) ? window : n;
-    int64_t j, cnt, b0, b1;
+    int64_t j, cnt;
     int d, rc = 0;
-    double *K, *V, *logit, *q, m, l;
+    double *K, *V, *logit, m, l;
 
-    if (n < 0)
-        L = 0;
-    b0 = tok_begin < 0 ? 0 : tok_begin;
-    b1 = tok_end < L ? tok_end : L;
     for (d = 0; d < head_dim; ++d)
         o[d] = 0.0;
     *m_out = -INFINITY;
@@ -407,9 +401,6 @@ int oracle_decode_partial(double* o, double* m_out, double* l_out, const void* q
     K = (double*)malloc(sizeof(double) * (size_t)cnt * head_dim);
     V = (double*)malloc(sizeof(double) * (size_t)cnt * head_dim);
     logit = (double*)malloc(sizeof(double) * (size_t)cnt);
-    q = (double*)malloc(sizeof(double) * (size_t)head_dim);
-    for (d = 0; d < head_dim; ++d)
-        q[d] = (double)or_load(query, q_code, ((size_t)s * num_heads + h) * head_dim + d);
     for (j = 0; j < cnt; ++j) {
         int64_t slot = b0 + j;
         int64_t blk = block_tables[(int64_t)s * max_blocks_per_seq + slot / block_size];
@@ -455,6 +446,41 @@ int oracle_decode_partial(double* o, double* m_out, double* l_out, const void* q
     free(K);
     free(V);
     free(logit);
+    return rc;
+}
+
+/*
+ * Partial attention of query head h of sequence s over its slots
+ * [tok_begin, tok_end) intersected with [0, L_s) (see or_attend for the
+ * outputs and the return value).
+ */
+int oracle_decode_partial(double* o, double* m_out, double* l_out, const void* query,
+                          const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, const int32_t* context_lens,
+                          int s, int h, int num_heads, int num_kv_heads, int head_dim,
+                          int block_size, int64_t num_blocks, int max_blocks_per_seq,
+                          double scale, int window, int q_code, int cache_code,
+                          float k_scale, float v_scale, const float* k_scales,
+                          const float* v_scales, int64_t tok_begin, int64_t tok_end)
+{
+    int G = num_heads / num_kv_heads;
+    int g = h / G; /* contiguous groups of query heads share one kv head */
+    int64_t n = context_lens[s];
+    int64_t L = (window > 0 && n > window) ? window : n;
+    int64_t b0, b1;
+    int d, rc;
+    double* q;
+
+    if (n < 0)
+        L = 0;
+    b0 = tok_begin < 0 ? 0 : tok_begin;
+    b1 = tok_end < L ? tok_end : L;
+    q = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    for (d = 0; d < head_dim; ++d)
+        q[d] = (double)or_load(query, q_code, ((size_t)s * num_heads + h) * head_dim + d);
+    rc = or_attend(o, m_out, l_out, q, s, g, k_cache, v_cache, block_tables, num_kv_heads,
+                   head_dim, block_size, num_blocks, max_blocks_per_seq, scale, cache_code,
+                   k_scale, v_scale, k_scales, v_scales, b0, b1);
     free(q);
     return rc;
 }
@@ -486,6 +512,56 @@ int64_t oracle_decode_rows(double* out, const void* query, const void* k_cache,
                                   head_dim, block_size, num_blocks, max_blocks_per_seq, scale,
                                   window, q_code, cache_code, k_scale, v_scale, k_scales,
                                   v_scales, 0, (int64_t)1 << 62) != 0)
+            ++bad;
+    }
+    return bad;
+}
+
+/*
+ * Multi-query (prefill) attention over the paged cache: query token t belongs
+ * to sequence q_seq[t] at absolute position q_pos[t] and attends causally to
+ * the positions 0 .. q_pos[t] of that sequence, read through its block table
+ * (slot = position; no window). Its own K/V and those of the tokens before it
+ * are expected in the cache already. query / out are [T][Hq][D] (out fp64).
+ * A token with q_pos < 0 is padding (its rows of out are 0). Returns the
+ * number of (token, head) rows that met an out-of-range sequence, position or
+ * block id (their rows are NaN).
+ */
+int64_t oracle_prefill_rows(double* out, const void* query, const int32_t* q_seq,
+                            const int32_t* q_pos, int64_t num_tokens, const void* k_cache,
+                            const void* v_cache, const int32_t* block_tables, int num_seqs,
+                            int num_heads, int num_kv_heads, int head_dim, int block_size,
+                            int64_t num_blocks, int max_blocks_per_seq, double scale,
+                            int q_code, int cache_code, float k_scale, float v_scale,
+                            const float* k_scales, const float* v_scales)
+{
+    int64_t i, bad = 0;
+    int G = num_heads / num_kv_heads;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+    for (i = 0; i < num_tokens * num_heads; ++i) {
+        int64_t t = i / num_heads;
+        int h = (int)(i % num_heads), d;
+        int s = q_seq[t];
+        int64_t p = q_pos[t];
+        double* o = out + (size_t)i * head_dim;
+        double m, l, q[512];
+        if (p < 0) {
+            for (d = 0; d < head_dim; ++d)
+                o[d] = 0.0;
+            continue;
+        }
+        if (s < 0 || s >= num_seqs || p >= (int64_t)max_blocks_per_seq * block_size ||
+            head_dim > 512) {
+            for (d = 0; d < head_dim; ++d)
+                o[d] = NAN;
+            ++bad;
+            continue;
+        }
+        for (d = 0; d < head_dim; ++d)
+            q[d] = (double)or_load(query, q_code, (size_t)i * head_dim + d);
+        if (or_attend(o, &m, &l, q, s, h / G, k_cache, v_cache, block_tables, num_kv_heads,
+                      head_dim, block_size, num_blocks, max_blocks_per_seq, scale, cache_code,
+                      k_scale, v_scale, k_scales, v_scales, 0, p + 1) != 0)
             ++bad;
     }
     return bad;

@@ -287,6 +287,21 @@ def empty_scales(case: DecodeCase, device: str = "cpu"):
     return k, k.clone()
 
 
+def prefill_queries(case: DecodeCase, per_seq: int, seed: int, device: str = "cpu"):
+    """Query rows for a prefill chunk: the last min(per_seq, n_s) positions of
+    every sequence, in sequence order. Returns (query [T, Hq, D] of q_dtype,
+    q_seq int32 [T], q_pos int32 [T]); values N(0, 1) from their own seed."""
+    seqs, pos = [], []
+    for s in range(case.num_seqs):
+        n = int(case.context_lens[s])
+        for p in range(max(0, n - per_seq), n):
+            seqs.append(s)
+            pos.append(p)
+    g = torch.Generator().manual_seed(seed)
+    q = _normal(g, (len(pos), case.num_heads, case.head_dim), case.q_dtype, "cpu").to(device)
+    return (q, torch.tensor(seqs, dtype=torch.int32), torch.tensor(pos, dtype=torch.int32))
+
+
 # ------------------------------------------------------------------ named workloads
 CONFIG_NAMES = ("tiny", "mistral_bf16", "ring_bf16", "fp8_phi3", "prefix_bf16")
 
