@@ -237,6 +237,42 @@ pa_status pa_decode_int8(void* out, const void* query,
                          void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_prefill -- causal multi-query attention over the paged cache.
+ *
+ * Source: "PagedAttention in mistral.rs" (a prefill phase runs beside the
+ * paged decode, "FlashAttention V2/V3 + PagedAttention"; speculative
+ * decoding in the feature list): several query tokens of a sequence attend
+ * to its paged K/V at once. Sequence s owns query tokens [cu_q[s], cu_q[s+1])
+ * (q_len_s of them, q_len_s <= max_q_len); they are the LAST q_len_s
+ * positions of its context of n_s = context_lens[s] tokens, whose K and V
+ * are already in the cache (written by pa_reshape_and_cache). Token i of the
+ * chunk is at position p = n_s - q_len_s + i and
+ *   out[cu_q[s] + i][h][:] = softmax_j<=p(scale * q . K_j) V_j,
+ * kv head h / G, fp32 accumulation, P rounded to the input type before P.V
+ * (tensor cores), output rounded to q_dtype. No window.
+ *
+ * out, query   : [T][Hq][D] of q_dtype (BF16 or F16, else PA_ERR_DTYPE).
+ * k_cache,
+ * v_cache      : [NB][Hkv][bs][D] of q_dtype.
+ * block_tables : int32 [S][MB].  cu_q : int32 [S + 1].  context_lens :
+ *                int32 [S].
+ * Supported: D in {64, 128} (PA_ERR_HEAD_DIM); bs in {16, 32, 64}
+ * (PA_ERR_BLOCK_SIZE); G in 1..8; 1 <= max_q_len <= T (PA_ERR_SHAPE).
+ * Device-side checks: offsets that do not fit [0, T] or a q_len above
+ * max_q_len set PA_DEVERR_SEQ and that sequence is not written; n_s < q_len_s
+ * or n_s > MB * bs sets PA_DEVERR_CONTEXT_LEN and its rows are zero; a block
+ * id outside [0, NB) sets PA_DEVERR_BLOCK_ID and reads as zeros. Pointers
+ * 16-byte aligned. T == 0 or S == 0 is a no-op.
+ */
+pa_status pa_prefill(void* out, const void* query,
+                     const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, const int32_t* cu_q,
+                     const int32_t* context_lens, int num_tokens, int num_seqs,
+                     int num_heads, int num_kv_heads, int head_dim, int block_size,
+                     int num_blocks, int max_blocks_per_seq, int max_q_len, float scale,
+                     pa_dtype q_dtype, pa_stream_t stream);
+
+/*
  * pa_decode_plan -- a split plan for pa_decode_partials at these sizes.
  * Writes the number of context splits per (sequence, kv head) and the pages
  * (blocks) each split covers; split i covers slots

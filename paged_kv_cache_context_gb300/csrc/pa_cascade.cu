@@ -303,6 +303,211 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Causal prefill over the paged cache: one CTA per (64-row query tile, kv
+// head, sequence), with the tiles, fragments and online softmax of the prefix
+// kernel above. The CTA's rows are (token, head-in-group) pairs of one
+// sequence; it streams that sequence's pages from position 0 up to the
+// position of its last row, and masks key t for a row at position pos when
+// t > pos. Every row sees position 0, so its running maximum is finite from
+// the first tile on.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_attention_kernel(const __grid_constant__ PrefillParams p) {
+  constexpr int CPR = D / 8;
+  constexpr int TILE = kPrefixTile;
+  constexpr int TBYTES = TILE * D * 2;
+  constexpr int KS = D / 16;
+  constexpr int NT = TILE / 8;
+  constexpr int NO = D / 8;
+  static_assert(CPR >= 8, "the swizzle needs 8 chunks per row");
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* sq = smem;                        // [64][D]
+  uint8_t* sk = smem + kPrefixRows * D * 2;  // [2][TILE][D]
+  uint8_t* sv = sk + 2 * TBYTES;             // [2][TILE][D]
+
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int Hq = p.num_heads, Hkv = p.num_kv_heads, G = p.group, bs = p.block_size;
+  const int MB = p.max_blocks_per_seq;
+  const bool reporter = qt == 0 && g == 0 && tid == 0;  // flags a sequence's errors once
+
+  // this sequence's query tokens [q0, q0 + q_len) and context of n tokens
+  const int q0 = p.cu_q[s];
+  int q_len = p.cu_q[s + 1] - q0;
+  const int n = p.context_lens[s];
+  if (q_len < 0 || q0 < 0 || q0 > p.num_tokens - max(q_len, 0) || q_len > p.max_q_len) {
+    if (reporter) raise_error(p.err, PA_DEVERR_SEQ);
+    return;  // offsets that do not fit the batch: nothing of this sequence is written
+  }
+  const int rows_total = q_len * G;
+  if (qt * kPrefixRows >= rows_total) return;
+  T* out = static_cast<T*>(p.out);
+  if (n < q_len || n > MB * bs) {  // the chunk does not fit its context: zero rows
+    if (reporter) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
+    for (int i = tid; i < kPrefixRows * D; i += kThreads) {
+      const int r = qt * kPrefixRows + i / D;
+      if (r < rows_total)
+        out[((size_t)(q0 + r / G) * Hq + g * G + r % G) * D + i % D] = Elem<T>::from_f32(0.f);
+    }
+    return;
+  }
+  const int pos0 = n - q_len;  // position of the chunk's first token
+  const int r_last = min(qt * kPrefixRows + kPrefixRows, rows_total) - 1;
+  const int kv_end = pos0 + r_last / G + 1;  // keys this CTA needs: positions [0, kv_end)
+
+  // Q rows of this CTA -> shared memory (rows past the sequence's are zero)
+  const uint32_t sq_u = smem_u32(sq), sk_u = smem_u32(sk), sv_u = smem_u32(sv);
+  for (int i = tid; i < kPrefixRows * CPR; i += kThreads) {
+    const int rr = i / CPR, c = i % CPR, r = qt * kPrefixRows + rr;
+    const bool ok = r < rows_total;
+    const size_t row = ok ? (size_t)(q0 + r / G) * Hq + g * G + r % G : 0;
+    cp_async16(sq_u + swz<CPR>(rr, c),
+               static_cast<const uint8_t*>(p.query) + (row * D + c * 8) * 2, ok);
+  }
+  const size_t head_stride = (size_t)bs * D * 2;  // bytes of one (block, kv head) page
+  const int32_t* table = p.block_tables + (size_t)s * MB;
+  auto load_tile = [&](int tile, int buf) {
+    const int t0 = tile * TILE;
+    for (int i = tid; i < TILE * CPR; i += kThreads) {
+      const int rr = i / CPR, c = i % CPR, t = t0 + rr;
+      int b = -1;
+      if (t < kv_end) {
+        b = __ldg(table + t / bs);
+        if (b < 0 || b >= p.num_blocks) {
+          if (c == 0) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+          b = -1;
+        }
+      }
+      const bool ok = b >= 0;
+      const size_t off = ok ? ((size_t)b * Hkv + g) * head_stride + (size_t)(t % bs) * D * 2 + c * 16
+                            : 0;
+      cp_async16(sk_u + buf * TBYTES + swz<CPR>(rr, c), p.k_cache + off, ok);
+      cp_async16(sv_u + buf * TBYTES + swz<CPR>(rr, c), p.v_cache + off, ok);
+    }
+  };
+  const int ntiles = (kv_end + TILE - 1) / TILE;
+  load_tile(0, 0);
+  cp_async_commit();  // group: Q + tile 0
+
+  cp_async_wait<0>();
+  __syncthreads();
+  uint32_t qa[KS][4];
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk)
+    ldsm_x4(sq_u + swz<CPR>(warp * 16 + (lane & 15), 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1],
+            qa[kk][2], qa[kk][3]);
+
+  // positions of this lane's two rows (a row past the sequence's takes the
+  // CTA's last position: finite values that are never stored)
+  const int rA = qt * kPrefixRows + warp * 16 + (lane >> 2), rB = rA + 8;
+  const int posA = rA < rows_total ? pos0 + rA / G : kv_end - 1;
+  const int posB = rB < rows_total ? pos0 + rB / G : kv_end - 1;
+
+  float o[NO][4];
+#pragma unroll
+  for (int nn = 0; nn < NO; ++nn) o[nn][0] = o[nn][1] = o[nn][2] = o[nn][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows rA and rB
+  const int tq = lane & 3;
+
+  for (int tile = 0; tile < ntiles; ++tile) {
+    const int buf = tile & 1;
+    if (tile + 1 < ntiles) load_tile(tile + 1, buf ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();  // this tile's copies are done
+    __syncthreads();
+    const uint32_t kb = sk_u + buf * TBYTES, vb = sv_u + buf * TBYTES;
+
+    float sc[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KS; kk += 2) {
+      uint32_t b2[NT], b3[NT];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        uint32_t b0, b1;
+        ldsm_x4(kb + swz<CPR>(8 * j + (lane & 7), 2 * kk + (lane >> 3)), b0, b1, b2[j], b3[j]);
+        Mma<T>::run(sc[j], qa[kk], b0, b1);
+      }
+#pragma unroll
+      for (int j = 0; j < NT; ++j) Mma<T>::run(sc[j], qa[kk + 1], b2[j], b3[j]);
+    }
+    // scale to log2 units, causal mask, running maximum
+    const int t0 = tile * TILE;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = t0 + 8 * j + 2 * tq + (e & 1);
+        const bool ok = t <= (e < 2 ? posA : posB);
+        sc[j][e] = ok ? sc[j][e] * p.scale_log2 : -INFINITY;
+        if (e < 2) mx0 = fmaxf(mx0, sc[j][e]);
+        else mx1 = fmaxf(mx1, sc[j][e]);
+      }
+#pragma unroll
+    for (int off = 1; off <= 2; off *= 2) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    // m0, m1 are finite after the first tile (position 0 is always seen), so
+    // a tile wholly past a row's position leaves it unchanged (factor 1, p 0)
+    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+    const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+    l0 *= a0;
+    l1 *= a1;
+#pragma unroll
+    for (int nn = 0; nn < NO; ++nn) {
+      o[nn][0] *= a0;
+      o[nn][1] *= a0;
+      o[nn][2] *= a1;
+      o[nn][3] *= a1;
+    }
+    uint32_t pa[NT / 2][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const float p0 = exp2f(sc[j][0] - n0), p1 = exp2f(sc[j][1] - n0);
+      const float p2 = exp2f(sc[j][2] - n1), p3 = exp2f(sc[j][3] - n1);
+      l0 += p0 + p1;
+      l1 += p2 + p3;
+      pa[j / 2][(j & 1) * 2 + 0] = Mma<T>::pack(p0, p1);
+      pa[j / 2][(j & 1) * 2 + 1] = Mma<T>::pack(p2, p3);
+    }
+#pragma unroll
+    for (int kk = 0; kk < NT / 2; ++kk)
+#pragma unroll
+      for (int nn = 0; nn < NO; nn += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vb + swz<CPR>(16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1), nn + (lane >> 4)),
+                  b0, b1, b2, b3);
+        Mma<T>::run(o[nn], pa[kk], b0, b1);
+        Mma<T>::run(o[nn + 1], pa[kk], b2, b3);
+      }
+    __syncthreads();  // the buffer is refilled two tiles on
+  }
+
+#pragma unroll
+  for (int off = 1; off <= 2; off *= 2) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int r = half ? rB : rA;
+    if (r >= rows_total) continue;
+    const size_t row = (size_t)(q0 + r / G) * Hq + g * G + r % G;
+    const float inv = 1.f / (half ? l1 : l0);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(out + row * D);
+#pragma unroll
+    for (int nn = 0; nn < NO; ++nn)
+      dst[4 * nn + tq] = Mma<T>::pack(o[nn][2 * half] * inv, o[nn][2 * half + 1] * inv);
+  }
+}
+
 __global__ void copy_blocks_kernel(uint8_t* k_cache, uint8_t* v_cache, const int32_t* pairs,
                                    int num_blocks, size_t block_bytes, unsigned* err) {
   pdl_wait();
@@ -330,6 +535,17 @@ cudaError_t launch_prefix(const PrefixParams& p, cudaStream_t st) {
   return launch_pdl(kern, grid, dim3(kThreads), smem, st, p);
 }
 
+template <typename T, int D>
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t st) {
+  const int smem = kPrefixRows * D * 2 + 4 * kPrefixTile * D * 2;
+  auto kern = prefill_attention_kernel<T, D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const long long tiles = ((long long)p.max_q_len * p.group + kPrefixRows - 1) / kPrefixRows;
+  const dim3 grid(static_cast<unsigned>(tiles), p.num_kv_heads, p.num_seqs);
+  return launch_pdl(kern, grid, dim3(kThreads), smem, st, p);
+}
+
 }  // namespace
 
 cudaError_t launch_prefix_attention(const PrefixParams& p, int dtype, cudaStream_t st) {
@@ -339,6 +555,17 @@ cudaError_t launch_prefix_attention(const PrefixParams& p, int dtype, cudaStream
   } else if (dtype == PA_F16) {
     if (p.head_dim == 64) return launch_prefix<__half, 64>(p, st);
     if (p.head_dim == 128) return launch_prefix<__half, 128>(p, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prefill_attention(const PrefillParams& p, int dtype, cudaStream_t st) {
+  if (dtype == PA_BF16) {
+    if (p.head_dim == 64) return launch_prefill<__nv_bfloat16, 64>(p, st);
+    if (p.head_dim == 128) return launch_prefill<__nv_bfloat16, 128>(p, st);
+  } else if (dtype == PA_F16) {
+    if (p.head_dim == 64) return launch_prefill<__half, 64>(p, st);
+    if (p.head_dim == 128) return launch_prefill<__half, 128>(p, st);
   }
   return cudaErrorInvalidValue;
 }

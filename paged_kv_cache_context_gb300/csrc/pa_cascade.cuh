@@ -45,6 +45,32 @@ constexpr int kPrefixTile = 64;
 // for other element types or head dimensions (64 and 128 are built).
 cudaError_t launch_prefix_attention(const PrefixParams& p, int dtype, cudaStream_t stream);
 
+// Causal multi-query (prefill) attention over the paged cache ("PagedAttention
+// in mistral.rs": a prefill phase next to the paged decode, and speculative
+// decoding, both attend several query tokens of a sequence at once). Sequence
+// s owns query tokens [cu_q[s], cu_q[s+1]); they are the last q_len_s
+// positions of its context of n_s = context_lens[s] tokens, whose K/V are in
+// the cache already: token i sits at position n_s - q_len_s + i and attends
+// to positions 0 .. that position. For kv head g the rows of a sequence are
+// its q_len_s * G (token, head-in-group) pairs, so Q K^T and P V are dense
+// contractions over the sequence's pages.
+struct PrefillParams {
+  void* out;                    // [T][Hq][D], same element type as the query
+  const void* query;            // [T][Hq][D]
+  const uint8_t* k_cache;       // [NB][Hkv][bs][D]
+  const uint8_t* v_cache;
+  const int32_t* block_tables;  // [S][MB]
+  const int32_t* cu_q;          // [S + 1]: query token offsets
+  const int32_t* context_lens;  // [S]: context length including the chunk
+  unsigned* err;
+  int num_seqs, num_heads, num_kv_heads, group, head_dim, block_size, num_blocks;
+  int num_tokens, max_blocks_per_seq, max_q_len;
+  float scale_log2;  // scale * log2(e)
+};
+
+// dtype: 1 = bf16, 2 = f16. Head dims 64 and 128 are built.
+cudaError_t launch_prefill_attention(const PrefillParams& p, int dtype, cudaStream_t stream);
+
 // Copies whole blocks (all kv heads, K and V) src -> dst for each pair of
 // block_pairs [n][2]; block ids outside [0, num_blocks) set PA_DEVERR_BLOCK_ID
 // and are skipped. block_bytes (a multiple of 16) = Hkv * bs * D * element size.

@@ -62,6 +62,7 @@ def lib() -> ctypes.CDLL:
             "pa_block_budget": [I, ctypes.c_double, Z, I, I, I, I, I, I],
             "pa_reshape_and_cache_int8": [P, P, P, P, P, P, P, I, I, I, I, I, I, P],
             "pa_decode_int8": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, Z, P],
+            "pa_prefill": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P],
             "pa_decode_static_scratch": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F,
                                          F, P],
             "pa_get_device_error": [P, P],
@@ -155,6 +156,21 @@ def decode_int8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
                                 _ptr(context_lens), S, Hq, num_kv_heads, D, bs, NB, MB, scale,
                                 window, _DTYPE[query.dtype], _ptr(workspace), ws_bytes,
                                 _stream(stream)), "pa_decode_int8")
+
+
+def prefill(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+            v_cache: torch.Tensor, block_tables: torch.Tensor, cu_q: torch.Tensor,
+            context_lens: torch.Tensor, num_kv_heads: int, max_q_len: int, scale: float,
+            stream=None):
+    """pa_prefill: causal attention of query [T, Hq, D] (the last tokens of each
+    sequence's context, offsets cu_q [S + 1]) over the paged cache."""
+    T, Hq, D = query.shape
+    NB, _, bs, _ = k_cache.shape
+    S, MB = block_tables.shape
+    _check(lib().pa_prefill(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache),
+                            _ptr(block_tables), _ptr(cu_q), _ptr(context_lens), T, S, Hq,
+                            num_kv_heads, D, bs, NB, MB, max_q_len, scale, _DTYPE[query.dtype],
+                            _stream(stream)), "pa_prefill")
 
 
 def decode_plan(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,

@@ -31,6 +31,7 @@ def test_header_declares_the_boundary():
                  "pa_decode_partials", "pa_decode_plan", "pa_decode_workspace_size",
                  "pa_decode_cascade", "pa_decode_cascade_workspace_size", "pa_copy_blocks",
                  "pa_block_budget", "pa_reshape_and_cache_int8", "pa_decode_int8",
+                 "pa_prefill",
                  "pa_get_device_error", "pa_status_string", "pa_version"):
         assert want in names
 
@@ -258,3 +259,24 @@ def test_int8_entry_points_reject_bad_arguments_on_host(L):
     assert L.pa_decode(P, P, P, P, P, P, 4, 8, 2, 128, 32, 10, 8, 0.1, 0, 1, 2, 1.0, 1.0, None,
                        0, None) == -2
     assert L.pa_reshape_and_cache(P, P, P, P, P, 4, 2, 128, 32, 10, 1, 2, 1.0, 1.0, None) == -2
+
+
+def test_prefill_rejects_bad_arguments_on_host(L):
+    f = L.pa_prefill
+
+    def call(**kw):
+        a = dict(out=P, q=P, k=P, v=P, bt=P, cu=P, cl=P, T=40, S=4, Hq=8, Hkv=2, D=128, bs=32,
+                 NB=10, MB=8, mq=16, scale=0.1, qd=1)
+        a.update(kw)
+        return f(a["out"], a["q"], a["k"], a["v"], a["bt"], a["cu"], a["cl"], a["T"], a["S"],
+                 a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"], a["MB"], a["mq"], a["scale"],
+                 a["qd"], None)
+
+    assert call(T=0, q=None) == 0 and call(S=0, q=None) == 0
+    assert call(T=-1) == -3 and call(S=70000) == -3
+    assert call(cu=None) == -1 and call(cl=None) == -1 and call(bt=None) == -1
+    assert call(qd=0) == -2 and call(qd=4) == -2
+    assert call(Hq=6, Hkv=4) == -3 and call(Hq=32, Hkv=2) == -3
+    assert call(D=96) == -4 and call(bs=8) == -5
+    assert call(mq=0) == -3 and call(mq=41) == -3
+    assert call(out=P + 2) == -10 and call(k=P + 8) == -10
