@@ -5,6 +5,12 @@ sizes to the same-named C entry point of ``libpagedattn.so`` on the current
 torch stream, and raises ``PagedAttentionError`` on a non-zero status. All
 computation runs in the library's CUDA kernels; there is no fallback: if the
 library is missing, loading fails loudly.
+
+The sizes the C calls receive are read from the tensors' shapes, so before a
+call the binding checks what the C side cannot see: that every tensor is a
+CUDA tensor on one device (the library takes raw device pointers) and that
+the shapes and element types of the arguments agree with each other. A
+mismatch raises ``ValueError`` and nothing is enqueued.
 """
 from __future__ import annotations
 
@@ -97,6 +103,71 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return t.data_ptr()
 
 
+def _is_device_tensor(t: torch.Tensor) -> bool:
+    return t.is_cuda
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _on_device(**named):
+    """Every tensor argument is a CUDA tensor, all on one device."""
+    dev = None
+    for name, t in named.items():
+        if t is None:
+            continue
+        _need(isinstance(t, torch.Tensor), f"{name}: expected a torch tensor")
+        _need(_is_device_tensor(t), f"{name}: must be a CUDA tensor (the library takes device "
+                                    "pointers)")
+        if dev is None:
+            dev = t.device
+        _need(t.device == dev, f"{name}: every tensor must be on {dev}")
+
+
+def _shape(name: str, t: torch.Tensor, shape):
+    _need(tuple(t.shape) == tuple(shape),
+          f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _dtype(name: str, t: torch.Tensor, dt: torch.dtype):
+    _need(t.dtype == dt, f"{name}: dtype {t.dtype}, expected {dt}")
+
+
+_CACHE_DTYPE = {"fp8_e4m3": torch.uint8, "int8": torch.int8}
+
+
+def _check_caches(k_cache, v_cache, num_kv_heads: int, head_dim: int, dtype: torch.dtype):
+    _need(k_cache.dim() == 4, "k_cache: expected [num_blocks, num_kv_heads, block_size, D]")
+    _shape("v_cache", v_cache, k_cache.shape)
+    _need(k_cache.shape[1] == num_kv_heads and k_cache.shape[3] == head_dim,
+          f"k_cache: shape {tuple(k_cache.shape)} does not hold {num_kv_heads} kv heads of "
+          f"dimension {head_dim}")
+    _dtype("k_cache", k_cache, dtype)
+    _dtype("v_cache", v_cache, dtype)
+
+
+def _check_scales(k_scales, v_scales, k_cache):
+    for name, t in (("k_scales", k_scales), ("v_scales", v_scales)):
+        _shape(name, t, k_cache.shape[:3])
+        _dtype(name, t, torch.float32)
+
+
+def _check_decode_args(out, query, k_cache, v_cache, block_tables, context_lens,
+                       num_kv_heads: int, cache_dtype: torch.dtype):
+    _need(query.dim() == 3, "query: expected [num_seqs, num_heads, head_dim]")
+    S, Hq, D = query.shape
+    _shape("out", out, query.shape)
+    _dtype("out", out, query.dtype)
+    _check_caches(k_cache, v_cache, num_kv_heads, D, cache_dtype)
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == S,
+          f"block_tables: expected [{S}, max_blocks_per_seq]")
+    _dtype("block_tables", block_tables, torch.int32)
+    _shape("context_lens", context_lens, (S,))
+    _dtype("context_lens", context_lens, torch.int32)
+
+
 def _stream(stream: Optional[torch.cuda.Stream]) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
@@ -110,6 +181,15 @@ def _check(rc: int, what: str):
 def slot_mapping(out: torch.Tensor, block_tables: torch.Tensor, seq_idx: Optional[torch.Tensor],
                  positions: torch.Tensor, block_size: int, window: int = 0, stream=None):
     """pa_slot_mapping: out[t] = cache slot of token t (ring-aware)."""
+    _on_device(out=out, block_tables=block_tables, seq_idx=seq_idx, positions=positions)
+    _need(block_tables.dim() == 2, "block_tables: expected [num_seqs, max_blocks_per_seq]")
+    _dtype("block_tables", block_tables, torch.int32)
+    _dtype("positions", positions, torch.int32)
+    _shape("out", out, (positions.numel(),))
+    _dtype("out", out, torch.int64)
+    if seq_idx is not None:
+        _shape("seq_idx", seq_idx, (positions.numel(),))
+        _dtype("seq_idx", seq_idx, torch.int32)
     S, MB = block_tables.shape
     _check(lib().pa_slot_mapping(_ptr(out), _ptr(block_tables), _ptr(seq_idx), _ptr(positions),
                                  positions.numel(), S, MB, block_size, window, _stream(stream)),
@@ -120,6 +200,15 @@ def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Ten
                       v_cache: torch.Tensor, slot_mapping_: torch.Tensor, kv_dtype: str = "auto",
                       k_scale: float = 1.0, v_scale: float = 1.0, stream=None):
     """pa_reshape_and_cache: key/value [T, Hkv, D] into caches [NB, Hkv, bs, D]."""
+    _on_device(key=key, value=value, k_cache=k_cache, v_cache=v_cache,
+               slot_mapping=slot_mapping_)
+    _need(key.dim() == 3, "key: expected [num_tokens, num_kv_heads, head_dim]")
+    _shape("value", value, key.shape)
+    _dtype("value", value, key.dtype)
+    _check_caches(k_cache, v_cache, key.shape[1], key.shape[2],
+                  _CACHE_DTYPE.get(kv_dtype, key.dtype))
+    _shape("slot_mapping", slot_mapping_, (key.shape[0],))
+    _dtype("slot_mapping", slot_mapping_, torch.int64)
     T, H, D = key.shape
     NB, _, bs, _ = k_cache.shape
     _check(lib().pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
@@ -133,6 +222,15 @@ def reshape_and_cache_int8(key: torch.Tensor, value: torch.Tensor, k_cache: torc
                            slot_mapping_: torch.Tensor, stream=None):
     """pa_reshape_and_cache_int8: key/value [T, Hkv, D] into int8 caches
     [NB, Hkv, bs, D] and fp32 row scales [NB, Hkv, bs]."""
+    _on_device(key=key, value=value, k_cache=k_cache, v_cache=v_cache, k_scales=k_scales,
+               v_scales=v_scales, slot_mapping=slot_mapping_)
+    _need(key.dim() == 3, "key: expected [num_tokens, num_kv_heads, head_dim]")
+    _shape("value", value, key.shape)
+    _dtype("value", value, key.dtype)
+    _check_caches(k_cache, v_cache, key.shape[1], key.shape[2], torch.int8)
+    _check_scales(k_scales, v_scales, k_cache)
+    _shape("slot_mapping", slot_mapping_, (key.shape[0],))
+    _dtype("slot_mapping", slot_mapping_, torch.int64)
     T, H, D = key.shape
     NB, _, bs, _ = k_cache.shape
     _check(lib().pa_reshape_and_cache_int8(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
@@ -147,6 +245,12 @@ def decode_int8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
                 scale: float, window: int = 0, workspace: Optional[torch.Tensor] = None,
                 stream=None):
     """pa_decode_int8: pa_decode over an INT8 cache with per-row scales."""
+    _on_device(out=out, query=query, k_cache=k_cache, v_cache=v_cache, k_scales=k_scales,
+               v_scales=v_scales, block_tables=block_tables, context_lens=context_lens,
+               workspace=workspace)
+    _check_decode_args(out, query, k_cache, v_cache, block_tables, context_lens, num_kv_heads,
+                       torch.int8)
+    _check_scales(k_scales, v_scales, k_cache)
     S, Hq, D = query.shape
     NB, _, bs, _ = k_cache.shape
     MB = block_tables.shape[1]
@@ -164,6 +268,19 @@ def prefill(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
             stream=None):
     """pa_prefill: causal attention of query [T, Hq, D] (the last tokens of each
     sequence's context, offsets cu_q [S + 1]) over the paged cache."""
+    _on_device(out=out, query=query, k_cache=k_cache, v_cache=v_cache,
+               block_tables=block_tables, cu_q=cu_q, context_lens=context_lens)
+    _need(query.dim() == 3, "query: expected [num_tokens, num_heads, head_dim]")
+    _shape("out", out, query.shape)
+    _dtype("out", out, query.dtype)
+    _check_caches(k_cache, v_cache, num_kv_heads, query.shape[2], query.dtype)
+    _need(block_tables.dim() == 2, "block_tables: expected [num_seqs, max_blocks_per_seq]")
+    _dtype("block_tables", block_tables, torch.int32)
+    S = block_tables.shape[0]
+    _shape("cu_q", cu_q, (S + 1,))
+    _dtype("cu_q", cu_q, torch.int32)
+    _shape("context_lens", context_lens, (S,))
+    _dtype("context_lens", context_lens, torch.int32)
     T, Hq, D = query.shape
     NB, _, bs, _ = k_cache.shape
     S, MB = block_tables.shape
@@ -194,6 +311,10 @@ def decode(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor, v_cach
            scale: float, window: int = 0, kv_dtype: str = "auto", k_scale: float = 1.0,
            v_scale: float = 1.0, workspace: Optional[torch.Tensor] = None, stream=None):
     """pa_decode: out [S, Hq, D] = paged attention of query [S, Hq, D]."""
+    _on_device(out=out, query=query, k_cache=k_cache, v_cache=v_cache,
+               block_tables=block_tables, context_lens=context_lens, workspace=workspace)
+    _check_decode_args(out, query, k_cache, v_cache, block_tables, context_lens, num_kv_heads,
+                       _CACHE_DTYPE.get(kv_dtype, query.dtype))
     S, Hq, D = query.shape
     NB, _, bs, _ = k_cache.shape
     MB = block_tables.shape[1]
@@ -211,6 +332,10 @@ def decode_balanced(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tenso
                     stream=None) -> int:
     """pa_decode_balanced: the balanced path's decode launch (arrival counters
     must be zero: see decode_workspace_clear); returns num_ctas."""
+    _on_device(out=out, query=query, k_cache=k_cache, v_cache=v_cache,
+               block_tables=block_tables, context_lens=context_lens, workspace=workspace)
+    _check_decode_args(out, query, k_cache, v_cache, block_tables, context_lens, num_kv_heads,
+                       _CACHE_DTYPE.get(kv_dtype, query.dtype))
     S, Hq, D = query.shape
     NB, _, bs, _ = k_cache.shape
     MB = block_tables.shape[1]
@@ -226,6 +351,7 @@ def decode_balanced(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tenso
 
 def decode_workspace_clear(workspace: torch.Tensor, stream=None):
     """pa_decode_workspace_clear: zero the balanced path's arrival counters."""
+    _on_device(workspace=workspace)
     _check(lib().pa_decode_workspace_clear(_ptr(workspace),
                                            workspace.numel() * workspace.element_size(),
                                            _stream(stream)), "pa_decode_workspace_clear")
@@ -242,6 +368,10 @@ def decode_cascade(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor
                    num_kv_heads: int, scale: float, prefix_pages: int,
                    workspace: torch.Tensor, stream=None):
     """pa_decode_cascade: decode of a batch sharing its first prefix_pages blocks."""
+    _on_device(out=out, query=query, k_cache=k_cache, v_cache=v_cache,
+               block_tables=block_tables, context_lens=context_lens, workspace=workspace)
+    _check_decode_args(out, query, k_cache, v_cache, block_tables, context_lens, num_kv_heads,
+                       query.dtype)
     S, Hq, D = query.shape
     NB, _, bs, _ = k_cache.shape
     MB = block_tables.shape[1]
@@ -255,6 +385,12 @@ def decode_cascade(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor
 def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_pairs: torch.Tensor,
                 stream=None):
     """pa_copy_blocks: block_pairs int32 [n, 2] = (source, destination)."""
+    _on_device(k_cache=k_cache, v_cache=v_cache, block_pairs=block_pairs)
+    _need(k_cache.dim() == 4, "k_cache: expected [num_blocks, num_kv_heads, block_size, D]")
+    _shape("v_cache", v_cache, k_cache.shape)
+    _dtype("v_cache", v_cache, k_cache.dtype)
+    _need(block_pairs.dim() == 2 and block_pairs.shape[1] == 2, "block_pairs: expected [n, 2]")
+    _dtype("block_pairs", block_pairs, torch.int32)
     NB, H, bs, D = k_cache.shape
     _check(lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs),
                                 block_pairs.shape[0], H, D, bs, NB, k_cache.element_size(),
@@ -294,7 +430,17 @@ def decode_partials(tmp_out: torch.Tensor, max_logits: torch.Tensor, exp_sums: t
                     stream=None):
     """pa_decode_partials: split partials tmp_out [S, Hq, NS, D], max_logits and
     exp_sums [S, Hq, NS]."""
+    _on_device(tmp_out=tmp_out, max_logits=max_logits, exp_sums=exp_sums, query=query,
+               k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+               context_lens=context_lens)
+    _check_decode_args(query, query, k_cache, v_cache, block_tables, context_lens, num_kv_heads,
+                       _CACHE_DTYPE.get(kv_dtype, query.dtype))
     S, Hq, D = query.shape
+    _shape("tmp_out", tmp_out, (S, Hq, num_splits, D))
+    for name, t in (("max_logits", max_logits), ("exp_sums", exp_sums)):
+        _shape(name, t, (S, Hq, num_splits))
+        _dtype(name, t, torch.float32)
+    _dtype("tmp_out", tmp_out, torch.float32)
     NB, _, bs, _ = k_cache.shape
     MB = block_tables.shape[1]
     _check(lib().pa_decode_partials(_ptr(tmp_out), _ptr(max_logits), _ptr(exp_sums),
@@ -308,7 +454,14 @@ def decode_partials(tmp_out: torch.Tensor, max_logits: torch.Tensor, exp_sums: t
 def reduce(out: torch.Tensor, tmp_out: torch.Tensor, max_logits: torch.Tensor,
            exp_sums: torch.Tensor, stream=None):
     """pa_reduce: LSE combination of [S, Hq, NS, D] partials into out [S, Hq, D]."""
+    _on_device(out=out, tmp_out=tmp_out, max_logits=max_logits, exp_sums=exp_sums)
+    _need(tmp_out.dim() == 4, "tmp_out: expected [num_seqs, num_heads, num_splits, D]")
     S, Hq, NS, D = tmp_out.shape
+    _shape("out", out, (S, Hq, D))
+    _dtype("tmp_out", tmp_out, torch.float32)
+    for name, t in (("max_logits", max_logits), ("exp_sums", exp_sums)):
+        _shape(name, t, (S, Hq, NS))
+        _dtype(name, t, torch.float32)
     _check(lib().pa_reduce(_ptr(out), _ptr(tmp_out), _ptr(max_logits), _ptr(exp_sums), S, Hq,
                            D, NS, _DTYPE[out.dtype], _stream(stream)), "pa_reduce")
 
