@@ -118,21 +118,24 @@ def _on_device(**named):
     for name, t in named.items():
         if t is None:
             continue
-        _need(isinstance(t, torch.Tensor), f"{name}: expected a torch tensor")
-        _need(_is_device_tensor(t), f"{name}: must be a CUDA tensor (the library takes device "
-                                    "pointers)")
+        if not isinstance(t, torch.Tensor):
+            raise ValueError(f"{name}: expected a torch tensor")
+        if not _is_device_tensor(t):
+            raise ValueError(f"{name}: must be a CUDA tensor (the library takes device pointers)")
         if dev is None:
             dev = t.device
-        _need(t.device == dev, f"{name}: every tensor must be on {dev}")
+        elif t.device != dev:
+            raise ValueError(f"{name}: every tensor must be on {dev}")
 
 
 def _shape(name: str, t: torch.Tensor, shape):
-    _need(tuple(t.shape) == tuple(shape),
-          f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.shape != shape:
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
 def _dtype(name: str, t: torch.Tensor, dt: torch.dtype):
-    _need(t.dtype == dt, f"{name}: dtype {t.dtype}, expected {dt}")
+    if t.dtype != dt:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dt}")
 
 
 _CACHE_DTYPE = {"fp8_e4m3": torch.uint8, "int8": torch.int8}
@@ -141,9 +144,9 @@ _CACHE_DTYPE = {"fp8_e4m3": torch.uint8, "int8": torch.int8}
 def _check_caches(k_cache, v_cache, num_kv_heads: int, head_dim: int, dtype: torch.dtype):
     _need(k_cache.dim() == 4, "k_cache: expected [num_blocks, num_kv_heads, block_size, D]")
     _shape("v_cache", v_cache, k_cache.shape)
-    _need(k_cache.shape[1] == num_kv_heads and k_cache.shape[3] == head_dim,
-          f"k_cache: shape {tuple(k_cache.shape)} does not hold {num_kv_heads} kv heads of "
-          f"dimension {head_dim}")
+    if k_cache.shape[1] != num_kv_heads or k_cache.shape[3] != head_dim:
+        raise ValueError(f"k_cache: shape {tuple(k_cache.shape)} does not hold {num_kv_heads} "
+                         f"kv heads of dimension {head_dim}")
     _dtype("k_cache", k_cache, dtype)
     _dtype("v_cache", v_cache, dtype)
 
@@ -161,8 +164,8 @@ def _check_decode_args(out, query, k_cache, v_cache, block_tables, context_lens,
     _shape("out", out, query.shape)
     _dtype("out", out, query.dtype)
     _check_caches(k_cache, v_cache, num_kv_heads, D, cache_dtype)
-    _need(block_tables.dim() == 2 and block_tables.shape[0] == S,
-          f"block_tables: expected [{S}, max_blocks_per_seq]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError(f"block_tables: expected [{S}, max_blocks_per_seq]")
     _dtype("block_tables", block_tables, torch.int32)
     _shape("context_lens", context_lens, (S,))
     _dtype("context_lens", context_lens, torch.int32)
