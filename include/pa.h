@@ -170,6 +170,8 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
  *                context. Contents on entry do not matter; on exit undefined.
  * Supported: D in {64, 96, 128}; bs in {16, 32, 64}; G = Hq/Hkv in 1..8;
  * q_dtype F32/BF16/F16; AUTO caches hold q_dtype. Pointers 16-byte aligned.
+ * kv_dtype PA_KV_INT8 is refused with PA_ERR_DTYPE here (its row scales go
+ * through pa_decode_int8).
  */
 pa_status pa_decode(void* out, const void* query,
                     const void* k_cache, const void* v_cache,

@@ -280,3 +280,16 @@ def test_prefill_rejects_bad_arguments_on_host(L):
     assert call(D=96) == -4 and call(bs=8) == -5
     assert call(mq=0) == -3 and call(mq=41) == -3
     assert call(out=P + 2) == -10 and call(k=P + 8) == -10
+
+
+def test_int8_widening_identity_holds_for_every_code():
+    """The decode widens INT8 codes without a conversion instruction: with the
+    code's sign bit flipped, u = c + 128 is placed as the low byte of the
+    binary32 bit pattern 0x4B0000uu (= 2^23 + u), and 2^23 + 128 is
+    subtracted. Restated here in numpy for all 256 codes: the result is c,
+    exactly."""
+    import numpy as np
+    c = np.arange(-128, 128, dtype=np.int32)
+    u = (c.astype(np.uint32) & 0xFF) ^ 0x80
+    f = (np.uint32(0x4B000000) | u).view(np.float32)
+    assert np.array_equal(f - np.float32(8388736.0), c.astype(np.float32))
