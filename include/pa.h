@@ -431,7 +431,8 @@ pa_status pa_reduce(void* out, const float* tmp_out, const float* max_logits,
  * time). It computes exactly what pa_decode computes, with the same kernels,
  * but keeps the partial results in an array the library itself holds in
  * device memory: PA_STATIC_SCRATCH_BYTES (8 MiB) on every GPU where the
- * library is loaded, kept until the process exits. It allocates nothing.
+ * library's device code has been loaded, kept until the process exits. It
+ * allocates nothing.
  *
  *  - Limit: when these sizes need more partial storage than
  *    PA_STATIC_SCRATCH_BYTES (pa_decode_workspace_size() larger than it), the
@@ -439,9 +440,13 @@ pa_status pa_reduce(void* out, const float* tmp_out, const float* max_logits,
  *    dimension and group size pa_decode supports fits. This size check comes
  *    before the argument checks of pa_decode; every other argument rule and
  *    error of pa_decode applies unchanged.
- *  - Set-up: the first call on a device (that device current) looks up the
- *    array's device address once (cudaGetSymbolAddress); make that first call
- *    on each device before any stream capture begins.
+ *  - Set-up: each call looks up the array's address on the current device
+ *    (cudaGetSymbolAddress); `stream` must belong to that device. The first
+ *    call on a device may be the first use of the library's device code
+ *    there, in which case the CUDA runtime loads that code and reserves the
+ *    array then (a device allocation and an implicit synchronisation inside
+ *    the runtime, not by this library): make the first call on each device
+ *    during set-up, before any stream capture begins.
  *  - Sharing: all calls on a device share the one array, which keeps whatever
  *    the last call left in it. Nothing in it needs to start at zero (each call
  *    clears the counters it relies on). Calls
@@ -498,6 +503,21 @@ int64_t pa_block_budget(pa_budget_kind kind, double amount, size_t available_byt
  * some were, PA_ERR_CUDA when the synchronisation itself failed.
  */
 pa_status pa_get_device_error(pa_stream_t stream, uint32_t* error_bits);
+
+/*
+ * pa_test_set_unarmed_page -- test hook for the bounded waits (no page of the
+ * pages describes it). With page >= 0, every decode launched afterwards by
+ * this process (pa_decode, pa_decode_balanced, pa_decode_partials and the
+ * calls built on them) stops its producer, in every CTA, before it arms the
+ * stage of the CTA's page number `page` (counted from the CTA's first page):
+ * no copy is issued for that stage or after it. The consumer warps' wait for
+ * that stage then gives up after its limit (200 ms), sets
+ * PA_DEVERR_TIMEOUT and the CTA ends in order, having waited for every copy
+ * it did issue; the outputs of such a launch are unspecified. A negative page
+ * (the initial state) switches the hook off. Not thread-safe with respect to
+ * launches in flight on other host threads; for tests only.
+ */
+void pa_test_set_unarmed_page(int page);
 
 /* Static English text for a pa_status value (never NULL). */
 const char* pa_status_string(int status);

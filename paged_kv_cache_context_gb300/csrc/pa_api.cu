@@ -1,10 +1,13 @@
 // pa_api.cu -- the C ABI of include/pa.h: host-side validation and planning,
 // the small kernels (slot mapping, cache write, split reduction) and the
 // per-device error word. The decode kernels live in pa_decode_<q>_<cache>.cu.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -318,6 +321,9 @@ static pa_status check_decode(const DecodeShape& a, const void* out, const void*
       !(isfinite(a.k_scale) && a.k_scale > 0.f && isfinite(a.v_scale) && a.v_scale > 0.f))
     return PA_ERR_SCALE;
   if (!aligned16(out) || !aligned16(query) || !aligned16(kc) || !aligned16(vc)) return PA_ERR_ALIGN;
+  if (tc_eligible(a.q_dtype, a.kv_dtype, a.D, group_bucket(a.Hq / a.Hkv), a.bs) &&
+      (long long)a.NB * a.Hkv * a.bs > (1LL << 31) - 1)
+    return PA_ERR_SHAPE;
   return PA_OK;
 }
 
@@ -344,9 +350,90 @@ static void plan(int S, int Hkv, int MB, int bs, int window, int* ns, int* pps) 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 
-static cudaError_t run_decode(const DecodeParams& prm, const DecodeShape& a, dim3 grid, int mode,
-                              int* ctas, cudaStream_t st) {
+// ================================================================ tensor maps
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point
+// (nothing links against the driver library itself).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// The rows of a cache [NB * Hkv * bs][D] of 16-bit elements as a 2-D tensor
+// map for the tensor-core decode: boxes of 64 elements x bs rows, 128-byte
+// swizzle. Encodings are kept in a small ring keyed by (address, type, D,
+// rows, bs), so steady-state calls on the same caches skip the encode.
+struct TmapKey {
+  const void* base;
+  long long rows;
+  int dtype, D, bs;
+};
+static std::mutex g_tmap_mu;
+static constexpr int kTmapSlots = 16;
+static TmapKey g_tmap_key[kTmapSlots];
+static CUtensorMap g_tmap_val[kTmapSlots];
+static int g_tmap_used = 0, g_tmap_next = 0;
+
+static bool page_tensor_map(CUtensorMap* out, const void* base, int dtype, int D, long long rows,
+                            int bs) {
+  {
+    std::lock_guard<std::mutex> lk(g_tmap_mu);
+    for (int i = 0; i < g_tmap_used; ++i) {
+      const TmapKey& k = g_tmap_key[i];
+      if (k.base == base && k.rows == rows && k.dtype == dtype && k.D == D && k.bs == bs) {
+        *out = g_tmap_val[i];
+        return true;
+      }
+    }
+  }
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bs)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  if (fn(&m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+         2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lk(g_tmap_mu);
+  const int i = g_tmap_used < kTmapSlots ? g_tmap_used++ : g_tmap_next;
+  g_tmap_next = (i + 1) % kTmapSlots;
+  g_tmap_key[i] = TmapKey{base, rows, dtype, D, bs};
+  g_tmap_val[i] = m;
+  *out = m;
+  return true;
+}
+
+// Most rows a cache read by the tensor-core decode may have: a row index is
+// a 32-bit signed tensor coordinate.
+constexpr long long kMaxTcRows = (1LL << 31) - 1;
+
+static bool decode_is_tc(const DecodeShape& a) {
+  return tc_eligible(a.q_dtype, a.kv_dtype, a.D, group_bucket(a.Hq / a.Hkv), a.bs);
+}
+
+static cudaError_t run_decode(const DecodeParams& prm_in, const DecodeShape& a, dim3 grid,
+                              int mode, int* ctas, cudaStream_t st) {
   const int GT = group_bucket(a.Hq / a.Hkv);
+  DecodeParams prm = prm_in;
+  if (decode_is_tc(a)) {
+    const long long rows = (long long)a.NB * a.Hkv * a.bs;
+    if (rows > kMaxTcRows ||
+        !page_tensor_map(&prm.tm_k, prm.k_cache, a.q_dtype, a.D, rows, a.bs) ||
+        !page_tensor_map(&prm.tm_v, prm.v_cache, a.q_dtype, a.D, rows, a.bs))
+      return cudaErrorInvalidValue;
+  }
   if (a.kv_dtype == PA_KV_AUTO) {
     switch (a.q_dtype) {
       case PA_F32: return pa_dispatch_decode_f32_f32(prm, grid, a.D, GT, a.bs, mode, ctas, st);
@@ -393,11 +480,15 @@ static BalancedWs balanced_carve(void* ws, int GT, int D) {
   return w;
 }
 
+// Test hook of pa_test_set_unarmed_page (negative = off).
+static std::atomic<int> g_unarmed_page{-1};
+
 static DecodeParams make_params(const DecodeShape& a, const void* query, const void* kc,
                                 const void* vc, const int32_t* bt, const int32_t* cl,
                                 float scale, unsigned* err) {
   constexpr float kLog2e = 1.4426950408889634f;
   DecodeParams p{};
+  p.unarmed_page = g_unarmed_page.load(std::memory_order_relaxed);
   p.query = query;
   p.k_cache = static_cast<const uint8_t*>(kc);
   p.v_cache = static_cast<const uint8_t*>(vc);
@@ -996,6 +1087,8 @@ PA_API int64_t pa_block_budget(pa_budget_kind kind, double amount, size_t availa
   if (blocks > 9.0e18) return PA_ERR_SHAPE;
   return static_cast<int64_t>(blocks);
 }
+
+PA_API void pa_test_set_unarmed_page(int page) { g_unarmed_page.store(page < 0 ? -1 : page); }
 
 PA_API pa_status pa_get_device_error(pa_stream_t stream, uint32_t* error_bits) {
   if (error_bits) *error_bits = 0;

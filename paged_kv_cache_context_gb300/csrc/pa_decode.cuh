@@ -43,8 +43,18 @@
 //          weighted, so stale or NaN cache rows cannot reach the output.
 //     At the end of a piece the warps merge (m, l, acc) through the piece's
 //     last stage (reused as scratch before it is released) and store.
+//  * tensor-core consumers (16-bit cache read with queries of the same type,
+//    G >= 4, head_dim 64 or 128): the pages are staged by 2-D tensor copies
+//    with the 128-byte swizzle, and each of the 4 consumer warps takes 16
+//    rows of a page per iteration: S = Q K^T and O += P V as m16n8k16 MMAs
+//    with the G query rows of the kv head as the m16 rows (the rest zero),
+//    K and V fragments read by ldmatrix (conflict-free on the swizzled
+//    layout), the softmax weights P rounded to the cache type (as the MMA
+//    takes them) and the running sum taken over those rounded weights.
 // Every K/V byte is read from HBM once per kv head. All waits are bounded.
 #pragma once
+
+#include <cuda.h>
 
 #include "pa_device.cuh"
 
@@ -71,7 +81,44 @@ namespace pa {
 #define PA_REG_BUDGET_WIDE 128
 #endif
 
+// Tensor-core consumers on or off, the smallest group they serve, and the
+// shared-memory budget of their stages (build-time tunables).
+#ifndef PA_DECODE_TC
+#define PA_DECODE_TC 1
+#endif
+#ifndef PA_TC_MIN_GROUP
+#define PA_TC_MIN_GROUP 4
+#endif
+#ifndef PA_TC_STAGE_BYTES
+#define PA_TC_STAGE_BYTES 70000
+#endif
+
 enum : int { kModeSplit = 0, kModeBalanced = 1 };
+
+// Whether a (query type, cache type, head_dim, group bucket, block size)
+// instantiation runs the tensor-core consumers; the host side asks the same
+// question with the C ABI's type codes to know when to build tensor maps.
+constexpr bool tc_eligible(int q_dtype, int kv_dtype, int D, int GT, int BS) {
+  return PA_DECODE_TC != 0 && kv_dtype == PA_KV_AUTO && (q_dtype == PA_BF16 || q_dtype == PA_F16) &&
+         GT >= PA_TC_MIN_GROUP && (D == 64 || D == 128) && BS >= 16 && BS <= 64;
+}
+template <typename T>
+struct DtypeCode {
+  static constexpr int value = -1;
+};
+template <>
+struct DtypeCode<__nv_bfloat16> {
+  static constexpr int value = PA_BF16;
+};
+template <>
+struct DtypeCode<__half> {
+  static constexpr int value = PA_F16;
+};
+template <typename QT, typename CT, int D, int GT, int BS>
+constexpr bool uses_tc() {
+  return std::is_same<QT, CT>::value && DtypeCode<QT>::value >= 0 &&
+         tc_eligible(DtypeCode<QT>::value, PA_KV_AUTO, D, GT, BS);
+}
 
 // Stage-descriptor flags.
 enum : int {
@@ -89,6 +136,11 @@ constexpr int kPieceSlots = 2;
 constexpr int kMaxBalancedCtas = 152 * 4;
 
 struct DecodeParams {
+  // tensor-core consumers: the K and V caches as 2-D tensors of
+  // [NB * Hkv * bs rows][D elements], boxes of 64 elements x bs rows with the
+  // 128-byte swizzle (one box per 64 columns of a page)
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
   // outputs
   void* out;            // [S][Hq][D] of QT
   float* tmp_out;       // split mode partials: [S][Hq][NS][D]
@@ -116,6 +168,11 @@ struct DecodeParams {
   // this one writes and has itself waited for everything before it)
   int join_at_end;
   int partials;   // split mode: 1 = write split partials, 0 = final output
+  // test hook (negative = off): the producer of every CTA stops before
+  // arming the stage of its page number `unarmed_page` (counted from the
+  // CTA's first page), as if it had given up, so that the consumers' bounded
+  // wait for that stage runs out with no copy in flight for it
+  int unarmed_page;
   float q_scale;  // scale * log2(e) (* k_scale for FP8)
   float v_scale;  // FP8: v_scale, else 1 (an INT8 cache scales each row instead)
 };
@@ -145,8 +202,10 @@ struct Layout {
   static constexpr int QB = Elem<QT>::bytes;
   static constexpr int ROWB = D * EB;      // bytes of one cached row
   static constexpr int PAGE = BS * ROWB;   // bytes of one (block, kv head) page
+  static constexpr bool TC = uses_tc<QT, CT, D, GT, BS>();
   static constexpr int TPW = 8;            // rows per consumer warp per page
-  static constexpr int NC = BS / TPW;      // consumer warps
+  static constexpr int NC = TC ? 4 : BS / TPW;  // consumer warps
+  static constexpr int SPP = BS / 16;      // tensor-core consumers: 16-row slices per page
   static constexpr int THREADS = (NC + 1) * 32;
   static constexpr int LPR = choose_lpr(D, GT);
   static constexpr int EPL = D / LPR;      // elements of a row per lane
@@ -158,7 +217,9 @@ struct Layout {
   static constexpr int RPW = 32 / LPR;     // rows a warp covers per step
   static constexpr int NST = TPW / RPW;    // steps per page
   // pages a consumer warp takes per iteration (one weight round per R pages)
-  static constexpr int R = (2 * PAGE <= 8192)    ? 2 * PA_PAGES_PER_ITER
+  // (tensor-core consumers: one 16-row slice of one page per warp)
+  static constexpr int R = TC                    ? cmax(1, NC / cmax(SPP, 1))
+                           : (2 * PAGE <= 8192)  ? 2 * PA_PAGES_PER_ITER
                            : (2 * PAGE <= 16384) ? PA_PAGES_PER_ITER
                                                  : 1;
   static constexpr int TPI = TPW * R;      // rows per warp per iteration
@@ -174,15 +235,19 @@ struct Layout {
   static constexpr int HB0 = NV >= LPR ? 0 : ilog2(RED);
   static constexpr int NHB = NV >= LPR ? ilog2(cmax(GT / NFIN, 1)) : ilog2(GT);
   static constexpr int HEAD_MASK = ((1 << NHB) - 1) << HB0;
-  static constexpr int STAGES = cmax(2 * R, cmin(PA_MAX_STAGES, PA_STAGE_BYTES / (2 * PAGE)));
   static constexpr int QSLOT = round_up(GT * D * QB, 16);        // q rows of a piece
   // an INT8 cache stages its pages' row scales too (BS floats each for K and V)
   static constexpr bool ROW_SCALES = std::is_same<CT, I8>::value;
   static constexpr int SCB = ROW_SCALES ? BS * 4 : 0;
   static constexpr int OFF_Q = 2 * PAGE + 2 * SCB;
-  // K page | V page | (K row scales | V row scales) | q rows
-  static constexpr int STAGE = round_up(OFF_Q + QSLOT, 128);
-  static constexpr int SCR = round_up(TPI * GT, 4);              // per-warp weights
+  // K page | V page | (K row scales | V row scales) | q rows; the swizzled
+  // boxes of the tensor-core layout start on 1024-byte boundaries
+  static constexpr int STAGE = round_up(OFF_Q + QSLOT, TC ? 1024 : 128);
+  static constexpr int STAGES =
+      TC ? cmax(2 * R, cmin(PA_MAX_STAGES, PA_TC_STAGE_BYTES / STAGE))
+         : cmax(2 * R, cmin(PA_MAX_STAGES, PA_STAGE_BYTES / (2 * PAGE)));
+  static constexpr int BOXB = BS * 128;   // bytes of one 64-column box of a page
+  static constexpr int SCR = TC ? 0 : round_up(TPI * GT, 4);     // per-warp weights
   static constexpr int MACC = NC * GT * D * 4;                   // merge accumulators
   static constexpr bool MERGE_IN_STAGE = MACC <= STAGE;
   // dynamic shared memory layout
@@ -193,7 +258,11 @@ struct Layout {
   static constexpr int OFF_MACC = round_up(OFF_MSTAT + 3 * NC * GT * 4, 16);
   static constexpr int OFF_MISC = OFF_MACC + (MERGE_IN_STAGE ? 0 : MACC);
   // misc: 4 ints, 2 int64 (range start, total pages), 2 cut-piece records
-  static constexpr int SMEM = OFF_MISC + 32 + 2 * 24;
+  static constexpr int SMEM_USED = OFF_MISC + 32 + 2 * 24;
+  // the tensor-core layout rounds the dynamic shared memory's base up to
+  // 1024 bytes itself (it may start anywhere 16-byte aligned)
+  static constexpr int ALIGN_PAD = TC ? 1024 : 0;
+  static constexpr int SMEM = SMEM_USED + ALIGN_PAD;
   // CTAs per SM to plan registers for: what the shared memory allows (228 KB
   // per SM, 1 KB reserved per CTA), at most 4, and no more than keeps a
   // register budget per thread (96 for one or two heads per kv head, else
@@ -208,6 +277,9 @@ struct Layout {
   static_assert(EPP % 2 == 0, "pieces hold whole fp32 pairs");
   static_assert(PAGE % 16 == 0 && SCB % 16 == 0, "bulk copies move multiples of 16 bytes");
   static_assert(STAGE % 128 == 0 && OFF_BAR % 8 == 0, "stage and mbarrier alignment");
+  static_assert(!TC || (D % 64 == 0 && BS % 16 == 0 && NC % SPP == 0 && PAGE % 1024 == 0 &&
+                        BOXB % 1024 == 0),
+                "tensor-core layout: whole 64-column boxes and 16-row slices");
   static_assert(OFF_DESC % 16 == 0 && OFF_SCR % 16 == 0 && OFF_MSTAT % 16 == 0 &&
                     OFF_MACC % 16 == 0 && OFF_MISC % 16 == 0 && (SCR * 4) % 16 == 0,
                 "16-byte vector accesses need 16-byte aligned shared-memory regions");
@@ -458,6 +530,150 @@ __device__ __forceinline__ void process_pages(PieceState<Ly, GT>& st,
   __syncwarp();
 }
 
+// ------------------------------------------------------ tensor-core consumers
+// Lane l of a consumer warp is (g = l / 4, t = l % 4) in the m16n8k16
+// fragments: it owns query head g of the group (m16 rows g >= G and 8..15
+// are zero padding), logits of tokens 2t, 2t+1, 8+2t, 9+2t of the warp's
+// 16-row slice, and output elements 8j + 2t, 8j + 2t + 1 of head g.
+template <int D>
+struct TcState {
+  uint32_t qa[D / 16][2];  // A fragments of q: head g, dims 16kk + 2t (+1) and 16kk + 8 + 2t (+1)
+  float o[D / 8][4];       // C fragments of P V: [0..1] head g, [2..3] padding rows
+  float m_run;             // running (lazy) max of head g, log2 units
+  float l_run;             // this lane's share of head g's running sum
+  float s_top;             // largest logit of head g seen
+};
+
+// Start a piece: q rows (G of them, row-major [G][D] of QT in shared memory).
+template <typename QT, int D>
+__device__ __forceinline__ void begin_piece_tc(TcState<D>& st, const uint8_t* qrows, int G,
+                                               int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t* q = reinterpret_cast<const uint32_t*>(qrows) + g * (D / 2);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    st.qa[kk][0] = g < G ? q[8 * kk + t] : 0u;
+    st.qa[kk][1] = g < G ? q[8 * kk + 4 + t] : 0u;
+  }
+#pragma unroll
+  for (int j = 0; j < D / 8; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) st.o[j][e] = 0.f;
+  st.m_run = -INFINITY;
+  st.l_run = 0.f;
+  st.s_top = -INFINITY;
+}
+
+// Shared-memory address of 16-byte chunk `ch` (8 elements) of row `row` of a
+// page staged as D/64 boxes of BS rows x 128 bytes with the 128-byte swizzle
+// (the chunk index is XORed with the row index mod 8).
+template <typename Ly>
+__device__ __forceinline__ uint32_t tc_chunk(uint32_t page, int row, int ch) {
+  return page + (ch >> 3) * Ly::BOXB + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+}
+
+// One consumer iteration: the warp takes rows [r0, r0 + 16) of page
+// pr = warp / SPP of the R staged pages (r0 = 16 (warp mod SPP)); rows[r] is
+// the number of attended rows of page r (0 for pages not in this iteration).
+template <typename QT, typename Ly, int D>
+__device__ __forceinline__ void process_tc(TcState<D>& st, const uint8_t* const (&Kp)[Ly::R],
+                                           const uint8_t* const (&Vp)[Ly::R],
+                                           const int (&rows)[Ly::R], int warp, int lane,
+                                           float q_scale, int G) {
+  constexpr int R = Ly::R, SPP = Ly::SPP;
+  constexpr float kLazy = 8.f;  // weights stay <= 2^kLazy
+  using M = Mma<QT>;
+  const int pr = warp / SPP, r0 = 16 * (warp % SPP);
+  const uint8_t* kp = Kp[0];
+  const uint8_t* vp = Vp[0];
+  int n = rows[0];
+#pragma unroll
+  for (int r = 1; r < R; ++r)
+    if (pr == r) {
+      kp = Kp[r];
+      vp = Vp[r];
+      n = rows[r];
+    }
+  const int lim = n - r0;  // attended rows of the slice (warp-uniform)
+  if (lim <= 0) return;
+  const int g = lane >> 2, t = lane & 3, mi = lane >> 3;
+  const bool real = g < G;
+
+  // ---- S = Q K^T over the slice's 16 tokens (two n8 tiles)
+  float sacc[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+  {
+    // matrix mi of an x4 load: tokens r0 + 8 (mi / 2) .. + 7, chunk 2 kk + mi % 2
+    const uint32_t kb = smem_u32(kp);
+    const int krow = r0 + ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(tc_chunk<Ly>(kb, krow, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+      const uint32_t a[4] = {st.qa[kk][0], 0u, st.qa[kk][1], 0u};
+      M::run(sacc[0], a, b0, b1);
+      M::run(sacc[1], a, b2, b3);
+    }
+  }
+
+  // ---- logits of head g (log2 units), masked past the context; lazy max
+  float x[4] = {sacc[0][0] * q_scale, sacc[0][1] * q_scale, sacc[1][0] * q_scale,
+                sacc[1][1] * q_scale};
+  const int tok[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) x[j] = (real && tok[j] < lim) ? x[j] : -INFINITY;
+  float tm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
+  tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
+  st.s_top = fmaxf(st.s_top, tm);
+  if (__any_sync(0xffffffffu, tm > st.m_run + kLazy)) {
+    const float mn = fmaxf(st.m_run, tm);
+    const float al = mn == -INFINITY ? 1.f : exp2f(st.m_run - mn);
+    st.m_run = mn;
+    st.l_run *= al;
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) {
+      st.o[j][0] *= al;
+      st.o[j][1] *= al;
+    }
+  }
+
+  // ---- weights 2^(s - m), rounded to the cache type as the MMA takes them
+  uint32_t pa0 = M::pack(exp2f(x[0] - st.m_run), exp2f(x[1] - st.m_run));
+  uint32_t pa2 = M::pack(exp2f(x[2] - st.m_run), exp2f(x[3] - st.m_run));
+  if (!real) pa0 = pa2 = 0u;  // padding rows: m_run stays -inf, weights would be NaN
+  st.l_run += M::sum2(pa0) + M::sum2(pa2);
+  const uint32_t a[4] = {pa0, 0u, pa2, 0u};
+
+  // ---- O += P V (16 n8 tiles of head_dim for D 128); rows past the
+  // context are zeroed in the fragments (they may hold anything, NaN too)
+  const uint32_t vb = smem_u32(vp);
+  // matrix mi of an x4.trans load: tokens r0 + 8 (mi % 2) .. + 7, chunk 2 jj + mi / 2
+  const int vrow = r0 + ((mi & 1) << 3) + (lane & 7);
+  if (lim >= 16) {
+#pragma unroll
+    for (int jj = 0; jj < D / 16; ++jj) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(tc_chunk<Ly>(vb, vrow, 2 * jj + (mi >> 1)), b0, b1, b2, b3);
+      M::run(st.o[2 * jj], a, b0, b1);
+      M::run(st.o[2 * jj + 1], a, b2, b3);
+    }
+  } else {
+    const uint32_t mk0 = (tok[0] < lim ? 0x0000FFFFu : 0u) | (tok[1] < lim ? 0xFFFF0000u : 0u);
+    const uint32_t mk1 = (tok[2] < lim ? 0x0000FFFFu : 0u) | (tok[3] < lim ? 0xFFFF0000u : 0u);
+#pragma unroll
+    for (int jj = 0; jj < D / 16; ++jj) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(tc_chunk<Ly>(vb, vrow, 2 * jj + (mi >> 1)), b0, b1, b2, b3);
+      M::run(st.o[2 * jj], a, b0 & mk0, b1 & mk1);
+      M::run(st.o[2 * jj + 1], a, b2 & mk0, b3 & mk1);
+    }
+  }
+}
+
 // Bounded barrier among the NC consumer warps (an mbarrier with one arrival
 // per warp), so a consumer that gave up on a wait can never hang the others.
 __device__ __forceinline__ void consumer_sync(uint64_t* bar, uint32_t& phase, int lane,
@@ -467,6 +683,11 @@ __device__ __forceinline__ void consumer_sync(uint64_t* bar, uint32_t& phase, in
   if (!mbar_wait_bounded(bar, phase & 1)) raise_error(err, PA_DEVERR_TIMEOUT);
   ++phase;
 }
+
+template <typename Ly, int GT, int D, typename Sink>
+__device__ __forceinline__ void merge_warps(const float* mstat, const float* macc, uint64_t* cbar,
+                                            uint32_t& cphase, int G, int warp, int lane,
+                                            float v_scale, unsigned* err, Sink&& sink);
 
 // End of a piece: reduce each warp's state, merge the NC warps through shared
 // memory, and hand every (head, element) result to `sink`:
@@ -479,7 +700,6 @@ __device__ __forceinline__ void finish_piece(PieceState<Ly, GT>& st, float* msta
                                              int lane, int c, int rg, float v_scale, unsigned* err,
                                              Sink&& sink) {
   constexpr int NC = Ly::NC, LPR = Ly::LPR, NFIN = Ly::NFIN, EL2 = Ly::EL2, EP2 = Ly::EP2;
-  constexpr float kLn2 = 0.69314718055994530942f;
   float mh[GT], lh[GT], th[GT];
   {
     float lsum[NFIN], tmax[NFIN];
@@ -534,6 +754,22 @@ __device__ __forceinline__ void finish_piece(PieceState<Ly, GT>& st, float* msta
               st.acc[h][kk * EP2 + j2];
   }
   consumer_sync(cbar, cphase, lane, err);
+  merge_warps<Ly, GT, D>(mstat, macc, cbar, cphase, G, warp, lane, v_scale, err, sink);
+}
+
+// The second half of a piece's end, shared by both consumer kinds: every warp
+// has stored its running max, sum and largest logit per head (mstat) and its
+// un-normalised output rows (macc); merge the NC warps and hand every (head,
+// element) result to `sink`, then release the stage memory used as scratch.
+template <typename Ly, int GT, int D, typename Sink>
+__device__ __forceinline__ void merge_warps(const float* mstat, const float* macc, uint64_t* cbar,
+                                            uint32_t& cphase, int G, int warp, int lane,
+                                            float v_scale, unsigned* err, Sink&& sink) {
+  constexpr int NC = Ly::NC;
+  constexpr float kLn2 = 0.69314718055994530942f;
+  const float* mm = mstat;
+  const float* ml = mstat + NC * GT;
+  const float* mt = mstat + 2 * NC * GT;
   for (int i = warp * 32 + lane; i < G * D; i += NC * 32) {
     const int h = i / D, d = i % D;
     float M = -INFINITY, T = -INFINITY;
@@ -562,6 +798,35 @@ __device__ __forceinline__ void finish_piece(PieceState<Ly, GT>& st, float* msta
   // bulk copies that will refill it
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   consumer_sync(cbar, cphase, lane, err);
+}
+
+// End of a piece on the tensor-core path: each warp stores its state per
+// head (the running sum reduced over the 4 lanes of a head), then the warps
+// are merged as on the CUDA-core path.
+template <typename Ly, int GT, int D, typename Sink>
+__device__ __forceinline__ void finish_piece_tc(TcState<D>& st, float* mstat, float* macc,
+                                                uint64_t* cbar, uint32_t& cphase, int G,
+                                                int warp, int lane, float v_scale, unsigned* err,
+                                                Sink&& sink) {
+  constexpr int NC = Ly::NC;
+  const int g = lane >> 2, t = lane & 3;
+  float l = st.l_run;
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  consumer_sync(cbar, cphase, lane, err);  // every warp is done with the stage
+  if (g < GT) {
+    if (t == 0) {
+      mstat[warp * GT + g] = st.m_run;
+      mstat[NC * GT + warp * GT + g] = l;
+      mstat[2 * NC * GT + warp * GT + g] = st.s_top;
+    }
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j)
+      *reinterpret_cast<float2*>(&macc[(warp * GT + g) * D + 8 * j + 2 * t]) =
+          make_float2(st.o[j][0], st.o[j][1]);
+  }
+  consumer_sync(cbar, cphase, lane, err);
+  merge_warps<Ly, GT, D>(mstat, macc, cbar, cphase, G, warp, lane, v_scale, err, sink);
 }
 
 // Attended slots of sequence s (window- and table-limited); flags bad lengths.
@@ -715,7 +980,11 @@ template <typename QT, typename CT, int D, int GT, int BS, int MODE>
 __device__ __forceinline__ void decode_body(const DecodeParams& p) {
   using Ly = Layout<QT, CT, D, GT, BS>;
   constexpr int NC = Ly::NC, STAGES = Ly::STAGES, R = Ly::R, TPW = Ly::TPW;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // the tensor-core layout's swizzled boxes need 1024-byte aligned stages
+  uint8_t* smem = smem_raw;
+  if constexpr (Ly::TC)
+    smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = p.num_heads, Hkv = p.num_kv_heads, G = p.group;
@@ -887,6 +1156,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
           raise_error(p.err, PA_DEVERR_TIMEOUT);
           aborted = true;
         }
+        if (k == p.unarmed_page) aborted = true;  // test hook: issue nothing more
         if (!aborted) {
           const bool ok = bid >= 0 && bid < p.num_blocks;
           if (!ok) raise_error(p.err, PA_DEVERR_BLOCK_ID);
@@ -899,7 +1169,15 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
               (ok ? 2u * (Ly::PAGE + Ly::SCB) : 0u) + (piece_start ? qbytes : 0u);
           if (bytes) {
             mbar_arrive_expect_tx(&full[slot], bytes);
-            if (ok) {
+            if (ok && Ly::TC) {
+              // one tensor copy per 64-column box of the K page and of the V page
+              const int y = (bid * Hkv + g) * BS;
+#pragma unroll
+              for (int j = 0; j < D / 64; ++j) {
+                tma_load_2d(stage + j * Ly::BOXB, &p.tm_k, 64 * j, y, &full[slot]);
+                tma_load_2d(stage + Ly::PAGE + j * Ly::BOXB, &p.tm_v, 64 * j, y, &full[slot]);
+              }
+            } else if (ok) {
               const size_t off = (size_t)bid * blk_stride + (size_t)g * Ly::PAGE;
               bulk_g2s(stage, p.k_cache + off, Ly::PAGE, &full[slot]);
               bulk_g2s(stage + Ly::PAGE, p.v_cache + off, Ly::PAGE, &full[slot]);
@@ -978,7 +1256,16 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
   float* wscr = reinterpret_cast<float*>(smem + Ly::OFF_SCR) + warp * Ly::SCR;
   float* mstat = reinterpret_cast<float*>(smem + Ly::OFF_MSTAT);
   uint32_t cphase = 0;
-  PieceState<Ly, GT> st;
+  typename std::conditional<Ly::TC, TcState<D>, PieceState<Ly, GT>>::type st;
+  // end of a piece: the consumer kind's own reduction, then the shared merge
+  auto finish = [&](float* macc, auto&& sink) {
+    if constexpr (Ly::TC)
+      finish_piece_tc<Ly, GT, D>(st, mstat, macc, cbar, cphase, G, warp, lane, p.v_scale, p.err,
+                                 sink);
+    else
+      finish_piece<Ly, GT, D>(st, mstat, macc, cbar, cphase, G, warp, lane, c, rg, p.v_scale,
+                              p.err, sink);
+  };
 
   int k = 0;
   bool aborted = false, tail_cut = false;
@@ -988,11 +1275,12 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
     const uint8_t* Vp[R];
     const float* Ks[R];
     const float* Vs[R];
-    int lim[R];
+    int lim[R], rows[R];
     int n_here = 0, last_flags = 0, seg = 0, last_slot = 0;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       lim[r] = 0;
+      rows[r] = 0;
       Kp[r] = smem;
       Vp[r] = smem;
       Ks[r] = reinterpret_cast<const float*>(smem);
@@ -1008,20 +1296,29 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
       uint8_t* stage = smem + slot * Ly::STAGE;
       if (r == 0) {
         seg = d.y;
-        if (d.z & kFirst) begin_piece<QT, Ly, GT, D>(st, stage + Ly::OFF_Q, G, c, p.q_scale);
+        if (d.z & kFirst) {
+          if constexpr (Ly::TC)
+            begin_piece_tc<QT, D>(st, stage + Ly::OFF_Q, G, lane);
+          else
+            begin_piece<QT, Ly, GT, D>(st, stage + Ly::OFF_Q, G, c, p.q_scale);
+        }
       }
       Kp[r] = stage;
       Vp[r] = stage + Ly::PAGE;
       Ks[r] = reinterpret_cast<const float*>(stage + 2 * Ly::PAGE);
       Vs[r] = reinterpret_cast<const float*>(stage + 2 * Ly::PAGE + Ly::SCB);
       lim[r] = d.x - warp * TPW;
+      rows[r] = d.x;
       last_flags = d.z;
       last_slot = slot;
       n_here = r + 1;
     }
     if (__any_sync(0xffffffffu, aborted)) break;
 
-    process_pages<CT, Ly, GT>(st, Kp, Vp, Ks, Vs, lim, wscr, warp, lane, c, rg);
+    if constexpr (Ly::TC)
+      process_tc<QT, Ly, D>(st, Kp, Vp, rows, warp, lane, p.q_scale, G);
+    else
+      process_pages<CT, Ly, GT>(st, Kp, Vp, Ks, Vs, lim, wscr, warp, lane, c, rg);
 
     const bool ends_piece = (last_flags & kLast) != 0;
     if (lane == 0) {
@@ -1040,9 +1337,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
         float* max_logits = p.max_logits;
         float* exp_sums = p.exp_sums;
         const size_t row0 = (size_t)s * Hq + (size_t)g * G;
-        finish_piece<Ly, GT, D>(
-            st, mstat, macc, cbar, cphase, G, warp, lane, c, rg, p.v_scale, p.err,
-            [=](int h, int d, float o, float m_nat, float l) {
+        finish(macc, [=](int h, int d, float o, float m_nat, float l) {
               const size_t row = row0 + h;
               if (partials) {
                 const size_t pi = row * nsplit + split;
@@ -1063,9 +1358,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
         QT* out = reinterpret_cast<QT*>(p.out) + ((size_t)s * Hq + (size_t)g * G) * D;
         float* piece_o = p.piece_o + base * GT * D;
         float* piece_ml = p.piece_ml + base * GT * 2;
-        finish_piece<Ly, GT, D>(
-            st, mstat, macc, cbar, cphase, G, warp, lane, c, rg, p.v_scale, p.err,
-            [=](int h, int d, float o, float m_nat, float l) {
+        finish(macc, [=](int h, int d, float o, float m_nat, float l) {
               if (whole) {
                 out[h * D + d] = Elem<QT>::from_f32(o);
               } else {

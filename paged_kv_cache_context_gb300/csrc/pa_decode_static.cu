@@ -11,36 +11,31 @@
 // kernels pa_decode runs.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "../../include/pa.h"
 
 #define PA_API extern "C" __attribute__((visibility("default")))
 
 namespace {
 
-// Split partials of pa_decode_static_scratch. It lives in every GPU's memory as
-// soon as the library is loaded there, and stays until the process exits.
+// Split partials of pa_decode_static_scratch. The CUDA runtime reserves it on
+// a GPU when the library's device code is loaded there: with lazy module
+// loading (the default) that happens at the first use of this code on that
+// device -- the first launch of one of its kernels, or the first address
+// lookup below -- not when the library is loaded into the process. It then
+// stays reserved until the process exits.
 static __device__ __align__(256) unsigned char g_static_scratch[PA_STATIC_SCRATCH_BYTES];
 
-std::mutex g_scratch_mu;
-void* g_scratch_dev_ptr[64];  // device address of the array, per device id
-
 // In host code the array's name is only a host-side stand-in; the kernels must
-// be given its device address, looked up once per device (that device current).
+// be given its device address, looked up on the device that is current (the
+// one the stream belongs to). The lookup is repeated on every call, so the
+// address stays right after the device's primary context has been reset and
+// recreated; after the first call on a device it is a table lookup inside the
+// runtime.
 cudaError_t scratch_on_current_device(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_dev_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_dev_ptr[dev] = p;
-  }
-  *out = g_scratch_dev_ptr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

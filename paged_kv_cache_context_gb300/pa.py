@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_cascade_workspace_size.restype = Z
         L.pa_block_budget.restype = ctypes.c_int64
         L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_test_set_unarmed_page.argtypes = [I]
+        L.pa_test_set_unarmed_page.restype = None
         _lib = L
     return _lib
 
@@ -467,6 +469,12 @@ def reduce(out: torch.Tensor, tmp_out: torch.Tensor, max_logits: torch.Tensor,
         _dtype(name, t, torch.float32)
     _check(lib().pa_reduce(_ptr(out), _ptr(tmp_out), _ptr(max_logits), _ptr(exp_sums), S, Hq,
                            D, NS, _DTYPE[out.dtype], _stream(stream)), "pa_reduce")
+
+
+def test_set_unarmed_page(page: int) -> None:
+    """pa_test_set_unarmed_page: test hook; the producer of every CTA of later
+    decodes stops before arming its page number ``page`` (negative: off)."""
+    lib().pa_test_set_unarmed_page(int(page))
 
 
 def get_device_error(stream=None) -> int:

@@ -37,6 +37,32 @@ def oracle_caches(case: wl.DecodeCase, with_new: bool = True):
     return kc, vc
 
 
+def sampled_seqs(case: wl.DecodeCase, count: int = 4, seed: int = 7):
+    """The longest and the shortest context and seeded random others, sorted:
+    the sequences a full-size test checks against the oracle row by row."""
+    lens = case.context_lens.tolist()
+    pick = {int(np.argmax(lens)), int(np.argmin(lens))}
+    g = torch.Generator().manual_seed(seed)
+    while len(pick) < min(count, case.num_seqs):
+        pick.add(int(torch.randint(0, case.num_seqs, (1,), generator=g)))
+    return sorted(pick)
+
+
+def oracle_caches_for(case: wl.DecodeCase, seqs):
+    """CPU caches holding only the rows of the listed sequences (each written by
+    its own oracle calls: slot mapping, then reshape_and_cache; a shared prefix
+    comes with every sequence that uses it)."""
+    kc, vc = wl.empty_caches(case)
+    for s in seqs:
+        pos, key, val = case.tokens_of(s)
+        sm, bad = oracle.slot_mapping(case.block_tables, torch.full_like(pos, s), pos,
+                                      case.block_size, case.window)
+        assert bad == 0
+        assert oracle.reshape_and_cache(key, val, kc, vc, sm, case.block_size, case.kv_dtype,
+                                        case.k_scale, case.v_scale) == 0
+    return kc, vc
+
+
 def oracle_int8_caches(case: wl.DecodeCase):
     """INT8 caches and their per-row scales (kc, vc, ks, vs), written by the
     oracle's slot mapping and INT8 write in the same order as oracle_caches."""

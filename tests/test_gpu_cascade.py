@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from _gpu import DEV, assert_close, bits, device_errors, gpu_caches, gpu_decode, to_dev
-from _helpers import oracle_caches, oracle_decode
+from _helpers import oracle_caches, oracle_caches_for, oracle_decode, sampled_seqs
 from paged_kv_cache_context_gb300 import build, pa
 from paged_kv_cache_context_gb300 import workloads as wl
 
@@ -72,13 +72,23 @@ def test_cascade_with_part_of_the_prefix_and_many_query_tiles():
     assert device_errors() == 0
 
 
-def test_cascade_full_size_prefix_workload_agrees_with_decode():
+def test_cascade_full_size_prefix_workload():
     """prefix_bf16 at its full size (128 sequences, a 2048-token shared
-    prefix): the cascade agrees with pa_decode within the bf16 tolerance on
-    every row, and with the oracle on sampled rows."""
+    prefix: several prefix ranges and one suffix CTA per sequence and kv head,
+    as the benchmark's cascade path runs it): every query head of the
+    longest, the shortest and two random sequences against the oracle, and
+    every row of the batch within the bf16 tolerance of pa_decode."""
     case = wl.config("prefix_bf16", value_device=DEV)
     kg, vg = gpu_caches(case)
     out = cascade(case, kg, vg, 64)
+    torch.cuda.synchronize()
+    assert device_errors() == 0
+    assert torch.isfinite(out.float()).all()
+    seqs = sampled_seqs(case)
+    ko, vo = oracle_caches_for(case, seqs)
+    rows = [s * case.num_heads + h for s in seqs for h in range(case.num_heads)]
+    ref = oracle_decode(case, ko, vo, rows=rows)
+    assert_close(case, out, ref, rows=rows, what="cascade prefix_bf16, sampled rows")
     dec = gpu_decode(case, kg, vg)
     diff = (out.float() - dec.float()).abs().max().item()
     assert diff <= 2e-2, diff

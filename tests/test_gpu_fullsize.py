@@ -5,12 +5,12 @@ sequences bit for bit, and properties of the whole output (finite, no device
 error). Values are drawn on the GPU with a seeded CUDA generator; the oracle
 gets host copies of exactly those rows.
 """
-import numpy as np
 import pytest
 import torch
 
 import oracle
 from _gpu import DEV, assert_close, bits, device_errors, gpu_caches, gpu_decode
+from _helpers import oracle_caches_for, sampled_seqs
 from paged_kv_cache_context_gb300 import build, pa
 from paged_kv_cache_context_gb300 import workloads as wl
 
@@ -24,20 +24,6 @@ def _lib():
     device_errors()
 
 
-def oracle_caches_for(case, seqs):
-    """CPU caches holding only the rows of the listed sequences (each written by
-    its own oracle calls: slot mapping, then reshape_and_cache)."""
-    kc, vc = wl.empty_caches(case)
-    for s in seqs:
-        pos, key, val = case.tokens_of(s)
-        sm, bad = oracle.slot_mapping(case.block_tables, torch.full_like(pos, s), pos,
-                                      case.block_size, case.window)
-        assert bad == 0
-        assert oracle.reshape_and_cache(key, val, kc, vc, sm, case.block_size, case.kv_dtype,
-                                        case.k_scale, case.v_scale) == 0
-    return kc, vc
-
-
 @pytest.mark.parametrize("name", wl.CONFIG_NAMES)
 def test_full_size_workload_sampled(name):
     case = wl.config(name, value_device=DEV)
@@ -47,12 +33,7 @@ def test_full_size_workload_sampled(name):
     assert device_errors() == 0
     assert torch.isfinite(out.float()).all()
 
-    lens = case.context_lens.tolist()
-    g = torch.Generator().manual_seed(7)
-    pick = {int(np.argmax(lens)), int(np.argmin(lens))}
-    while len(pick) < min(4, case.num_seqs):
-        pick.add(int(torch.randint(0, case.num_seqs, (1,), generator=g)))
-    seqs = sorted(pick)
+    seqs = sampled_seqs(case)
     ko, vo = oracle_caches_for(case, seqs)
     # the sampled sequences' blocks are bit-identical
     blocks = torch.unique(case.block_tables[seqs].flatten())

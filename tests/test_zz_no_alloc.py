@@ -5,8 +5,9 @@ that owns all device memory, or code that must never call cudaMalloc) use this
 entry point; it keeps the split partials in the library's own fixed device
 array. These tests call it through the C ABI and check that two calls in a
 row (different shapes, so the second starts from what the first left in the
-shared array) give what pa_decode gives, within the decode tolerance, and that
-a plan too large for the array is refused without launching anything.
+shared array) match the oracle's decode, and what pa_decode gives, within the
+decode tolerance, and that a plan too large for the array is refused without
+launching anything.
 
 This file is collected last on purpose, so that a run stopping at its first
 failure has already run every other test.
@@ -41,8 +42,9 @@ def call_static(f, out, q, kc, vc, bt, cl, case, stream):
 
 
 @pytest.mark.gpu
-def test_static_scratch_matches_pa_decode_on_two_calls_in_a_row():
+def test_static_scratch_matches_oracle_and_pa_decode_on_two_calls_in_a_row():
     from _gpu import DEV, assert_close, device_errors, gpu_caches, gpu_decode, to_dev
+    from _helpers import oracle_caches, oracle_decode
     f = _fn()
     stream = torch.cuda.current_stream().cuda_stream
     device_errors()
@@ -54,14 +56,18 @@ def test_static_scratch_matches_pa_decode_on_two_calls_in_a_row():
                                         case.max_blocks_per_seq, case.window)
         assert 0 < need <= STATIC_SCRATCH_BYTES  # the split path really runs
         kc, vc = gpu_caches(case)
-        ref = gpu_decode(case, kc, vc, split=True).float().cpu().double().numpy()
-        prepared.append((case, kc, vc, ref))
-    for case, kc, vc, ref in prepared:  # two calls in a row through the C ABI
+        ko, vo = oracle_caches(case)
+        ref = oracle_decode(case, ko, vo)
+        dec = gpu_decode(case, kc, vc, split=True).float().cpu()
+        prepared.append((case, kc, vc, ref, dec))
+    for case, kc, vc, ref, dec in prepared:  # two calls in a row through the C ABI
         out = torch.full(case.query.shape, float("nan"), dtype=case.q_dtype, device=DEV)
         rc = call_static(f, out, to_dev(case.query), kc, vc, to_dev(case.block_tables),
                          to_dev(case.context_lens), case, stream)
         assert rc == 0, pa.status_string(rc)
-        assert_close(case, out, ref, what=f"static scratch, {case.name}")
+        assert_close(case, out, ref, what=f"static scratch vs oracle, {case.name}")
+        assert_close(case, out, dec.double().numpy(), what=f"static scratch vs pa_decode, "
+                                                          f"{case.name}")
     assert device_errors() == 0
 
 
