@@ -45,8 +45,8 @@
 //     last stage (reused as scratch before it is released) and store.
 //  * tensor-core consumers (16-bit cache read with queries of the same type,
 //    G >= 4, head_dim 64 or 128): the pages are staged by 2-D tensor copies
-//    with the 128-byte swizzle, and each of the 4 consumer warps takes 16
-//    rows of a page per iteration: S = Q K^T and O += P V as m16n8k16 MMAs
+//    with the 128-byte swizzle, and each consumer warp takes 16 rows of a
+//    page per iteration: S = Q K^T and O += P V as m16n8k16 MMAs
 //    with the G query rows of the kv head as the m16 rows (the rest zero),
 //    K and V fragments read by ldmatrix (conflict-free on the swizzled
 //    layout), the softmax weights P rounded to the cache type (as the MMA
@@ -91,6 +91,9 @@ namespace pa {
 #endif
 #ifndef PA_TC_STAGE_BYTES
 #define PA_TC_STAGE_BYTES 70000
+#endif
+#ifndef PA_TC_WARPS
+#define PA_TC_WARPS 4
 #endif
 
 enum : int { kModeSplit = 0, kModeBalanced = 1 };
@@ -204,7 +207,7 @@ struct Layout {
   static constexpr int PAGE = BS * ROWB;   // bytes of one (block, kv head) page
   static constexpr bool TC = uses_tc<QT, CT, D, GT, BS>();
   static constexpr int TPW = 8;            // rows per consumer warp per page
-  static constexpr int NC = TC ? 4 : BS / TPW;  // consumer warps
+  static constexpr int NC = TC ? PA_TC_WARPS : BS / TPW;  // consumer warps
   static constexpr int SPP = BS / 16;      // tensor-core consumers: 16-row slices per page
   static constexpr int THREADS = (NC + 1) * 32;
   static constexpr int LPR = choose_lpr(D, GT);
