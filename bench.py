@@ -178,10 +178,13 @@ def step_bytes(case) -> dict:
     kv = case.kv_bytes()  # with an INT8 cache, the rows' scales too
     pages = sum(-(-case.attended(s) // bs) for s in range(S))
     new_rows = int((case.new_pos >= 0).sum())
-    kernel = kv + S * Hq * D * qb + pages * 4 + S * 4  # what the split kernel must read
+    # what the decode launch must move: K/V of the attended rows once per kv
+    # head, the queries read and the outputs written, one table entry per
+    # page of a sequence, the context lengths
+    kernel = kv + S * Hq * D * 2 * qb + pages * 4 + S * 4
     row_scale = 4 if case.kv_dtype == "int8" else 0
     write = new_rows * Hkv * (D * (sb + cb) + row_scale) * 2 + S * 8
-    total = kernel + S * Hq * D * qb + write
+    total = kernel + write
     return {"kv": kv, "kernel": kernel, "write": write, "total": total}
 
 
@@ -420,6 +423,11 @@ def run_ours(args, rank, local_rank, world):
     peak, peak_kind = peaks()
     achieved = sb["kernel"] / split_mean / 1e9
 
+    # ---- the cache write at prefill scale: every context token of the batch
+    write_prefill = None
+    if args.path != "int8" and case.pre_key.shape[0] > 0:
+        write_prefill = prefill_scale_write(case, pa, dev, stream, bt, reps)
+
     # ---- e2e: the public pa_decode call with host buffers
     e2e = run_e2e(args, case, pa, L, dev, stream, reps, new_sm, bt, cl, q, new_k, new_v, out,
                   sb, world)
@@ -456,6 +464,7 @@ def run_ours(args, rank, local_rank, world):
                      "kernel_us_mean": round(split_mean * 1e6, 2),
                      "kernel_us_median": round(statistics.median(split_ms) * 1e3, 2)},
         "e2e": e2e,
+        "write_prefill_scale": write_prefill,
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
         "wall_s_timed": round(t1 - t0, 4),
@@ -463,6 +472,40 @@ def run_ours(args, rank, local_rank, world):
     if rank == 0:
         result["cpu_baseline"] = cpu_baseline(case, args)
         print(json.dumps(result), flush=True)
+
+
+def prefill_scale_write(case, pa, dev, stream, bt, reps):
+    """pa_reshape_and_cache of every context token of the batch in one call
+    (T = sum of the context lengths minus the step's new tokens), timed with
+    CUDA events on the launching stream, alternating cache replicas."""
+    S, Hkv, D = case.num_seqs, case.num_kv_heads, case.head_dim
+    T = int(case.pre_key.shape[0])
+    key = case.pre_key.to(dev).contiguous()
+    val = case.pre_value.to(dev).contiguous()
+    sm = torch.empty(T, dtype=torch.int64, device=dev)
+    pa.slot_mapping(sm, bt, case.pre_seq.to(dev), case.pre_pos.to(dev), case.block_size,
+                    case.window)
+    sb = key.element_size()
+    cb = 1 if case.kv_dtype == "fp8_e4m3" else sb
+    nbytes = T * Hkv * D * (sb + cb) * 2 + T * 8
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(8)]
+    for i in range(3 + len(ev)):
+        k_, v_ = reps[i % len(reps)][:2]
+        if i >= 3:
+            ev[i - 3][0].record(stream)
+        pa.reshape_and_cache(key, val, k_, v_, sm, case.kv_dtype, case.k_scale, case.v_scale,
+                             stream=stream)
+        if i >= 3:
+            ev[i - 3][1].record(stream)
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+    peak, kind = peaks()
+    return {"tokens": T, "bytes": nbytes, "us": round(us, 2),
+            "value": round(nbytes / us / 1e3, 1), "unit": "GB/s",
+            "frac": round(nbytes / us / 1e3 / peak, 4), "peak_kind": kind,
+            "what": "pa_reshape_and_cache of every context token (read rows, write pages, "
+                    "slots), one call, CUDA events, median of 8"}
 
 
 def run_e2e(args, case, pa, L, dev, stream, reps, new_sm, bt, cl, q, new_k, new_v, out, sb,
@@ -522,7 +565,9 @@ def run_e2e(args, case, pa, L, dev, stream, reps, new_sm, bt, cl, q, new_k, new_
 
 
 def cpu_baseline(case, args):
-    """The oracle on the host cores, bounded to ~10-20 s."""
+    """The oracle on the host cores, bounded to ~10-20 s: the whole batch on
+    every core, then a sample of rows on one thread."""
+    import oracle  # test infrastructure: only this CPU-baseline leg uses it
     rows_total = case.num_seqs * case.num_heads
     times, sbytes, nrows = oracle_step_time(case, rows_total, 1)
     per = times[0]
@@ -530,10 +575,23 @@ def cpu_baseline(case, args):
     if reps > 1:
         times, sbytes, nrows = oracle_step_time(case, rows_total, reps)
     t = statistics.median(times)
+    # one thread, on the rows of the first sequences (about 5 s of work)
+    per_row = t * cores() / max(nrows, 1)
+    rows1 = max(1, min(rows_total, int(5.0 / max(per_row, 1e-6))))
+    prev = oracle.set_threads(1)
+    try:
+        t1, b1, n1 = oracle_step_time(case, rows1, 1)
+    finally:
+        oracle.set_threads(prev)
+    one = {"value": round(b1 / t1[0] / 1e9, 4), "unit": "GB/s", "cores": 1,
+           "seconds_per_step": round(t1[0] / n1 * rows_total, 4),
+           "sample": f"{n1} of {rows_total} sequence-head rows; seconds_per_step "
+                     "scales the sample's time per row to the whole batch"}
     return {"value": round(sbytes / t / 1e9, 4), "unit": "GB/s", "cores": cores(),
             "kind": "oracle", "seconds_per_step": round(t, 4),
             "sample": f"whole batch ({nrows} sequence-head rows) x {len(times)} reps: oracle "
-                      "write of the new rows + fp64 decode, OpenMP over rows"}
+                      "write of the new rows + fp64 decode, OpenMP over rows",
+            "single_thread": one}
 
 
 # ------------------------------------------------------------------ reference arm

@@ -41,6 +41,8 @@ def lib():
     if _lib is None:
         path = _build.build()
         L = ctypes.CDLL(path)
+        L.oracle_set_threads.restype = _int
+        L.oracle_set_threads.argtypes = [_int]
         L.oracle_e4m3_encode.restype = ctypes.c_uint8
         L.oracle_e4m3_encode.argtypes = [_flt]
         L.oracle_e4m3_decode.restype = _flt
@@ -183,6 +185,12 @@ def _row_scales(kv_dtype, k_scales, v_scales):
     ks, vs = _cpu(k_scales), _cpu(v_scales)
     assert ks.dtype == torch.float32 and vs.dtype == torch.float32
     return ks, vs
+
+
+def set_threads(n: int) -> int:
+    """Host threads of the oracle's parallel loops (n > 0 sets it); returns the
+    previous setting. Timing only: results do not depend on it."""
+    return int(lib().oracle_set_threads(int(n)))
 
 
 def decode(query, k_cache, v_cache, block_tables, context_lens, num_kv_heads: int,

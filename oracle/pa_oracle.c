@@ -39,6 +39,25 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Host threads of the parallel loops below (n > 0 sets it); returns the
+ * previous setting, 1 when built without OpenMP. Timing only: the results do
+ * not depend on it (every row is computed by one thread in a fixed order). */
+int oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    int prev = omp_get_max_threads();
+    if (n > 0)
+        omp_set_num_threads(n);
+    return prev;
+#else
+    (void)n;
+    return 1;
+#endif
+}
 
 /* Element codes of this oracle's own interface. */
 #define OR_F32 0

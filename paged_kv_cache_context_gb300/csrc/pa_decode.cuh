@@ -90,7 +90,7 @@ namespace pa {
 #define PA_TC_MIN_GROUP 4
 #endif
 #ifndef PA_TC_STAGE_BYTES
-#define PA_TC_STAGE_BYTES 70000
+#define PA_TC_STAGE_BYTES 105000
 #endif
 #ifndef PA_TC_WARPS
 #define PA_TC_WARPS 4

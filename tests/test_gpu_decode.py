@@ -63,6 +63,10 @@ SHAPES = [  # (D, Hq, Hkv, bs, q dtype, kv)
     (64, 14, 2, 16, torch.float32, "fp8_e4m3"),  # G = 7
     (96, 6, 6, 64, torch.float16, "fp8_e4m3"),
     (128, 40, 5, 32, torch.float16, "auto"),    # G = 8
+    # tensor-core consumers with other stage counts and slice layouts
+    (64, 16, 4, 32, torch.bfloat16, "auto"),    # G = 4, D 64: 7 stages
+    (64, 32, 4, 16, torch.float16, "auto"),     # G = 8, bs 16: 4 pages per iteration
+    (128, 32, 8, 64, torch.bfloat16, "auto"),   # G = 4, bs 64: one page per iteration
 ]
 
 
