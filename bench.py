@@ -594,6 +594,161 @@ def cpu_baseline(case, args):
             "single_thread": one}
 
 
+# ------------------------------------------------------------------ paged prefill
+def run_prefill(args, rank, local_rank, world):
+    """--path prefill: pa_prefill, causal multi-query attention over the paged
+    cache, on the workload's batch with its whole context already cached: the
+    last --prefill-tokens positions of every sequence (fewer when shorter) are
+    the query chunk. A dense contraction, so the roofline is the tensor pipe:
+    algorithmic FLOPs = 4 * D * Hq * sum over query tokens of (position + 1)
+    (Q K^T and P V, two operations per multiply-add), against the measured
+    bf16 tensor throughput."""
+    from paged_kv_cache_context_gb300 import build, pa
+    from paged_kv_cache_context_gb300 import workloads as wl
+    build.build()
+    pa.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    case = wl.config(args.workload, value_device=str(dev),
+                     seed=None if rank == 0 else 50_000 + rank)
+    if case.kv_dtype != "auto" or case.q_dtype == torch.float32 or case.window:
+        raise SystemExit("--path prefill needs a bf16/f16 workload without a window")
+    S, Hq, Hkv, D, bs = (case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim,
+                         case.block_size)
+    bt = case.block_tables.to(dev)
+    cl = case.context_lens.to(dev)
+    kc, vc = wl.empty_caches(case, device=str(dev))
+    for seq, pos, key, val in [(case.pre_seq[a:b], case.pre_pos[a:b], case.pre_key[a:b],
+                                case.pre_value[a:b]) for a, b in case.pre_chunks if b > a] + \
+            [(None, case.new_pos, case.new_key, case.new_value)]:
+        sm = torch.empty(pos.numel(), dtype=torch.int64, device=dev)
+        pa.slot_mapping(sm, bt, None if seq is None else seq.to(dev), pos.to(dev), bs, 0)
+        pa.reshape_and_cache(key.to(dev).contiguous(), val.to(dev).contiguous(), kc, vc, sm)
+    reps = [(kc, vc)] + [(kc.clone(), vc.clone()) for _ in range(args.replicas - 1)]
+    query, q_seq, q_pos = wl.prefill_queries(case, args.prefill_tokens, seed=7001)
+    q_lens = [int((q_seq == s_).sum()) for s_ in range(S)]
+    cu = torch.tensor([0] + list(torch.cumsum(torch.tensor(q_lens), 0).tolist()),
+                      dtype=torch.int32)
+    max_q = max(q_lens)
+    T = query.shape[0]
+    qd = query.to(dev).contiguous()
+    cud = cu.to(dev)
+    out = torch.empty(T, Hq, D, dtype=case.q_dtype, device=dev)
+    flops = 4.0 * D * Hq * float((q_pos.to(torch.int64) + 1).sum())
+    elem = torch.finfo(case.q_dtype).bits // 8
+    kv_bytes = sum(-(-int(n) // bs) for n in case.context_lens.tolist()) * bs * Hkv * D * 2 * elem
+
+    def launch(i):
+        k_, v_ = reps[i % len(reps)]
+        pa.prefill(out, qd, k_, v_, bt, cud, cl, Hkv, max_q, case.scale, stream=stream)
+
+    for i in range(args.warmup):
+        launch(i)
+    torch.cuda.synchronize()
+    if pa.get_device_error():
+        raise RuntimeError("device error word set after warm-up")
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    phys = int(vis[local_rank]) if local_rank < len(vis) and vis[local_rank].strip().isdigit() \
+        else local_rank
+    clocks = ClockSampler(phys)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        evs[i][0].record(stream)
+        launch(i)
+        evs[i][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    barrier(dev)
+    clk = clocks.stop(t0, t1)
+    if pa.get_device_error():
+        raise RuntimeError("device error word set in the timed region")
+    elapsed = all_reduce(e0.elapsed_time(e1) / 1e3, "max", dev)
+    per = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
+    flops_all = all_reduce(flops * K, "sum", dev)
+    peak_tf, peak_kind = 1907.2, "fallback"
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak_tf, peak_kind = float(json.load(f)["bf16_tflops"]), "measured (burst)"
+    except (OSError, KeyError, ValueError):
+        pass
+    achieved = flops / per / 1e12
+
+    # e2e: query chunk, offsets, lengths and tables from pinned host memory,
+    # output back to pinned host memory, every step
+    host = {n: t.cpu().pin_memory() for n, t in (("q", query), ("cu", cu), ("cl", cl), ("bt", bt))}
+    dbuf = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step(i):
+        for n, t in host.items():
+            dbuf[n].copy_(t, non_blocking=True)
+        k_, v_ = reps[i % len(reps)]
+        pa.prefill(out, dbuf["q"], k_, v_, dbuf["bt"], dbuf["cu"], dbuf["cl"], Hkv, max_q,
+                   case.scale, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a_.record(stream)
+    for i in range(K):
+        e2e_step(i)
+    b_.record(stream)
+    torch.cuda.synchronize()
+    e2e_t = all_reduce(a_.elapsed_time(b_) / 1e3, "max", dev)
+    result = {
+        "metric": "paged prefill attention: achieved TFLOP/s", "value":
+        round(flops_all / elapsed / 1e12, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(elapsed / K * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "impl": "ours",
+        "config": {"workload": args.workload, "path": "prefill", "num_seqs": S,
+                   "num_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "block_size": bs,
+                   "query_tokens": T, "max_q_len": max_q, "flops_per_step": flops,
+                   "kv_bytes_per_step": kv_bytes,
+                   "l2": f"{args.replicas} rotating cache replicas (> L2)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_tf,
+                     "peak_kind": peak_kind, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_tf, 4), "traffic": None,
+                     "kernel": "prefill_attention_kernel (mma.sync m16n8k16, bf16 in, fp32 acc)",
+                     "kernel_us_mean": round(per * 1e6, 2)},
+        "e2e": {"value": round(flops_all / e2e_t / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
+                "d2h_bytes_per_step": out_h.numel() * out_h.element_size()},
+        "gpu_launches": K, "clocks": clk, "wall_s_timed": round(t1 - t0, 4),
+    }
+    if rank == 0:
+        import oracle  # test infrastructure: only this CPU-baseline leg uses it
+        ko, vo = kc.cpu(), vc.cpu()
+        n_rows = 0
+        pick = torch.nonzero(q_seq == 0).flatten()[:64]
+        tq = time.perf_counter()
+        reps_o = 0
+        while time.perf_counter() - tq < 10.0 and reps_o < 50:
+            oracle.prefill(query[pick], q_seq[pick], q_pos[pick], ko, vo, case.block_tables, Hkv,
+                           bs, case.scale)
+            reps_o += 1
+        t_o = (time.perf_counter() - tq) / reps_o
+        f_o = 4.0 * D * Hq * float((q_pos[pick].to(torch.int64) + 1).sum())
+        result["cpu_baseline"] = {"value": round(f_o / t_o / 1e12, 6), "unit": "TFLOP/s",
+                                  "cores": cores(), "kind": "oracle",
+                                  "sample": f"{pick.numel()} query tokens of sequence 0 "
+                                            f"(all heads) x {reps_o} reps"}
+        print(json.dumps(result), flush=True)
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, rank, world):
     if rank != 0:
@@ -639,10 +794,14 @@ def main(argv=None):
     ap.add_argument("--workload", default="mistral_bf16",
                     choices=("tiny", "mistral_bf16", "ring_bf16", "fp8_phi3", "prefix_bf16"))
     ap.add_argument("--replicas", type=int, default=4)
-    ap.add_argument("--path", choices=("balanced", "cascade", "int8"), default="balanced",
-                    help="decode entry point timed: pa_decode's balanced path, "
-                         "pa_decode_cascade (workloads with a shared prefix), or "
-                         "pa_decode_int8 over the workload held as an INT8 cache")
+    ap.add_argument("--prefill-tokens", type=int, default=512,
+                    help="--path prefill: query tokens per sequence (its last positions)")
+    ap.add_argument("--path", choices=("balanced", "cascade", "int8", "prefill"),
+                    default="balanced",
+                    help="entry point timed: pa_decode's balanced path, "
+                         "pa_decode_cascade (workloads with a shared prefix), "
+                         "pa_decode_int8 over the workload held as an INT8 cache, or "
+                         "pa_prefill over the workload's last --prefill-tokens positions")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -654,6 +813,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.path == "prefill":
+            run_prefill(args, rank, local_rank, world)
         else:
             run_ours(args, rank, local_rank, world)
     finally:

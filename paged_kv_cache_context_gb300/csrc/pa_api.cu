@@ -382,6 +382,8 @@ static TmapKey g_tmap_key[kTmapSlots];
 static CUtensorMap g_tmap_val[kTmapSlots];
 static int g_tmap_used = 0, g_tmap_next = 0;
 
+// dtype: PA_BF16 / PA_F16 (16-bit elements, boxes of 64) or -1 (bytes, an
+// INT8 cache: boxes of 128).
 static bool page_tensor_map(CUtensorMap* out, const void* base, int dtype, int D, long long rows,
                             int bs) {
   {
@@ -396,13 +398,16 @@ static bool page_tensor_map(CUtensorMap* out, const void* base, int dtype, int D
   }
   const PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
   if (!fn) return false;
+  const int eb = dtype < 0 ? 1 : 2;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bs)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * eb};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(bs)};
   const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType ty = dtype < 0         ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap m;
-  if (fn(&m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-         2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  if (fn(&m, ty, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
@@ -429,9 +434,9 @@ static cudaError_t run_decode(const DecodeParams& prm_in, const DecodeShape& a, 
   DecodeParams prm = prm_in;
   if (decode_is_tc(a)) {
     const long long rows = (long long)a.NB * a.Hkv * a.bs;
-    if (rows > kMaxTcRows ||
-        !page_tensor_map(&prm.tm_k, prm.k_cache, a.q_dtype, a.D, rows, a.bs) ||
-        !page_tensor_map(&prm.tm_v, prm.v_cache, a.q_dtype, a.D, rows, a.bs))
+    const int mt = a.kv_dtype == PA_KV_INT8 ? -1 : a.q_dtype;
+    if (rows > kMaxTcRows || !page_tensor_map(&prm.tm_k, prm.k_cache, mt, a.D, rows, a.bs) ||
+        !page_tensor_map(&prm.tm_v, prm.v_cache, mt, a.D, rows, a.bs))
       return cudaErrorInvalidValue;
   }
   if (a.kv_dtype == PA_KV_AUTO) {

@@ -50,7 +50,9 @@
 //    with the G query rows of the kv head as the m16 rows (the rest zero),
 //    K and V fragments read by ldmatrix (conflict-free on the swizzled
 //    layout), the softmax weights P rounded to the cache type (as the MMA
-//    takes them) and the running sum taken over those rounded weights.
+//    takes them) and the running sum taken over those rounded weights. An
+//    INT8 cache at head_dim 128 takes the same path: its codes are widened
+//    exactly to the query type in registers (see process_tci).
 // Every K/V byte is read from HBM once per kv head. All waits are bounded.
 #pragma once
 
@@ -101,9 +103,13 @@ enum : int { kModeSplit = 0, kModeBalanced = 1 };
 // Whether a (query type, cache type, head_dim, group bucket, block size)
 // instantiation runs the tensor-core consumers; the host side asks the same
 // question with the C ABI's type codes to know when to build tensor maps.
+// (An INT8 cache qualifies at head_dim 128, where a row is one 128-byte
+// swizzle row.)
 constexpr bool tc_eligible(int q_dtype, int kv_dtype, int D, int GT, int BS) {
-  return PA_DECODE_TC != 0 && kv_dtype == PA_KV_AUTO && (q_dtype == PA_BF16 || q_dtype == PA_F16) &&
-         GT >= PA_TC_MIN_GROUP && (D == 64 || D == 128) && BS >= 16 && BS <= 64;
+  return PA_DECODE_TC != 0 && (q_dtype == PA_BF16 || q_dtype == PA_F16) &&
+         ((kv_dtype == PA_KV_AUTO && (D == 64 || D == 128)) ||
+          (kv_dtype == PA_KV_INT8 && D == 128)) &&
+         GT >= PA_TC_MIN_GROUP && BS >= 16 && BS <= 64;
 }
 template <typename T>
 struct DtypeCode {
@@ -121,6 +127,11 @@ template <typename QT, typename CT, int D, int GT, int BS>
 constexpr bool uses_tc() {
   return std::is_same<QT, CT>::value && DtypeCode<QT>::value >= 0 &&
          tc_eligible(DtypeCode<QT>::value, PA_KV_AUTO, D, GT, BS);
+}
+template <typename QT, typename CT, int D, int GT, int BS>
+constexpr bool uses_tci() {
+  return std::is_same<CT, I8>::value && DtypeCode<QT>::value >= 0 &&
+         tc_eligible(DtypeCode<QT>::value, PA_KV_INT8, D, GT, BS);
 }
 
 // Stage-descriptor flags.
@@ -205,9 +216,11 @@ struct Layout {
   static constexpr int QB = Elem<QT>::bytes;
   static constexpr int ROWB = D * EB;      // bytes of one cached row
   static constexpr int PAGE = BS * ROWB;   // bytes of one (block, kv head) page
-  static constexpr bool TC = uses_tc<QT, CT, D, GT, BS>();
+  static constexpr bool TC = uses_tc<QT, CT, D, GT, BS>();    // 16-bit cache on MMAs
+  static constexpr bool TCI = uses_tci<QT, CT, D, GT, BS>();  // INT8 cache on MMAs
+  static constexpr bool MMA = TC || TCI;
   static constexpr int TPW = 8;            // rows per consumer warp per page
-  static constexpr int NC = TC ? PA_TC_WARPS : BS / TPW;  // consumer warps
+  static constexpr int NC = MMA ? PA_TC_WARPS : BS / TPW;  // consumer warps
   static constexpr int SPP = BS / 16;      // tensor-core consumers: 16-row slices per page
   static constexpr int THREADS = (NC + 1) * 32;
   static constexpr int LPR = choose_lpr(D, GT);
@@ -221,7 +234,7 @@ struct Layout {
   static constexpr int NST = TPW / RPW;    // steps per page
   // pages a consumer warp takes per iteration (one weight round per R pages)
   // (tensor-core consumers: one 16-row slice of one page per warp)
-  static constexpr int R = TC                    ? cmax(1, NC / cmax(SPP, 1))
+  static constexpr int R = MMA                   ? cmax(1, NC / cmax(SPP, 1))
                            : (2 * PAGE <= 8192)  ? 2 * PA_PAGES_PER_ITER
                            : (2 * PAGE <= 16384) ? PA_PAGES_PER_ITER
                                                  : 1;
@@ -245,12 +258,13 @@ struct Layout {
   static constexpr int OFF_Q = 2 * PAGE + 2 * SCB;
   // K page | V page | (K row scales | V row scales) | q rows; the swizzled
   // boxes of the tensor-core layout start on 1024-byte boundaries
-  static constexpr int STAGE = round_up(OFF_Q + QSLOT, TC ? 1024 : 128);
+  static constexpr int STAGE = round_up(OFF_Q + QSLOT, MMA ? 1024 : 128);
   static constexpr int STAGES =
-      TC ? cmax(2 * R, cmin(PA_MAX_STAGES, PA_TC_STAGE_BYTES / STAGE))
-         : cmax(2 * R, cmin(PA_MAX_STAGES, PA_STAGE_BYTES / (2 * PAGE)));
-  static constexpr int BOXB = BS * 128;   // bytes of one 64-column box of a page
-  static constexpr int SCR = TC ? 0 : round_up(TPI * GT, 4);     // per-warp weights
+      MMA ? cmax(2 * R, cmin(PA_MAX_STAGES, PA_TC_STAGE_BYTES / STAGE))
+          : cmax(2 * R, cmin(PA_MAX_STAGES, PA_STAGE_BYTES / (2 * PAGE)));
+  static constexpr int BOXB = BS * 128;     // bytes of one 128-byte-wide box of a page
+  static constexpr int BOXES = ROWB / 128;  // boxes per page (MMA layouts)
+  static constexpr int SCR = MMA ? 0 : round_up(TPI * GT, 4);    // per-warp weights
   static constexpr int MACC = NC * GT * D * 4;                   // merge accumulators
   static constexpr bool MERGE_IN_STAGE = MACC <= STAGE;
   // dynamic shared memory layout
@@ -264,7 +278,7 @@ struct Layout {
   static constexpr int SMEM_USED = OFF_MISC + 32 + 2 * 24;
   // the tensor-core layout rounds the dynamic shared memory's base up to
   // 1024 bytes itself (it may start anywhere 16-byte aligned)
-  static constexpr int ALIGN_PAD = TC ? 1024 : 0;
+  static constexpr int ALIGN_PAD = MMA ? 1024 : 0;
   static constexpr int SMEM = SMEM_USED + ALIGN_PAD;
   // CTAs per SM to plan registers for: what the shared memory allows (228 KB
   // per SM, 1 KB reserved per CTA), at most 4, and no more than keeps a
@@ -280,9 +294,9 @@ struct Layout {
   static_assert(EPP % 2 == 0, "pieces hold whole fp32 pairs");
   static_assert(PAGE % 16 == 0 && SCB % 16 == 0, "bulk copies move multiples of 16 bytes");
   static_assert(STAGE % 128 == 0 && OFF_BAR % 8 == 0, "stage and mbarrier alignment");
-  static_assert(!TC || (D % 64 == 0 && BS % 16 == 0 && NC % SPP == 0 && PAGE % 1024 == 0 &&
-                        BOXB % 1024 == 0),
-                "tensor-core layout: whole 64-column boxes and 16-row slices");
+  static_assert(!MMA || (ROWB % 128 == 0 && BS % 16 == 0 && NC % SPP == 0 &&
+                         PAGE % 1024 == 0 && BOXB % 1024 == 0),
+                "tensor-core layout: whole 128-byte boxes and 16-row slices");
   static_assert(OFF_DESC % 16 == 0 && OFF_SCR % 16 == 0 && OFF_MSTAT % 16 == 0 &&
                     OFF_MACC % 16 == 0 && OFF_MISC % 16 == 0 && (SCR * 4) % 16 == 0,
                 "16-byte vector accesses need 16-byte aligned shared-memory regions");
@@ -677,6 +691,170 @@ __device__ __forceinline__ void process_tc(TcState<D>& st, const uint8_t* const 
   }
 }
 
+// ------------------------------------------------ tensor-core consumers, INT8
+// An INT8 cache (head_dim 128: a row is one 128-byte swizzle row) read with
+// 16-bit queries: the codes are widened exactly to the query type in
+// registers (|code| <= 127 is exact in bf16 and f16) and fed to the same
+// m16n8k16 MMAs. ldmatrix treats a 16-byte chunk of a row as eight 16-bit
+// elements, so lane (g, t) receives four consecutive codes of a row, dims
+// 16c + 4t .. +3 of chunk c: for S = Q K^T the k16 step of chunk c takes
+// them as its k indices (2t, 2t+1, 2t+8, 2t+9) and the q fragments use the
+// same permutation of dims. For P V the transposed load gives lane (g, t) the
+// codes of dims 16c + 2g and 16c + 2g + 1 of tokens 2t and 2t+1, so chunk c
+// feeds two n8 tiles, of its even dims and of its odd dims. The row scales
+// multiply the logits (K) and the softmax weights before they are rounded for
+// the MMA (V); the running sum takes the bare weights.
+template <int D>
+struct TciState {
+  uint32_t qa[D / 16][2];  // A fragments of q (head g): dims 16kk + 4t (+1) and 16kk + 4t + 2 (+3)
+  float o[D / 8][4];       // C fragments: tile 2c = even dims of chunk c, 2c + 1 = odd dims
+  float m_run, l_run, s_top;
+};
+
+template <typename QT, int D>
+__device__ __forceinline__ void begin_piece_tci(TciState<D>& st, const uint8_t* qrows, int G,
+                                                int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t* q = reinterpret_cast<const uint32_t*>(qrows) + g * (D / 2);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    st.qa[kk][0] = g < G ? q[8 * kk + 2 * t] : 0u;
+    st.qa[kk][1] = g < G ? q[8 * kk + 2 * t + 1] : 0u;
+  }
+#pragma unroll
+  for (int j = 0; j < D / 8; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) st.o[j][e] = 0.f;
+  st.m_run = -INFINITY;
+  st.l_run = 0.f;
+  st.s_top = -INFINITY;
+}
+
+// Two INT8 codes, bytes b0 and b1 of w (selectors 0..3), widened exactly and
+// packed as a pair of T (b0 in the low half).
+template <typename T>
+__device__ __forceinline__ uint32_t i8pair(uint32_t u, uint32_t sel) {
+  // u = codes with their sign bits flipped; 0x4B0000uu is 2^23 + u exactly
+  const float2 f = __fadd2_rn(
+      make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540 | (sel & 0xF))),
+                  __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540 | (sel >> 4)))),
+      make_float2(-8388736.f, -8388736.f));
+  return Mma<T>::pack(f.x, f.y);
+}
+
+// One consumer iteration of the INT8 tensor-core path (the warp's 16-row
+// slice of page warp / SPP, as in process_tc); Ks / Vs hold the pages' row
+// scales.
+template <typename QT, typename Ly, int D>
+__device__ __forceinline__ void process_tci(TciState<D>& st, const uint8_t* const (&Kp)[Ly::R],
+                                            const uint8_t* const (&Vp)[Ly::R],
+                                            const float* const (&Ks)[Ly::R],
+                                            const float* const (&Vs)[Ly::R],
+                                            const int (&rows)[Ly::R], int warp, int lane,
+                                            float q_scale, int G) {
+  constexpr int R = Ly::R, SPP = Ly::SPP;
+  constexpr float kLazy = 8.f;
+  using M = Mma<QT>;
+  const int pr = warp / SPP, r0 = 16 * (warp % SPP);
+  const uint8_t* kp = Kp[0];
+  const uint8_t* vp = Vp[0];
+  const float* ks = Ks[0];
+  const float* vs = Vs[0];
+  int n = rows[0];
+#pragma unroll
+  for (int r = 1; r < R; ++r)
+    if (pr == r) {
+      kp = Kp[r];
+      vp = Vp[r];
+      ks = Ks[r];
+      vs = Vs[r];
+      n = rows[r];
+    }
+  const int lim = n - r0;
+  if (lim <= 0) return;
+  const int g = lane >> 2, t = lane & 3, mi = lane >> 3;
+  const bool real = g < G;
+
+  // ---- S = Q K^T: chunk c of a row is the k16 step c (codes widened exactly)
+  float sacc[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+  {
+    const uint32_t kb = smem_u32(kp);
+    const int krow = r0 + ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+    for (int c2 = 0; c2 < D / 32; ++c2) {
+      uint32_t w0, w1, w2, w3;  // tokens 0-7 / 0-7 / 8-15 / 8-15, chunks 2c2 / 2c2+1 / 2c2 / 2c2+1
+      ldsm_x4(tc_chunk<Ly>(kb, krow, 2 * c2 + (mi & 1)), w0, w1, w2, w3);
+      w0 ^= 0x80808080u;
+      w1 ^= 0x80808080u;
+      w2 ^= 0x80808080u;
+      w3 ^= 0x80808080u;
+      const uint32_t a0[4] = {st.qa[2 * c2][0], 0u, st.qa[2 * c2][1], 0u};
+      const uint32_t a1[4] = {st.qa[2 * c2 + 1][0], 0u, st.qa[2 * c2 + 1][1], 0u};
+      M::run(sacc[0], a0, i8pair<QT>(w0, 0x10), i8pair<QT>(w0, 0x32));
+      M::run(sacc[1], a0, i8pair<QT>(w2, 0x10), i8pair<QT>(w2, 0x32));
+      M::run(sacc[0], a1, i8pair<QT>(w1, 0x10), i8pair<QT>(w1, 0x32));
+      M::run(sacc[1], a1, i8pair<QT>(w3, 0x10), i8pair<QT>(w3, 0x32));
+    }
+  }
+
+  // ---- logits (K row scales applied), masked past the context; lazy max
+  const int tok[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+  const float2 k01 = *reinterpret_cast<const float2*>(ks + r0 + 2 * t);
+  const float2 k89 = *reinterpret_cast<const float2*>(ks + r0 + 8 + 2 * t);
+  float x[4] = {sacc[0][0] * q_scale * k01.x, sacc[0][1] * q_scale * k01.y,
+                sacc[1][0] * q_scale * k89.x, sacc[1][1] * q_scale * k89.y};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) x[j] = (real && tok[j] < lim) ? x[j] : -INFINITY;
+  float tm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
+  tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
+  st.s_top = fmaxf(st.s_top, tm);
+  if (__any_sync(0xffffffffu, tm > st.m_run + kLazy)) {
+    const float mn = fmaxf(st.m_run, tm);
+    const float al = mn == -INFINITY ? 1.f : exp2f(st.m_run - mn);
+    st.m_run = mn;
+    st.l_run *= al;
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) {
+      st.o[j][0] *= al;
+      st.o[j][1] *= al;
+    }
+  }
+
+  // ---- weights: the bare ones into the running sum, times the V row scales
+  // (rows past the context: 0, whatever their scale) into the MMA
+  const float2 v01 = *reinterpret_cast<const float2*>(vs + r0 + 2 * t);
+  const float2 v89 = *reinterpret_cast<const float2*>(vs + r0 + 8 + 2 * t);
+  float pw[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) pw[j] = x[j] == -INFINITY ? 0.f : exp2f(x[j] - st.m_run);
+  if (real) st.l_run += (pw[0] + pw[1]) + (pw[2] + pw[3]);
+  const float pv[4] = {pw[0] == 0.f ? 0.f : pw[0] * v01.x, pw[1] == 0.f ? 0.f : pw[1] * v01.y,
+                       pw[2] == 0.f ? 0.f : pw[2] * v89.x, pw[3] == 0.f ? 0.f : pw[3] * v89.y};
+  const uint32_t a[4] = {M::pack(pv[0], pv[1]), 0u, M::pack(pv[2], pv[3]), 0u};
+
+  // ---- O += P V: the transposed load of chunk c gives even and odd dims
+  const uint32_t vb = smem_u32(vp);
+  const int vrow = r0 + ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+  for (int c2 = 0; c2 < D / 32; ++c2) {
+    uint32_t r0_, r1_, r2_, r3_;  // tokens 0-7 / 8-15 / 0-7 / 8-15, chunks 2c2 / 2c2 / 2c2+1 / 2c2+1
+    ldsm_x4_t(tc_chunk<Ly>(vb, vrow, 2 * c2 + (mi >> 1)), r0_, r1_, r2_, r3_);
+    r0_ ^= 0x80808080u;
+    r1_ ^= 0x80808080u;
+    r2_ ^= 0x80808080u;
+    r3_ ^= 0x80808080u;
+    M::run(st.o[4 * c2 + 0], a, i8pair<QT>(r0_, 0x20), i8pair<QT>(r1_, 0x20));
+    M::run(st.o[4 * c2 + 1], a, i8pair<QT>(r0_, 0x31), i8pair<QT>(r1_, 0x31));
+    M::run(st.o[4 * c2 + 2], a, i8pair<QT>(r2_, 0x20), i8pair<QT>(r3_, 0x20));
+    M::run(st.o[4 * c2 + 3], a, i8pair<QT>(r2_, 0x31), i8pair<QT>(r3_, 0x31));
+  }
+}
+
 // Bounded barrier among the NC consumer warps (an mbarrier with one arrival
 // per warp), so a consumer that gave up on a wait can never hang the others.
 __device__ __forceinline__ void consumer_sync(uint64_t* bar, uint32_t& phase, int lane,
@@ -830,6 +1008,33 @@ __device__ __forceinline__ void finish_piece_tc(TcState<D>& st, float* mstat, fl
   }
   consumer_sync(cbar, cphase, lane, err);
   merge_warps<Ly, GT, D>(mstat, macc, cbar, cphase, G, warp, lane, v_scale, err, sink);
+}
+
+// End of a piece on the INT8 tensor-core path: as finish_piece_tc, with the
+// output tiles of chunk c (even dims, odd dims) stored back in dim order.
+template <typename Ly, int GT, int D, typename Sink>
+__device__ __forceinline__ void finish_piece_tci(TciState<D>& st, float* mstat, float* macc,
+                                                 uint64_t* cbar, uint32_t& cphase, int G,
+                                                 int warp, int lane, unsigned* err, Sink&& sink) {
+  constexpr int NC = Ly::NC;
+  const int g = lane >> 2, t = lane & 3;
+  float l = st.l_run;
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  consumer_sync(cbar, cphase, lane, err);  // every warp is done with the stage
+  if (g < GT) {
+    if (t == 0) {
+      mstat[warp * GT + g] = st.m_run;
+      mstat[NC * GT + warp * GT + g] = l;
+      mstat[2 * NC * GT + warp * GT + g] = st.s_top;
+    }
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c)  // dims 16c + 4t .. +3: even tile c0, odd c0, even c1, odd c1
+      *reinterpret_cast<float4*>(&macc[(warp * GT + g) * D + 16 * c + 4 * t]) =
+          make_float4(st.o[2 * c][0], st.o[2 * c + 1][0], st.o[2 * c][1], st.o[2 * c + 1][1]);
+  }
+  consumer_sync(cbar, cphase, lane, err);
+  merge_warps<Ly, GT, D>(mstat, macc, cbar, cphase, G, warp, lane, 1.f, err, sink);
 }
 
 // Attended slots of sequence s (window- and table-limited); flags bad lengths.
@@ -986,7 +1191,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // the tensor-core layout's swizzled boxes need 1024-byte aligned stages
   uint8_t* smem = smem_raw;
-  if constexpr (Ly::TC)
+  if constexpr (Ly::MMA)
     smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1172,19 +1377,22 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
               (ok ? 2u * (Ly::PAGE + Ly::SCB) : 0u) + (piece_start ? qbytes : 0u);
           if (bytes) {
             mbar_arrive_expect_tx(&full[slot], bytes);
-            if (ok && Ly::TC) {
-              // one tensor copy per 64-column box of the K page and of the V page
+            if (ok && Ly::MMA) {
+              // one tensor copy per 128-byte-wide box of the K page and of the V page
               const int y = (bid * Hkv + g) * BS;
 #pragma unroll
-              for (int j = 0; j < D / 64; ++j) {
-                tma_load_2d(stage + j * Ly::BOXB, &p.tm_k, 64 * j, y, &full[slot]);
-                tma_load_2d(stage + Ly::PAGE + j * Ly::BOXB, &p.tm_v, 64 * j, y, &full[slot]);
+              for (int j = 0; j < Ly::BOXES; ++j) {
+                tma_load_2d(stage + j * Ly::BOXB, &p.tm_k, (128 / Ly::EB) * j, y, &full[slot]);
+                tma_load_2d(stage + Ly::PAGE + j * Ly::BOXB, &p.tm_v, (128 / Ly::EB) * j, y,
+                            &full[slot]);
               }
             } else if (ok) {
               const size_t off = (size_t)bid * blk_stride + (size_t)g * Ly::PAGE;
               bulk_g2s(stage, p.k_cache + off, Ly::PAGE, &full[slot]);
               bulk_g2s(stage + Ly::PAGE, p.v_cache + off, Ly::PAGE, &full[slot]);
-              if constexpr (Ly::ROW_SCALES) {
+            }
+            if constexpr (Ly::ROW_SCALES) {
+              if (ok) {
                 const size_t so = ((size_t)bid * Hkv + g) * BS;
                 bulk_g2s(stage + 2 * Ly::PAGE, p.k_scales + so, Ly::SCB, &full[slot]);
                 bulk_g2s(stage + 2 * Ly::PAGE + Ly::SCB, p.v_scales + so, Ly::SCB, &full[slot]);
@@ -1259,12 +1467,16 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
   float* wscr = reinterpret_cast<float*>(smem + Ly::OFF_SCR) + warp * Ly::SCR;
   float* mstat = reinterpret_cast<float*>(smem + Ly::OFF_MSTAT);
   uint32_t cphase = 0;
-  typename std::conditional<Ly::TC, TcState<D>, PieceState<Ly, GT>>::type st;
+  typename std::conditional<
+      Ly::TC, TcState<D>,
+      typename std::conditional<Ly::TCI, TciState<D>, PieceState<Ly, GT>>::type>::type st;
   // end of a piece: the consumer kind's own reduction, then the shared merge
   auto finish = [&](float* macc, auto&& sink) {
     if constexpr (Ly::TC)
       finish_piece_tc<Ly, GT, D>(st, mstat, macc, cbar, cphase, G, warp, lane, p.v_scale, p.err,
                                  sink);
+    else if constexpr (Ly::TCI)
+      finish_piece_tci<Ly, GT, D>(st, mstat, macc, cbar, cphase, G, warp, lane, p.err, sink);
     else
       finish_piece<Ly, GT, D>(st, mstat, macc, cbar, cphase, G, warp, lane, c, rg, p.v_scale,
                               p.err, sink);
@@ -1302,6 +1514,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
         if (d.z & kFirst) {
           if constexpr (Ly::TC)
             begin_piece_tc<QT, D>(st, stage + Ly::OFF_Q, G, lane);
+          else if constexpr (Ly::TCI)
+            begin_piece_tci<QT, D>(st, stage + Ly::OFF_Q, G, lane);
           else
             begin_piece<QT, Ly, GT, D>(st, stage + Ly::OFF_Q, G, c, p.q_scale);
         }
@@ -1320,6 +1534,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
 
     if constexpr (Ly::TC)
       process_tc<QT, Ly, D>(st, Kp, Vp, rows, warp, lane, p.q_scale, G);
+    else if constexpr (Ly::TCI)
+      process_tci<QT, Ly, D>(st, Kp, Vp, Ks, Vs, rows, warp, lane, p.q_scale, G);
     else
       process_pages<CT, Ly, GT>(st, Kp, Vp, Ks, Vs, lim, wscr, warp, lane, c, rg);
 

@@ -135,10 +135,11 @@ def test_int8_decode_full_size_mistral_shape_sampled_rows():
     assert device_errors() == 0
 
 
-def test_int8_decode_never_reads_rows_past_the_context():
+@pytest.mark.parametrize("D,Hq,Hkv", [(64, 8, 2), (128, 16, 4)])  # CUDA-core / MMA consumers
+def test_int8_decode_never_reads_rows_past_the_context(D, Hq, Hkv):
     """Unwritten rows hold code -128 and NaN scales; the output stays finite
     and equal to the oracle's."""
-    case = wl.make_case("d8_stale", 83, 9, 8, 2, 64, len_range=(1, 100), kv_dtype="int8",
+    case = wl.make_case(f"d8_stale{D}", 83, 9, Hq, Hkv, D, len_range=(1, 100), kv_dtype="int8",
                         extra_blocks=4)
     kg, vg, ksg, vsg = gpu_int8_caches(case)
     assert torch.isnan(ksg).any()
