@@ -151,7 +151,12 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
  *   logit_j = scale * sum_d q[s][h][d] * K_j[d]          (K_j dequantised)
  *   out[s][h][:] = sum_j softmax(logit)_j * V_j[:]       (0 when L_s == 0)
  * With FP8, K_j[d] = E4M3value(byte) * k_scale and V_j likewise with v_scale.
- * Accumulation is fp32. Bytes of the cache outside the L_s attended slots
+ * Accumulation is fp32. Where the products run on the tensor cores the
+ * operands are rounded as the MMAs take them: a 16-bit cache with G >= 4
+ * (head_dim 64 or 128) rounds the softmax weights to the cache type; an FP8
+ * or INT8 cache read with 16-bit queries carries q in f16 (exact for a bf16
+ * query inside f16's range, |q| < 65520) and rounds the weights to f16.
+ * Bytes of the cache outside the L_s attended slots
  * (tail rows of the last block, unused blocks) are never used, whatever they
  * hold (NaN included).
  *
@@ -170,6 +175,9 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
  *                context. Contents on entry do not matter; on exit undefined.
  * Supported: D in {64, 96, 128}; bs in {16, 32, 64}; G = Hq/Hkv in 1..8;
  * q_dtype F32/BF16/F16; AUTO caches hold q_dtype. Pointers 16-byte aligned.
+ * Calls whose pages are staged by tensor copies (16-bit queries with a
+ * 16-bit cache at G >= 4, or with an 8-bit cache at head_dim 128) need
+ * NB * Hkv * bs <= 2^31 - 1 cache rows (else PA_ERR_SHAPE).
  * kv_dtype PA_KV_INT8 is refused with PA_ERR_DTYPE here (its row scales go
  * through pa_decode_int8).
  */

@@ -321,7 +321,7 @@ static pa_status check_decode(const DecodeShape& a, const void* out, const void*
       !(isfinite(a.k_scale) && a.k_scale > 0.f && isfinite(a.v_scale) && a.v_scale > 0.f))
     return PA_ERR_SCALE;
   if (!aligned16(out) || !aligned16(query) || !aligned16(kc) || !aligned16(vc)) return PA_ERR_ALIGN;
-  if (tc_eligible(a.q_dtype, a.kv_dtype, a.D, group_bucket(a.Hq / a.Hkv), a.bs) &&
+  if (tma_staged(a.q_dtype, a.kv_dtype, a.D, group_bucket(a.Hq / a.Hkv), a.bs) &&
       (long long)a.NB * a.Hkv * a.bs > (1LL << 31) - 1)
     return PA_ERR_SHAPE;
   return PA_OK;
@@ -383,7 +383,7 @@ static CUtensorMap g_tmap_val[kTmapSlots];
 static int g_tmap_used = 0, g_tmap_next = 0;
 
 // dtype: PA_BF16 / PA_F16 (16-bit elements, boxes of 64) or -1 (bytes, an
-// INT8 cache: boxes of 128).
+// FP8 or INT8 cache: boxes of 128).
 static bool page_tensor_map(CUtensorMap* out, const void* base, int dtype, int D, long long rows,
                             int bs) {
   {
@@ -424,17 +424,17 @@ static bool page_tensor_map(CUtensorMap* out, const void* base, int dtype, int D
 // a 32-bit signed tensor coordinate.
 constexpr long long kMaxTcRows = (1LL << 31) - 1;
 
-static bool decode_is_tc(const DecodeShape& a) {
-  return tc_eligible(a.q_dtype, a.kv_dtype, a.D, group_bucket(a.Hq / a.Hkv), a.bs);
+static bool decode_is_tma_staged(const DecodeShape& a) {
+  return tma_staged(a.q_dtype, a.kv_dtype, a.D, group_bucket(a.Hq / a.Hkv), a.bs);
 }
 
 static cudaError_t run_decode(const DecodeParams& prm_in, const DecodeShape& a, dim3 grid,
                               int mode, int* ctas, cudaStream_t st) {
   const int GT = group_bucket(a.Hq / a.Hkv);
   DecodeParams prm = prm_in;
-  if (decode_is_tc(a)) {
+  if (decode_is_tma_staged(a)) {
     const long long rows = (long long)a.NB * a.Hkv * a.bs;
-    const int mt = a.kv_dtype == PA_KV_INT8 ? -1 : a.q_dtype;
+    const int mt = a.kv_dtype == PA_KV_AUTO ? a.q_dtype : -1;
     if (rows > kMaxTcRows || !page_tensor_map(&prm.tm_k, prm.k_cache, mt, a.D, rows, a.bs) ||
         !page_tensor_map(&prm.tm_v, prm.v_cache, mt, a.D, rows, a.bs))
       return cudaErrorInvalidValue;
@@ -932,15 +932,32 @@ PA_API pa_status pa_prefill(void* out, const void* query, const void* k_cache,
 // ================================================================ cascade
 // Split of the shared prefix into ranges of whole 64-token tiles: as many as
 // keep (query tiles x kv heads x splits) within one wave of two CTAs per SM
-// (a second, partial wave would double the time), at least one.
-static void cascade_plan(int S, int G, int Hkv, int prefix_tokens, int* nsp, int* tps) {
+// (a second, partial wave would double the time), at least one. The number
+// of splits never decreases as sms grows, so a workspace sized for kPlanSMs
+// holds the plan of any device with at most that many SMs.
+static void cascade_plan(int S, int G, int Hkv, int prefix_tokens, int sms, int* nsp, int* tps) {
   const int qtiles = (S * G + kPrefixRows - 1) / kPrefixRows;
   const int tiles = (prefix_tokens + kPrefixTile - 1) / kPrefixTile;
-  const int64_t want = (2 * 152) / ((int64_t)qtiles * Hkv);
+  const int64_t want = (2 * (int64_t)sms) / ((int64_t)qtiles * Hkv);
   int n = static_cast<int>(want < 1 ? 1 : (want > tiles ? tiles : want));
   const int tiles_per = (tiles + n - 1) / n;
   *tps = tiles_per * kPrefixTile;
   *nsp = (tiles + tiles_per - 1) / tiles_per;
+}
+
+// The current device's SM count for a launch-time plan, capped at kPlanSMs
+// (the count the workspace queries assume), read once per device.
+static int launch_plan_sms() {
+  static std::atomic<int> known[32];
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kPlanSMs;
+  if (dev < 32 && (sms = known[dev].load(std::memory_order_relaxed)) > 0) return sms;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0)
+    return kPlanSMs;
+  sms = sms < kPlanSMs ? sms : kPlanSMs;
+  if (dev < 32) known[dev].store(sms, std::memory_order_relaxed);
+  return sms;
 }
 
 static pa_status check_cascade(const DecodeShape& a, int prefix_pages) {
@@ -957,8 +974,8 @@ PA_API size_t pa_decode_cascade_workspace_size(int num_seqs, int num_heads, int 
       head_dim <= 0 || block_size <= 0 || prefix_pages <= 0)
     return 0;
   int nsp = 0, tps = 0;
-  cascade_plan(num_seqs, num_heads / num_kv_heads, num_kv_heads, prefix_pages * block_size, &nsp,
-               &tps);
+  cascade_plan(num_seqs, num_heads / num_kv_heads, num_kv_heads, prefix_pages * block_size,
+               kPlanSMs, &nsp, &tps);
   const size_t rows = (size_t)num_seqs * num_heads * (nsp + 1);
   return align256(rows * head_dim * 4) + 2 * align256(rows * 4);
 }
@@ -983,7 +1000,8 @@ PA_API pa_status pa_decode_cascade(void* out, const void* query, const void* k_c
   if (!aligned16(workspace)) return PA_ERR_ALIGN;
   const int G = num_heads / num_kv_heads;
   int nsp = 0, tps = 0;
-  cascade_plan(num_seqs, G, num_kv_heads, prefix_pages * block_size, &nsp, &tps);
+  cascade_plan(num_seqs, G, num_kv_heads, prefix_pages * block_size, launch_plan_sms(), &nsp,
+               &tps);
   const int ns = nsp + 1;
   const size_t rows = (size_t)num_seqs * num_heads * ns;
   uint8_t* w = static_cast<uint8_t*>(workspace);

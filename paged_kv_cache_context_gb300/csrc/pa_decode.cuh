@@ -50,9 +50,12 @@
 //    with the G query rows of the kv head as the m16 rows (the rest zero),
 //    K and V fragments read by ldmatrix (conflict-free on the swizzled
 //    layout), the softmax weights P rounded to the cache type (as the MMA
-//    takes them) and the running sum taken over those rounded weights. An
-//    INT8 cache at head_dim 128 takes the same path: its codes are widened
-//    exactly to the query type in registers (see process_tci).
+//    takes them) and the running sum taken over those rounded weights.
+//  * 8-bit tensor-core consumers (FP8 E4M3 or INT8 cache, 16-bit queries,
+//    any G up to 8): each consumer warp takes two 16-row slices per
+//    iteration; the cached rows are the m16 rows of the MMAs and the query
+//    heads the n8 columns (S^T = K Q^T, O^T = V^T P^T), the codes widened
+//    exactly to f16 in registers (see process_tc8).
 // Every K/V byte is read from HBM once per kv head. All waits are bounded.
 #pragma once
 
@@ -97,19 +100,52 @@ namespace pa {
 #ifndef PA_TC_WARPS
 #define PA_TC_WARPS 4
 #endif
+// 8-bit caches (FP8 E4M3, INT8) on the tensor cores, any group size up to 8
+// (off = the CUDA-core consumers), their consumer warps, the 16-row slices
+// each warp takes per iteration, and their stage budget and most stages
+// (build-time tunables).
+#ifndef PA_DECODE_TC8
+#define PA_DECODE_TC8 1
+#endif
+#ifndef PA_TC8_WARPS
+#define PA_TC8_WARPS 2
+#endif
+#ifndef PA_TC8_SLICES
+#define PA_TC8_SLICES 2
+#endif
+#ifndef PA_TC8_STAGE_BYTES
+#define PA_TC8_STAGE_BYTES 52000
+#endif
+#ifndef PA_TC8_MAX_STAGES
+#define PA_TC8_MAX_STAGES 16
+#endif
 
 enum : int { kModeSplit = 0, kModeBalanced = 1 };
 
-// Whether a (query type, cache type, head_dim, group bucket, block size)
-// instantiation runs the tensor-core consumers; the host side asks the same
-// question with the C ABI's type codes to know when to build tensor maps.
-// (An INT8 cache qualifies at head_dim 128, where a row is one 128-byte
-// swizzle row.)
-constexpr bool tc_eligible(int q_dtype, int kv_dtype, int D, int GT, int BS) {
+// Which consumers a (query type, cache type, head_dim, group bucket, block
+// size) instantiation runs, asked with the C ABI's type codes so that the
+// host side can ask the same questions:
+//  * tc16_eligible: a 16-bit cache read with queries of the same type, head
+//    dim 64 or 128, G >= PA_TC_MIN_GROUP (MMAs with the query heads as rows);
+//  * tc8_eligible: an 8-bit cache (FP8 or INT8) read with 16-bit queries, any
+//    G up to 8 (MMAs with the cached rows as rows);
+//  * tma_staged: the pages are staged by 2-D tensor copies with the 128-byte
+//    swizzle (the host builds tensor maps for exactly these): the 16-bit
+//    tensor-core consumers, and the 8-bit ones at head_dim 128, where a row
+//    is one 128-byte swizzle row.
+constexpr bool tc16_eligible(int q_dtype, int kv_dtype, int D, int GT, int BS) {
   return PA_DECODE_TC != 0 && (q_dtype == PA_BF16 || q_dtype == PA_F16) &&
-         ((kv_dtype == PA_KV_AUTO && (D == 64 || D == 128)) ||
-          (kv_dtype == PA_KV_INT8 && D == 128)) &&
-         GT >= PA_TC_MIN_GROUP && BS >= 16 && BS <= 64;
+         kv_dtype == PA_KV_AUTO && (D == 64 || D == 128) && GT >= PA_TC_MIN_GROUP && BS >= 16 &&
+         BS <= 64;
+}
+constexpr bool tc8_eligible(int q_dtype, int kv_dtype, int D, int GT, int BS) {
+  return PA_DECODE_TC8 != 0 && (q_dtype == PA_BF16 || q_dtype == PA_F16) &&
+         (kv_dtype == PA_KV_FP8_E4M3 || kv_dtype == PA_KV_INT8) && D % 32 == 0 && D <= 128 &&
+         GT <= 8 && BS >= 16 && BS <= 64 && BS % 16 == 0;
+}
+constexpr bool tma_staged(int q_dtype, int kv_dtype, int D, int GT, int BS) {
+  return tc16_eligible(q_dtype, kv_dtype, D, GT, BS) ||
+         (tc8_eligible(q_dtype, kv_dtype, D, GT, BS) && D == 128);
 }
 template <typename T>
 struct DtypeCode {
@@ -123,15 +159,27 @@ template <>
 struct DtypeCode<__half> {
   static constexpr int value = PA_F16;
 };
+template <typename CT>
+struct KvCode {
+  static constexpr int value = PA_KV_AUTO;
+};
+template <>
+struct KvCode<E4M3> {
+  static constexpr int value = PA_KV_FP8_E4M3;
+};
+template <>
+struct KvCode<I8> {
+  static constexpr int value = PA_KV_INT8;
+};
 template <typename QT, typename CT, int D, int GT, int BS>
 constexpr bool uses_tc() {
   return std::is_same<QT, CT>::value && DtypeCode<QT>::value >= 0 &&
-         tc_eligible(DtypeCode<QT>::value, PA_KV_AUTO, D, GT, BS);
+         tc16_eligible(DtypeCode<QT>::value, PA_KV_AUTO, D, GT, BS);
 }
 template <typename QT, typename CT, int D, int GT, int BS>
-constexpr bool uses_tci() {
-  return std::is_same<CT, I8>::value && DtypeCode<QT>::value >= 0 &&
-         tc_eligible(DtypeCode<QT>::value, PA_KV_INT8, D, GT, BS);
+constexpr bool uses_tc8() {
+  return DtypeCode<QT>::value >= 0 && KvCode<CT>::value != PA_KV_AUTO &&
+         tc8_eligible(DtypeCode<QT>::value, KvCode<CT>::value, D, GT, BS);
 }
 
 // Stage-descriptor flags.
@@ -217,10 +265,12 @@ struct Layout {
   static constexpr int ROWB = D * EB;      // bytes of one cached row
   static constexpr int PAGE = BS * ROWB;   // bytes of one (block, kv head) page
   static constexpr bool TC = uses_tc<QT, CT, D, GT, BS>();    // 16-bit cache on MMAs
-  static constexpr bool TCI = uses_tci<QT, CT, D, GT, BS>();  // INT8 cache on MMAs
-  static constexpr bool MMA = TC || TCI;
+  static constexpr bool TC8 = uses_tc8<QT, CT, D, GT, BS>();  // 8-bit cache on MMAs
+  static constexpr bool SLICES = TC || TC8;  // consumer warps take 16-row slices
+  static constexpr bool TMA = TC || (TC8 && ROWB == 128);  // staged by 2-D tensor copies
   static constexpr int TPW = 8;            // rows per consumer warp per page
-  static constexpr int NC = MMA ? PA_TC_WARPS : BS / TPW;  // consumer warps
+  static constexpr int NC = TC8 ? PA_TC8_WARPS : TC ? PA_TC_WARPS : BS / TPW;  // consumer warps
+  static constexpr int SW = TC8 ? PA_TC8_SLICES : 1;  // slices a consumer warp takes per iteration
   static constexpr int SPP = BS / 16;      // tensor-core consumers: 16-row slices per page
   static constexpr int THREADS = (NC + 1) * 32;
   static constexpr int LPR = choose_lpr(D, GT);
@@ -234,7 +284,7 @@ struct Layout {
   static constexpr int NST = TPW / RPW;    // steps per page
   // pages a consumer warp takes per iteration (one weight round per R pages)
   // (tensor-core consumers: one 16-row slice of one page per warp)
-  static constexpr int R = MMA                   ? cmax(1, NC / cmax(SPP, 1))
+  static constexpr int R = SLICES                ? cmax(1, NC * SW / cmax(SPP, 1))
                            : (2 * PAGE <= 8192)  ? 2 * PA_PAGES_PER_ITER
                            : (2 * PAGE <= 16384) ? PA_PAGES_PER_ITER
                                                  : 1;
@@ -258,13 +308,14 @@ struct Layout {
   static constexpr int OFF_Q = 2 * PAGE + 2 * SCB;
   // K page | V page | (K row scales | V row scales) | q rows; the swizzled
   // boxes of the tensor-core layout start on 1024-byte boundaries
-  static constexpr int STAGE = round_up(OFF_Q + QSLOT, MMA ? 1024 : 128);
+  static constexpr int STAGE = round_up(OFF_Q + QSLOT, TMA ? 1024 : 128);
   static constexpr int STAGES =
-      MMA ? cmax(2 * R, cmin(PA_MAX_STAGES, PA_TC_STAGE_BYTES / STAGE))
+      TC8      ? cmax(2 * R, cmin(PA_TC8_MAX_STAGES, PA_TC8_STAGE_BYTES / STAGE))
+      : SLICES ? cmax(2 * R, cmin(PA_MAX_STAGES, PA_TC_STAGE_BYTES / STAGE))
           : cmax(2 * R, cmin(PA_MAX_STAGES, PA_STAGE_BYTES / (2 * PAGE)));
   static constexpr int BOXB = BS * 128;     // bytes of one 128-byte-wide box of a page
-  static constexpr int BOXES = ROWB / 128;  // boxes per page (MMA layouts)
-  static constexpr int SCR = MMA ? 0 : round_up(TPI * GT, 4);    // per-warp weights
+  static constexpr int BOXES = ROWB / 128;  // boxes per page (tensor-copy layouts)
+  static constexpr int SCR = SLICES ? 0 : round_up(TPI * GT, 4);  // per-warp weights
   static constexpr int MACC = NC * GT * D * 4;                   // merge accumulators
   static constexpr bool MERGE_IN_STAGE = MACC <= STAGE;
   // dynamic shared memory layout
@@ -278,7 +329,7 @@ struct Layout {
   static constexpr int SMEM_USED = OFF_MISC + 32 + 2 * 24;
   // the tensor-core layout rounds the dynamic shared memory's base up to
   // 1024 bytes itself (it may start anywhere 16-byte aligned)
-  static constexpr int ALIGN_PAD = MMA ? 1024 : 0;
+  static constexpr int ALIGN_PAD = TMA ? 1024 : 0;
   static constexpr int SMEM = SMEM_USED + ALIGN_PAD;
   // CTAs per SM to plan registers for: what the shared memory allows (228 KB
   // per SM, 1 KB reserved per CTA), at most 4, and no more than keeps a
@@ -294,9 +345,11 @@ struct Layout {
   static_assert(EPP % 2 == 0, "pieces hold whole fp32 pairs");
   static_assert(PAGE % 16 == 0 && SCB % 16 == 0, "bulk copies move multiples of 16 bytes");
   static_assert(STAGE % 128 == 0 && OFF_BAR % 8 == 0, "stage and mbarrier alignment");
-  static_assert(!MMA || (ROWB % 128 == 0 && BS % 16 == 0 && NC % SPP == 0 &&
-                         PAGE % 1024 == 0 && BOXB % 1024 == 0),
-                "tensor-core layout: whole 128-byte boxes and 16-row slices");
+  static_assert(!TMA || (ROWB % 128 == 0 && PAGE % 1024 == 0 && BOXB % 1024 == 0),
+                "tensor-copy layout: whole 128-byte boxes");
+  static_assert(!SLICES || (BS % 16 == 0 && (NC * SW) % SPP == 0),
+                "tensor-core layout: 16-row slices, whole pages per iteration");
+  static_assert(!TC8 || D % 32 == 0, "8-bit tensor-core layout: 32-dim blocks");
   static_assert(OFF_DESC % 16 == 0 && OFF_SCR % 16 == 0 && OFF_MSTAT % 16 == 0 &&
                     OFF_MACC % 16 == 0 && OFF_MISC % 16 == 0 && (SCR * 4) % 16 == 0,
                 "16-byte vector accesses need 16-byte aligned shared-memory regions");
@@ -691,167 +744,309 @@ __device__ __forceinline__ void process_tc(TcState<D>& st, const uint8_t* const 
   }
 }
 
-// ------------------------------------------------ tensor-core consumers, INT8
-// An INT8 cache (head_dim 128: a row is one 128-byte swizzle row) read with
-// 16-bit queries: the codes are widened exactly to the query type in
-// registers (|code| <= 127 is exact in bf16 and f16) and fed to the same
-// m16n8k16 MMAs. ldmatrix treats a 16-byte chunk of a row as eight 16-bit
-// elements, so lane (g, t) receives four consecutive codes of a row, dims
-// 16c + 4t .. +3 of chunk c: for S = Q K^T the k16 step of chunk c takes
-// them as its k indices (2t, 2t+1, 2t+8, 2t+9) and the q fragments use the
-// same permutation of dims. For P V the transposed load gives lane (g, t) the
-// codes of dims 16c + 2g and 16c + 2g + 1 of tokens 2t and 2t+1, so chunk c
-// feeds two n8 tiles, of its even dims and of its odd dims. The row scales
-// multiply the logits (K) and the softmax weights before they are rounded for
-// the MMA (V); the running sum takes the bare weights.
+// ------------------------------------------------ tensor-core consumers, 8-bit
+// An 8-bit cache (FP8 E4M3 with per-tensor scales, or INT8 with a scale per
+// cached row) read with 16-bit queries, any group size up to 8 and head_dim
+// 64 / 96 / 128, on m16n8k16 f16 MMAs with the roles turned round: the 16
+// cached rows of a slice are the m16 rows and the (up to 8) query heads of
+// the kv head the n8 columns, so S^T = K Q^T and O^T = V^T P^T and no MMA
+// row is padding whatever G is. Codes widen exactly to f16: E4M3 two per cvt
+// (every E4M3 value is an f16 value); INT8 by a byte permute that makes
+// 1024 + (c + 128) an f16 bit pattern and one packed subtract of 1152. q is
+// carried in f16 (exact for a bf16 query inside f16's range); the scales
+// multiply the fp32 logits; the weights are rounded to f16 for the MMA.
+// FP8: the running sum takes the rounded weights, v_scale is applied at the
+// end. INT8: a row's K scale multiplies its logits, its V scale its weight
+// before the rounding, and the running sum takes the bare weights.
+// Staging: at head_dim 128 a row is one 128-byte swizzle row and the pages
+// come by 2-D tensor copies (chunk c of row r at chunk c ^ (r mod 8)); else
+// by 1-D bulk copies, rows of D bytes. The loads below are bank-conflict free
+// on both (D = 96 unswizzled, D = 128 swizzled) because of a fixed
+// permutation of a slice's rows: MMA row i < 8 reads cached row pi(i), row
+// 8 + i reads 8 + pi(i), pi = (0 1 2 3 5 4 7 6).
+//  * K: lane (g, t) reads bytes [D/4 t, D/4 (t + 1)) of rows pi(g) and
+//    8 + pi(g); its four codes of step kk (dims D/4 t + 4 kk .. +3) are the
+//    step's k indices (2t, 2t+1, 2t+8, 2t+9), and q's B fragments follow the
+//    same permutation of dims.
+//  * P: the C fragment of S^T (row = cached row, column = head) becomes P^T's
+//    B fragment by movmatrix (an 8 x 8 transpose in registers).
+//  * V: lane (g, t) reads 4-code words at dims 4x .. 4x + 3, x = g + 8j, of
+//    rows pi(2t), pi(2t+1), 8 + pi(2t), 8 + pi(2t+1); a byte permute pairs
+//    the two rows' codes of a dim, which is one A register of V^T. Tile 2j
+//    takes dims 4x (MMA row g) and 4x + 1 (row g + 8), tile 2j + 1 dims 4x + 2
+//    and 4x + 3; the output is put back in dim order when it is stored.
 template <int D>
-struct TciState {
-  uint32_t qa[D / 16][2];  // A fragments of q (head g): dims 16kk + 4t (+1) and 16kk + 4t + 2 (+3)
-  float o[D / 8][4];       // C fragments: tile 2c = even dims of chunk c, 2c + 1 = odd dims
-  float m_run, l_run, s_top;
+struct Tc8State {
+  uint32_t qb[D / 16][2];  // B fragments of q^T: head g, dims D/4 t + 4 kk (+1) / (+2, +3)
+  float o[D / 16][4];      // C fragments of O^T: tile 2j + u, rows dims, columns heads
+  float m_run[2], l_run[2], s_top[2];  // heads 2t and 2t + 1
 };
 
+__device__ __forceinline__ int tc8_row(int i) { return i < 4 ? i : i ^ 1; }
+
+// Four codes of w as two f16x2 words (bytes 0, 1 -> lo; bytes 2, 3 -> hi).
+template <typename CT>
+__device__ __forceinline__ void widen8(uint32_t w, uint32_t& lo, uint32_t& hi);
+template <>
+__device__ __forceinline__ void widen8<E4M3>(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l16, h16;\n\tmov.b32 {l16, h16}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l16;\n\tcvt.rn.f16x2.e4m3x2 %1, h16;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+template <>
+__device__ __forceinline__ void widen8<I8>(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  // u = c + 128 per byte; 0x6400 | u is the f16 1024 + u, exactly
+  const uint32_t u = w ^ 0x80808080u;
+  const __half2 bias = __floats2half2_rn(1152.f, 1152.f);
+  uint32_t a = __byte_perm(u, 0x64646464u, 0x5140), b = __byte_perm(u, 0x64646464u, 0x7362);
+  const __half2 x = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  const __half2 y = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  lo = *reinterpret_cast<const uint32_t*>(&x);
+  hi = *reinterpret_cast<const uint32_t*>(&y);
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+template <typename QT>
+__device__ __forceinline__ uint32_t q_pair_f16(const QT* q) {
+  const __half2 h = __floats2half2_rn(Elem<QT>::to_f32(q[0]), Elem<QT>::to_f32(q[1]));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Byte `b` of row `r` of a staged page (swizzled rows of 128 bytes when the
+// layout is staged by tensor copies).
+template <typename Ly>
+__device__ __forceinline__ const uint8_t* tc8_at(const uint8_t* page, int r, int b) {
+  if constexpr (Ly::TMA)
+    return page + r * 128 + ((((b >> 4) ^ r) & 7) << 4) + (b & 15);
+  else
+    return page + r * Ly::ROWB + b;
+}
+
 template <typename QT, int D>
-__device__ __forceinline__ void begin_piece_tci(TciState<D>& st, const uint8_t* qrows, int G,
+__device__ __forceinline__ void begin_piece_tc8(Tc8State<D>& st, const uint8_t* qrows, int G,
                                                 int lane) {
   const int g = lane >> 2, t = lane & 3;
-  const uint32_t* q = reinterpret_cast<const uint32_t*>(qrows) + g * (D / 2);
+  const QT* q = reinterpret_cast<const QT*>(qrows) + g * D + (D / 4) * t;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    st.qa[kk][0] = g < G ? q[8 * kk + 2 * t] : 0u;
-    st.qa[kk][1] = g < G ? q[8 * kk + 2 * t + 1] : 0u;
+    st.qb[kk][0] = g < G ? q_pair_f16(q + 4 * kk) : 0u;
+    st.qb[kk][1] = g < G ? q_pair_f16(q + 4 * kk + 2) : 0u;
   }
 #pragma unroll
-  for (int j = 0; j < D / 8; ++j)
+  for (int j = 0; j < D / 16; ++j)
 #pragma unroll
     for (int e = 0; e < 4; ++e) st.o[j][e] = 0.f;
-  st.m_run = -INFINITY;
-  st.l_run = 0.f;
-  st.s_top = -INFINITY;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    st.m_run[h] = -INFINITY;
+    st.l_run[h] = 0.f;
+    st.s_top[h] = -INFINITY;
+  }
 }
 
-// Two INT8 codes, bytes b0 and b1 of w (selectors 0..3), widened exactly and
-// packed as a pair of T (b0 in the low half).
-template <typename T>
-__device__ __forceinline__ uint32_t i8pair(uint32_t u, uint32_t sel) {
-  // u = codes with their sign bits flipped; 0x4B0000uu is 2^23 + u exactly
-  const float2 f = __fadd2_rn(
-      make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540 | (sel & 0xF))),
-                  __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540 | (sel >> 4)))),
-      make_float2(-8388736.f, -8388736.f));
-  return Mma<T>::pack(f.x, f.y);
+// S^T = K Q^T over the slice of rows [r0, r0 + 16) of a staged K page: the
+// log2-unit logits of heads 2t (x[0], x[2]) and 2t + 1 (x[1], x[3]) for rows
+// r0 + kr (x[0], x[1]) and r0 + 8 + kr (x[2], x[3]); rows at or past r0 + lim
+// are masked. ks: the page's K row scales (INT8), else unused.
+template <typename Ly, typename CT, int D>
+__device__ __forceinline__ void tc8_logits(const Tc8State<D>& st, const uint8_t* kpage,
+                                           const float* ks, int r0, int kr, int t, int lim,
+                                           float q_scale, float (&x)[4]) {
+  using M = Mma<__half>;
+  float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t w0[D / 16], w1[D / 16];
+  const int ra = r0 + kr, rb = r0 + 8 + kr;
+  if constexpr ((D / 4) % 16 == 0) {
+#pragma unroll
+    for (int i = 0; i < D / 64; ++i) {
+      const uint4 a = *reinterpret_cast<const uint4*>(tc8_at<Ly>(kpage, ra, (D / 4) * t + 16 * i));
+      const uint4 b = *reinterpret_cast<const uint4*>(tc8_at<Ly>(kpage, rb, (D / 4) * t + 16 * i));
+      w0[4 * i] = a.x; w0[4 * i + 1] = a.y; w0[4 * i + 2] = a.z; w0[4 * i + 3] = a.w;
+      w1[4 * i] = b.x; w1[4 * i + 1] = b.y; w1[4 * i + 2] = b.z; w1[4 * i + 3] = b.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) {
+      const uint2 a = *reinterpret_cast<const uint2*>(tc8_at<Ly>(kpage, ra, (D / 4) * t + 8 * i));
+      const uint2 b = *reinterpret_cast<const uint2*>(tc8_at<Ly>(kpage, rb, (D / 4) * t + 8 * i));
+      w0[2 * i] = a.x; w0[2 * i + 1] = a.y;
+      w1[2 * i] = b.x; w1[2 * i + 1] = b.y;
+    }
+  }
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    uint32_t a[4];
+    widen8<CT>(w0[kk], a[0], a[2]);
+    widen8<CT>(w1[kk], a[1], a[3]);
+    M::run(sacc, a, st.qb[kk][0], st.qb[kk][1]);
+  }
+  float sa = q_scale, sb = q_scale;
+  if constexpr (Ly::ROW_SCALES) {
+    sa *= ks[ra];
+    sb *= ks[rb];
+  }
+  const bool ok0 = kr < lim, ok1 = kr + 8 < lim;
+  x[0] = ok0 ? sacc[0] * sa : -INFINITY;
+  x[1] = ok0 ? sacc[1] * sa : -INFINITY;
+  x[2] = ok1 ? sacc[2] * sb : -INFINITY;
+  x[3] = ok1 ? sacc[3] * sb : -INFINITY;
 }
 
-// One consumer iteration of the INT8 tensor-core path (the warp's 16-row
-// slice of page warp / SPP, as in process_tc); Ks / Vs hold the pages' row
-// scales.
-template <typename QT, typename Ly, int D>
-__device__ __forceinline__ void process_tci(TciState<D>& st, const uint8_t* const (&Kp)[Ly::R],
+// O^T += V^T P^T over the slice of rows [r0, r0 + 16) of a staged V page;
+// with MASK, the codes of rows at or past r0 + lim are zeroed first (they
+// may hold anything, NaN codes too).
+template <typename Ly, typename CT, int D, bool MASK>
+__device__ __forceinline__ void tc8_pv(Tc8State<D>& st, const uint8_t* vpage, int r0,
+                                       uint32_t pb0, uint32_t pb1, int g, int t, int lim) {
+  using M = Mma<__half>;
+  const int ra = tc8_row(2 * t), rb = tc8_row(2 * t + 1);
+  const bool oka = ra < lim, okb = rb < lim, okc = ra + 8 < lim, okd = rb + 8 < lim;
+#pragma unroll
+  for (int j = 0; j < D / 32; ++j) {
+    const int b = 4 * g + 32 * j;
+    uint32_t wa = *reinterpret_cast<const uint32_t*>(tc8_at<Ly>(vpage, r0 + ra, b));
+    uint32_t wb = *reinterpret_cast<const uint32_t*>(tc8_at<Ly>(vpage, r0 + rb, b));
+    uint32_t wc = *reinterpret_cast<const uint32_t*>(tc8_at<Ly>(vpage, r0 + 8 + ra, b));
+    uint32_t wd = *reinterpret_cast<const uint32_t*>(tc8_at<Ly>(vpage, r0 + 8 + rb, b));
+    if constexpr (MASK) {
+      // an INT8 zero code is the byte 0; an E4M3 zero too
+      wa = oka ? wa : 0u;
+      wb = okb ? wb : 0u;
+      wc = okc ? wc : 0u;
+      wd = okd ? wd : 0u;
+    }
+    uint32_t a0[4], a1[4];
+    widen8<CT>(__byte_perm(wa, wb, 0x5140), a0[0], a0[1]);  // dims 4x, 4x+1; rows a, b
+    widen8<CT>(__byte_perm(wc, wd, 0x5140), a0[2], a0[3]);  // rows 8+a, 8+b
+    widen8<CT>(__byte_perm(wa, wb, 0x7362), a1[0], a1[1]);  // dims 4x+2, 4x+3
+    widen8<CT>(__byte_perm(wc, wd, 0x7362), a1[2], a1[3]);
+    M::run(st.o[2 * j], a0, pb0, pb1);
+    M::run(st.o[2 * j + 1], a1, pb0, pb1);
+  }
+}
+
+// One consumer iteration of the 8-bit tensor-core path: the warp takes SW
+// slices, slice warp * SW + j being rows [r0, r0 + 16) of page pr of the R
+// staged pages (pr = slice / SPP, r0 = 16 (slice mod SPP)); rows[r] is the
+// number of attended rows of page r (0 for pages not in this iteration); Ks
+// and Vs hold the pages' row scales (INT8). The slices share one
+// running-max update.
+template <typename Ly, typename CT, int D>
+__device__ __forceinline__ void process_tc8(Tc8State<D>& st, const uint8_t* const (&Kp)[Ly::R],
                                             const uint8_t* const (&Vp)[Ly::R],
                                             const float* const (&Ks)[Ly::R],
                                             const float* const (&Vs)[Ly::R],
                                             const int (&rows)[Ly::R], int warp, int lane,
-                                            float q_scale, int G) {
-  constexpr int R = Ly::R, SPP = Ly::SPP;
+                                            float q_scale) {
+  constexpr int R = Ly::R, SPP = Ly::SPP, SW = Ly::SW;
   constexpr float kLazy = 8.f;
-  using M = Mma<QT>;
-  const int pr = warp / SPP, r0 = 16 * (warp % SPP);
-  const uint8_t* kp = Kp[0];
-  const uint8_t* vp = Vp[0];
-  const float* ks = Ks[0];
-  const float* vs = Vs[0];
-  int n = rows[0];
+  const int g = lane >> 2, t = lane & 3;
+  const int kr = tc8_row(g);
+  const uint8_t* kp[SW];
+  const uint8_t* vp[SW];
+  const float* ksc[SW];
+  const float* vsc[SW];
+  int r0[SW], lim[SW];
 #pragma unroll
-  for (int r = 1; r < R; ++r)
-    if (pr == r) {
-      kp = Kp[r];
-      vp = Vp[r];
-      ks = Ks[r];
-      vs = Vs[r];
-      n = rows[r];
-    }
-  const int lim = n - r0;
-  if (lim <= 0) return;
-  const int g = lane >> 2, t = lane & 3, mi = lane >> 3;
-  const bool real = g < G;
+  for (int j = 0; j < SW; ++j) {
+    const int si = warp * SW + j, pr = si / SPP;
+    kp[j] = Kp[0];
+    vp[j] = Vp[0];
+    ksc[j] = Ks[0];
+    vsc[j] = Vs[0];
+    int n = rows[0];
+#pragma unroll
+    for (int r = 1; r < R; ++r)
+      if (pr == r) {
+        kp[j] = Kp[r];
+        vp[j] = Vp[r];
+        ksc[j] = Ks[r];
+        vsc[j] = Vs[r];
+        n = rows[r];
+      }
+    r0[j] = 16 * (si % SPP);
+    lim[j] = n - r0[j];  // warp-uniform
+  }
+  // the slices run in row order, so an empty first slice means no work
+  if (lim[0] <= 0) return;
 
-  // ---- S = Q K^T: chunk c of a row is the k16 step c (codes widened exactly)
-  float sacc[2][4];
+  // ---- logits of every slice; one lazy running-max update for all of them
+  float x[SW][4];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
+  for (int j = 0; j < SW; ++j) {
+    if (j == 0 || lim[j] > 0) {
+      tc8_logits<Ly, CT, D>(st, kp[j], ksc[j], r0[j], kr, t, lim[j], q_scale, x[j]);
+    } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
-  {
-    const uint32_t kb = smem_u32(kp);
-    const int krow = r0 + ((mi >> 1) << 3) + (lane & 7);
+      for (int e = 0; e < 4; ++e) x[j][e] = -INFINITY;
+    }
+  }
+  float tm0 = fmaxf(x[0][0], x[0][2]), tm1 = fmaxf(x[0][1], x[0][3]);
 #pragma unroll
-    for (int c2 = 0; c2 < D / 32; ++c2) {
-      uint32_t w0, w1, w2, w3;  // tokens 0-7 / 0-7 / 8-15 / 8-15, chunks 2c2 / 2c2+1 / 2c2 / 2c2+1
-      ldsm_x4(tc_chunk<Ly>(kb, krow, 2 * c2 + (mi & 1)), w0, w1, w2, w3);
-      w0 ^= 0x80808080u;
-      w1 ^= 0x80808080u;
-      w2 ^= 0x80808080u;
-      w3 ^= 0x80808080u;
-      const uint32_t a0[4] = {st.qa[2 * c2][0], 0u, st.qa[2 * c2][1], 0u};
-      const uint32_t a1[4] = {st.qa[2 * c2 + 1][0], 0u, st.qa[2 * c2 + 1][1], 0u};
-      M::run(sacc[0], a0, i8pair<QT>(w0, 0x10), i8pair<QT>(w0, 0x32));
-      M::run(sacc[1], a0, i8pair<QT>(w2, 0x10), i8pair<QT>(w2, 0x32));
-      M::run(sacc[0], a1, i8pair<QT>(w1, 0x10), i8pair<QT>(w1, 0x32));
-      M::run(sacc[1], a1, i8pair<QT>(w3, 0x10), i8pair<QT>(w3, 0x32));
+  for (int j = 1; j < SW; ++j) {
+    tm0 = fmaxf(tm0, fmaxf(x[j][0], x[j][2]));
+    tm1 = fmaxf(tm1, fmaxf(x[j][1], x[j][3]));
+  }
+#pragma unroll
+  for (int off = 4; off < 32; off *= 2) {
+    tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, off));
+    tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, off));
+  }
+  st.s_top[0] = fmaxf(st.s_top[0], tm0);
+  st.s_top[1] = fmaxf(st.s_top[1], tm1);
+  if (__any_sync(0xffffffffu, tm0 > st.m_run[0] + kLazy || tm1 > st.m_run[1] + kLazy)) {
+    const float mn0 = fmaxf(st.m_run[0], tm0), mn1 = fmaxf(st.m_run[1], tm1);
+    const float al0 = mn0 == -INFINITY ? 1.f : exp2f(st.m_run[0] - mn0);
+    const float al1 = mn1 == -INFINITY ? 1.f : exp2f(st.m_run[1] - mn1);
+    st.m_run[0] = mn0;
+    st.m_run[1] = mn1;
+    st.l_run[0] *= al0;
+    st.l_run[1] *= al1;
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      st.o[i][0] *= al0;
+      st.o[i][2] *= al0;
+      st.o[i][1] *= al1;
+      st.o[i][3] *= al1;
     }
   }
 
-  // ---- logits (K row scales applied), masked past the context; lazy max
-  const int tok[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
-  const float2 k01 = *reinterpret_cast<const float2*>(ks + r0 + 2 * t);
-  const float2 k89 = *reinterpret_cast<const float2*>(ks + r0 + 8 + 2 * t);
-  float x[4] = {sacc[0][0] * q_scale * k01.x, sacc[0][1] * q_scale * k01.y,
-                sacc[1][0] * q_scale * k89.x, sacc[1][1] * q_scale * k89.y};
+  // ---- weights 2^(s - m) rounded to f16, P^T's B fragments by transposes,
+  // then O^T += V^T P^T slice by slice
 #pragma unroll
-  for (int j = 0; j < 4; ++j) x[j] = (real && tok[j] < lim) ? x[j] : -INFINITY;
-  float tm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-  tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
-  tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
-  st.s_top = fmaxf(st.s_top, tm);
-  if (__any_sync(0xffffffffu, tm > st.m_run + kLazy)) {
-    const float mn = fmaxf(st.m_run, tm);
-    const float al = mn == -INFINITY ? 1.f : exp2f(st.m_run - mn);
-    st.m_run = mn;
-    st.l_run *= al;
+  for (int j = 0; j < SW; ++j) {
+    if (j > 0 && lim[j] <= 0) continue;
+    float pw[4];
 #pragma unroll
-    for (int j = 0; j < D / 8; ++j) {
-      st.o[j][0] *= al;
-      st.o[j][1] *= al;
+    for (int e = 0; e < 4; ++e)
+      pw[e] = x[j][e] == -INFINITY ? 0.f : exp2f(x[j][e] - st.m_run[e & 1]);
+    __half2 p01, p23;
+    if constexpr (Ly::ROW_SCALES) {
+      // masked rows keep a zero weight, whatever their scale holds
+      const float va = vsc[j][r0[j] + kr], vb = vsc[j][r0[j] + 8 + kr];
+      st.l_run[0] += pw[0] + pw[2];
+      st.l_run[1] += pw[1] + pw[3];
+      p01 = __floats2half2_rn(pw[0] == 0.f ? 0.f : pw[0] * va, pw[1] == 0.f ? 0.f : pw[1] * va);
+      p23 = __floats2half2_rn(pw[2] == 0.f ? 0.f : pw[2] * vb, pw[3] == 0.f ? 0.f : pw[3] * vb);
+    } else {
+      p01 = __floats2half2_rn(pw[0], pw[1]);
+      p23 = __floats2half2_rn(pw[2], pw[3]);
+      const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
+      st.l_run[0] += f01.x + f23.x;
+      st.l_run[1] += f01.y + f23.y;
     }
-  }
-
-  // ---- weights: the bare ones into the running sum, times the V row scales
-  // (rows past the context: 0, whatever their scale) into the MMA
-  const float2 v01 = *reinterpret_cast<const float2*>(vs + r0 + 2 * t);
-  const float2 v89 = *reinterpret_cast<const float2*>(vs + r0 + 8 + 2 * t);
-  float pw[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) pw[j] = x[j] == -INFINITY ? 0.f : exp2f(x[j] - st.m_run);
-  if (real) st.l_run += (pw[0] + pw[1]) + (pw[2] + pw[3]);
-  const float pv[4] = {pw[0] == 0.f ? 0.f : pw[0] * v01.x, pw[1] == 0.f ? 0.f : pw[1] * v01.y,
-                       pw[2] == 0.f ? 0.f : pw[2] * v89.x, pw[3] == 0.f ? 0.f : pw[3] * v89.y};
-  const uint32_t a[4] = {M::pack(pv[0], pv[1]), 0u, M::pack(pv[2], pv[3]), 0u};
-
-  // ---- O += P V: the transposed load of chunk c gives even and odd dims
-  const uint32_t vb = smem_u32(vp);
-  const int vrow = r0 + ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-  for (int c2 = 0; c2 < D / 32; ++c2) {
-    uint32_t r0_, r1_, r2_, r3_;  // tokens 0-7 / 8-15 / 0-7 / 8-15, chunks 2c2 / 2c2 / 2c2+1 / 2c2+1
-    ldsm_x4_t(tc_chunk<Ly>(vb, vrow, 2 * c2 + (mi >> 1)), r0_, r1_, r2_, r3_);
-    r0_ ^= 0x80808080u;
-    r1_ ^= 0x80808080u;
-    r2_ ^= 0x80808080u;
-    r3_ ^= 0x80808080u;
-    M::run(st.o[4 * c2 + 0], a, i8pair<QT>(r0_, 0x20), i8pair<QT>(r1_, 0x20));
-    M::run(st.o[4 * c2 + 1], a, i8pair<QT>(r0_, 0x31), i8pair<QT>(r1_, 0x31));
-    M::run(st.o[4 * c2 + 2], a, i8pair<QT>(r2_, 0x20), i8pair<QT>(r3_, 0x20));
-    M::run(st.o[4 * c2 + 3], a, i8pair<QT>(r2_, 0x31), i8pair<QT>(r3_, 0x31));
+    const uint32_t pb0 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&p01));
+    const uint32_t pb1 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&p23));
+    if (lim[j] >= 16)
+      tc8_pv<Ly, CT, D, false>(st, vp[j], r0[j], pb0, pb1, g, t, lim[j]);
+    else
+      tc8_pv<Ly, CT, D, true>(st, vp[j], r0[j], pb0, pb1, g, t, lim[j]);
   }
 }
 
@@ -1010,31 +1205,41 @@ __device__ __forceinline__ void finish_piece_tc(TcState<D>& st, float* mstat, fl
   merge_warps<Ly, GT, D>(mstat, macc, cbar, cphase, G, warp, lane, v_scale, err, sink);
 }
 
-// End of a piece on the INT8 tensor-core path: as finish_piece_tc, with the
-// output tiles of chunk c (even dims, odd dims) stored back in dim order.
+// End of a piece on the 8-bit tensor-core path: lane (g, t) holds heads 2t and
+// 2t + 1; the running sums are reduced over the 8 lanes of a head, and the
+// output is stored back in dim order (dims 4x .. 4x + 3 from tiles 2j, 2j+1).
 template <typename Ly, int GT, int D, typename Sink>
-__device__ __forceinline__ void finish_piece_tci(TciState<D>& st, float* mstat, float* macc,
+__device__ __forceinline__ void finish_piece_tc8(Tc8State<D>& st, float* mstat, float* macc,
                                                  uint64_t* cbar, uint32_t& cphase, int G,
-                                                 int warp, int lane, unsigned* err, Sink&& sink) {
+                                                 int warp, int lane, float v_scale, unsigned* err,
+                                                 Sink&& sink) {
   constexpr int NC = Ly::NC;
   const int g = lane >> 2, t = lane & 3;
-  float l = st.l_run;
-  l += __shfl_xor_sync(0xffffffffu, l, 1);
-  l += __shfl_xor_sync(0xffffffffu, l, 2);
-  consumer_sync(cbar, cphase, lane, err);  // every warp is done with the stage
-  if (g < GT) {
-    if (t == 0) {
-      mstat[warp * GT + g] = st.m_run;
-      mstat[NC * GT + warp * GT + g] = l;
-      mstat[2 * NC * GT + warp * GT + g] = st.s_top;
-    }
+  float l[2] = {st.l_run[0], st.l_run[1]};
 #pragma unroll
-    for (int c = 0; c < D / 16; ++c)  // dims 16c + 4t .. +3: even tile c0, odd c0, even c1, odd c1
-      *reinterpret_cast<float4*>(&macc[(warp * GT + g) * D + 16 * c + 4 * t]) =
-          make_float4(st.o[2 * c][0], st.o[2 * c + 1][0], st.o[2 * c][1], st.o[2 * c + 1][1]);
+  for (int off = 4; off < 32; off *= 2) {
+    l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+    l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+  }
+  consumer_sync(cbar, cphase, lane, err);  // every warp is done with the stage
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int h = 2 * t + hh;
+    if (h < GT) {
+      if (g == 0) {
+        mstat[warp * GT + h] = st.m_run[hh];
+        mstat[NC * GT + warp * GT + h] = l[hh];
+        mstat[2 * NC * GT + warp * GT + h] = st.s_top[hh];
+      }
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j)
+        *reinterpret_cast<float4*>(&macc[(warp * GT + h) * D + 4 * (g + 8 * j)]) =
+            make_float4(st.o[2 * j][hh], st.o[2 * j][2 + hh], st.o[2 * j + 1][hh],
+                        st.o[2 * j + 1][2 + hh]);
+    }
   }
   consumer_sync(cbar, cphase, lane, err);
-  merge_warps<Ly, GT, D>(mstat, macc, cbar, cphase, G, warp, lane, 1.f, err, sink);
+  merge_warps<Ly, GT, D>(mstat, macc, cbar, cphase, G, warp, lane, v_scale, err, sink);
 }
 
 // Attended slots of sequence s (window- and table-limited); flags bad lengths.
@@ -1191,7 +1396,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // the tensor-core layout's swizzled boxes need 1024-byte aligned stages
   uint8_t* smem = smem_raw;
-  if constexpr (Ly::MMA)
+  if constexpr (Ly::TMA)
     smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1252,7 +1457,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
         total += warp_sum_int(pg);
       }
       const long long P = total * Hkv;
-      const long long lo = (long long)cta * P / C, hi = (long long)(cta + 1) * P / C;
+      const long long lo = range_lo(cta, P, C), hi = range_lo(cta + 1, P, C);
       int ls0 = 0, lg0 = 0, lpg0 = 0;
       if (lo < hi) {
         long long run = 0;  // pages of the sequences before this chunk
@@ -1377,7 +1582,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
               (ok ? 2u * (Ly::PAGE + Ly::SCB) : 0u) + (piece_start ? qbytes : 0u);
           if (bytes) {
             mbar_arrive_expect_tx(&full[slot], bytes);
-            if (ok && Ly::MMA) {
+            if (ok && Ly::TMA) {
               // one tensor copy per 128-byte-wide box of the K page and of the V page
               const int y = (bid * Hkv + g) * BS;
 #pragma unroll
@@ -1469,14 +1674,15 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
   uint32_t cphase = 0;
   typename std::conditional<
       Ly::TC, TcState<D>,
-      typename std::conditional<Ly::TCI, TciState<D>, PieceState<Ly, GT>>::type>::type st;
+      typename std::conditional<Ly::TC8, Tc8State<D>, PieceState<Ly, GT>>::type>::type st;
   // end of a piece: the consumer kind's own reduction, then the shared merge
   auto finish = [&](float* macc, auto&& sink) {
     if constexpr (Ly::TC)
       finish_piece_tc<Ly, GT, D>(st, mstat, macc, cbar, cphase, G, warp, lane, p.v_scale, p.err,
                                  sink);
-    else if constexpr (Ly::TCI)
-      finish_piece_tci<Ly, GT, D>(st, mstat, macc, cbar, cphase, G, warp, lane, p.err, sink);
+    else if constexpr (Ly::TC8)
+      finish_piece_tc8<Ly, GT, D>(st, mstat, macc, cbar, cphase, G, warp, lane, p.v_scale,
+                                  p.err, sink);
     else
       finish_piece<Ly, GT, D>(st, mstat, macc, cbar, cphase, G, warp, lane, c, rg, p.v_scale,
                               p.err, sink);
@@ -1514,8 +1720,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
         if (d.z & kFirst) {
           if constexpr (Ly::TC)
             begin_piece_tc<QT, D>(st, stage + Ly::OFF_Q, G, lane);
-          else if constexpr (Ly::TCI)
-            begin_piece_tci<QT, D>(st, stage + Ly::OFF_Q, G, lane);
+          else if constexpr (Ly::TC8)
+            begin_piece_tc8<QT, D>(st, stage + Ly::OFF_Q, G, lane);
           else
             begin_piece<QT, Ly, GT, D>(st, stage + Ly::OFF_Q, G, c, p.q_scale);
         }
@@ -1534,8 +1740,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
 
     if constexpr (Ly::TC)
       process_tc<QT, Ly, D>(st, Kp, Vp, rows, warp, lane, p.q_scale, G);
-    else if constexpr (Ly::TCI)
-      process_tci<QT, Ly, D>(st, Kp, Vp, Ks, Vs, rows, warp, lane, p.q_scale, G);
+    else if constexpr (Ly::TC8)
+      process_tc8<Ly, CT, D>(st, Kp, Vp, Ks, Vs, rows, warp, lane, p.q_scale);
     else
       process_pages<CT, Ly, GT>(st, Kp, Vp, Ks, Vs, lim, wscr, warp, lane, c, rg);
 

@@ -67,6 +67,12 @@ SHAPES = [  # (D, Hq, Hkv, bs, q dtype, kv)
     (64, 16, 4, 32, torch.bfloat16, "auto"),    # G = 4, D 64: 7 stages
     (64, 32, 4, 16, torch.float16, "auto"),     # G = 8, bs 16: 4 pages per iteration
     (128, 32, 8, 64, torch.bfloat16, "auto"),   # G = 4, bs 64: one page per iteration
+    # FP8 tensor-core consumers: every head_dim, group bucket and slice layout
+    (64, 16, 8, 16, torch.bfloat16, "fp8_e4m3"),   # G = 2, bs 16: 4 pages per iteration
+    (128, 16, 2, 64, torch.float16, "fp8_e4m3"),   # G = 8, bs 64: one page per iteration
+    (96, 24, 8, 32, torch.bfloat16, "fp8_e4m3"),   # G = 3 (bucket 4)
+    (128, 8, 8, 16, torch.bfloat16, "fp8_e4m3"),   # G = 1, D 128
+    (64, 40, 5, 64, torch.float16, "fp8_e4m3"),    # G = 8, D 64
 ]
 
 

@@ -93,6 +93,8 @@ def test_int8_write_padding_zero_rows_and_bad_slots():
     (64, 16, 2, 64, torch.bfloat16),    # G = 8, bs 64
     (64, 12, 4, 32, torch.float16),     # G = 3
     (128, 8, 4, 64, torch.float16),     # G = 2
+    (128, 8, 8, 32, torch.bfloat16),    # G = 1, swizzled rows
+    (96, 32, 4, 16, torch.float16),     # G = 8, bs 16: four pages per iteration
 ])
 def test_int8_decode_matches_oracle_both_modes(D, Hq, Hkv, bs, qd):
     case = wl.make_case(f"d8_{D}_{Hq}_{Hkv}_{bs}", 70 + D + Hq + bs, 23, Hq, Hkv, D, bs,
@@ -135,7 +137,7 @@ def test_int8_decode_full_size_mistral_shape_sampled_rows():
     assert device_errors() == 0
 
 
-@pytest.mark.parametrize("D,Hq,Hkv", [(64, 8, 2), (128, 16, 4)])  # CUDA-core / MMA consumers
+@pytest.mark.parametrize("D,Hq,Hkv", [(64, 8, 2), (128, 16, 4)])  # plain / swizzled staged rows
 def test_int8_decode_never_reads_rows_past_the_context(D, Hq, Hkv):
     """Unwritten rows hold code -128 and NaN scales; the output stays finite
     and equal to the oracle's."""
