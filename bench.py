@@ -66,9 +66,10 @@ def csrc_digest() -> str:
     return m.hexdigest()[:16]
 
 
-def measured_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu capture of this
-    workload, or None when there is none or the sources changed since."""
+def measured_traffic(key: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    capture keyed `key` (the workload for the balanced decode, else
+    workload/path), or None when there is none or the sources changed since."""
     path = os.path.join(ROOT, "profiles", "paged_decode_kernel_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -76,7 +77,7 @@ def measured_traffic(workload: str):
     with open(path) as fh:
         for line in fh:
             parts = line.split()
-            if len(parts) == 3 and not line.startswith("#") and parts[0] == workload \
+            if len(parts) == 3 and not line.startswith("#") and parts[0] == key \
                     and parts[1] == digest:
                 return int(parts[2])
     return None
@@ -453,8 +454,9 @@ def run_ours(args, rank, local_rank, world):
         "pct_of_nominal_8tbs": round(100 * bytes_all / elapsed_max / 1e9 / NOMINAL_HBM_GBS, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": (measured_traffic(args.workload)
-                                 if args.path == "balanced" else None),
+                     "traffic": (measured_traffic(args.workload) if args.path == "balanced"
+                                 else measured_traffic(f"{args.workload}/{args.path}")
+                                 if args.path == "int8" else None),
                      "kernel": {"cascade": "pa_decode_cascade: prefix attention + suffix "
                                            "decode + reduce",
                                 "int8": "pa_decode_int8: counter clear + paged_decode_kernel "
@@ -721,7 +723,8 @@ def run_prefill(args, rank, local_rank, world):
                    "l2": f"{args.replicas} rotating cache replicas (> L2)"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_tf,
                      "peak_kind": peak_kind, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak_tf, 4), "traffic": None,
+                     "frac": round(achieved / peak_tf, 4),
+                     "traffic": measured_traffic(f"{args.workload}/prefill"),
                      "kernel": "prefill_attention_kernel (mma.sync m16n8k16, bf16 in, fp32 acc)",
                      "kernel_us_mean": round(per * 1e6, 2)},
         "e2e": {"value": round(flops_all / e2e_t / 1e12, 2), "unit": "TFLOP/s",

@@ -297,7 +297,7 @@ pa_status pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head
  * Bytes of workspace for pa_decode's balanced path (and for
  * pa_decode_balanced). It depends only on the query-head group size and
  * head_dim, not on the batch: one arrival counter per persistent CTA, then
- * the partial results of at most two pieces per persistent CTA (about 2.5 MB
+ * the partial results of at most two pieces per persistent CTA (about 3.8 MB
  * for G = 4, D = 128). 0 for invalid head counts.
  */
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
@@ -310,7 +310,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
  * kernel alone or clear the workspace once for several decodes.
  *
  * pa_decode_workspace_clear: enqueues a zero fill of the workspace's arrival
- * counters (its first 2560 bytes). Errors: PA_ERR_NULL, PA_ERR_WORKSPACE
+ * counters (its first 3840 bytes). Errors: PA_ERR_NULL, PA_ERR_WORKSPACE
  * (fewer bytes), PA_ERR_ALIGN, PA_ERR_CUDA.
  *
  * pa_decode_balanced: one launch. The pages of every (sequence, kv head)

@@ -468,7 +468,7 @@ struct BalancedWs {
   float* piece_ml;
 };
 static constexpr size_t kCounterBytes = (kMaxBalancedCtas * 4 + 255) / 256 * 256;
-static_assert(kCounterBytes == 2560, "the header documents 2560 bytes of counters");
+static_assert(kCounterBytes == 3840, "the header documents 3840 bytes of counters");
 static size_t balanced_bytes(int GT, int D) {
   const size_t slots = (size_t)kMaxBalancedCtas * kPieceSlots;
   return kCounterBytes + align256(slots * GT * D * 4) + align256(slots * GT * 2 * 4);

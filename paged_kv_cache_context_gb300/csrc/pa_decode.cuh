@@ -102,8 +102,9 @@ namespace pa {
 #endif
 // 8-bit caches (FP8 E4M3, INT8) on the tensor cores, any group size up to 8
 // (off = the CUDA-core consumers), their consumer warps, the 16-row slices
-// each warp takes per iteration, and their stage budget and most stages
-// (build-time tunables).
+// each warp takes per iteration, and their stage budgets (FP8: five CTAs per
+// SM at head_dim 96; INT8, whose stages also carry row scales: four) and most
+// stages (build-time tunables).
 #ifndef PA_DECODE_TC8
 #define PA_DECODE_TC8 1
 #endif
@@ -114,7 +115,10 @@ namespace pa {
 #define PA_TC8_SLICES 2
 #endif
 #ifndef PA_TC8_STAGE_BYTES
-#define PA_TC8_STAGE_BYTES 52000
+#define PA_TC8_STAGE_BYTES 40000
+#endif
+#ifndef PA_TC8_I8_STAGE_BYTES
+#define PA_TC8_I8_STAGE_BYTES 52000
 #endif
 #ifndef PA_TC8_MAX_STAGES
 #define PA_TC8_MAX_STAGES 16
@@ -193,9 +197,9 @@ enum : int {
 };
 
 // Balanced mode: partial slots per CTA and the most CTAs a workspace is
-// sized for (152 SMs x 4 resident CTAs).
+// sized for (152 SMs x 6 resident CTAs).
 constexpr int kPieceSlots = 2;
-constexpr int kMaxBalancedCtas = 152 * 4;
+constexpr int kMaxBalancedCtas = 152 * 6;
 
 struct DecodeParams {
   // tensor-core consumers: the K and V caches as 2-D tensors of
@@ -310,7 +314,9 @@ struct Layout {
   // boxes of the tensor-core layout start on 1024-byte boundaries
   static constexpr int STAGE = round_up(OFF_Q + QSLOT, TMA ? 1024 : 128);
   static constexpr int STAGES =
-      TC8      ? cmax(2 * R, cmin(PA_TC8_MAX_STAGES, PA_TC8_STAGE_BYTES / STAGE))
+      TC8      ? cmax(2 * R, cmin(PA_TC8_MAX_STAGES,
+                                   (ROW_SCALES ? PA_TC8_I8_STAGE_BYTES : PA_TC8_STAGE_BYTES) /
+                                       STAGE))
       : SLICES ? cmax(2 * R, cmin(PA_MAX_STAGES, PA_TC_STAGE_BYTES / STAGE))
           : cmax(2 * R, cmin(PA_MAX_STAGES, PA_STAGE_BYTES / (2 * PAGE)));
   static constexpr int BOXB = BS * 128;     // bytes of one 128-byte-wide box of a page

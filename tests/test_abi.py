@@ -123,7 +123,7 @@ def test_split_plan_is_host_only_and_covers_the_context():
 
 
 def test_balanced_workspace_depends_only_on_group_and_head_dim():
-    """An arrival counter per persistent CTA (2560 bytes for 152 x 4 CTAs), then
+    """An arrival counter per persistent CTA (3840 bytes for 152 x 6 CTAs), then
     two partial slots of G' x D floats (G' = group rounded up to 1, 2, 4 or 8)
     plus their (max, sum) per CTA."""
     from paged_kv_cache_context_gb300 import pa
@@ -132,9 +132,9 @@ def test_balanced_workspace_depends_only_on_group_and_head_dim():
                  for S, MB in [(1, 1), (32, 128), (4096, 4096)]}
         assert len(sizes) == 1
         ws = sizes.pop()
-        slots = 152 * 4 * 2
-        assert ws >= 2560 + slots * (gt * D * 4 + gt * 2 * 4)
-        assert ws <= 2560 + slots * (gt * D * 4 + gt * 2 * 4) + 2 * 256
+        slots = 152 * 6 * 2
+        assert ws >= 3840 + slots * (gt * D * 4 + gt * 2 * 4)
+        assert ws <= 3840 + slots * (gt * D * 4 + gt * 2 * 4) + 2 * 256
     assert pa.decode_workspace_size(2, 6, 4, 128, 32, 8, 0) == 0  # 6 % 4 != 0
     assert pa.decode_workspace_size(2, 32, 4, 128, 32, 8, 0) <= 8 << 20  # G = 8, D = 128
 

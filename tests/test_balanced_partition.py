@@ -76,7 +76,7 @@ def test_enumeration_finds_exactly_the_written_pieces(seed):
     for _ in range(200):
         S = rng.randint(1, 40)
         Hkv = rng.choice([1, 2, 4, 8, 32])
-        C = rng.choice([1, 2, 3, 7, 152, 456, 608])
+        C = rng.choice([1, 2, 3, 7, 152, 456, 608, 760, 912])
         mx = rng.choice([1, 2, 5, 40, 300])
         pages = [rng.randint(0, mx) for _ in range(S)]
         segs, P, cut_pieces, counts = walk(pages, Hkv, C)
@@ -100,7 +100,7 @@ def test_counter_index_is_unique_per_cut_segment():
     rng = random.Random(7)
     for _ in range(2000):
         pages = [rng.randint(0, 90) for _ in range(rng.randint(1, 30))]
-        Hkv, C = rng.choice([1, 4, 8]), rng.choice([5, 152, 456, 608])
+        Hkv, C = rng.choice([1, 4, 8]), rng.choice([5, 152, 456, 608, 760, 912])
         _, _, _, counts = walk(pages, Hkv, C)
         idx = [c for (_, c) in counts]
         assert len(idx) == len(set(idx))
@@ -108,6 +108,6 @@ def test_counter_index_is_unique_per_cut_segment():
 
 def test_equal_shares():
     for P in (1, 7, 455, 456, 18_432, 147_456):
-        for C in (456, 608):
+        for C in (456, 608, 760, 912):
             sizes = [range_lo(c + 1, P, C) - range_lo(c, P, C) for c in range(C)]
             assert sum(sizes) == P and max(sizes) - min(sizes) <= 1

@@ -30,7 +30,7 @@ def test_c_program_links_and_calls_the_abi(tmp_path):
     assert int(got["version"]) >= 1 << 16
     assert got["status_shape"] == "inconsistent or unsupported sizes"
     assert got["plan_rc"] == "0" and got["plan_covers"] == "1"
-    assert int(got["ws_g4_d128"]) > 2560
+    assert int(got["ws_g4_d128"]) > 3840
     assert got["budget_mb"] == "1024" and got["budget_ctx"] == "32"
     assert got["decode_empty"] == "0"
     assert got["decode_head_dim"] == "-4" and got["decode_group"] == "-3"

@@ -257,5 +257,5 @@ def test_balanced_launch_without_clear_after_a_clean_launch():
                                to_dev(case.context_lens), case.num_kv_heads, case.scale, ws)
         assert n > 0
         assert torch.equal(bits(out), bits(ref))
-    assert torch.all(ws[:2560] == 0)
+    assert torch.all(ws[:3840] == 0)
     assert device_errors() == 0
