@@ -931,14 +931,14 @@ PA_API pa_status pa_prefill(void* out, const void* query, const void* k_cache,
 
 // ================================================================ cascade
 // Split of the shared prefix into ranges of whole 64-token tiles: as many as
-// keep (query tiles x kv heads x splits) within one wave of two CTAs per SM
-// (a second, partial wave would double the time), at least one. The number
-// of splits never decreases as sms grows, so a workspace sized for kPlanSMs
-// holds the plan of any device with at most that many SMs.
+// keep (128-row query tiles x kv heads x splits) within one wave of one CTA
+// per SM (a second, partial wave would double the time), at least one. The
+// number of splits never decreases as sms grows, so a workspace sized for
+// kPlanSMs holds the plan of any device with at most that many SMs.
 static void cascade_plan(int S, int G, int Hkv, int prefix_tokens, int sms, int* nsp, int* tps) {
-  const int qtiles = (S * G + kPrefixRows - 1) / kPrefixRows;
+  const int qtiles = (S * G + kPrefixTcRows - 1) / kPrefixTcRows;
   const int tiles = (prefix_tokens + kPrefixTile - 1) / kPrefixTile;
-  const int64_t want = (2 * (int64_t)sms) / ((int64_t)qtiles * Hkv);
+  const int64_t want = (int64_t)sms / ((int64_t)qtiles * Hkv);
   int n = static_cast<int>(want < 1 ? 1 : (want > tiles ? tiles : want));
   const int tiles_per = (tiles + n - 1) / n;
   *tps = tiles_per * kPrefixTile;
@@ -965,6 +965,8 @@ static pa_status check_cascade(const DecodeShape& a, int prefix_pages) {
     return PA_ERR_DTYPE;
   if (a.D != 64 && a.D != 128) return PA_ERR_HEAD_DIM;
   if (prefix_pages < 1 || prefix_pages > a.MB) return PA_ERR_SHAPE;
+  // the prefix kernel stages pages by tensor copies: 32-bit row coordinates
+  if ((long long)a.NB * a.Hkv * a.bs > kMaxTcRows) return PA_ERR_SHAPE;
   return PA_OK;
 }
 
@@ -1040,6 +1042,12 @@ PA_API pa_status pa_decode_cascade(void* out, const void* query, const void* k_c
   q.num_prefix_splits = nsp;
   q.tokens_per_split = tps;
   q.scale_log2 = scale * 1.4426950408889634f;
+  {
+    const long long rows = (long long)num_blocks * num_kv_heads * block_size;
+    if (!page_tensor_map(&q.tm_k, k_cache, q_dtype, head_dim, rows, block_size) ||
+        !page_tensor_map(&q.tm_v, v_cache, q_dtype, head_dim, rows, block_size))
+      return PA_ERR_CUDA;
+  }
   if (launch_prefix_attention(q, q_dtype, st) != cudaSuccess) return PA_ERR_CUDA;
   // slot 0: each sequence's own pages after the prefix, one CTA per (sequence, kv head)
   DecodeParams p = make_params(a, query, k_cache, v_cache, block_tables, context_lens, scale, err);

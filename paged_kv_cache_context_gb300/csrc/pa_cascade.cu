@@ -1,18 +1,17 @@
-// pa_cascade.cu -- shared-prefix attention on the tensor cores, and block
-// copies for copy-on-write.
+// pa_cascade.cu -- shared-prefix attention on the tensor cores, paged
+// prefill attention, and block copies for copy-on-write.
 //
 // The prefix part of a cascade decode is a real dense contraction (every
 // K/V row of the shared prefix is used by all S * G query rows of its kv
-// head), so it runs on warp-level MMAs (m16n8k16, bf16/f16 in, fp32
-// accumulate), flash-attention style: a CTA holds 64 query rows (16 per
-// warp) in registers, streams the prefix in tiles of 64 tokens through
-// double-buffered shared memory (16-byte async copies into an XOR-swizzled
-// layout, so that the 8 rows an ldmatrix reads fall in 8 different bank
-// groups), computes S = Q K^T, keeps a running maximum and sum per row, and
-// accumulates O = P V with P rounded to the input type. The decode kernel
-// proper stays on CUDA cores: there each K/V row has one query row per head.
+// head), so it runs on the fifth-generation tensor cores (tcgen05 MMAs with
+// TMEM accumulators, operands staged by tensor copies), flash-attention
+// style; see prefix_attention_kernel. The prefill kernel runs warp-level MMAs
+// (m16n8k16, bf16/f16 in, fp32 accumulate) over 64-row query tiles with K/V
+// tiles in double-buffered, XOR-swizzled shared memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "pa_cascade.cuh"
 #include "pa_device.cuh"
@@ -42,21 +41,53 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>(r * CPR * 16 + ((c ^ (r & 7)) << 4));
 }
 
+// Shared-prefix attention on the fifth-generation tensor cores. A CTA takes
+// 128 query rows (all sequences' query heads of one kv head, row r = s G + h)
+// and one range of the prefix, in tiles of 64 tokens:
+//   S = Q K^T   (M 128 x N 64, K = D)        -> TMEM, two buffers
+//   softmax     (one thread per row, lazy running maximum in log2 units)
+//   O += P V    (M 128 x N D, K = 64 tokens) -> TMEM
+// Q is staged once, K/V tiles come by 2-D tensor copies of whole pages (the
+// prefix's block ids from row 0 of the block tables), P is written to shared
+// memory by the softmax threads; all three operands use the 128-byte swizzle.
+// Warps 0-3: softmax (thread t owns row t, TMEM lane t); warp 4: MMA issue
+// and TMEM allocation; warp 5: tensor copies. Every wait is bounded.
+constexpr int kTcRows = kPrefixTcRows;
+constexpr int kTcTile = kPrefixTile;
+constexpr int kTcStages = 3;
+constexpr int kTcThreads = 192;
+
+template <int D>
+struct PrefixTcLayout {
+  static constexpr int KB = D / 64;                  // 128-byte column blocks of a row
+  static constexpr int QBYTES = KB * kTcRows * 128;  // Q: [KB][128 rows][128 B]
+  static constexpr int TBYTES = KB * kTcTile * 128;  // one K or V tile: [KB][64 tokens][128 B]
+  static constexpr int PBYTES = kTcRows * 128;       // P: [128 rows][64 tokens = 128 B]
+  static constexpr int OFF_KV = QBYTES;
+  static constexpr int OFF_P = OFF_KV + kTcStages * 2 * TBYTES;
+  static constexpr int OFF_BAR = OFF_P + 2 * PBYTES;
+  static constexpr int NBAR = 2 * kTcStages + 8;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + alignment of the base to 1024
+  static constexpr uint32_t TMEM_COLS = 256;         // S: 2 x 64, O: D
+  static_assert(2 * kTcTile + D <= 256, "TMEM columns");
+};
+
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
     prefix_attention_kernel(const __grid_constant__ PrefixParams p) {
-  constexpr int CPR = D / 8;                // 16-byte chunks per row
-  constexpr int TILE = kPrefixTile;         // tokens per K/V tile
-  constexpr int TBYTES = TILE * D * 2;      // bytes of one K or V tile
-  constexpr int KS = D / 16;                // k-steps of Q K^T
-  constexpr int NT = TILE / 8;              // 8-token n-tiles of S
-  constexpr int NO = D / 8;                 // 8-column n-tiles of O
-  static_assert(CPR >= 8, "the swizzle needs 8 chunks per row");
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* sq = smem;                       // [64][D]
-  uint8_t* sk = smem + kPrefixRows * D * 2; // [2][TILE][D]
-  uint8_t* sv = sk + 2 * TBYTES;            // [2][TILE][D]
-  int* sblk = reinterpret_cast<int*>(sv + 2 * TBYTES);  // the split's block ids
+  using Ly = PrefixTcLayout<D>;
+  constexpr int KB = Ly::KB;
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + Ly::OFF_BAR);
+  uint64_t* kv_empty = kv_full + kTcStages;
+  uint64_t* s_full = kv_empty + kTcStages;  // [2]
+  uint64_t* s_free = s_full + 2;            // [2]
+  uint64_t* p_full = s_free + 2;            // [2]
+  uint64_t* pv_done = p_full + 2;           // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::OFF_MISC);
 
   pdl_wait();
   pdl_trigger();
@@ -74,16 +105,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
     const int nctas = gridDim.x * gridDim.y * gridDim.z;
     for (int s = 1 + cta; s < S; s += nctas)
-      for (int i = tid; i < p.prefix_pages; i += kThreads)
+      for (int i = tid; i < p.prefix_pages; i += kTcThreads)
         if (p.block_tables[(size_t)s * p.max_blocks_per_seq + i] != p.block_tables[i])
           raise_error(p.err, PA_DEVERR_BLOCK_ID);
-    for (int s = cta * kThreads + tid; s < S; s += nctas * kThreads)
+    for (int s = cta * kTcThreads + tid; s < S; s += nctas * kTcThreads)
       if (p.context_lens[s] < p.prefix_tokens) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
   }
-
   if (t_begin >= t_end) {  // a split with no prefix token: empty partials
-    for (int i = tid; i < kPrefixRows; i += kThreads) {
-      const int r = qt * kPrefixRows + i;
+    for (int i = tid; i < kTcRows; i += kTcThreads) {
+      const int r = qt * kTcRows + i;
       if (r < rows_total) {
         const size_t row = (size_t)(r / G) * Hq + g * G + r % G;
         p.max_logits[row * p.num_slots + slot] = -INFINITY;
@@ -92,165 +122,253 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     return;
   }
-  // block ids of the split's pages
-  const int pg_begin = t_begin / bs, pg_end = (t_end + bs - 1) / bs;
-  for (int i = pg_begin + tid; i < pg_end; i += kThreads) {
-    int b = p.block_tables[i];
-    if (b < 0 || b >= p.num_blocks) {
-      raise_error(p.err, PA_DEVERR_BLOCK_ID);
-      b = -1;
-    }
-    sblk[i - pg_begin] = b;
-  }
+  const int ntiles = (t_end - t_begin + kTcTile - 1) / kTcTile;
 
-  // Q rows of this CTA -> shared memory (rows past S * G are zero)
-  const uint32_t sq_u = smem_u32(sq), sk_u = smem_u32(sk), sv_u = smem_u32(sv);
-  for (int i = tid; i < kPrefixRows * CPR; i += kThreads) {
-    const int rr = i / CPR, c = i % CPR, r = qt * kPrefixRows + rr;
+  // ---- set-up: barriers, TMEM, Q rows (rows past S * G are zero)
+  if (tid == 0) {
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], kTcRows);
+      mbar_init(&p_full[i], kTcRows);
+      mbar_init(&pv_done[i], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    __syncwarp();
+    tmem_alloc(tmem_slot, Ly::TMEM_COLS);
+  }
+  const uint32_t sq = smem_u32(smem);
+  for (int i = tid; i < kTcRows * KB * 8; i += kTcThreads) {
+    const int rr = i / (KB * 8), c = i % (KB * 8), r = qt * kTcRows + rr;
     const bool ok = r < rows_total;
     const size_t row = ok ? (size_t)(r / G) * Hq + g * G + r % G : 0;
-    cp_async16(sq_u + swz<CPR>(rr, c),
-               static_cast<const uint8_t*>(p.query) + (row * D + c * 8) * 2, ok);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (ok) v = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.query) +
+                                               (row * D + c * 8) * 2);
+    const int kb = c >> 3, ch = c & 7;
+    *reinterpret_cast<uint4*>(smem + kb * (kTcRows * 128) + rr * 128 + ((ch ^ (rr & 7)) << 4)) = v;
   }
-  __syncthreads();  // sblk
-  const size_t head_stride = (size_t)bs * D * 2;  // bytes of one (block, kv head) page
-  auto load_tile = [&](int tile, int buf) {
-    const int t0 = t_begin + tile * TILE;
-    for (int i = tid; i < TILE * CPR; i += kThreads) {
-      const int rr = i / CPR, c = i % CPR, t = t0 + rr;
-      int b = -1;
-      if (t < t_end) b = sblk[t / bs - pg_begin];
-      const bool ok = b >= 0;
-      const size_t off = ok ? ((size_t)b * Hkv + g) * head_stride + (size_t)(t % bs) * D * 2 + c * 16
-                            : 0;
-      cp_async16(sk_u + buf * TBYTES + swz<CPR>(rr, c), p.k_cache + off, ok);
-      cp_async16(sv_u + buf * TBYTES + swz<CPR>(rr, c), p.v_cache + off, ok);
-    }
-  };
-  const int ntiles = (t_end - t_begin + TILE - 1) / TILE;
-  load_tile(0, 0);
-  cp_async_commit();  // group: Q + tile 0
-
-  // Q fragments of this warp's 16 rows
-  cp_async_wait<0>();
+  fence_proxy_async_smem();
+  tc05_fence_before();
   __syncthreads();
-  uint32_t qa[KS][4];
-#pragma unroll
-  for (int kk = 0; kk < KS; ++kk)
-    ldsm_x4(sq_u + swz<CPR>(warp * 16 + (lane & 15), 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1],
-            qa[kk][2], qa[kk][3]);
+  tc05_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_s = tmem, t_o = tmem + 2 * kTcTile;  // S buffers at columns 0 / 64, O at 128
+  bool failed = false;
 
-  float o[NO][4];
+  if (warp == 5) {
+    // ================================================ tensor copies of K/V tiles
+    if (lane == 0) {
+      const long long rows = (long long)p.num_blocks * Hkv * bs;
+      int issued = 0;
+      for (int i = 0; i < ntiles && !failed; ++i) {
+        const int st = i % kTcStages;
+        if (i >= kTcStages && !mbar_wait_bounded(&kv_empty[st], ((i / kTcStages) - 1) & 1)) {
+          raise_error(p.err, PA_DEVERR_TIMEOUT);
+          failed = true;
+          break;
+        }
+        mbar_arrive_expect_tx(&kv_full[st], 2 * Ly::TBYTES);
+        uint8_t* kdst = smem + Ly::OFF_KV + st * 2 * Ly::TBYTES;
+        uint8_t* vdst = kdst + Ly::TBYTES;
+        const int t0 = t_begin + i * kTcTile;
+        for (int pp = 0; pp < kTcTile / bs; ++pp) {
+          const int t = t0 + pp * bs;
+          // pages past the range and bad block ids read as zeros (a box
+          // wholly past the tensor is filled with zeros)
+          int y = static_cast<int>(rows);
+          if (t < t_end) {
+            const int b = __ldg(p.block_tables + t / bs);
+            if (b >= 0 && b < p.num_blocks)
+              y = (b * Hkv + g) * bs;
+            else
+              raise_error(p.err, PA_DEVERR_BLOCK_ID);
+          }
 #pragma unroll
-  for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows lane/4 and lane/4 + 8
-  const int tq = lane & 3;
-
-  for (int tile = 0; tile < ntiles; ++tile) {
-    const int buf = tile & 1;
-    if (tile + 1 < ntiles) load_tile(tile + 1, buf ^ 1);
-    cp_async_commit();
-    cp_async_wait<1>();  // this tile's copies are done
-    __syncthreads();
-    const uint32_t kb = sk_u + buf * TBYTES, vb = sv_u + buf * TBYTES;
-
-    // S = Q K^T for 16 rows x 64 tokens; the 8 token tiles are independent
-    // accumulators, so each k-step issues 8 MMAs that do not wait on each
-    // other
-    float s[NT][4];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < KS; kk += 2) {
-      uint32_t b2[NT], b3[NT];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        uint32_t b0, b1;
-        ldsm_x4(kb + swz<CPR>(8 * j + (lane & 7), 2 * kk + (lane >> 3)), b0, b1, b2[j], b3[j]);
-        Mma<T>::run(s[j], qa[kk], b0, b1);
+          for (int j = 0; j < KB; ++j) {
+            tma_load_2d(kdst + j * (kTcTile * 128) + pp * bs * 128, &p.tm_k, 64 * j, y, &kv_full[st]);
+            tma_load_2d(vdst + j * (kTcTile * 128) + pp * bs * 128, &p.tm_v, 64 * j, y, &kv_full[st]);
+          }
+        }
+        ++issued;
       }
-#pragma unroll
-      for (int j = 0; j < NT; ++j) Mma<T>::run(s[j], qa[kk + 1], b2[j], b3[j]);
+      // never leave with copies in flight
+      for (int k = issued > kTcStages ? issued - kTcStages : 0; k < issued; ++k)
+        if (!mbar_wait_bounded(&kv_full[k % kTcStages], (k / kTcStages) & 1))
+          raise_error(p.err, PA_DEVERR_TIMEOUT);
     }
-    // scale to log2 units, mask tokens past the range, running maximum
-    const int t0 = t_begin + tile * TILE;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+  } else if (warp == 4) {
+    // ================================================ MMA issue (one thread)
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = umma_idesc_f16(kBf16, kTcRows, kTcTile, false);
+      constexpr uint32_t idesc_o = umma_idesc_f16(kBf16, kTcRows, D, true);
+      const uint32_t skv = smem_u32(smem + Ly::OFF_KV), sp = smem_u32(smem + Ly::OFF_P);
+      auto issue_s = [&](int i) -> bool {
+        const int st = i % kTcStages;
+        if (!mbar_wait_bounded(&kv_full[st], (i / kTcStages) & 1)) return false;
+        if (i >= 2 && !mbar_wait_bounded(&s_free[i & 1], ((i >> 1) - 1) & 1)) return false;
+        tc05_fence_after();
+        const uint32_t kt = skv + st * 2 * Ly::TBYTES;
 #pragma unroll
-    for (int j = 0; j < NT; ++j)
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qa = sq + (kk >> 2) * (kTcRows * 128) + (kk & 3) * 32;
+          const uint32_t kbd = kt + (kk >> 2) * (kTcTile * 128) + (kk & 3) * 32;
+          umma_f16(t_s + (i & 1) * kTcTile, umma_sdesc_sw128(qa, 16, 1024),
+                   umma_sdesc_sw128(kbd, 16, 1024), idesc_s, kk > 0);
+        }
+        umma_commit(&s_full[i & 1]);
+        return true;
+      };
+      bool ok = issue_s(0);
+      for (int i = 0; i < ntiles && ok; ++i) {
+        if (i + 1 < ntiles) ok = issue_s(i + 1);
+        if (!ok) break;
+        if (!mbar_wait_bounded(&p_full[i & 1], (i >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc05_fence_after();
+        const uint32_t vt = skv + (i % kTcStages) * 2 * Ly::TBYTES + Ly::TBYTES;
+        const uint32_t pa = sp + (i & 1) * Ly::PBYTES;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bool ok = t0 + 8 * j + 2 * tq + (e & 1) < t_end;
-        s[j][e] = ok ? s[j][e] * p.scale_log2 : -INFINITY;
-        if (e < 2) mx0 = fmaxf(mx0, s[j][e]);
-        else mx1 = fmaxf(mx1, s[j][e]);
+        for (int kk = 0; kk < kTcTile / 16; ++kk)
+          umma_f16(t_o, umma_sdesc_sw128(pa + kk * 32, 16, 1024),
+                   umma_sdesc_sw128(vt + kk * 2048, kTcTile * 128, 1024), idesc_o,
+                   i > 0 || kk > 0);
+        umma_commit(&pv_done[i & 1]);
+        if (i + kTcStages < ntiles) umma_commit(&kv_empty[i % kTcStages]);  // a later tile refills it
       }
-#pragma unroll
-    for (int off = 1; off <= 2; off *= 2) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      if (!ok) raise_error(p.err, PA_DEVERR_TIMEOUT);
     }
-    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-    // every tile holds at least one valid token, so n0, n1 are finite
-    const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
-    m0 = n0;
-    m1 = n1;
-    l0 *= a0;
-    l1 *= a1;
-#pragma unroll
-    for (int n = 0; n < NO; ++n) {
-      o[n][0] *= a0;
-      o[n][1] *= a0;
-      o[n][2] *= a1;
-      o[n][3] *= a1;
-    }
-    // P as A fragments (16 tokens per k-step), row sums from the fp32 values
-    uint32_t pa[NT / 2][4];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const float p0 = exp2f(s[j][0] - n0), p1 = exp2f(s[j][1] - n0);
-      const float p2 = exp2f(s[j][2] - n1), p3 = exp2f(s[j][3] - n1);
-      l0 += p0 + p1;
-      l1 += p2 + p3;
-      pa[j / 2][(j & 1) * 2 + 0] = Mma<T>::pack(p0, p1);
-      pa[j / 2][(j & 1) * 2 + 1] = Mma<T>::pack(p2, p3);
-    }
-    // O += P V
-#pragma unroll
-    for (int kk = 0; kk < NT / 2; ++kk)
-#pragma unroll
-      for (int n = 0; n < NO; n += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb + swz<CPR>(16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1), n + (lane >> 4)), b0,
-                  b1, b2, b3);
-        Mma<T>::run(o[n], pa[kk], b0, b1);
-        Mma<T>::run(o[n + 1], pa[kk], b2, b3);
+  } else {
+    // ================================================ softmax, one row per thread
+    // (tcgen05.ld / st are warp-wide: every decision that leads to one is
+    // taken by the whole warp)
+    const int row_in = tid;  // 0 .. 127 = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    constexpr float kLazy = 8.f;
+    float m = -INFINITY, l = 0.f;
+    uint8_t* prow = smem + Ly::OFF_P + row_in * 128;
+    for (int i = 0; i < ntiles; ++i) {
+      if (__any_sync(0xffffffffu, !mbar_wait_bounded(&s_full[i & 1], (i >> 1) & 1))) {
+        raise_error(p.err, PA_DEVERR_TIMEOUT);
+        failed = true;
+        break;
       }
-    __syncthreads();  // the buffer is refilled two tiles on
+      tc05_fence_after();
+      __syncwarp();
+      uint32_t sr[2][32];
+      tmem_ld32(t_s + (i & 1) * kTcTile + lane_off, sr[0]);
+      tmem_ld32(t_s + (i & 1) * kTcTile + 32 + lane_off, sr[1]);
+      tmem_wait_ld();
+      tc05_fence_before();
+      mbar_arrive(&s_free[i & 1]);
+      const int valid = t_end - (t_begin + i * kTcTile);  // >= 1
+      float x[kTcTile];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kTcTile; ++c) {
+        x[c] = c < valid ? __uint_as_float(sr[c >> 5][c & 31]) * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, x[c]);
+      }
+      if (__any_sync(0xffffffffu, mx > m + kLazy)) {
+        const float mn = fmaxf(m, mx);
+        if (i > 0) {
+          // O holds the tiles so far: scale it by 2^(m - mn) once the last
+          // P V has landed
+          if (__any_sync(0xffffffffu,
+                         !mbar_wait_bounded(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1))) {
+            raise_error(p.err, PA_DEVERR_TIMEOUT);
+            failed = true;
+            break;
+          }
+          tc05_fence_after();
+          __syncwarp();
+          const float al = exp2f(m - mn);
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c0 + lane_off, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * al);
+            tmem_st32(t_o + c0 + lane_off, o);
+          }
+          tmem_wait_st();
+          l *= al;
+        }
+        m = mn;
+      }
+      // weights rounded to the input type for the MMA; the running sum takes
+      // the fp32 values
+      uint32_t pk[kTcTile / 2];
+#pragma unroll
+      for (int c = 0; c < kTcTile; c += 2) {
+        const float p0 = exp2f(x[c] - m), p1 = exp2f(x[c + 1] - m);
+        l += p0 + p1;
+        pk[c / 2] = Mma<T>::pack(p0, p1);
+      }
+      if (i >= 2 &&
+          __any_sync(0xffffffffu, !mbar_wait_bounded(&pv_done[i & 1], ((i >> 1) - 1) & 1))) {
+        raise_error(p.err, PA_DEVERR_TIMEOUT);
+        failed = true;
+        break;
+      }
+      uint8_t* pb = prow + (i & 1) * Ly::PBYTES;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(pb + ((ch ^ (row_in & 7)) << 4)) =
+            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      fence_proxy_async_smem();
+      tc05_fence_before();
+      mbar_arrive(&p_full[i & 1]);
+    }
+    // ---- the row's partial: O / l, the maximum in natural-log units, l
+    if (!failed && __any_sync(0xffffffffu, !mbar_wait_bounded(&pv_done[(ntiles - 1) & 1],
+                                                             ((ntiles - 1) >> 1) & 1))) {
+      raise_error(p.err, PA_DEVERR_TIMEOUT);
+      failed = true;
+    }
+    tc05_fence_after();
+    __syncwarp();
+    const int r = qt * kTcRows + row_in;
+    if (!failed) {  // warp-uniform
+      constexpr float kLn2 = 0.69314718055994530942f;
+      const bool mine = r < rows_total;
+      const size_t row = mine ? (size_t)(r / G) * Hq + g * G + r % G : 0;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float* dst = p.tmp_out + (row * p.num_slots + slot) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(t_o + c0 + lane_off, o);
+        tmem_wait_ld();
+        if (mine) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + c0 + e) =
+                make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                            __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+        }
+      }
+      if (mine) {
+        p.max_logits[row * p.num_slots + slot] = l > 0.f ? m * kLn2 : -INFINITY;
+        p.exp_sums[row * p.num_slots + slot] = l;
+      }
+    }
   }
-
-  // row sums over the quad, then the partials of this warp's rows
-#pragma unroll
-  for (int off = 1; off <= 2; off *= 2) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-  }
-  constexpr float kLn2 = 0.69314718055994530942f;
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int r = qt * kPrefixRows + warp * 16 + (lane >> 2) + 8 * half;
-    if (r >= rows_total) continue;
-    const size_t row = (size_t)(r / G) * Hq + g * G + r % G;
-    const float l = half ? l1 : l0, m = half ? m1 : m0;
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    float* dst = p.tmp_out + (row * p.num_slots + slot) * D;
-#pragma unroll
-    for (int n = 0; n < NO; ++n)
-      *reinterpret_cast<float2*>(dst + 8 * n + 2 * tq) =
-          make_float2(o[n][2 * half] * inv, o[n][2 * half + 1] * inv);
-    if (tq == 0) {
-      p.max_logits[row * p.num_slots + slot] = l > 0.f ? m * kLn2 : -INFINITY;
-      p.exp_sums[row * p.num_slots + slot] = l;
-    }
+  // every TMEM access is done before the columns are released
+  tc05_fence_before();
+  __syncthreads();
+  tc05_fence_after();
+  if (warp == 4) {
+    __syncwarp();
+    tmem_dealloc(tmem, Ly::TMEM_COLS);
   }
 }
 
@@ -476,14 +594,13 @@ __global__ void copy_blocks_kernel(uint8_t* k_cache, uint8_t* v_cache, const int
 
 template <typename T, int D>
 cudaError_t launch_prefix(const PrefixParams& p, cudaStream_t st) {
-  const int smem = kPrefixRows * D * 2 + 4 * kPrefixTile * D * 2 +
-                   4 * ((p.tokens_per_split + p.block_size - 1) / p.block_size + 1);
+  const int smem = PrefixTcLayout<D>::SMEM;
   auto kern = prefix_attention_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((p.num_seqs * p.group + kPrefixRows - 1) / kPrefixRows, p.num_prefix_splits,
+  const dim3 grid((p.num_seqs * p.group + kPrefixTcRows - 1) / kPrefixTcRows, p.num_prefix_splits,
                   p.num_kv_heads);
-  return launch_pdl(kern, grid, dim3(kThreads), smem, st, p);
+  return launch_pdl(kern, grid, dim3(kTcThreads), smem, st, p);
 }
 
 template <typename T, int D>

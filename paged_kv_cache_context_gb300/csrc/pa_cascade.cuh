@@ -3,6 +3,7 @@
 // point that also runs the suffix decode and the combine).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,6 +23,10 @@ namespace pa {
 // (normalised output, largest logit in natural-log units, sum of
 // exp(logit - max); a range with no token gives -inf / 0 and leaves tmp_out).
 struct PrefixParams {
+  // the K and V caches as 2-D tensors of [NB * Hkv * bs rows][D elements],
+  // boxes of 64 elements x bs rows with the 128-byte swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
   float* tmp_out;
   float* max_logits;
   float* exp_sums;
@@ -37,8 +42,10 @@ struct PrefixParams {
   float scale_log2;  // scale * log2(e)
 };
 
-// Rows of query heads one CTA takes, and tokens per staged K/V tile.
+// Rows of query heads one CTA takes (prefill: 64; shared prefix: 128, the
+// M of one tensor-core MMA), and tokens per staged K/V tile.
 constexpr int kPrefixRows = 64;
+constexpr int kPrefixTcRows = 128;
 constexpr int kPrefixTile = 64;
 
 // dtype: 1 = bf16, 2 = f16 (pa_dtype values). Returns cudaErrorInvalidValue
