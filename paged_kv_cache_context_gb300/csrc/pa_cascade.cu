@@ -54,7 +54,10 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 // and TMEM allocation; warp 5: tensor copies. Every wait is bounded.
 constexpr int kTcRows = kPrefixTcRows;
 constexpr int kTcTile = kPrefixTile;
-constexpr int kTcStages = 3;
+#ifndef PA_PREFIX_STAGES
+#define PA_PREFIX_STAGES 4
+#endif
+constexpr int kTcStages = PA_PREFIX_STAGES;
 constexpr int kTcThreads = 192;
 
 template <int D>
@@ -143,16 +146,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tmem_alloc(tmem_slot, Ly::TMEM_COLS);
   }
   const uint32_t sq = smem_u32(smem);
+  // asynchronous 16-byte copies, all in flight at once (zero-filled rows
+  // past S * G)
   for (int i = tid; i < kTcRows * KB * 8; i += kTcThreads) {
     const int rr = i / (KB * 8), c = i % (KB * 8), r = qt * kTcRows + rr;
     const bool ok = r < rows_total;
     const size_t row = ok ? (size_t)(r / G) * Hq + g * G + r % G : 0;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (ok) v = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.query) +
-                                               (row * D + c * 8) * 2);
     const int kb = c >> 3, ch = c & 7;
-    *reinterpret_cast<uint4*>(smem + kb * (kTcRows * 128) + rr * 128 + ((ch ^ (rr & 7)) << 4)) = v;
+    cp_async16(sq + kb * (kTcRows * 128) + rr * 128 + ((ch ^ (rr & 7)) << 4),
+               static_cast<const uint8_t*>(p.query) + (row * D + c * 8) * 2, ok);
   }
+  cp_async_commit();
+  cp_async_wait<0>();
   fence_proxy_async_smem();
   tc05_fence_before();
   __syncthreads();
@@ -268,14 +273,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tmem_wait_ld();
       tc05_fence_before();
       mbar_arrive(&s_free[i & 1]);
+      // logits in log2 units; columns past the range (only in a partial
+      // last tile) are -inf
       const int valid = t_end - (t_begin + i * kTcTile);  // >= 1
+      const float sl = p.scale_log2;
       float x[kTcTile];
-      float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kTcTile; ++c) {
-        x[c] = c < valid ? __uint_as_float(sr[c >> 5][c & 31]) * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, x[c]);
+      for (int c = 0; c < kTcTile; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]) * sl;
+      if (valid < kTcTile) {  // CTA-uniform
+#pragma unroll
+        for (int c = 0; c < kTcTile; ++c) x[c] = c < valid ? x[c] : -INFINITY;
       }
+      float mx = x[0];
+#pragma unroll
+      for (int c = 1; c < kTcTile; ++c) mx = fmaxf(mx, x[c]);
       if (__any_sync(0xffffffffu, mx > m + kLazy)) {
         const float mn = fmaxf(m, mx);
         if (i > 0) {
@@ -307,12 +318,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // weights rounded to the input type for the MMA; the running sum takes
       // the fp32 values
       uint32_t pk[kTcTile / 2];
+      float l0 = 0.f, l1 = 0.f;
 #pragma unroll
       for (int c = 0; c < kTcTile; c += 2) {
-        const float p0 = exp2f(x[c] - m), p1 = exp2f(x[c + 1] - m);
-        l += p0 + p1;
+        const float p0 = ex2_approx(x[c] - m), p1 = ex2_approx(x[c + 1] - m);
+        l0 += p0;
+        l1 += p1;
         pk[c / 2] = Mma<T>::pack(p0, p1);
       }
+      l += l0 + l1;
       if (i >= 2 &&
           __any_sync(0xffffffffu, !mbar_wait_bounded(&pv_done[i & 1], ((i >> 1) - 1) & 1))) {
         raise_error(p.err, PA_DEVERR_TIMEOUT);

@@ -97,6 +97,11 @@ namespace pa {
 #ifndef PA_TC_STAGE_BYTES
 #define PA_TC_STAGE_BYTES 105000
 #endif
+// split mode (one CTA per (split, kv head, sequence), usually a few pages
+// each): smaller rings, so more CTAs are resident and start at once
+#ifndef PA_TC_SPLIT_STAGE_BYTES
+#define PA_TC_SPLIT_STAGE_BYTES 52000
+#endif
 #ifndef PA_TC_WARPS
 #define PA_TC_WARPS 4
 #endif
@@ -262,7 +267,7 @@ constexpr int choose_pb(int bytes) {
   return bytes % 16 == 0 ? 16 : bytes % 8 == 0 ? 8 : bytes % 4 == 0 ? 4 : bytes % 2 == 0 ? 2 : 1;
 }
 
-template <typename QT, typename CT, int D, int GT, int BS>
+template <typename QT, typename CT, int D, int GT, int BS, int MODE = kModeBalanced>
 struct Layout {
   static constexpr int EB = Elem<CT>::bytes;
   static constexpr int QB = Elem<QT>::bytes;
@@ -317,7 +322,9 @@ struct Layout {
       TC8      ? cmax(2 * R, cmin(PA_TC8_MAX_STAGES,
                                    (ROW_SCALES ? PA_TC8_I8_STAGE_BYTES : PA_TC8_STAGE_BYTES) /
                                        STAGE))
-      : SLICES ? cmax(2 * R, cmin(PA_MAX_STAGES, PA_TC_STAGE_BYTES / STAGE))
+      : SLICES ? cmax(2 * R, cmin(PA_MAX_STAGES, (MODE == kModeSplit ? PA_TC_SPLIT_STAGE_BYTES
+                                                                   : PA_TC_STAGE_BYTES) /
+                                                    STAGE))
           : cmax(2 * R, cmin(PA_MAX_STAGES, PA_STAGE_BYTES / (2 * PAGE)));
   static constexpr int BOXB = BS * 128;     // bytes of one 128-byte-wide box of a page
   static constexpr int BOXES = ROWB / 128;  // boxes per page (tensor-copy layouts)
@@ -1397,7 +1404,7 @@ __device__ __forceinline__ void publish_piece(const DecodeParams& p, const CutPi
 
 template <typename QT, typename CT, int D, int GT, int BS, int MODE>
 __device__ __forceinline__ void decode_body(const DecodeParams& p) {
-  using Ly = Layout<QT, CT, D, GT, BS>;
+  using Ly = Layout<QT, CT, D, GT, BS, MODE>;
   constexpr int NC = Ly::NC, STAGES = Ly::STAGES, R = Ly::R, TPW = Ly::TPW;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // the tensor-core layout's swizzled boxes need 1024-byte aligned stages
@@ -1841,8 +1848,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p) {
 }
 
 template <typename QT, typename CT, int D, int GT, int BS, int MODE>
-__global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
-                                  Layout<QT, CT, D, GT, BS>::MIN_CTAS)
+__global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS, MODE>::THREADS,
+                                  Layout<QT, CT, D, GT, BS, MODE>::MIN_CTAS)
     paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   if constexpr (MODE == kModeSplit) {
     if (!p.join_at_end) pdl_wait();
@@ -1861,7 +1868,7 @@ __global__ void __launch_bounds__(Layout<QT, CT, D, GT, BS>::THREADS,
 // at most kMaxBalancedCtas); the grid size used is returned in *ctas.
 template <typename QT, typename CT, int D, int GT, int BS, int MODE>
 cudaError_t launch_decode(const DecodeParams& prm, dim3 grid, int* ctas, cudaStream_t stream) {
-  using Ly = Layout<QT, CT, D, GT, BS>;
+  using Ly = Layout<QT, CT, D, GT, BS, MODE>;
   auto kern = paged_decode_kernel<QT, CT, D, GT, BS, MODE>;
   static int configured_devices = 0;  // bit per device id < 32
   static int capacity[32] = {};       // resident CTAs per device

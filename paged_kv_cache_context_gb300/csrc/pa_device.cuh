@@ -114,6 +114,14 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, in
       : "memory");
 }
 
+// 2^x by the special-function unit (ex2.approx, flushing subnormal results
+// to zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- tcgen05
 // Fifth-generation tensor-core MMAs with accumulators in tensor memory
 // (TMEM: 128 lanes x 512 columns of 32 bits per SM), issued by one thread,
