@@ -19,7 +19,7 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 128;  // 4 warps x 16 query rows
+constexpr int kPrefillThreads = 256;  // 8 warps x 16 query rows
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   // 16 bytes global -> shared, zero-filled when !valid (src is not read then)
@@ -386,15 +386,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-// Causal prefill over the paged cache: one CTA per (64-row query tile, kv
-// head, sequence), with the tiles, fragments and online softmax of the prefix
-// kernel above. The CTA's rows are (token, head-in-group) pairs of one
+// Causal prefill over the paged cache: one CTA per (128-row query tile, kv
+// head, sequence), eight warps of 16 rows each, every K/V tile staged once
+// for all 128 rows. The CTA's rows are (token, head-in-group) pairs of one
 // sequence; it streams that sequence's pages from position 0 up to the
 // position of its last row, and masks key t for a row at position pos when
 // t > pos. Every row sees position 0, so its running maximum is finite from
 // the first tile on.
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_attention_kernel(const __grid_constant__ PrefillParams p) {
   constexpr int CPR = D / 8;
   constexpr int TILE = kPrefixTile;
@@ -404,8 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NO = D / 8;
   static_assert(CPR >= 8, "the swizzle needs 8 chunks per row");
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* sq = smem;                        // [64][D]
-  uint8_t* sk = smem + kPrefixRows * D * 2;  // [2][TILE][D]
+  uint8_t* sq = smem;                         // [128][D]
+  uint8_t* sk = smem + kPrefillRows * D * 2;  // [2][TILE][D]
   uint8_t* sv = sk + 2 * TBYTES;             // [2][TILE][D]
 
   pdl_wait();
@@ -425,25 +425,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;  // offsets that do not fit the batch: nothing of this sequence is written
   }
   const int rows_total = q_len * G;
-  if (qt * kPrefixRows >= rows_total) return;
+  if (qt * kPrefillRows >= rows_total) return;
   T* out = static_cast<T*>(p.out);
   if (n < q_len || n > MB * bs) {  // the chunk does not fit its context: zero rows
     if (reporter) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
-    for (int i = tid; i < kPrefixRows * D; i += kThreads) {
-      const int r = qt * kPrefixRows + i / D;
+    for (int i = tid; i < kPrefillRows * D; i += kPrefillThreads) {
+      const int r = qt * kPrefillRows + i / D;
       if (r < rows_total)
         out[((size_t)(q0 + r / G) * Hq + g * G + r % G) * D + i % D] = Elem<T>::from_f32(0.f);
     }
     return;
   }
   const int pos0 = n - q_len;  // position of the chunk's first token
-  const int r_last = min(qt * kPrefixRows + kPrefixRows, rows_total) - 1;
+  const int r_last = min(qt * kPrefillRows + kPrefillRows, rows_total) - 1;
   const int kv_end = pos0 + r_last / G + 1;  // keys this CTA needs: positions [0, kv_end)
 
   // Q rows of this CTA -> shared memory (rows past the sequence's are zero)
   const uint32_t sq_u = smem_u32(sq), sk_u = smem_u32(sk), sv_u = smem_u32(sv);
-  for (int i = tid; i < kPrefixRows * CPR; i += kThreads) {
-    const int rr = i / CPR, c = i % CPR, r = qt * kPrefixRows + rr;
+  for (int i = tid; i < kPrefillRows * CPR; i += kPrefillThreads) {
+    const int rr = i / CPR, c = i % CPR, r = qt * kPrefillRows + rr;
     const bool ok = r < rows_total;
     const size_t row = ok ? (size_t)(q0 + r / G) * Hq + g * G + r % G : 0;
     cp_async16(sq_u + swz<CPR>(rr, c),
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* table = p.block_tables + (size_t)s * MB;
   auto load_tile = [&](int tile, int buf) {
     const int t0 = tile * TILE;
-    for (int i = tid; i < TILE * CPR; i += kThreads) {
+    for (int i = tid; i < TILE * CPR; i += kPrefillThreads) {
       const int rr = i / CPR, c = i % CPR, t = t0 + rr;
       int b = -1;
       if (t < kv_end) {
@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // positions of this lane's two rows (a row past the sequence's takes the
   // CTA's last position: finite values that are never stored)
-  const int rA = qt * kPrefixRows + warp * 16 + (lane >> 2), rB = rA + 8;
+  const int rA = qt * kPrefillRows + warp * 16 + (lane >> 2), rB = rA + 8;
   const int posA = rA < rows_total ? pos0 + rA / G : kv_end - 1;
   const int posB = rB < rows_total ? pos0 + rB / G : kv_end - 1;
 
@@ -619,13 +619,13 @@ cudaError_t launch_prefix(const PrefixParams& p, cudaStream_t st) {
 
 template <typename T, int D>
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t st) {
-  const int smem = kPrefixRows * D * 2 + 4 * kPrefixTile * D * 2;
+  const int smem = kPrefillRows * D * 2 + 4 * kPrefixTile * D * 2;
   auto kern = prefill_attention_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long tiles = ((long long)p.max_q_len * p.group + kPrefixRows - 1) / kPrefixRows;
+  const long long tiles = ((long long)p.max_q_len * p.group + kPrefillRows - 1) / kPrefillRows;
   const dim3 grid(static_cast<unsigned>(tiles), p.num_kv_heads, p.num_seqs);
-  return launch_pdl(kern, grid, dim3(kThreads), smem, st, p);
+  return launch_pdl(kern, grid, dim3(kPrefillThreads), smem, st, p);
 }
 
 }  // namespace

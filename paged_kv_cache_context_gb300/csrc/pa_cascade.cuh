@@ -42,9 +42,9 @@ struct PrefixParams {
   float scale_log2;  // scale * log2(e)
 };
 
-// Rows of query heads one CTA takes (prefill: 64; shared prefix: 128, the
-// M of one tensor-core MMA), and tokens per staged K/V tile.
-constexpr int kPrefixRows = 64;
+// Rows of query heads one CTA takes (prefill: 128 on 8 warps; shared prefix:
+// 128, the M of one tensor-core MMA), and tokens per staged K/V tile.
+constexpr int kPrefillRows = 128;
 constexpr int kPrefixTcRows = 128;
 constexpr int kPrefixTile = 64;
 

@@ -1,6 +1,6 @@
 """The paged prefill kernel's index arithmetic, restated on the CPU.
 
-The kernel runs one CTA per (64-row query tile, kv head, sequence); its rows
+The kernel runs one CTA per (128-row query tile, kv head, sequence); its rows
 are the (token, head-in-group) pairs r = i * G + j of one sequence's chunk,
 token i sitting at position n - q_len + i. It streams keys of positions
 [0, kv_end) in 64-token tiles, with kv_end one past the position of the
@@ -14,7 +14,7 @@ import random
 
 import pytest
 
-ROWS, TILE = 64, 64
+ROWS, TILE = 128, 64
 
 
 def kernel_accesses(q_lens, ctx, G, Hkv, Hq, bs, MB, NB, D, tables):
