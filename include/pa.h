@@ -267,7 +267,9 @@ pa_status pa_decode_int8(void* out, const void* query,
  * block_tables : int32 [S][MB].  cu_q : int32 [S + 1].  context_lens :
  *                int32 [S].
  * Supported: D in {64, 128} (PA_ERR_HEAD_DIM); bs in {16, 32, 64}
- * (PA_ERR_BLOCK_SIZE); G in 1..8; 1 <= max_q_len <= T (PA_ERR_SHAPE).
+ * (PA_ERR_BLOCK_SIZE); G in 1..8; 1 <= max_q_len <= T and
+ * NB * Hkv * bs <= 2^31 - 1 cache rows (pages are staged by tensor copies)
+ * (PA_ERR_SHAPE).
  * Device-side checks: offsets that do not fit [0, T] or a q_len above
  * max_q_len set PA_DEVERR_SEQ and that sequence is not written; n_s < q_len_s
  * or n_s > MB * bs sets PA_DEVERR_CONTEXT_LEN and its rows are zero; a block
@@ -349,8 +351,8 @@ pa_status pa_decode_balanced(void* out, const void* query,
  *      one CTA per (sequence, kv head), into partial slot 0;
  *   2. the shared prefix (pages 0 .. prefix_pages - 1 of row 0 of
  *      block_tables) for all S * G query heads of each kv head at once, on
- *      the tensor cores, cut into up to (prefix tokens / 64) token ranges,
- *      into slots 1 .. ;
+ *      the tensor cores in 128-row tiles, cut into up to (prefix tokens /
+ *      64) token ranges, into slots 1 .. ;
  *   3. pa_reduce of the slots into `out`.
  * The prefix K/V is read once per kv head for the whole batch instead of
  * once per sequence.
@@ -359,7 +361,8 @@ pa_status pa_decode_balanced(void* out, const void* query,
  * (else PA_DEVERR_BLOCK_ID), and every context_lens[s] >= prefix_pages * bs
  * (else PA_DEVERR_CONTEXT_LEN). Supported: AUTO caches of q_dtype BF16 or F16
  * (else PA_ERR_DTYPE), D in {64, 128} (else PA_ERR_HEAD_DIM),
- * 1 <= prefix_pages <= MB (else PA_ERR_SHAPE). workspace: at least
+ * 1 <= prefix_pages <= MB and NB * Hkv * bs <= 2^31 - 1 cache rows (else
+ * PA_ERR_SHAPE). workspace: at least
  * pa_decode_cascade_workspace_size() bytes (PA_ERR_NULL / PA_ERR_WORKSPACE),
  * 16-byte aligned; contents on entry do not matter. Other arguments and
  * errors as pa_decode. Accuracy: the prefix's softmax weights are rounded to

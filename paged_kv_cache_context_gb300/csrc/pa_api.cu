@@ -900,10 +900,16 @@ PA_API pa_status pa_prefill(void* out, const void* query, const void* k_cache,
   if (num_blocks <= 0 || max_blocks_per_seq <= 0 || max_q_len < 1 || max_q_len > num_tokens)
     return PA_ERR_SHAPE;
   if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PA_ERR_SHAPE;
+  // pages are staged by tensor copies: 32-bit row coordinates
+  const long long cache_rows = (long long)num_blocks * num_kv_heads * block_size;
+  if (cache_rows > kMaxTcRows) return PA_ERR_SHAPE;
   if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
     return PA_ERR_ALIGN;
   constexpr float kLog2e = 1.4426950408889634f;
   PrefillParams p{};
+  if (!page_tensor_map(&p.tm_k, k_cache, q_dtype, head_dim, cache_rows, block_size) ||
+      !page_tensor_map(&p.tm_v, v_cache, q_dtype, head_dim, cache_rows, block_size))
+    return PA_ERR_CUDA;
   p.out = out;
   p.query = query;
   p.k_cache = static_cast<const uint8_t*>(k_cache);

@@ -42,9 +42,8 @@ struct PrefixParams {
   float scale_log2;  // scale * log2(e)
 };
 
-// Rows of query heads one CTA takes (prefill: 128 on 8 warps; shared prefix:
-// 128, the M of one tensor-core MMA), and tokens per staged K/V tile.
-constexpr int kPrefillRows = 128;
+// Rows of query heads one CTA takes (the M of one tensor-core MMA; shared
+// prefix and prefill alike), and tokens per staged K/V tile.
 constexpr int kPrefixTcRows = 128;
 constexpr int kPrefixTile = 64;
 
@@ -62,6 +61,9 @@ cudaError_t launch_prefix_attention(const PrefixParams& p, int dtype, cudaStream
 // its q_len_s * G (token, head-in-group) pairs, so Q K^T and P V are dense
 // contractions over the sequence's pages.
 struct PrefillParams {
+  // the K and V caches as 2-D tensors (as in PrefixParams)
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
   void* out;                    // [T][Hq][D], same element type as the query
   const void* query;            // [T][Hq][D]
   const uint8_t* k_cache;       // [NB][Hkv][bs][D]
