@@ -285,6 +285,31 @@ pa_status pa_prefill(void* out, const void* query,
                      pa_dtype q_dtype, pa_stream_t stream);
 
 /*
+ * pa_prefill_int8 -- pa_prefill over an INT8 cache with per-row scales.
+ *
+ * Source: "libmir-metal trace/kv.rs" (INT8 per-token/head pages, dequantised
+ * inside the paged attention) with the prefill of "PagedAttention in
+ * mistral.rs". Same computation, arguments and errors as pa_prefill, with
+ *   K_j[d] = k_cache[blk][g][row][d] * k_scales[blk][g][row]
+ * and V_j likewise (the caches and scales written by
+ * pa_reshape_and_cache_int8). k_cache, v_cache: int8 [NB][Hkv][bs][D];
+ * k_scales, v_scales: fp32 [NB][Hkv][bs]. On the tensor cores the codes are
+ * widened exactly to f16, q is carried in f16 (exact for a bf16 query inside
+ * f16's range), the K row scale multiplies the logit and the V row scale the
+ * softmax weight before it is rounded to f16; fp32 accumulation. Pages are
+ * moved by 1-D bulk copies (no limit on the cache's rows). NULL scales ->
+ * PA_ERR_NULL; scales not 16-byte aligned -> PA_ERR_ALIGN.
+ */
+pa_status pa_prefill_int8(void* out, const void* query,
+                          const int8_t* k_cache, const int8_t* v_cache,
+                          const float* k_scales, const float* v_scales,
+                          const int32_t* block_tables, const int32_t* cu_q,
+                          const int32_t* context_lens, int num_tokens, int num_seqs,
+                          int num_heads, int num_kv_heads, int head_dim, int block_size,
+                          int num_blocks, int max_blocks_per_seq, int max_q_len, float scale,
+                          pa_dtype q_dtype, pa_stream_t stream);
+
+/*
  * pa_decode_plan -- a split plan for pa_decode_partials at these sizes.
  * Writes the number of context splits per (sequence, kv head) and the pages
  * (blocks) each split covers; split i covers slots

@@ -929,7 +929,61 @@ PA_API pa_status pa_prefill(void* out, const void* query, const void* k_cache,
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.max_q_len = max_q_len;
   p.scale_log2 = scale * kLog2e;
-  return launch_prefill_attention(p, q_dtype, reinterpret_cast<cudaStream_t>(stream)) ==
+  return launch_prefill_attention(p, q_dtype, false, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_prefill_int8(void* out, const void* query, const int8_t* k_cache,
+                                 const int8_t* v_cache, const float* k_scales,
+                                 const float* v_scales, const int32_t* block_tables,
+                                 const int32_t* cu_q, const int32_t* context_lens,
+                                 int num_tokens, int num_seqs, int num_heads, int num_kv_heads,
+                                 int head_dim, int block_size, int num_blocks,
+                                 int max_blocks_per_seq, int max_q_len, float scale,
+                                 pa_dtype q_dtype, pa_stream_t stream) {
+  if (num_tokens < 0 || num_seqs < 0 || num_seqs > 65535) return PA_ERR_SHAPE;
+  if (num_tokens == 0 || num_seqs == 0) return PA_OK;
+  if (!out || !query || !k_cache || !v_cache || !k_scales || !v_scales || !block_tables ||
+      !cu_q || !context_lens)
+    return PA_ERR_NULL;
+  if (q_dtype != PA_BF16 && q_dtype != PA_F16) return PA_ERR_DTYPE;
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_kv_heads > 65535 ||
+      num_heads % num_kv_heads != 0 || num_heads / num_kv_heads > 8)
+    return PA_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_HEAD_DIM;
+  if (block_size != 16 && block_size != 32 && block_size != 64) return PA_ERR_BLOCK_SIZE;
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0 || max_q_len < 1 || max_q_len > num_tokens)
+    return PA_ERR_SHAPE;
+  if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PA_ERR_SHAPE;
+  if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(k_scales) || !aligned16(v_scales))
+    return PA_ERR_ALIGN;
+  constexpr float kLog2e = 1.4426950408889634f;
+  PrefillParams p{};
+  p.out = out;
+  p.query = query;
+  p.k_cache = reinterpret_cast<const uint8_t*>(k_cache);
+  p.v_cache = reinterpret_cast<const uint8_t*>(v_cache);
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  p.block_tables = block_tables;
+  p.cu_q = cu_q;
+  p.context_lens = context_lens;
+  p.err = error_word();
+  p.num_seqs = num_seqs;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.num_tokens = num_tokens;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.max_q_len = max_q_len;
+  p.scale_log2 = scale * kLog2e;
+  return launch_prefill_attention(p, q_dtype, true, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;

@@ -38,78 +38,109 @@ __device__ __forceinline__ void cp_async_wait() {
 //   S = Q K^T   (M 128 x N 64, K = D)        -> TMEM, two buffers
 //   softmax     (one thread per row, lazy running maximum in log2 units)
 //   O += P V    (M 128 x N D, K = 64 tokens) -> TMEM
-// Q is staged once, K/V tiles come by 2-D tensor copies of whole pages, P is
-// written to shared memory by the softmax threads; all three operands use the
-// 128-byte swizzle. Warps 0-3: softmax (thread t owns row t, TMEM lane t);
-// warp 4: MMA issue and TMEM allocation; warp 5: tensor copies. Every wait is
-// bounded, and every warp-wide TMEM access is taken by the whole warp.
+// Q is staged once, K/V tiles of 16-bit caches come by 2-D tensor copies of
+// whole pages, P is written to shared memory by the softmax threads; all
+// three operands use the 128-byte swizzle. Warps 0-3: softmax (thread t owns
+// row t, TMEM lane t); warp 4: MMA issue and TMEM allocation; warp 5: copies.
+// An INT8 cache (I8) comes by 1-D bulk copies of its pages and row scales
+// into a raw ring, and warps 6-9 widen the codes exactly to f16 into the
+// swizzled K/V tiles (one row per thread); q is carried in f16 (exact inside
+// f16's range), the K row scales multiply the logits, the V row scales the
+// weights before they are rounded, and the running sum takes the bare
+// weights. Every wait is bounded, and every warp-wide TMEM access is taken by
+// the whole warp.
 constexpr int kTcRows = kPrefixTcRows;
 constexpr int kTcTile = kPrefixTile;
 #ifndef PA_PREFIX_STAGES
 #define PA_PREFIX_STAGES 4
 #endif
-constexpr int kTcStages = PA_PREFIX_STAGES;
-constexpr int kTcThreads = 192;
 
-template <int D>
+template <int D, bool I8>
 struct PrefixTcLayout {
   static constexpr int KB = D / 64;                  // 128-byte column blocks of a row
+  static constexpr int STAGES = I8 ? 3 : PA_PREFIX_STAGES;  // f16/bf16 K/V tiles
+  static constexpr int RSTAGES = I8 ? 2 : 0;         // raw INT8 tiles
+  static constexpr int THREADS = I8 ? 320 : 192;
   static constexpr int QBYTES = KB * kTcRows * 128;  // Q: [KB][128 rows][128 B]
   static constexpr int TBYTES = KB * kTcTile * 128;  // one K or V tile: [KB][64 tokens][128 B]
   static constexpr int PBYTES = kTcRows * 128;       // P: [128 rows][64 tokens = 128 B]
+  static constexpr int RAWT = kTcTile * D;           // INT8 codes of one K or V tile
+  static constexpr int RAWB = 2 * RAWT + 2 * kTcTile * 4;  // codes + row scales
   static constexpr int OFF_KV = QBYTES;
-  static constexpr int OFF_P = OFF_KV + kTcStages * 2 * TBYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * PBYTES;
-  static constexpr int NBAR = 2 * kTcStages + 8;
+  static constexpr int OFF_P = OFF_KV + STAGES * 2 * TBYTES;
+  static constexpr int OFF_SC = OFF_P + 2 * PBYTES;  // INT8: [STAGES][K, V][64] row scales
+  static constexpr int OFF_RAW = OFF_SC + (I8 ? STAGES * 2 * kTcTile * 4 : 0);
+  static constexpr int OFF_BAR = OFF_RAW + RSTAGES * RAWB;
+  static constexpr int NBAR = 2 * STAGES + 8 + (I8 ? 2 * RSTAGES + STAGES : 0);
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + alignment of the base to 1024
   static constexpr uint32_t TMEM_COLS = 256;         // S: 2 x 64, O: D
   static_assert(2 * kTcTile + D <= 256, "TMEM columns");
+  static_assert(OFF_RAW % 16 == 0 && RAWB % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
-// One CTA's attention. Arguments:
-//   tm_k, tm_v   tensor maps of the caches ([NB Hkv bs rows][D], boxes of 64
-//                elements x bs rows, 128-byte swizzle)
-//   q_base       any valid query address (the source of the zero-filling
-//                copies, which read nothing)
-//   g, Hkv, bs, num_blocks   the kv head and the cache's shape
-//   k_begin, k_end           key positions attended (k_begin a multiple of bs)
-//   q_row(rr)    the global address of tile row rr's D query elements, or
-//                nullptr (a padding row: zeros)
+// Where the CTA's keys and queries are.
+struct Tc05Args {
+  const CUtensorMap* tm_k;  // 16-bit caches as [NB Hkv bs rows][D]: boxes of 64 x bs, 128-B swizzle
+  const CUtensorMap* tm_v;
+  const uint8_t* k_codes;   // INT8 caches [NB][Hkv][bs][D] and row scales [NB][Hkv][bs]
+  const uint8_t* v_codes;
+  const float* k_scales;
+  const float* v_scales;
+  const void* q_base;       // any valid query address (source of zero-filling copies)
+  int g, Hkv, bs, num_blocks;
+  int k_begin, k_end;       // key positions attended (k_begin a multiple of bs)
+  int min_pos;              // CAUSAL: the smallest row position of the tile
+  float scale_log2;
+  unsigned* err;
+};
+
+// One CTA's attention. QT is the query type; the MMAs take T = QT (16-bit
+// caches) or f16 (INT8). Callbacks:
+//   q_row(rr)      the global address of tile row rr's D query elements, or
+//                  nullptr (a padding row: zeros)
 //   page_block(t)  block id of the page holding key position t (its range is
-//                checked here: a bad id is flagged and reads as zeros)
-//   CAUSAL, row_pos(rr), min_pos   row rr attends keys <= row_pos(rr);
-//                min_pos is the smallest row_pos of the tile
-//   sink(rr, c0, o, inv_l, m_log2, l)   receives row rr's output columns
-//                [c0, c0 + 32) (un-normalised, times inv_l = 1 / l), called
-//                for every chunk by every softmax thread
-// Returns false when a wait ran out (PA_DEVERR_TIMEOUT is raised).
-template <typename T, int D, bool CAUSAL, typename QRow, typename PageBlock, typename RowPos,
-          typename Sink>
-__device__ __forceinline__ void tc05_attention_cta(
-    uint8_t* smem, const CUtensorMap* tm_k, const CUtensorMap* tm_v, const void* q_base, int g,
-    int Hkv, int bs,
-    int num_blocks, int k_begin, int k_end, int min_pos, float scale_log2, unsigned* err,
-    QRow q_row, PageBlock page_block, RowPos row_pos, Sink sink) {
-  using Ly = PrefixTcLayout<D>;
-  constexpr int KB = Ly::KB;
+//                  checked here: a bad id is flagged and reads as zeros)
+//   row_pos(rr)    CAUSAL: row rr attends keys <= row_pos(rr)
+//   sink(rr, c0, o, inv_l, m_log2, l)   row rr's output columns [c0, c0 + 32)
+//                  (un-normalised; times inv_l = 1 / l), called for every
+//                  chunk by every softmax thread
+template <typename QT, int D, bool CAUSAL, bool I8, typename QRow, typename PageBlock,
+          typename RowPos, typename Sink>
+__device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args& a, QRow q_row,
+                                                   PageBlock page_block, RowPos row_pos,
+                                                   Sink sink) {
+  using Ly = PrefixTcLayout<D, I8>;
+  using T = typename std::conditional<I8, __half, QT>::type;  // MMA operand type
+  constexpr int KB = Ly::KB, ST = Ly::STAGES, RS = Ly::RSTAGES;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-  uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + Ly::OFF_BAR);
-  uint64_t* kv_empty = kv_full + kTcStages;
-  uint64_t* s_full = kv_empty + kTcStages;  // [2]
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + Ly::OFF_BAR);  // [ST] 16-bit: copies done
+  uint64_t* kv_empty = kv_full + ST;        // [ST] P V of the tile done
+  uint64_t* s_full = kv_empty + ST;         // [2]
   uint64_t* s_free = s_full + 2;            // [2]
   uint64_t* p_full = s_free + 2;            // [2]
   uint64_t* pv_done = p_full + 2;           // [2]
+  uint64_t* raw_full = pv_done + 2;         // [RS] INT8: codes and scales landed
+  uint64_t* raw_empty = raw_full + RS;      // [RS] INT8: widened
+  uint64_t* conv_full = raw_empty + RS;     // [ST] INT8: tile widened into slot
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::OFF_MISC);
+  float* sc = reinterpret_cast<float*>(smem + Ly::OFF_SC);  // INT8 row scales of the slots
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ntiles = (k_end - k_begin + kTcTile - 1) / kTcTile;
+  const int ntiles = (a.k_end - a.k_begin + kTcTile - 1) / kTcTile;
+  unsigned* err = a.err;
 
   // ---- set-up: barriers, TMEM, Q rows (asynchronous 16-byte copies, all in
   // flight at once; padding rows zero-filled)
   if (tid == 0) {
-    for (int i = 0; i < kTcStages; ++i) {
+    for (int i = 0; i < ST; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
+      if (I8) mbar_init(&conv_full[i], kTcRows);
+    }
+    for (int i = 0; i < RS; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], kTcRows);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -124,15 +155,31 @@ __device__ __forceinline__ void tc05_attention_cta(
     tmem_alloc(tmem_slot, Ly::TMEM_COLS);
   }
   const uint32_t sq = smem_u32(smem);
-  for (int i = tid; i < kTcRows * KB * 8; i += kTcThreads) {
+  for (int i = tid; i < kTcRows * KB * 8; i += Ly::THREADS) {
     const int rr = i / (KB * 8), c = i % (KB * 8);
     const uint8_t* src = q_row(rr);
     const int kb = c >> 3, ch = c & 7;
     cp_async16(sq + kb * (kTcRows * 128) + rr * 128 + ((ch ^ (rr & 7)) << 4),
-               src ? src + c * 16 : q_base, src != nullptr);
+               src ? src + c * 16 : a.q_base, src != nullptr);
   }
   cp_async_commit();
   cp_async_wait<0>();
+  if constexpr (I8 && std::is_same<QT, __nv_bfloat16>::value) {
+    // q to f16 in place, 16-byte chunk by chunk
+    __syncthreads();
+    for (int i = tid; i < kTcRows * KB * 8; i += Ly::THREADS) {
+      uint4* c = reinterpret_cast<uint4*>(smem + 16 * i);
+      uint4 v = *c;
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+        const __half2 h = __floats2half2_rn(__low2float(b), __high2float(b));
+        w[e] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *c = v;
+    }
+  }
   fence_proxy_async_smem();
   tc05_fence_before();
   __syncthreads();
@@ -142,44 +189,126 @@ __device__ __forceinline__ void tc05_attention_cta(
   bool failed = false;
 
   if (warp == 5) {
-    // ================================================ tensor copies of K/V tiles
+    // ================================================ copies of K/V tiles
     if (lane == 0) {
-      const long long rows = (long long)num_blocks * Hkv * bs;
+      const long long rows = (long long)a.num_blocks * a.Hkv * a.bs;
+      const int bs = a.bs;
       int issued = 0;
       for (int i = 0; i < ntiles; ++i) {
-        const int st = i % kTcStages;
-        if (i >= kTcStages && !mbar_wait_bounded(&kv_empty[st], ((i / kTcStages) - 1) & 1)) {
-          raise_error(err, PA_DEVERR_TIMEOUT);
-          break;
-        }
-        mbar_arrive_expect_tx(&kv_full[st], 2 * Ly::TBYTES);
-        uint8_t* kdst = smem + Ly::OFF_KV + st * 2 * Ly::TBYTES;
-        uint8_t* vdst = kdst + Ly::TBYTES;
-        const int t0 = k_begin + i * kTcTile;
-        for (int pp = 0; pp < kTcTile / bs; ++pp) {
-          const int t = t0 + pp * bs;
-          // pages past the range and bad block ids read as zeros (a box
-          // wholly past the tensor is filled with zeros)
-          int y = static_cast<int>(rows);
-          if (t < k_end) {
-            const int b = page_block(t);
-            if (b >= 0 && b < num_blocks)
-              y = (b * Hkv + g) * bs;
-            else
-              raise_error(err, PA_DEVERR_BLOCK_ID);
+        const int t0 = a.k_begin + i * kTcTile;
+        if constexpr (!I8) {
+          const int st = i % ST;
+          if (i >= ST && !mbar_wait_bounded(&kv_empty[st], ((i / ST) - 1) & 1)) {
+            raise_error(err, PA_DEVERR_TIMEOUT);
+            break;
           }
+          mbar_arrive_expect_tx(&kv_full[st], 2 * Ly::TBYTES);
+          uint8_t* kdst = smem + Ly::OFF_KV + st * 2 * Ly::TBYTES;
+          uint8_t* vdst = kdst + Ly::TBYTES;
+          for (int pp = 0; pp < kTcTile / bs; ++pp) {
+            const int t = t0 + pp * bs;
+            // pages past the range and bad block ids read as zeros (a box
+            // wholly past the tensor is filled with zeros)
+            int y = static_cast<int>(rows);
+            if (t < a.k_end) {
+              const int b = page_block(t);
+              if (b >= 0 && b < a.num_blocks)
+                y = (b * a.Hkv + a.g) * bs;
+              else
+                raise_error(err, PA_DEVERR_BLOCK_ID);
+            }
 #pragma unroll
-          for (int j = 0; j < KB; ++j) {
-            tma_load_2d(kdst + j * (kTcTile * 128) + pp * bs * 128, tm_k, 64 * j, y, &kv_full[st]);
-            tma_load_2d(vdst + j * (kTcTile * 128) + pp * bs * 128, tm_v, 64 * j, y, &kv_full[st]);
+            for (int j = 0; j < KB; ++j) {
+              tma_load_2d(kdst + j * (kTcTile * 128) + pp * bs * 128, a.tm_k, 64 * j, y,
+                          &kv_full[st]);
+              tma_load_2d(vdst + j * (kTcTile * 128) + pp * bs * 128, a.tm_v, 64 * j, y,
+                          &kv_full[st]);
+            }
+          }
+        } else {
+          const int rs = i % RS;
+          if (i >= RS && !mbar_wait_bounded(&raw_empty[rs], ((i / RS) - 1) & 1)) {
+            raise_error(err, PA_DEVERR_TIMEOUT);
+            break;
+          }
+          // pages past the range or with a bad block id are not copied (the
+          // widening writes zeros for their rows)
+          uint32_t bytes = 0;
+          for (int pp = 0; pp < kTcTile / bs; ++pp) {
+            const int t = t0 + pp * bs;
+            if (t < a.k_end) {
+              const int b = page_block(t);
+              if (b >= 0 && b < a.num_blocks)
+                bytes += 2u * bs * (D + 4);
+              else
+                raise_error(err, PA_DEVERR_BLOCK_ID);
+            }
+          }
+          mbar_arrive_expect_tx(&raw_full[rs], bytes);
+          uint8_t* raw = smem + Ly::OFF_RAW + rs * Ly::RAWB;
+          for (int pp = 0; pp < kTcTile / bs; ++pp) {
+            const int t = t0 + pp * bs;
+            if (t >= a.k_end) break;
+            const int b = page_block(t);
+            if (b < 0 || b >= a.num_blocks) continue;
+            const size_t row0 = ((size_t)b * a.Hkv + a.g) * bs;
+            bulk_g2s(raw + pp * bs * D, a.k_codes + row0 * D, bs * D, &raw_full[rs]);
+            bulk_g2s(raw + Ly::RAWT + pp * bs * D, a.v_codes + row0 * D, bs * D, &raw_full[rs]);
+            bulk_g2s(raw + 2 * Ly::RAWT + pp * bs * 4, a.k_scales + row0, bs * 4, &raw_full[rs]);
+            bulk_g2s(raw + 2 * Ly::RAWT + kTcTile * 4 + pp * bs * 4, a.v_scales + row0, bs * 4,
+                     &raw_full[rs]);
           }
         }
         ++issued;
       }
       // never leave with copies in flight
-      for (int k = issued > kTcStages ? issued - kTcStages : 0; k < issued; ++k)
-        if (!mbar_wait_bounded(&kv_full[k % kTcStages], (k / kTcStages) & 1))
+      constexpr int NB_ = I8 ? RS : ST;
+      uint64_t* done = I8 ? raw_full : kv_full;
+      for (int k = issued > NB_ ? issued - NB_ : 0; k < issued; ++k)
+        if (!mbar_wait_bounded(&done[k % NB_], (k / NB_) & 1)) raise_error(err, PA_DEVERR_TIMEOUT);
+    }
+  } else if (warp >= 6) {
+    // ================================================ INT8: widening to f16
+    if constexpr (I8) {
+      const int cid = tid - 6 * 32;  // 0 .. 127
+      const int row = cid & (kTcTile - 1);
+      const bool is_v = cid >= kTcTile;
+      for (int i = 0; i < ntiles; ++i) {
+        const int rs = i % RS, st = i % ST;
+        if (!mbar_wait_bounded(&raw_full[rs], (i / RS) & 1) ||
+            (i >= ST && !mbar_wait_bounded(&kv_empty[st], ((i / ST) - 1) & 1))) {
           raise_error(err, PA_DEVERR_TIMEOUT);
+          break;
+        }
+        const int t = a.k_begin + i * kTcTile + row;
+        bool ok = t < a.k_end;
+        if (ok) {
+          const int b = page_block(t);
+          ok = b >= 0 && b < a.num_blocks;
+        }
+        const uint8_t* raw = smem + Ly::OFF_RAW + rs * Ly::RAWB;
+        const uint8_t* src = raw + (is_v ? Ly::RAWT : 0) + row * D;
+        uint8_t* dst = smem + Ly::OFF_KV + st * 2 * Ly::TBYTES + (is_v ? Ly::TBYTES : 0);
+#pragma unroll
+        for (int k = 0; k < KB * 8; ++k) {
+          const int c = (k + row) & (KB * 8 - 1);  // rotated: rows of a warp hit different banks
+          uint4 out = make_uint4(0u, 0u, 0u, 0u);
+          if (ok) {
+            const uint2 w = *reinterpret_cast<const uint2*>(src + 8 * c);
+            widen8<::pa::I8>(w.x, out.x, out.y);
+            widen8<::pa::I8>(w.y, out.z, out.w);
+          }
+          const int kb = c >> 3, ch = c & 7;
+          *reinterpret_cast<uint4*>(dst + kb * (kTcTile * 128) + row * 128 +
+                                    ((ch ^ (row & 7)) << 4)) = out;
+        }
+        sc[(st * 2 + (is_v ? 1 : 0)) * kTcTile + row] =
+            ok ? reinterpret_cast<const float*>(raw + 2 * Ly::RAWT)[(is_v ? kTcTile : 0) + row]
+               : 0.f;
+        fence_proxy_async_smem();
+        mbar_arrive(&conv_full[st]);
+        mbar_arrive(&raw_empty[rs]);
+      }
     }
   } else if (warp == 4) {
     // ================================================ MMA issue (one thread)
@@ -187,9 +316,10 @@ __device__ __forceinline__ void tc05_attention_cta(
       constexpr uint32_t idesc_s = umma_idesc_f16(kBf16, kTcRows, kTcTile, false);
       constexpr uint32_t idesc_o = umma_idesc_f16(kBf16, kTcRows, D, true);
       const uint32_t skv = smem_u32(smem + Ly::OFF_KV), sp = smem_u32(smem + Ly::OFF_P);
+      uint64_t* ready = I8 ? conv_full : kv_full;
       auto issue_s = [&](int i) -> bool {
-        const int st = i % kTcStages;
-        if (!mbar_wait_bounded(&kv_full[st], (i / kTcStages) & 1)) return false;
+        const int st = i % ST;
+        if (!mbar_wait_bounded(&ready[st], (i / ST) & 1)) return false;
         if (i >= 2 && !mbar_wait_bounded(&s_free[i & 1], ((i >> 1) - 1) & 1)) return false;
         tc05_fence_after();
         const uint32_t kt = skv + st * 2 * Ly::TBYTES;
@@ -212,7 +342,7 @@ __device__ __forceinline__ void tc05_attention_cta(
           break;
         }
         tc05_fence_after();
-        const uint32_t vt = skv + (i % kTcStages) * 2 * Ly::TBYTES + Ly::TBYTES;
+        const uint32_t vt = skv + (i % ST) * 2 * Ly::TBYTES + Ly::TBYTES;
         const uint32_t pa = sp + (i & 1) * Ly::PBYTES;
 #pragma unroll
         for (int kk = 0; kk < kTcTile / 16; ++kk)
@@ -220,7 +350,7 @@ __device__ __forceinline__ void tc05_attention_cta(
                    umma_sdesc_sw128(vt + kk * 2048, kTcTile * 128, 1024), idesc_o,
                    i > 0 || kk > 0);
         umma_commit(&pv_done[i & 1]);
-        if (i + kTcStages < ntiles) umma_commit(&kv_empty[i % kTcStages]);  // a later tile refills it
+        if (i + ST < ntiles) umma_commit(&kv_empty[i % ST]);  // a later tile refills it
       }
       if (!ok) raise_error(err, PA_DEVERR_TIMEOUT);
     }
@@ -251,12 +381,24 @@ __device__ __forceinline__ void tc05_attention_cta(
       // logits in log2 units; keys past the range (a partial last tile) and,
       // causally, past the row's position (tiles that reach the diagonal)
       // are -inf
-      const int t0 = k_begin + i * kTcTile;
-      const int valid = k_end - t0;  // >= 1
+      const int t0 = a.k_begin + i * kTcTile;
+      const int valid = a.k_end - t0;  // >= 1
+      const float* ksc = sc + (i % ST) * 2 * kTcTile;  // INT8: the tile's K, then V row scales
+      if constexpr (I8) {
+        // the scales were written by the widening threads of this slot
+        if (__any_sync(0xffffffffu, !mbar_wait_bounded(&conv_full[i % ST], (i / ST) & 1))) {
+          raise_error(err, PA_DEVERR_TIMEOUT);
+          failed = true;
+          break;
+        }
+      }
       float x[kTcTile];
 #pragma unroll
-      for (int c = 0; c < kTcTile; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]) * scale_log2;
-      if (valid < kTcTile || (CAUSAL && t0 + kTcTile - 1 > min_pos)) {  // CTA-uniform
+      for (int c = 0; c < kTcTile; ++c) {
+        x[c] = __uint_as_float(sr[c >> 5][c & 31]) * a.scale_log2;
+        if constexpr (I8) x[c] *= ksc[c];
+      }
+      if (valid < kTcTile || (CAUSAL && t0 + kTcTile - 1 > a.min_pos)) {  // CTA-uniform
         const int lim = CAUSAL ? min(valid, my_pos - t0 + 1) : valid;
 #pragma unroll
         for (int c = 0; c < kTcTile; ++c) x[c] = c < lim ? x[c] : -INFINITY;
@@ -292,8 +434,8 @@ __device__ __forceinline__ void tc05_attention_cta(
         }
         m = mn;
       }
-      // weights rounded to the input type for the MMA; the running sum takes
-      // the fp32 values
+      // weights rounded to the MMA type (INT8: times the V row scale first);
+      // the running sum takes the fp32 weights
       uint32_t pk[kTcTile / 2];
       float l0 = 0.f, l1 = 0.f;
 #pragma unroll
@@ -301,7 +443,10 @@ __device__ __forceinline__ void tc05_attention_cta(
         const float p0 = ex2_approx(x[c] - m), p1 = ex2_approx(x[c + 1] - m);
         l0 += p0;
         l1 += p1;
-        pk[c / 2] = Mma<T>::pack(p0, p1);
+        if constexpr (I8)
+          pk[c / 2] = Mma<T>::pack(p0 * ksc[kTcTile + c], p1 * ksc[kTcTile + c + 1]);
+        else
+          pk[c / 2] = Mma<T>::pack(p0, p1);
       }
       l += l0 + l1;
       if (i >= 2 &&
@@ -315,10 +460,11 @@ __device__ __forceinline__ void tc05_attention_cta(
       for (int ch = 0; ch < 8; ++ch)
         *reinterpret_cast<uint4*>(pb + ((ch ^ (rr & 7)) << 4)) =
             make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      if (valid < kTcTile) {  // CTA-uniform
+      if (!I8 && valid < kTcTile) {  // CTA-uniform
         // V rows past the range may hold anything (rows past a context can
         // be NaN), and a zero weight times NaN is NaN in the MMA: zero them
-        uint8_t* vt = smem + Ly::OFF_KV + (i % kTcStages) * 2 * Ly::TBYTES + Ly::TBYTES;
+        // (the INT8 widening writes zeros for them already)
+        uint8_t* vt = smem + Ly::OFF_KV + (i % ST) * 2 * Ly::TBYTES + Ly::TBYTES;
         for (int c = rr; c < (kTcTile - valid) * KB * 8; c += kTcRows) {
           const int row = valid + c / (KB * 8), kb = (c / 8) % KB, ch = c % 8;
           *reinterpret_cast<uint4*>(vt + kb * (kTcTile * 128) + row * 128 + ch * 16) =
@@ -364,15 +510,16 @@ __device__ __forceinline__ void tc05_attention_cta(
 // partials (normalised output, maximum in natural-log units, sum) to its
 // slot for pa_reduce.
 template <typename T, int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(PrefixTcLayout<D, false>::THREADS, 1)
     prefix_attention_kernel(const __grid_constant__ PrefixParams p) {
+  constexpr int NT = PrefixTcLayout<D, false>::THREADS;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x;
   const int qt = blockIdx.x, split = blockIdx.y, g = blockIdx.z;
-  const int S = p.num_seqs, Hq = p.num_heads, Hkv = p.num_kv_heads, G = p.group;
+  const int S = p.num_seqs, Hq = p.num_heads, G = p.group;
   const int rows_total = S * G;
   const int t_begin = split * p.tokens_per_split;
   const int t_end = min(p.prefix_tokens, t_begin + p.tokens_per_split);
@@ -384,14 +531,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
     const int nctas = gridDim.x * gridDim.y * gridDim.z;
     for (int s = 1 + cta; s < S; s += nctas)
-      for (int i = tid; i < p.prefix_pages; i += kTcThreads)
+      for (int i = tid; i < p.prefix_pages; i += NT)
         if (p.block_tables[(size_t)s * p.max_blocks_per_seq + i] != p.block_tables[i])
           raise_error(p.err, PA_DEVERR_BLOCK_ID);
-    for (int s = cta * kTcThreads + tid; s < S; s += nctas * kTcThreads)
+    for (int s = cta * NT + tid; s < S; s += nctas * NT)
       if (p.context_lens[s] < p.prefix_tokens) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
   }
   if (t_begin >= t_end) {  // a split with no prefix token: empty partials
-    for (int i = tid; i < kTcRows; i += kTcThreads) {
+    for (int i = tid; i < kTcRows; i += NT) {
       const int r = qt * kTcRows + i;
       if (r < rows_total) {
         const size_t row = (size_t)(r / G) * Hq + g * G + r % G;
@@ -426,10 +573,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       p.exp_sums[(size_t)row * p.num_slots + slot] = l;
     }
   };
-  tc05_attention_cta<T, D, false>(smem, &p.tm_k, &p.tm_v, p.query, g, Hkv, p.block_size,
-                                  p.num_blocks,
-                                  t_begin, t_end, 0, p.scale_log2, p.err, q_row, page_block,
-                                  row_pos, sink);
+  Tc05Args a{};
+  a.tm_k = &p.tm_k;
+  a.tm_v = &p.tm_v;
+  a.q_base = p.query;
+  a.g = g;
+  a.Hkv = p.num_kv_heads;
+  a.bs = p.block_size;
+  a.num_blocks = p.num_blocks;
+  a.k_begin = t_begin;
+  a.k_end = t_end;
+  a.min_pos = 0;
+  a.scale_log2 = p.scale_log2;
+  a.err = p.err;
+  tc05_attention_cta<T, D, false, false>(smem, a, q_row, page_block, row_pos, sink);
 }
 
 // Causal prefill over the paged cache on the tensor cores: one CTA per
@@ -439,17 +596,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // one past its last row's position (kv_end) and masks key t for a row at
 // position pos when t > pos. Every row sees position 0, so its running
 // maximum is finite from the first tile on. Rows past the chunk's take the
-// tile's last position (finite values that are never stored).
-template <typename T, int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+// tile's last position (finite values that are never stored). I8: the cache
+// holds INT8 codes and row scales.
+template <typename QT, int D, bool I8>
+__global__ void __launch_bounds__(PrefixTcLayout<D, I8>::THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
+  constexpr int NT = PrefixTcLayout<D, I8>::THREADS;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x;
   const int qt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
-  const int Hq = p.num_heads, Hkv = p.num_kv_heads, G = p.group, bs = p.block_size;
+  const int Hq = p.num_heads, G = p.group, bs = p.block_size;
   const int MB = p.max_blocks_per_seq;
   const bool reporter = qt == 0 && g == 0 && tid == 0;  // flags a sequence's errors once
 
@@ -463,13 +622,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   const int rows_total = q_len * G;
   if (qt * kTcRows >= rows_total) return;
-  T* out = static_cast<T*>(p.out);
+  QT* out = static_cast<QT*>(p.out);
   if (n < q_len || n > MB * bs) {  // the chunk does not fit its context: zero rows
     if (reporter) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
-    for (int i = tid; i < kTcRows * D; i += kTcThreads) {
+    for (int i = tid; i < kTcRows * D; i += NT) {
       const int r = qt * kTcRows + i / D;
       if (r < rows_total)
-        out[((size_t)(q0 + r / G) * Hq + g * G + r % G) * D + i % D] = Elem<T>::from_f32(0.f);
+        out[((size_t)(q0 + r / G) * Hq + g * G + r % G) * D + i % D] = Elem<QT>::from_f32(0.f);
     }
     return;
   }
@@ -492,20 +651,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto sink = [&](int rr, int c0, const uint32_t(&o)[32], float inv, float, float) {
     const int r = r_first + rr;
     if (r >= rows_total) return;
-    T* dst = out + ((size_t)(q0 + r / G) * Hq + g * G + r % G) * D + c0;
+    QT* dst = out + ((size_t)(q0 + r / G) * Hq + g * G + r % G) * D + c0;
 #pragma unroll
     for (int e = 0; e < 32; e += 8) {
       uint4 v;
-      v.x = Mma<T>::pack(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-      v.y = Mma<T>::pack(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-      v.z = Mma<T>::pack(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-      v.w = Mma<T>::pack(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+      v.x = Mma<QT>::pack(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+      v.y = Mma<QT>::pack(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+      v.z = Mma<QT>::pack(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+      v.w = Mma<QT>::pack(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
       *reinterpret_cast<uint4*>(dst + e) = v;
     }
   };
-  tc05_attention_cta<T, D, true>(smem, &p.tm_k, &p.tm_v, p.query, g, Hkv, bs, p.num_blocks, 0,
-                                 kv_end, pos0 + r_first / G, p.scale_log2, p.err, q_row,
-                                 page_block, row_pos, sink);
+  Tc05Args a{};
+  a.tm_k = &p.tm_k;
+  a.tm_v = &p.tm_v;
+  a.k_codes = p.k_cache;
+  a.v_codes = p.v_cache;
+  a.k_scales = p.k_scales;
+  a.v_scales = p.v_scales;
+  a.q_base = p.query;
+  a.g = g;
+  a.Hkv = p.num_kv_heads;
+  a.bs = bs;
+  a.num_blocks = p.num_blocks;
+  a.k_begin = 0;
+  a.k_end = kv_end;
+  a.min_pos = pos0 + r_first / G;
+  a.scale_log2 = p.scale_log2;
+  a.err = p.err;
+  tc05_attention_cta<QT, D, true, I8>(smem, a, q_row, page_block, row_pos, sink);
 }
 
 __global__ void copy_blocks_kernel(uint8_t* k_cache, uint8_t* v_cache, const int32_t* pairs,
@@ -525,24 +699,24 @@ __global__ void copy_blocks_kernel(uint8_t* k_cache, uint8_t* v_cache, const int
 
 template <typename T, int D>
 cudaError_t launch_prefix(const PrefixParams& p, cudaStream_t st) {
-  const int smem = PrefixTcLayout<D>::SMEM;
+  using Ly = PrefixTcLayout<D, false>;
   auto kern = prefix_attention_kernel<T, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
   if (e != cudaSuccess) return e;
-  const dim3 grid((p.num_seqs * p.group + kPrefixTcRows - 1) / kPrefixTcRows, p.num_prefix_splits,
+  const dim3 grid((p.num_seqs * p.group + kTcRows - 1) / kTcRows, p.num_prefix_splits,
                   p.num_kv_heads);
-  return launch_pdl(kern, grid, dim3(kTcThreads), smem, st, p);
+  return launch_pdl(kern, grid, dim3(Ly::THREADS), Ly::SMEM, st, p);
 }
 
-template <typename T, int D>
+template <typename QT, int D, bool I8>
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t st) {
-  const int smem = PrefixTcLayout<D>::SMEM;
-  auto kern = prefill_tc_kernel<T, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  using Ly = PrefixTcLayout<D, I8>;
+  auto kern = prefill_tc_kernel<QT, D, I8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
   if (e != cudaSuccess) return e;
   const long long tiles = ((long long)p.max_q_len * p.group + kTcRows - 1) / kTcRows;
   const dim3 grid(static_cast<unsigned>(tiles), p.num_kv_heads, p.num_seqs);
-  return launch_pdl(kern, grid, dim3(kTcThreads), smem, st, p);
+  return launch_pdl(kern, grid, dim3(Ly::THREADS), Ly::SMEM, st, p);
 }
 
 }  // namespace
@@ -558,14 +732,28 @@ cudaError_t launch_prefix_attention(const PrefixParams& p, int dtype, cudaStream
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_prefill_attention(const PrefillParams& p, int dtype, cudaStream_t st) {
-  if (dtype == PA_BF16) {
-    if (p.head_dim == 64) return launch_prefill<__nv_bfloat16, 64>(p, st);
-    if (p.head_dim == 128) return launch_prefill<__nv_bfloat16, 128>(p, st);
-  } else if (dtype == PA_F16) {
-    if (p.head_dim == 64) return launch_prefill<__half, 64>(p, st);
-    if (p.head_dim == 128) return launch_prefill<__half, 128>(p, st);
+cudaError_t launch_prefill_attention(const PrefillParams& p, int dtype, bool int8,
+                                     cudaStream_t st) {
+#define PA_PREFILL_D(QT_, I8_)                                       \
+  switch (p.head_dim) {                                              \
+    case 64: return launch_prefill<QT_, 64, I8_>(p, st);             \
+    case 128: return launch_prefill<QT_, 128, I8_>(p, st);           \
+    default: return cudaErrorInvalidValue;                           \
   }
+  if (dtype == PA_BF16) {
+    if (int8) {
+      PA_PREFILL_D(__nv_bfloat16, true)
+    } else {
+      PA_PREFILL_D(__nv_bfloat16, false)
+    }
+  } else if (dtype == PA_F16) {
+    if (int8) {
+      PA_PREFILL_D(__half, true)
+    } else {
+      PA_PREFILL_D(__half, false)
+    }
+  }
+#undef PA_PREFILL_D
   return cudaErrorInvalidValue;
 }
 

@@ -71,14 +71,18 @@ struct PrefillParams {
   const int32_t* block_tables;  // [S][MB]
   const int32_t* cu_q;          // [S + 1]: query token offsets
   const int32_t* context_lens;  // [S]: context length including the chunk
+  const float* k_scales;        // INT8 caches: row scales [NB][Hkv][bs] (else unused)
+  const float* v_scales;
   unsigned* err;
   int num_seqs, num_heads, num_kv_heads, group, head_dim, block_size, num_blocks;
   int num_tokens, max_blocks_per_seq, max_q_len;
   float scale_log2;  // scale * log2(e)
 };
 
-// dtype: 1 = bf16, 2 = f16. Head dims 64 and 128 are built.
-cudaError_t launch_prefill_attention(const PrefillParams& p, int dtype, cudaStream_t stream);
+// dtype: 1 = bf16, 2 = f16 (the query's; the cache's too unless int8, an
+// INT8 cache with row scales). Head dims 64 and 128 are built.
+cudaError_t launch_prefill_attention(const PrefillParams& p, int dtype, bool int8,
+                                     cudaStream_t stream);
 
 // Copies whole blocks (all kv heads, K and V) src -> dst for each pair of
 // block_pairs [n][2]; block ids outside [0, num_blocks) set PA_DEVERR_BLOCK_ID

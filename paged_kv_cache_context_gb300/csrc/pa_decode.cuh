@@ -797,28 +797,6 @@ struct Tc8State {
 
 __device__ __forceinline__ int tc8_row(int i) { return i < 4 ? i : i ^ 1; }
 
-// Four codes of w as two f16x2 words (bytes 0, 1 -> lo; bytes 2, 3 -> hi).
-template <typename CT>
-__device__ __forceinline__ void widen8(uint32_t w, uint32_t& lo, uint32_t& hi);
-template <>
-__device__ __forceinline__ void widen8<E4M3>(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  asm("{\n\t.reg .b16 l16, h16;\n\tmov.b32 {l16, h16}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, l16;\n\tcvt.rn.f16x2.e4m3x2 %1, h16;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
-}
-template <>
-__device__ __forceinline__ void widen8<I8>(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  // u = c + 128 per byte; 0x6400 | u is the f16 1024 + u, exactly
-  const uint32_t u = w ^ 0x80808080u;
-  const __half2 bias = __floats2half2_rn(1152.f, 1152.f);
-  uint32_t a = __byte_perm(u, 0x64646464u, 0x5140), b = __byte_perm(u, 0x64646464u, 0x7362);
-  const __half2 x = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
-  const __half2 y = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
-  lo = *reinterpret_cast<const uint32_t*>(&x);
-  hi = *reinterpret_cast<const uint32_t*>(&y);
-}
-
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));

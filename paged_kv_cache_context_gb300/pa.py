@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
             "pa_reshape_and_cache_int8": [P, P, P, P, P, P, P, I, I, I, I, I, I, P],
             "pa_decode_int8": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, Z, P],
             "pa_prefill": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P],
+            "pa_prefill_int8": [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P],
             "pa_decode_static_scratch": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F,
                                          F, P],
             "pa_get_device_error": [P, P],
@@ -293,6 +294,36 @@ def prefill(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
                             _ptr(block_tables), _ptr(cu_q), _ptr(context_lens), T, S, Hq,
                             num_kv_heads, D, bs, NB, MB, max_q_len, scale, _DTYPE[query.dtype],
                             _stream(stream)), "pa_prefill")
+
+
+def prefill_int8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+                 v_cache: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor,
+                 block_tables: torch.Tensor, cu_q: torch.Tensor, context_lens: torch.Tensor,
+                 num_kv_heads: int, max_q_len: int, scale: float, stream=None):
+    """pa_prefill_int8: pa_prefill over an INT8 cache with per-row scales."""
+    _on_device(out=out, query=query, k_cache=k_cache, v_cache=v_cache, k_scales=k_scales,
+               v_scales=v_scales, block_tables=block_tables, cu_q=cu_q,
+               context_lens=context_lens)
+    _need(query.dim() == 3, "query: expected [num_tokens, num_heads, head_dim]")
+    _shape("out", out, query.shape)
+    _dtype("out", out, query.dtype)
+    _check_caches(k_cache, v_cache, num_kv_heads, query.shape[2], torch.int8)
+    _check_scales(k_scales, v_scales, k_cache)
+    _need(block_tables.dim() == 2, "block_tables: expected [num_seqs, max_blocks_per_seq]")
+    _dtype("block_tables", block_tables, torch.int32)
+    S = block_tables.shape[0]
+    _shape("cu_q", cu_q, (S + 1,))
+    _dtype("cu_q", cu_q, torch.int32)
+    _shape("context_lens", context_lens, (S,))
+    _dtype("context_lens", context_lens, torch.int32)
+    T, Hq, D = query.shape
+    NB, _, bs, _ = k_cache.shape
+    S, MB = block_tables.shape
+    _check(lib().pa_prefill_int8(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(k_scales), _ptr(v_scales), _ptr(block_tables), _ptr(cu_q),
+                                 _ptr(context_lens), T, S, Hq, num_kv_heads, D, bs, NB, MB,
+                                 max_q_len, scale, _DTYPE[query.dtype], _stream(stream)),
+           "pa_prefill_int8")
 
 
 def decode_plan(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
