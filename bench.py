@@ -618,16 +618,27 @@ def run_prefill(args, rank, local_rank, world):
         raise SystemExit("--path prefill needs a bf16/f16 workload without a window")
     S, Hq, Hkv, D, bs = (case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim,
                          case.block_size)
+    int8 = args.prefill_int8
+    if int8:
+        case = dataclasses.replace(case, kv_dtype="int8")
     bt = case.block_tables.to(dev)
     cl = case.context_lens.to(dev)
     kc, vc = wl.empty_caches(case, device=str(dev))
+    ks, vs = wl.empty_scales(case, device=str(dev)) if int8 else (None, None)
     for seq, pos, key, val in [(case.pre_seq[a:b], case.pre_pos[a:b], case.pre_key[a:b],
                                 case.pre_value[a:b]) for a, b in case.pre_chunks if b > a] + \
             [(None, case.new_pos, case.new_key, case.new_value)]:
         sm = torch.empty(pos.numel(), dtype=torch.int64, device=dev)
         pa.slot_mapping(sm, bt, None if seq is None else seq.to(dev), pos.to(dev), bs, 0)
-        pa.reshape_and_cache(key.to(dev).contiguous(), val.to(dev).contiguous(), kc, vc, sm)
-    reps = [(kc, vc)] + [(kc.clone(), vc.clone()) for _ in range(args.replicas - 1)]
+        if int8:
+            pa.reshape_and_cache_int8(key.to(dev).contiguous(), val.to(dev).contiguous(), kc, vc,
+                                      ks, vs, sm)
+        else:
+            pa.reshape_and_cache(key.to(dev).contiguous(), val.to(dev).contiguous(), kc, vc, sm)
+    reps = [(kc, vc, ks, vs)] + [(kc.clone(), vc.clone(),
+                                  None if ks is None else ks.clone(),
+                                  None if vs is None else vs.clone())
+                                 for _ in range(args.replicas - 1)]
     query, q_seq, q_pos = wl.prefill_queries(case, args.prefill_tokens, seed=7001)
     q_lens = [int((q_seq == s_).sum()) for s_ in range(S)]
     cu = torch.tensor([0] + list(torch.cumsum(torch.tensor(q_lens), 0).tolist()),
@@ -638,12 +649,20 @@ def run_prefill(args, rank, local_rank, world):
     cud = cu.to(dev)
     out = torch.empty(T, Hq, D, dtype=case.q_dtype, device=dev)
     flops = 4.0 * D * Hq * float((q_pos.to(torch.int64) + 1).sum())
-    elem = torch.finfo(case.q_dtype).bits // 8
-    kv_bytes = sum(-(-int(n) // bs) for n in case.context_lens.tolist()) * bs * Hkv * D * 2 * elem
+    elem = 1 if int8 else torch.finfo(case.q_dtype).bits // 8
+    kv_bytes = sum(-(-int(n) // bs) for n in case.context_lens.tolist()) * bs * Hkv * 2 * \
+        (D * elem + (4 if int8 else 0))
+
+    def run(i, q_, bt_, cu_, cl_):
+        k_, v_, ks_, vs_ = reps[i % len(reps)]
+        if int8:
+            pa.prefill_int8(out, q_, k_, v_, ks_, vs_, bt_, cu_, cl_, Hkv, max_q, case.scale,
+                            stream=stream)
+        else:
+            pa.prefill(out, q_, k_, v_, bt_, cu_, cl_, Hkv, max_q, case.scale, stream=stream)
 
     def launch(i):
-        k_, v_ = reps[i % len(reps)]
-        pa.prefill(out, qd, k_, v_, bt, cud, cl, Hkv, max_q, case.scale, stream=stream)
+        run(i, qd, bt, cud, cl)
 
     for i in range(args.warmup):
         launch(i)
@@ -695,9 +714,7 @@ def run_prefill(args, rank, local_rank, world):
     def e2e_step(i):
         for n, t in host.items():
             dbuf[n].copy_(t, non_blocking=True)
-        k_, v_ = reps[i % len(reps)]
-        pa.prefill(out, dbuf["q"], k_, v_, dbuf["bt"], dbuf["cu"], dbuf["cl"], Hkv, max_q,
-                   case.scale, stream=stream)
+        run(i, dbuf["q"], dbuf["bt"], dbuf["cu"], dbuf["cl"])
         out_h.copy_(out, non_blocking=True)
 
     for i in range(args.warmup):
@@ -716,7 +733,9 @@ def run_prefill(args, rank, local_rank, world):
         "warmup": args.warmup, "ms_per_step": round(elapsed / K * 1e3, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "impl": "ours",
-        "config": {"workload": args.workload, "path": "prefill", "num_seqs": S,
+        "config": {"workload": args.workload, "path": "prefill",
+                   "cache_dtype": "int8" if int8 else str(case.q_dtype).replace("torch.", ""),
+                   "num_seqs": S,
                    "num_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "block_size": bs,
                    "query_tokens": T, "max_q_len": max_q, "flops_per_step": flops,
                    "kv_bytes_per_step": kv_bytes,
@@ -724,8 +743,10 @@ def run_prefill(args, rank, local_rank, world):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_tf,
                      "peak_kind": peak_kind, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tf, 4),
-                     "traffic": measured_traffic(f"{args.workload}/prefill"),
-                     "kernel": "prefill_attention_kernel (mma.sync m16n8k16, bf16 in, fp32 acc)",
+                     "traffic": measured_traffic(f"{args.workload}/prefill" +
+                                                 ("_int8" if int8 else "")),
+                     "kernel": "prefill_tc_kernel (tcgen05 kind::f16, TMEM accumulators" +
+                               (", INT8 codes widened to f16 in shared memory)" if int8 else ")"),
                      "kernel_us_mean": round(per * 1e6, 2)},
         "e2e": {"value": round(flops_all / e2e_t / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
@@ -737,13 +758,15 @@ def run_prefill(args, rank, local_rank, world):
     elif rank == 0:
         import oracle  # test infrastructure: only this CPU-baseline leg uses it
         ko, vo = kc.cpu(), vc.cpu()
-        n_rows = 0
+        kso = None if ks is None else ks.cpu()
+        vso = None if vs is None else vs.cpu()
         pick = torch.nonzero(q_seq == 0).flatten()[:64]
         tq = time.perf_counter()
         reps_o = 0
         while time.perf_counter() - tq < 10.0 and reps_o < 50:
             oracle.prefill(query[pick], q_seq[pick], q_pos[pick], ko, vo, case.block_tables, Hkv,
-                           bs, case.scale)
+                           bs, case.scale, "int8" if int8 else "auto", k_scales=kso,
+                           v_scales=vso)
             reps_o += 1
         t_o = (time.perf_counter() - tq) / reps_o
         f_o = 4.0 * D * Hq * float((q_pos[pick].to(torch.int64) + 1).sum())
@@ -803,6 +826,9 @@ def main(argv=None):
                     help="leave out the oracle timing (for profiler runs of the same line)")
     ap.add_argument("--prefill-tokens", type=int, default=512,
                     help="--path prefill: query tokens per sequence (its last positions)")
+    ap.add_argument("--prefill-int8", action="store_true",
+                    help="with --path prefill: the cache held as INT8 codes with row scales "
+                         "(pa_prefill_int8)")
     ap.add_argument("--path", choices=("balanced", "cascade", "int8", "prefill"),
                     default="balanced",
                     help="entry point timed: pa_decode's balanced path, "
