@@ -996,7 +996,7 @@ PA_API pa_status pa_prefill_int8(void* out, const void* query, const int8_t* k_c
 // number of splits never decreases as sms grows, so a workspace sized for
 // kPlanSMs holds the plan of any device with at most that many SMs.
 static void cascade_plan(int S, int G, int Hkv, int prefix_tokens, int sms, int* nsp, int* tps) {
-  const int qtiles = (S * G + kPrefixTcRows - 1) / kPrefixTcRows;
+  const int qtiles = (S * G + kPrefixCtaRows - 1) / kPrefixCtaRows;
   const int tiles = (prefix_tokens + kPrefixTile - 1) / kPrefixTile;
   const int64_t want = (int64_t)sms / ((int64_t)qtiles * Hkv);
   int n = static_cast<int>(want < 1 ? 1 : (want > tiles ? tiles : want));

@@ -55,27 +55,37 @@ constexpr int kTcTile = kPrefixTile;
 #define PA_PREFIX_STAGES 4
 #endif
 
-template <int D, bool I8>
+template <int D, bool I8, int QTILES>
 struct PrefixTcLayout {
   static constexpr int KB = D / 64;                  // 128-byte column blocks of a row
-  static constexpr int STAGES = I8 ? 3 : PA_PREFIX_STAGES;  // f16/bf16 K/V tiles
+  // 128-row query tiles per CTA (two share every K/V tile; an INT8 cache's
+  // raw ring leaves room for one)
+  static constexpr int QTL = QTILES;
+  static_assert(QTL == 1 || (QTL == 2 && !I8), "query tiles per CTA");
+  static constexpr int ROWS = QTL * kTcRows;          // query rows per CTA
+  static constexpr int SMX = 4 * QTL;                 // softmax warps (one thread per row)
+  static constexpr int MMA_WARP = SMX, COPY_WARP = SMX + 1, CONV_WARP = SMX + 2;
+  static constexpr int THREADS = (SMX + 2 + (I8 ? 4 : 0)) * 32;
+  static constexpr int STAGES = I8 ? 3 : (QTL == 2 && D == 128 ? 3 : PA_PREFIX_STAGES);
   static constexpr int RSTAGES = I8 ? 2 : 0;         // raw INT8 tiles
-  static constexpr int THREADS = I8 ? 320 : 192;
-  static constexpr int QBYTES = KB * kTcRows * 128;  // Q: [KB][128 rows][128 B]
+  static constexpr int QBYTES1 = KB * kTcRows * 128;  // one Q tile: [KB][128 rows][128 B]
+  static constexpr int QBYTES = QTL * QBYTES1;
   static constexpr int TBYTES = KB * kTcTile * 128;  // one K or V tile: [KB][64 tokens][128 B]
-  static constexpr int PBYTES = kTcRows * 128;       // P: [128 rows][64 tokens = 128 B]
+  static constexpr int PBYTES = kTcRows * 128;       // P of one Q tile: [128 rows][64 tokens]
   static constexpr int RAWT = kTcTile * D;           // INT8 codes of one K or V tile
   static constexpr int RAWB = 2 * RAWT + 2 * kTcTile * 4;  // codes + row scales
   static constexpr int OFF_KV = QBYTES;
-  static constexpr int OFF_P = OFF_KV + STAGES * 2 * TBYTES;
-  static constexpr int OFF_SC = OFF_P + 2 * PBYTES;  // INT8: [STAGES][K, V][64] row scales
+  static constexpr int OFF_P = OFF_KV + STAGES * 2 * TBYTES;  // [2 buffers][QTL][PBYTES]
+  static constexpr int OFF_SC = OFF_P + 2 * QTL * PBYTES;  // INT8: [STAGES][K, V][64] row scales
   static constexpr int OFF_RAW = OFF_SC + (I8 ? STAGES * 2 * kTcTile * 4 : 0);
   static constexpr int OFF_BAR = OFF_RAW + RSTAGES * RAWB;
   static constexpr int NBAR = 2 * STAGES + 8 + (I8 ? 2 * RSTAGES + STAGES : 0);
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + alignment of the base to 1024
-  static constexpr uint32_t TMEM_COLS = 256;         // S: 2 x 64, O: D
-  static_assert(2 * kTcTile + D <= 256, "TMEM columns");
+  // TMEM columns: S of tile q, buffer b at q 128 + b 64; O of tile q at
+  // QTL 128 + q D
+  static constexpr uint32_t TMEM_COLS = QTL * (2 * kTcTile + D) <= 256 ? 256 : 512;
+  static_assert(QTL * (2 * kTcTile + D) <= 512, "TMEM columns");
   static_assert(OFF_RAW % 16 == 0 && RAWB % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -106,14 +116,14 @@ struct Tc05Args {
 //   sink(rr, c0, o, inv_l, m_log2, l)   row rr's output columns [c0, c0 + 32)
 //                  (un-normalised; times inv_l = 1 / l), called for every
 //                  chunk by every softmax thread
-template <typename QT, int D, bool CAUSAL, bool I8, typename QRow, typename PageBlock,
-          typename RowPos, typename Sink>
+template <typename QT, int D, bool CAUSAL, bool I8, int QTILES, typename QRow,
+          typename PageBlock, typename RowPos, typename Sink>
 __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args& a, QRow q_row,
                                                    PageBlock page_block, RowPos row_pos,
                                                    Sink sink) {
-  using Ly = PrefixTcLayout<D, I8>;
+  using Ly = PrefixTcLayout<D, I8, QTILES>;
   using T = typename std::conditional<I8, __half, QT>::type;  // MMA operand type
-  constexpr int KB = Ly::KB, ST = Ly::STAGES, RS = Ly::RSTAGES;
+  constexpr int KB = Ly::KB, ST = Ly::STAGES, RS = Ly::RSTAGES, QTL = Ly::QTL, ROWS = Ly::ROWS;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + Ly::OFF_BAR);  // [ST] 16-bit: copies done
   uint64_t* kv_empty = kv_full + ST;        // [ST] P V of the tile done
@@ -144,22 +154,22 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], kTcRows);
-      mbar_init(&p_full[i], kTcRows);
+      mbar_init(&s_free[i], ROWS);
+      mbar_init(&p_full[i], ROWS);
       mbar_init(&pv_done[i], 1);
     }
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == Ly::MMA_WARP) {
     __syncwarp();
     tmem_alloc(tmem_slot, Ly::TMEM_COLS);
   }
   const uint32_t sq = smem_u32(smem);
-  for (int i = tid; i < kTcRows * KB * 8; i += Ly::THREADS) {
+  for (int i = tid; i < ROWS * KB * 8; i += Ly::THREADS) {
     const int rr = i / (KB * 8), c = i % (KB * 8);
     const uint8_t* src = q_row(rr);
-    const int kb = c >> 3, ch = c & 7;
-    cp_async16(sq + kb * (kTcRows * 128) + rr * 128 + ((ch ^ (rr & 7)) << 4),
+    const int q = rr / kTcRows, r1 = rr % kTcRows, kb = c >> 3, ch = c & 7;
+    cp_async16(sq + q * Ly::QBYTES1 + kb * (kTcRows * 128) + r1 * 128 + ((ch ^ (r1 & 7)) << 4),
                src ? src + c * 16 : a.q_base, src != nullptr);
   }
   cp_async_commit();
@@ -167,7 +177,7 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
   if constexpr (I8 && std::is_same<QT, __nv_bfloat16>::value) {
     // q to f16 in place, 16-byte chunk by chunk
     __syncthreads();
-    for (int i = tid; i < kTcRows * KB * 8; i += Ly::THREADS) {
+    for (int i = tid; i < ROWS * KB * 8; i += Ly::THREADS) {
       uint4* c = reinterpret_cast<uint4*>(smem + 16 * i);
       uint4 v = *c;
       uint32_t* w = reinterpret_cast<uint32_t*>(&v);
@@ -185,10 +195,10 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
   __syncthreads();
   tc05_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s = tmem, t_o = tmem + 2 * kTcTile;  // S buffers at columns 0 / 64, O at 128
+  const uint32_t t_s = tmem, t_o = tmem + QTL * 2 * kTcTile;  // S of tile q at q 128, O at QTL 128
   bool failed = false;
 
-  if (warp == 5) {
+  if (warp == Ly::COPY_WARP) {
     // ================================================ copies of K/V tiles
     if (lane == 0) {
       const long long rows = (long long)a.num_blocks * a.Hkv * a.bs;
@@ -267,10 +277,10 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
       for (int k = issued > NB_ ? issued - NB_ : 0; k < issued; ++k)
         if (!mbar_wait_bounded(&done[k % NB_], (k / NB_) & 1)) raise_error(err, PA_DEVERR_TIMEOUT);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= Ly::CONV_WARP) {
     // ================================================ INT8: widening to f16
     if constexpr (I8) {
-      const int cid = tid - 6 * 32;  // 0 .. 127
+      const int cid = tid - Ly::CONV_WARP * 32;  // 0 .. 127
       const int row = cid & (kTcTile - 1);
       const bool is_v = cid >= kTcTile;
       for (int i = 0; i < ntiles; ++i) {
@@ -310,7 +320,7 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
         mbar_arrive(&raw_empty[rs]);
       }
     }
-  } else if (warp == 4) {
+  } else if (warp == Ly::MMA_WARP) {
     // ================================================ MMA issue (one thread)
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma_idesc_f16(kBf16, kTcRows, kTcTile, false);
@@ -324,12 +334,14 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
         tc05_fence_after();
         const uint32_t kt = skv + st * 2 * Ly::TBYTES;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qa = sq + (kk >> 2) * (kTcRows * 128) + (kk & 3) * 32;
-          const uint32_t kbd = kt + (kk >> 2) * (kTcTile * 128) + (kk & 3) * 32;
-          umma_f16(t_s + (i & 1) * kTcTile, umma_sdesc_sw128(qa, 16, 1024),
-                   umma_sdesc_sw128(kbd, 16, 1024), idesc_s, kk > 0);
-        }
+        for (int q = 0; q < QTL; ++q)
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t qa = sq + q * Ly::QBYTES1 + (kk >> 2) * (kTcRows * 128) + (kk & 3) * 32;
+            const uint32_t kbd = kt + (kk >> 2) * (kTcTile * 128) + (kk & 3) * 32;
+            umma_f16(t_s + q * 2 * kTcTile + (i & 1) * kTcTile, umma_sdesc_sw128(qa, 16, 1024),
+                     umma_sdesc_sw128(kbd, 16, 1024), idesc_s, kk > 0);
+          }
         umma_commit(&s_full[i & 1]);
         return true;
       };
@@ -343,12 +355,15 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
         }
         tc05_fence_after();
         const uint32_t vt = skv + (i % ST) * 2 * Ly::TBYTES + Ly::TBYTES;
-        const uint32_t pa = sp + (i & 1) * Ly::PBYTES;
 #pragma unroll
-        for (int kk = 0; kk < kTcTile / 16; ++kk)
-          umma_f16(t_o, umma_sdesc_sw128(pa + kk * 32, 16, 1024),
-                   umma_sdesc_sw128(vt + kk * 2048, kTcTile * 128, 1024), idesc_o,
-                   i > 0 || kk > 0);
+        for (int q = 0; q < QTL; ++q) {
+          const uint32_t pa = sp + ((i & 1) * QTL + q) * Ly::PBYTES;
+#pragma unroll
+          for (int kk = 0; kk < kTcTile / 16; ++kk)
+            umma_f16(t_o + q * D, umma_sdesc_sw128(pa + kk * 32, 16, 1024),
+                     umma_sdesc_sw128(vt + kk * 2048, kTcTile * 128, 1024), idesc_o,
+                     i > 0 || kk > 0);
+        }
         umma_commit(&pv_done[i & 1]);
         if (i + ST < ntiles) umma_commit(&kv_empty[i % ST]);  // a later tile refills it
       }
@@ -358,12 +373,15 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
     // ================================================ softmax, one row per thread
     // (tcgen05.ld / st are warp-wide: every decision that leads to one is
     // taken by the whole warp)
-    const int rr = tid;  // 0 .. 127 = TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int rr = tid;             // the CTA's row
+    const int q = rr / kTcRows;     // its query tile
+    const int r1 = rr % kTcRows;    // its TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_sq = t_s + q * 2 * kTcTile, t_oq = t_o + q * D;
     constexpr float kLazy = 8.f;
     const int my_pos = CAUSAL ? row_pos(rr) : 0;
     float m = -INFINITY, l = 0.f;
-    uint8_t* prow = smem + Ly::OFF_P + rr * 128;
+    uint8_t* prow = smem + Ly::OFF_P + q * Ly::PBYTES + r1 * 128;
     for (int i = 0; i < ntiles; ++i) {
       if (__any_sync(0xffffffffu, !mbar_wait_bounded(&s_full[i & 1], (i >> 1) & 1))) {
         raise_error(err, PA_DEVERR_TIMEOUT);
@@ -373,8 +391,8 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
       tc05_fence_after();
       __syncwarp();
       uint32_t sr[2][32];
-      tmem_ld32(t_s + (i & 1) * kTcTile + lane_off, sr[0]);
-      tmem_ld32(t_s + (i & 1) * kTcTile + 32 + lane_off, sr[1]);
+      tmem_ld32(t_sq + (i & 1) * kTcTile + lane_off, sr[0]);
+      tmem_ld32(t_sq + (i & 1) * kTcTile + 32 + lane_off, sr[1]);
       tmem_wait_ld();
       tc05_fence_before();
       mbar_arrive(&s_free[i & 1]);
@@ -423,11 +441,11 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
-            tmem_ld32(t_o + c0 + lane_off, o);
+            tmem_ld32(t_oq + c0 + lane_off, o);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * al);
-            tmem_st32(t_o + c0 + lane_off, o);
+            tmem_st32(t_oq + c0 + lane_off, o);
           }
           tmem_wait_st();
           l *= al;
@@ -455,17 +473,17 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
         failed = true;
         break;
       }
-      uint8_t* pb = prow + (i & 1) * Ly::PBYTES;
+      uint8_t* pb = prow + (i & 1) * QTL * Ly::PBYTES;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(pb + ((ch ^ (rr & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(pb + ((ch ^ (r1 & 7)) << 4)) =
             make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
       if (!I8 && valid < kTcTile) {  // CTA-uniform
         // V rows past the range may hold anything (rows past a context can
         // be NaN), and a zero weight times NaN is NaN in the MMA: zero them
         // (the INT8 widening writes zeros for them already)
         uint8_t* vt = smem + Ly::OFF_KV + (i % ST) * 2 * Ly::TBYTES + Ly::TBYTES;
-        for (int c = rr; c < (kTcTile - valid) * KB * 8; c += kTcRows) {
+        for (int c = rr; c < (kTcTile - valid) * KB * 8; c += ROWS) {
           const int row = valid + c / (KB * 8), kb = (c / 8) % KB, ch = c % 8;
           *reinterpret_cast<uint4*>(vt + kb * (kTcTile * 128) + row * 128 + ch * 16) =
               make_uint4(0u, 0u, 0u, 0u);
@@ -488,7 +506,7 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
-        tmem_ld32(t_o + c0 + lane_off, o);
+        tmem_ld32(t_oq + c0 + lane_off, o);
         tmem_wait_ld();
         sink(rr, c0, o, inv, m, l);
       }
@@ -498,7 +516,7 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
   tc05_fence_before();
   __syncthreads();
   tc05_fence_after();
-  if (warp == 4) {
+  if (warp == Ly::MMA_WARP) {
     __syncwarp();
     tmem_dealloc(tmem, Ly::TMEM_COLS);
   }
@@ -510,9 +528,10 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
 // partials (normalised output, maximum in natural-log units, sum) to its
 // slot for pa_reduce.
 template <typename T, int D>
-__global__ void __launch_bounds__(PrefixTcLayout<D, false>::THREADS, 1)
+__global__ void __launch_bounds__(PrefixTcLayout<D, false, 1>::THREADS, 1)
     prefix_attention_kernel(const __grid_constant__ PrefixParams p) {
-  constexpr int NT = PrefixTcLayout<D, false>::THREADS;
+  constexpr int NT = PrefixTcLayout<D, false, 1>::THREADS, ROWS = PrefixTcLayout<D, false, 1>::ROWS;
+  static_assert(ROWS == kPrefixCtaRows, "the host's plan counts rows per CTA");
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   pdl_wait();
@@ -538,8 +557,8 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, false>::THREADS, 1)
       if (p.context_lens[s] < p.prefix_tokens) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
   }
   if (t_begin >= t_end) {  // a split with no prefix token: empty partials
-    for (int i = tid; i < kTcRows; i += NT) {
-      const int r = qt * kTcRows + i;
+    for (int i = tid; i < ROWS; i += NT) {
+      const int r = qt * ROWS + i;
       if (r < rows_total) {
         const size_t row = (size_t)(r / G) * Hq + g * G + r % G;
         p.max_logits[row * p.num_slots + slot] = -INFINITY;
@@ -549,7 +568,7 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, false>::THREADS, 1)
     return;
   }
   auto row_of = [&](int rr) -> long long {
-    const int r = qt * kTcRows + rr;
+    const int r = qt * ROWS + rr;
     return r < rows_total ? (long long)(r / G) * Hq + g * G + r % G : -1;
   };
   auto q_row = [&](int rr) -> const uint8_t* {
@@ -586,11 +605,11 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, false>::THREADS, 1)
   a.min_pos = 0;
   a.scale_log2 = p.scale_log2;
   a.err = p.err;
-  tc05_attention_cta<T, D, false, false>(smem, a, q_row, page_block, row_pos, sink);
+  tc05_attention_cta<T, D, false, false, 1>(smem, a, q_row, page_block, row_pos, sink);
 }
 
 // Causal prefill over the paged cache on the tensor cores: one CTA per
-// (128-row query tile, kv head, sequence). The CTA's rows are (token,
+// (query tile of 256 rows, 128 with an INT8 cache; kv head; sequence). The CTA's rows are (token,
 // head-in-group) pairs r = i G + j of one sequence's chunk, token i at
 // position n - q_len + i; it streams that sequence's pages from position 0 to
 // one past its last row's position (kv_end) and masks key t for a row at
@@ -599,9 +618,10 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, false>::THREADS, 1)
 // tile's last position (finite values that are never stored). I8: the cache
 // holds INT8 codes and row scales.
 template <typename QT, int D, bool I8>
-__global__ void __launch_bounds__(PrefixTcLayout<D, I8>::THREADS, 1)
+__global__ void __launch_bounds__(PrefixTcLayout<D, I8, I8 ? 1 : 2>::THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
-  constexpr int NT = PrefixTcLayout<D, I8>::THREADS;
+  using Ly = PrefixTcLayout<D, I8, I8 ? 1 : 2>;
+  constexpr int NT = Ly::THREADS, ROWS = Ly::ROWS;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   pdl_wait();
@@ -621,20 +641,20 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, I8>::THREADS, 1)
     return;  // offsets that do not fit the batch: nothing of this sequence is written
   }
   const int rows_total = q_len * G;
-  if (qt * kTcRows >= rows_total) return;
+  if (qt * ROWS >= rows_total) return;
   QT* out = static_cast<QT*>(p.out);
   if (n < q_len || n > MB * bs) {  // the chunk does not fit its context: zero rows
     if (reporter) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
-    for (int i = tid; i < kTcRows * D; i += NT) {
-      const int r = qt * kTcRows + i / D;
+    for (int i = tid; i < ROWS * D; i += NT) {
+      const int r = qt * ROWS + i / D;
       if (r < rows_total)
         out[((size_t)(q0 + r / G) * Hq + g * G + r % G) * D + i % D] = Elem<QT>::from_f32(0.f);
     }
     return;
   }
   const int pos0 = n - q_len;  // position of the chunk's first token
-  const int r_first = qt * kTcRows;
-  const int r_last = min(r_first + kTcRows, rows_total) - 1;
+  const int r_first = qt * ROWS;
+  const int r_last = min(r_first + ROWS, rows_total) - 1;
   const int kv_end = pos0 + r_last / G + 1;  // keys this CTA needs: positions [0, kv_end)
   const int32_t* table = p.block_tables + (size_t)s * MB;
   auto q_row = [&](int rr) -> const uint8_t* {
@@ -679,7 +699,7 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, I8>::THREADS, 1)
   a.min_pos = pos0 + r_first / G;
   a.scale_log2 = p.scale_log2;
   a.err = p.err;
-  tc05_attention_cta<QT, D, true, I8>(smem, a, q_row, page_block, row_pos, sink);
+  tc05_attention_cta<QT, D, true, I8, I8 ? 1 : 2>(smem, a, q_row, page_block, row_pos, sink);
 }
 
 __global__ void copy_blocks_kernel(uint8_t* k_cache, uint8_t* v_cache, const int32_t* pairs,
@@ -699,22 +719,22 @@ __global__ void copy_blocks_kernel(uint8_t* k_cache, uint8_t* v_cache, const int
 
 template <typename T, int D>
 cudaError_t launch_prefix(const PrefixParams& p, cudaStream_t st) {
-  using Ly = PrefixTcLayout<D, false>;
+  using Ly = PrefixTcLayout<D, false, 1>;
   auto kern = prefix_attention_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
   if (e != cudaSuccess) return e;
-  const dim3 grid((p.num_seqs * p.group + kTcRows - 1) / kTcRows, p.num_prefix_splits,
+  const dim3 grid((p.num_seqs * p.group + Ly::ROWS - 1) / Ly::ROWS, p.num_prefix_splits,
                   p.num_kv_heads);
   return launch_pdl(kern, grid, dim3(Ly::THREADS), Ly::SMEM, st, p);
 }
 
 template <typename QT, int D, bool I8>
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t st) {
-  using Ly = PrefixTcLayout<D, I8>;
+  using Ly = PrefixTcLayout<D, I8, I8 ? 1 : 2>;
   auto kern = prefill_tc_kernel<QT, D, I8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
   if (e != cudaSuccess) return e;
-  const long long tiles = ((long long)p.max_q_len * p.group + kTcRows - 1) / kTcRows;
+  const long long tiles = ((long long)p.max_q_len * p.group + Ly::ROWS - 1) / Ly::ROWS;
   const dim3 grid(static_cast<unsigned>(tiles), p.num_kv_heads, p.num_seqs);
   return launch_pdl(kern, grid, dim3(Ly::THREADS), Ly::SMEM, st, p);
 }

@@ -42,9 +42,10 @@ struct PrefixParams {
   float scale_log2;  // scale * log2(e)
 };
 
-// Rows of query heads one CTA takes (the M of one tensor-core MMA; shared
-// prefix and prefill alike), and tokens per staged K/V tile.
+// Rows of one tensor-core query tile (the M of one MMA), rows of query heads
+// one shared-prefix CTA takes, and tokens per staged K/V tile.
 constexpr int kPrefixTcRows = 128;
+constexpr int kPrefixCtaRows = 128;
 constexpr int kPrefixTile = 64;
 
 // dtype: 1 = bf16, 2 = f16 (pa_dtype values). Returns cudaErrorInvalidValue
