@@ -67,7 +67,10 @@ struct PrefixTcLayout {
   static constexpr int MMA_WARP = SMX, COPY_WARP = SMX + 1, CONV_WARP = SMX + 2;
   static constexpr int THREADS = (SMX + 2 + (I8 ? 4 : 0)) * 32;
   static constexpr int STAGES = I8 ? 3 : (QTL == 2 && D == 128 ? 3 : PA_PREFIX_STAGES);
-  static constexpr int RSTAGES = I8 ? 2 : 0;         // raw INT8 tiles
+#ifndef PA_PREFILL_RAW_STAGES
+#define PA_PREFILL_RAW_STAGES 3
+#endif
+  static constexpr int RSTAGES = I8 ? PA_PREFILL_RAW_STAGES : 0;  // raw INT8 tiles
   static constexpr int QBYTES1 = KB * kTcRows * 128;  // one Q tile: [KB][128 rows][128 B]
   static constexpr int QBYTES = QTL * QBYTES1;
   static constexpr int TBYTES = KB * kTcTile * 128;  // one K or V tile: [KB][64 tokens][128 B]
