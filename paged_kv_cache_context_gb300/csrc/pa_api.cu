@@ -211,9 +211,12 @@ __global__ void cache_int8_kernel(const IT* key, const IT* value, int8_t* k_cach
   }
 }
 
-// LSE combination of split partials: one warp per (sequence, head) row. Lane j
-// computes the weight of split j; the partial rows of up to 8 splits are
-// loaded before they are accumulated, so their latencies overlap.
+// LSE combination of split partials: one warp per (sequence, head) row; a
+// lane owns the 4-float chunks lane, lane + 32, ... of the row. With at most
+// kFewSplits splits every load of the row (each split's maximum, sum and
+// chunks) is issued in one round; more splits take rounds of 8, lane j
+// computing the weight of split j.
+constexpr int kFewSplits = 8;
 template <typename OT, int MAXC>
 __global__ void __launch_bounds__(128)
     reduce_kernel(OT* out, const float* tmp_out, const float* max_logits, const float* exp_sums,
@@ -225,6 +228,63 @@ __global__ void __launch_bounds__(128)
   if (row >= rows) return;
   const float* ml = max_logits + row * NS;
   const float* es = exp_sums + row * NS;
+  if (NS <= kFewSplits) {
+    const int nchunk = D / 4;
+    const float4* base = reinterpret_cast<const float4*>(tmp_out + row * NS * (int64_t)D);
+    float mj[kFewSplits], lj[kFewSplits];
+    float4 v[kFewSplits][MAXC];
+#pragma unroll
+    for (int j = 0; j < kFewSplits; ++j) {
+      mj[j] = j < NS ? ml[j] : -INFINITY;
+      lj[j] = j < NS ? es[j] : 0.f;
+#pragma unroll
+      for (int c = 0; c < MAXC; ++c) {
+        const int d4 = lane + 32 * c;
+        // an empty split's chunks may hold anything: loaded, never used
+        v[j][c] = (j < NS && d4 < nchunk) ? base[(int64_t)j * nchunk + d4]
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kFewSplits; ++j)
+      if (lj[j] > 0.f) M = fmaxf(M, mj[j]);
+    OT* o = out + row * D;
+    if (M == -INFINITY) {
+      for (int d = lane; d < D; d += 32) o[d] = Elem<OT>::from_f32(0.f);
+      return;
+    }
+    float4 acc[MAXC];
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+#pragma unroll
+    for (int j = 0; j < kFewSplits; ++j) {
+      if (lj[j] > 0.f) {
+        const float w = lj[j] * expf(mj[j] - M);
+        wsum += w;
+#pragma unroll
+        for (int c = 0; c < MAXC; ++c) {
+          acc[c].x = fmaf(w, v[j][c].x, acc[c].x);
+          acc[c].y = fmaf(w, v[j][c].y, acc[c].y);
+          acc[c].z = fmaf(w, v[j][c].z, acc[c].z);
+          acc[c].w = fmaf(w, v[j][c].w, acc[c].w);
+        }
+      }
+    }
+    const float inv = 1.f / wsum;
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c) {
+      const int d4 = lane + 32 * c;
+      if (d4 < nchunk) {
+        o[4 * d4 + 0] = Elem<OT>::from_f32(acc[c].x * inv);
+        o[4 * d4 + 1] = Elem<OT>::from_f32(acc[c].y * inv);
+        o[4 * d4 + 2] = Elem<OT>::from_f32(acc[c].z * inv);
+        o[4 * d4 + 3] = Elem<OT>::from_f32(acc[c].w * inv);
+      }
+    }
+    return;
+  }
   float M = -INFINITY;
   for (int j = lane; j < NS; j += 32)
     if (es[j] > 0.f) M = fmaxf(M, ml[j]);

@@ -119,11 +119,13 @@ struct Tc05Args {
 //   sink(rr, c0, o, inv_l, m_log2, l)   row rr's output columns [c0, c0 + 32)
 //                  (un-normalised; times inv_l = 1 / l), called for every
 //                  chunk by every softmax thread
+//   copy_idle(lane)  side work for the copy warp once its copies are issued
+//                  (lanes 1-31 start it while lane 0 is still issuing)
 template <typename QT, int D, bool CAUSAL, bool I8, int QTILES, typename QRow,
-          typename PageBlock, typename RowPos, typename Sink>
+          typename PageBlock, typename RowPos, typename Sink, typename Idle>
 __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args& a, QRow q_row,
                                                    PageBlock page_block, RowPos row_pos,
-                                                   Sink sink) {
+                                                   Sink sink, Idle copy_idle) {
   using Ly = PrefixTcLayout<D, I8, QTILES>;
   using T = typename std::conditional<I8, __half, QT>::type;  // MMA operand type
   constexpr int KB = Ly::KB, ST = Ly::STAGES, RS = Ly::RSTAGES, QTL = Ly::QTL, ROWS = Ly::ROWS;
@@ -280,6 +282,7 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
       for (int k = issued > NB_ ? issued - NB_ : 0; k < issued; ++k)
         if (!mbar_wait_bounded(&done[k % NB_], (k / NB_) & 1)) raise_error(err, PA_DEVERR_TIMEOUT);
     }
+    copy_idle(lane);
   } else if (warp >= Ly::CONV_WARP) {
     // ================================================ INT8: widening to f16
     if constexpr (I8) {
@@ -547,19 +550,21 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, false, 1>::THREADS, 1)
   const int t_end = min(p.prefix_tokens, t_begin + p.tokens_per_split);
   const int slot = p.slot0 + split;
 
-  // the precondition, checked on a slice per CTA: every row's first
-  // prefix_pages entries equal row 0's, and every context covers the prefix
-  {
+  // the precondition, checked on a slice per CTA by n threads: every row's
+  // first prefix_pages entries equal row 0's, and every context covers the
+  // prefix (off the critical path: by the copy warp once its copies are out)
+  auto check = [&](int t, int n) {
     const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
     const int nctas = gridDim.x * gridDim.y * gridDim.z;
     for (int s = 1 + cta; s < S; s += nctas)
-      for (int i = tid; i < p.prefix_pages; i += NT)
+      for (int i = t; i < p.prefix_pages; i += n)
         if (p.block_tables[(size_t)s * p.max_blocks_per_seq + i] != p.block_tables[i])
           raise_error(p.err, PA_DEVERR_BLOCK_ID);
-    for (int s = cta * NT + tid; s < S; s += nctas * NT)
+    for (int s = cta * n + t; s < S; s += nctas * n)
       if (p.context_lens[s] < p.prefix_tokens) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
-  }
+  };
   if (t_begin >= t_end) {  // a split with no prefix token: empty partials
+    check(tid, NT);
     for (int i = tid; i < ROWS; i += NT) {
       const int r = qt * ROWS + i;
       if (r < rows_total) {
@@ -608,7 +613,8 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, false, 1>::THREADS, 1)
   a.min_pos = 0;
   a.scale_log2 = p.scale_log2;
   a.err = p.err;
-  tc05_attention_cta<T, D, false, false, 1>(smem, a, q_row, page_block, row_pos, sink);
+  tc05_attention_cta<T, D, false, false, 1>(smem, a, q_row, page_block, row_pos, sink,
+                                            [&](int lane) { check(lane, 32); });
 }
 
 // Causal prefill over the paged cache on the tensor cores: one CTA per
@@ -702,7 +708,8 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, I8, I8 ? 1 : 2>::THREADS, 1)
   a.min_pos = pos0 + r_first / G;
   a.scale_log2 = p.scale_log2;
   a.err = p.err;
-  tc05_attention_cta<QT, D, true, I8, I8 ? 1 : 2>(smem, a, q_row, page_block, row_pos, sink);
+  tc05_attention_cta<QT, D, true, I8, I8 ? 1 : 2>(smem, a, q_row, page_block, row_pos, sink,
+                                                   [](int) {});
 }
 
 __global__ void copy_blocks_kernel(uint8_t* k_cache, uint8_t* v_cache, const int32_t* pairs,

@@ -127,11 +127,13 @@ def test_many_splits_forced_through_partials_and_reduce():
     assert device_errors() == 0
 
 
-@pytest.mark.parametrize("odt", [torch.float32, torch.bfloat16, torch.float16])
-def test_reduce_matches_oracle_on_generated_partials(odt):
-    """pa_reduce on seeded partials (some splits empty with NaN garbage rows)."""
-    g = torch.Generator().manual_seed(80)
-    S, Hq, NS, D = 5, 6, 7, 96
+@pytest.mark.parametrize("odt,NS", [(torch.float32, 7), (torch.bfloat16, 7), (torch.float16, 7),
+                                    (torch.float32, 8), (torch.bfloat16, 13), (torch.float32, 40)])
+def test_reduce_matches_oracle_on_generated_partials(odt, NS):
+    """pa_reduce on seeded partials (some splits empty with NaN garbage rows):
+    up to 8 splits are loaded in one round, more in rounds of 8."""
+    g = torch.Generator().manual_seed(80 + NS)
+    S, Hq, D = 5, 6, 96
     o = torch.randn(S, Hq, NS, D, generator=g)
     m = torch.randn(S, Hq, NS, generator=g) * 5
     l = torch.rand(S, Hq, NS, generator=g) * 10 + 0.1
