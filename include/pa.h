@@ -310,6 +310,29 @@ pa_status pa_prefill_int8(void* out, const void* query,
                           pa_dtype q_dtype, pa_stream_t stream);
 
 /*
+ * pa_prefill_fp8 -- pa_prefill over an FP8 E4M3 cache with per-tensor scales.
+ *
+ * Source: "PagedAttention in mistral.rs", section "KV Cache Quantization"
+ * (an FP8 E4M3 paged cache, dequantised in the attention), with the same
+ * page's prefill. Same computation, arguments and errors as pa_prefill, with
+ *   K_j[d] = e4m3(k_cache[blk][g][row][d]) * k_scale
+ * and V_j likewise with v_scale (the caches written by pa_reshape_and_cache
+ * with PA_KV_FP8_E4M3). k_cache, v_cache: E4M3 bytes [NB][Hkv][bs][D]. On the
+ * tensor cores the codes are widened exactly to f16 and q is carried in f16
+ * (exact for a bf16 query inside f16's range); k_scale multiplies the logit
+ * scale and v_scale the output; fp32 accumulation. Pages are moved by 1-D
+ * bulk copies (no limit on the cache's rows). k_scale or v_scale not finite
+ * and positive -> PA_ERR_SCALE.
+ */
+pa_status pa_prefill_fp8(void* out, const void* query,
+                         const uint8_t* k_cache, const uint8_t* v_cache,
+                         const int32_t* block_tables, const int32_t* cu_q,
+                         const int32_t* context_lens, int num_tokens, int num_seqs,
+                         int num_heads, int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, int max_blocks_per_seq, int max_q_len, float scale,
+                         float k_scale, float v_scale, pa_dtype q_dtype, pa_stream_t stream);
+
+/*
  * pa_decode_plan -- a split plan for pa_decode_partials at these sizes.
  * Writes the number of context splits per (sequence, kv head) and the pages
  * (blocks) each split covers; split i covers slots
@@ -385,7 +408,8 @@ pa_status pa_decode_balanced(void* out, const void* query,
  * prefix_pages entries of every row of block_tables are the same blocks
  * (else PA_DEVERR_BLOCK_ID), and every context_lens[s] >= prefix_pages * bs
  * (else PA_DEVERR_CONTEXT_LEN). Supported: AUTO caches of q_dtype BF16 or F16
- * (else PA_ERR_DTYPE), D in {64, 128} (else PA_ERR_HEAD_DIM),
+ * (else PA_ERR_DTYPE; 8-bit caches: pa_decode_cascade_fp8 / _int8 below),
+ * D in {64, 128} (else PA_ERR_HEAD_DIM),
  * 1 <= prefix_pages <= MB and NB * Hkv * bs <= 2^31 - 1 cache rows (else
  * PA_ERR_SHAPE). workspace: at least
  * pa_decode_cascade_workspace_size() bytes (PA_ERR_NULL / PA_ERR_WORKSPACE),
@@ -404,6 +428,38 @@ pa_status pa_decode_cascade(void* out, const void* query,
                             int block_size, int num_blocks, int max_blocks_per_seq,
                             float scale, pa_dtype q_dtype, int prefix_pages,
                             void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_decode_cascade_fp8 / pa_decode_cascade_int8 -- pa_decode_cascade over
+ * an FP8 E4M3 cache with per-tensor scales (k_scale, v_scale; as pa_decode
+ * with PA_KV_FP8_E4M3) or over an INT8 cache with per-row scales (k_scales,
+ * v_scales fp32 [NB][Hkv][bs]; as pa_decode_int8). Same launches, result,
+ * preconditions, workspace and errors as pa_decode_cascade; the shared
+ * prefix's 8-bit pages come by 1-D bulk copies (no limit on the cache's rows)
+ * and are widened exactly to f16 in shared memory for the tensor cores, q is
+ * carried in f16 (exact for a bf16 query inside f16's range); FP8: k_scale
+ * multiplies the logit scale and v_scale the output; INT8: the K row scale
+ * multiplies the logit and the V row scale the weight before it is rounded
+ * to f16. The sequences' own pages go through the decode of that cache kind.
+ * k_scale or v_scale not finite and positive -> PA_ERR_SCALE; NULL row scales
+ * -> PA_ERR_NULL, not 16-byte aligned -> PA_ERR_ALIGN.
+ */
+pa_status pa_decode_cascade_fp8(void* out, const void* query,
+                                const uint8_t* k_cache, const uint8_t* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, int num_blocks, int max_blocks_per_seq,
+                                float scale, float k_scale, float v_scale, pa_dtype q_dtype,
+                                int prefix_pages, void* workspace, size_t workspace_bytes,
+                                pa_stream_t stream);
+pa_status pa_decode_cascade_int8(void* out, const void* query,
+                                 const int8_t* k_cache, const int8_t* v_cache,
+                                 const float* k_scales, const float* v_scales,
+                                 const int32_t* block_tables, const int32_t* context_lens,
+                                 int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int num_blocks, int max_blocks_per_seq,
+                                 float scale, pa_dtype q_dtype, int prefix_pages,
+                                 void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
  * pa_copy_blocks -- copy whole cache blocks, for copy-on-write of shared

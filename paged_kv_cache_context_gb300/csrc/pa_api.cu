@@ -989,24 +989,25 @@ PA_API pa_status pa_prefill(void* out, const void* query, const void* k_cache,
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.max_q_len = max_q_len;
   p.scale_log2 = scale * kLog2e;
-  return launch_prefill_attention(p, q_dtype, false, reinterpret_cast<cudaStream_t>(stream)) ==
+  return launch_prefill_attention(p, q_dtype, 0, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }
 
-PA_API pa_status pa_prefill_int8(void* out, const void* query, const int8_t* k_cache,
-                                 const int8_t* v_cache, const float* k_scales,
-                                 const float* v_scales, const int32_t* block_tables,
-                                 const int32_t* cu_q, const int32_t* context_lens,
-                                 int num_tokens, int num_seqs, int num_heads, int num_kv_heads,
-                                 int head_dim, int block_size, int num_blocks,
-                                 int max_blocks_per_seq, int max_q_len, float scale,
-                                 pa_dtype q_dtype, pa_stream_t stream) {
+// Prefill over an 8-bit cache: kind 1 = INT8 codes with row scales
+// (k_scales, v_scales), kind 2 = FP8 E4M3 codes (k_scale, v_scale).
+static pa_status prefill_8bit(int kind, void* out, const void* query, const void* k_cache,
+                              const void* v_cache, const float* k_scales, const float* v_scales,
+                              float k_scale, float v_scale, const int32_t* block_tables,
+                              const int32_t* cu_q, const int32_t* context_lens, int num_tokens,
+                              int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                              int block_size, int num_blocks, int max_blocks_per_seq,
+                              int max_q_len, float scale, pa_dtype q_dtype, pa_stream_t stream) {
   if (num_tokens < 0 || num_seqs < 0 || num_seqs > 65535) return PA_ERR_SHAPE;
   if (num_tokens == 0 || num_seqs == 0) return PA_OK;
-  if (!out || !query || !k_cache || !v_cache || !k_scales || !v_scales || !block_tables ||
-      !cu_q || !context_lens)
+  if (!out || !query || !k_cache || !v_cache || !block_tables || !cu_q || !context_lens ||
+      (kind == 1 && (!k_scales || !v_scales)))
     return PA_ERR_NULL;
   if (q_dtype != PA_BF16 && q_dtype != PA_F16) return PA_ERR_DTYPE;
   if (num_heads <= 0 || num_kv_heads <= 0 || num_kv_heads > 65535 ||
@@ -1017,15 +1018,17 @@ PA_API pa_status pa_prefill_int8(void* out, const void* query, const int8_t* k_c
   if (num_blocks <= 0 || max_blocks_per_seq <= 0 || max_q_len < 1 || max_q_len > num_tokens)
     return PA_ERR_SHAPE;
   if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PA_ERR_SHAPE;
+  if (kind == 2 && !(isfinite(k_scale) && k_scale > 0.f && isfinite(v_scale) && v_scale > 0.f))
+    return PA_ERR_SCALE;
   if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache) ||
-      !aligned16(k_scales) || !aligned16(v_scales))
+      (kind == 1 && (!aligned16(k_scales) || !aligned16(v_scales))))
     return PA_ERR_ALIGN;
   constexpr float kLog2e = 1.4426950408889634f;
   PrefillParams p{};
   p.out = out;
   p.query = query;
-  p.k_cache = reinterpret_cast<const uint8_t*>(k_cache);
-  p.v_cache = reinterpret_cast<const uint8_t*>(v_cache);
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
   p.k_scales = k_scales;
   p.v_scales = v_scales;
   p.block_tables = block_tables;
@@ -1042,11 +1045,39 @@ PA_API pa_status pa_prefill_int8(void* out, const void* query, const int8_t* k_c
   p.num_tokens = num_tokens;
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.max_q_len = max_q_len;
-  p.scale_log2 = scale * kLog2e;
-  return launch_prefill_attention(p, q_dtype, true, reinterpret_cast<cudaStream_t>(stream)) ==
+  p.scale_log2 = scale * kLog2e * (kind == 2 ? k_scale : 1.f);
+  p.v_scale = kind == 2 ? v_scale : 1.f;
+  return launch_prefill_attention(p, q_dtype, kind, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_prefill_int8(void* out, const void* query, const int8_t* k_cache,
+                                 const int8_t* v_cache, const float* k_scales,
+                                 const float* v_scales, const int32_t* block_tables,
+                                 const int32_t* cu_q, const int32_t* context_lens,
+                                 int num_tokens, int num_seqs, int num_heads, int num_kv_heads,
+                                 int head_dim, int block_size, int num_blocks,
+                                 int max_blocks_per_seq, int max_q_len, float scale,
+                                 pa_dtype q_dtype, pa_stream_t stream) {
+  return prefill_8bit(1, out, query, k_cache, v_cache, k_scales, v_scales, 1.f, 1.f,
+                      block_tables, cu_q, context_lens, num_tokens, num_seqs, num_heads,
+                      num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
+                      max_q_len, scale, q_dtype, stream);
+}
+
+PA_API pa_status pa_prefill_fp8(void* out, const void* query, const uint8_t* k_cache,
+                                const uint8_t* v_cache, const int32_t* block_tables,
+                                const int32_t* cu_q, const int32_t* context_lens, int num_tokens,
+                                int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, int num_blocks, int max_blocks_per_seq,
+                                int max_q_len, float scale, float k_scale, float v_scale,
+                                pa_dtype q_dtype, pa_stream_t stream) {
+  return prefill_8bit(2, out, query, k_cache, v_cache, nullptr, nullptr, k_scale, v_scale,
+                      block_tables, cu_q, context_lens, num_tokens, num_seqs, num_heads,
+                      num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
+                      max_q_len, scale, q_dtype, stream);
 }
 
 // ================================================================ cascade
@@ -1081,12 +1112,12 @@ static int launch_plan_sms() {
 }
 
 static pa_status check_cascade(const DecodeShape& a, int prefix_pages) {
-  if (a.kv_dtype != PA_KV_AUTO || (a.q_dtype != PA_BF16 && a.q_dtype != PA_F16))
-    return PA_ERR_DTYPE;
+  if (a.q_dtype != PA_BF16 && a.q_dtype != PA_F16) return PA_ERR_DTYPE;
   if (a.D != 64 && a.D != 128) return PA_ERR_HEAD_DIM;
   if (prefix_pages < 1 || prefix_pages > a.MB) return PA_ERR_SHAPE;
-  // the prefix kernel stages pages by tensor copies: 32-bit row coordinates
-  if ((long long)a.NB * a.Hkv * a.bs > kMaxTcRows) return PA_ERR_SHAPE;
+  // the prefix kernel stages 16-bit pages by tensor copies: 32-bit row coordinates
+  if (a.kv_dtype == PA_KV_AUTO && (long long)a.NB * a.Hkv * a.bs > kMaxTcRows)
+    return PA_ERR_SHAPE;
   return PA_OK;
 }
 
@@ -1102,17 +1133,25 @@ PA_API size_t pa_decode_cascade_workspace_size(int num_seqs, int num_heads, int 
   return align256(rows * head_dim * 4) + 2 * align256(rows * 4);
 }
 
-PA_API pa_status pa_decode_cascade(void* out, const void* query, const void* k_cache,
-                                   const void* v_cache, const int32_t* block_tables,
-                                   const int32_t* context_lens, int num_seqs, int num_heads,
-                                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                                   int max_blocks_per_seq, float scale, pa_dtype q_dtype,
-                                   int prefix_pages, void* workspace, size_t workspace_bytes,
-                                   pa_stream_t stream) {
-  DecodeShape a{num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                max_blocks_per_seq, 0, q_dtype, PA_KV_AUTO, 1.f, 1.f};
-  pa_status rc = check_decode(a, out, query, k_cache, v_cache, block_tables, context_lens);
+// The cascade for every cache kind: a.kv_dtype AUTO (16-bit, the query's
+// type), FP8_E4M3 (a.k_scale, a.v_scale) or INT8 (row scales k_scales,
+// v_scales).
+static pa_status cascade_impl(void* out, const void* query, const void* k_cache,
+                              const void* v_cache, const float* k_scales, const float* v_scales,
+                              const int32_t* block_tables, const int32_t* context_lens,
+                              DecodeShape a, float scale, int prefix_pages, void* workspace,
+                              size_t workspace_bytes, pa_stream_t stream) {
+  const int num_seqs = a.S, num_heads = a.Hq, num_kv_heads = a.Hkv, head_dim = a.D;
+  const int block_size = a.bs, num_blocks = a.NB, max_blocks_per_seq = a.MB;
+  const int q_dtype = a.q_dtype;
+  const bool int8 = a.kv_dtype == PA_KV_INT8;
+  // the shared checks (an INT8 cache on the shape with a native cache)
+  DecodeShape chk = a;
+  if (int8) chk.kv_dtype = PA_KV_AUTO;
+  pa_status rc = check_decode(chk, out, query, k_cache, v_cache, block_tables, context_lens);
   if (rc != PA_OK || num_seqs == 0) return rc;
+  if (int8 && (!k_scales || !v_scales)) return PA_ERR_NULL;
+  if (int8 && (!aligned16(k_scales) || !aligned16(v_scales))) return PA_ERR_ALIGN;
   rc = check_cascade(a, prefix_pages);
   if (rc != PA_OK) return rc;
   if (!workspace) return PA_ERR_NULL;
@@ -1161,16 +1200,23 @@ PA_API pa_status pa_decode_cascade(void* out, const void* query, const void* k_c
   q.slot0 = 1;
   q.num_prefix_splits = nsp;
   q.tokens_per_split = tps;
-  q.scale_log2 = scale * 1.4426950408889634f;
-  {
+  const bool fp8 = a.kv_dtype == PA_KV_FP8_E4M3;
+  q.scale_log2 = scale * 1.4426950408889634f * (fp8 ? a.k_scale : 1.f);
+  q.v_scale = fp8 ? a.v_scale : 1.f;
+  q.k_scales = k_scales;
+  q.v_scales = v_scales;
+  if (a.kv_dtype == PA_KV_AUTO) {
     const long long rows = (long long)num_blocks * num_kv_heads * block_size;
     if (!page_tensor_map(&q.tm_k, k_cache, q_dtype, head_dim, rows, block_size) ||
         !page_tensor_map(&q.tm_v, v_cache, q_dtype, head_dim, rows, block_size))
       return PA_ERR_CUDA;
   }
-  if (launch_prefix_attention(q, q_dtype, st) != cudaSuccess) return PA_ERR_CUDA;
+  const int kind = int8 ? 1 : fp8 ? 2 : 0;
+  if (launch_prefix_attention(q, q_dtype, kind, st) != cudaSuccess) return PA_ERR_CUDA;
   // slot 0: each sequence's own pages after the prefix, one CTA per (sequence, kv head)
   DecodeParams p = make_params(a, query, k_cache, v_cache, block_tables, context_lens, scale, err);
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
   p.tmp_out = tmp;
   p.max_logits = ml;
   p.exp_sums = es;
@@ -1186,6 +1232,47 @@ PA_API pa_status pa_decode_cascade(void* out, const void* query, const void* k_c
                  cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_decode_cascade(void* out, const void* query, const void* k_cache,
+                                   const void* v_cache, const int32_t* block_tables,
+                                   const int32_t* context_lens, int num_seqs, int num_heads,
+                                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                   int max_blocks_per_seq, float scale, pa_dtype q_dtype,
+                                   int prefix_pages, void* workspace, size_t workspace_bytes,
+                                   pa_stream_t stream) {
+  const DecodeShape a{num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                      max_blocks_per_seq, 0, q_dtype, PA_KV_AUTO, 1.f, 1.f};
+  return cascade_impl(out, query, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens,
+                      a, scale, prefix_pages, workspace, workspace_bytes, stream);
+}
+
+PA_API pa_status pa_decode_cascade_fp8(void* out, const void* query, const uint8_t* k_cache,
+                                       const uint8_t* v_cache, const int32_t* block_tables,
+                                       const int32_t* context_lens, int num_seqs, int num_heads,
+                                       int num_kv_heads, int head_dim, int block_size,
+                                       int num_blocks, int max_blocks_per_seq, float scale,
+                                       float k_scale, float v_scale, pa_dtype q_dtype,
+                                       int prefix_pages, void* workspace, size_t workspace_bytes,
+                                       pa_stream_t stream) {
+  const DecodeShape a{num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                      max_blocks_per_seq, 0, q_dtype, PA_KV_FP8_E4M3, k_scale, v_scale};
+  return cascade_impl(out, query, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens,
+                      a, scale, prefix_pages, workspace, workspace_bytes, stream);
+}
+
+PA_API pa_status pa_decode_cascade_int8(void* out, const void* query, const int8_t* k_cache,
+                                        const int8_t* v_cache, const float* k_scales,
+                                        const float* v_scales, const int32_t* block_tables,
+                                        const int32_t* context_lens, int num_seqs, int num_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int num_blocks, int max_blocks_per_seq, float scale,
+                                        pa_dtype q_dtype, int prefix_pages, void* workspace,
+                                        size_t workspace_bytes, pa_stream_t stream) {
+  const DecodeShape a{num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                      max_blocks_per_seq, 0, q_dtype, PA_KV_INT8, 1.f, 1.f};
+  return cascade_impl(out, query, k_cache, v_cache, k_scales, v_scales, block_tables,
+                      context_lens, a, scale, prefix_pages, workspace, workspace_bytes, stream);
 }
 
 PA_API pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs,

@@ -42,15 +42,21 @@ __device__ __forceinline__ void cp_async_wait() {
 // whole pages, P is written to shared memory by the softmax threads; all
 // three operands use the 128-byte swizzle. Warps 0-3: softmax (thread t owns
 // row t, TMEM lane t); warp 4: MMA issue and TMEM allocation; warp 5: copies.
-// An INT8 cache (I8) comes by 1-D bulk copies of its pages and row scales
-// into a raw ring, and warps 6-9 widen the codes exactly to f16 into the
-// swizzled K/V tiles (one row per thread); q is carried in f16 (exact inside
-// f16's range), the K row scales multiply the logits, the V row scales the
-// weights before they are rounded, and the running sum takes the bare
-// weights. Every wait is bounded, and every warp-wide TMEM access is taken by
-// the whole warp.
+// An 8-bit cache (INT8 with row scales, or FP8 E4M3) comes by 1-D bulk
+// copies of its pages (and INT8 row scales) into a raw ring, and warps 6-9
+// widen the codes exactly to f16 into the swizzled K/V tiles (one row per
+// thread); q is carried in f16 (exact inside f16's range). INT8: the K row
+// scales multiply the logits, the V row scales the weights before they are
+// rounded, and the running sum takes the bare weights. E4M3: the callers
+// fold k_scale into the logit scale and v_scale into the output. Every wait
+// is bounded, and every warp-wide TMEM access is taken by the whole warp.
 constexpr int kTcRows = kPrefixTcRows;
 constexpr int kTcTile = kPrefixTile;
+// Cache kinds of the routine: 16-bit elements (the MMA type), or 8-bit codes
+// widened to f16 in shared memory: INT8 with a scale per cached row, or FP8
+// E4M3 whose per-tensor scales the callers fold into the logit scale and the
+// output.
+enum : int { kKc16 = 0, kKcI8 = 1, kKcE4 = 2 };
 #ifndef PA_PREFIX_STAGES
 #define PA_PREFIX_STAGES 4
 #endif
@@ -121,11 +127,13 @@ struct Tc05Args {
 //                  chunk by every softmax thread
 //   copy_idle(lane)  side work for the copy warp once its copies are issued
 //                  (lanes 1-31 start it while lane 0 is still issuing)
-template <typename QT, int D, bool CAUSAL, bool I8, int QTILES, typename QRow,
+template <typename QT, int D, bool CAUSAL, int KC, int QTILES, typename QRow,
           typename PageBlock, typename RowPos, typename Sink, typename Idle>
 __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args& a, QRow q_row,
                                                    PageBlock page_block, RowPos row_pos,
                                                    Sink sink, Idle copy_idle) {
+  constexpr bool I8 = KC != kKc16;   // 8-bit codes, widened by the converter warps
+  constexpr bool ROW_SC = KC == kKcI8;   // with a scale per cached row
   using Ly = PrefixTcLayout<D, I8, QTILES>;
   using T = typename std::conditional<I8, __half, QT>::type;  // MMA operand type
   constexpr int KB = Ly::KB, ST = Ly::STAGES, RS = Ly::RSTAGES, QTL = Ly::QTL, ROWS = Ly::ROWS;
@@ -254,7 +262,7 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
             if (t < a.k_end) {
               const int b = page_block(t);
               if (b >= 0 && b < a.num_blocks)
-                bytes += 2u * bs * (D + 4);
+                bytes += 2u * bs * (D + (ROW_SC ? 4 : 0));
               else
                 raise_error(err, PA_DEVERR_BLOCK_ID);
             }
@@ -269,9 +277,12 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
             const size_t row0 = ((size_t)b * a.Hkv + a.g) * bs;
             bulk_g2s(raw + pp * bs * D, a.k_codes + row0 * D, bs * D, &raw_full[rs]);
             bulk_g2s(raw + Ly::RAWT + pp * bs * D, a.v_codes + row0 * D, bs * D, &raw_full[rs]);
-            bulk_g2s(raw + 2 * Ly::RAWT + pp * bs * 4, a.k_scales + row0, bs * 4, &raw_full[rs]);
-            bulk_g2s(raw + 2 * Ly::RAWT + kTcTile * 4 + pp * bs * 4, a.v_scales + row0, bs * 4,
-                     &raw_full[rs]);
+            if constexpr (ROW_SC) {
+              bulk_g2s(raw + 2 * Ly::RAWT + pp * bs * 4, a.k_scales + row0, bs * 4,
+                       &raw_full[rs]);
+              bulk_g2s(raw + 2 * Ly::RAWT + kTcTile * 4 + pp * bs * 4, a.v_scales + row0, bs * 4,
+                       &raw_full[rs]);
+            }
           }
         }
         ++issued;
@@ -284,7 +295,7 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
     }
     copy_idle(lane);
   } else if (warp >= Ly::CONV_WARP) {
-    // ================================================ INT8: widening to f16
+    // ================================================ 8-bit codes: widening to f16
     if constexpr (I8) {
       const int cid = tid - Ly::CONV_WARP * 32;  // 0 .. 127
       const int row = cid & (kTcTile - 1);
@@ -311,16 +322,18 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
           uint4 out = make_uint4(0u, 0u, 0u, 0u);
           if (ok) {
             const uint2 w = *reinterpret_cast<const uint2*>(src + 8 * c);
-            widen8<::pa::I8>(w.x, out.x, out.y);
-            widen8<::pa::I8>(w.y, out.z, out.w);
+            using Code = typename std::conditional<ROW_SC, ::pa::I8, E4M3>::type;
+            widen8<Code>(w.x, out.x, out.y);
+            widen8<Code>(w.y, out.z, out.w);
           }
           const int kb = c >> 3, ch = c & 7;
           *reinterpret_cast<uint4*>(dst + kb * (kTcTile * 128) + row * 128 +
                                     ((ch ^ (row & 7)) << 4)) = out;
         }
-        sc[(st * 2 + (is_v ? 1 : 0)) * kTcTile + row] =
-            ok ? reinterpret_cast<const float*>(raw + 2 * Ly::RAWT)[(is_v ? kTcTile : 0) + row]
-               : 0.f;
+        if constexpr (ROW_SC)
+          sc[(st * 2 + (is_v ? 1 : 0)) * kTcTile + row] =
+              ok ? reinterpret_cast<const float*>(raw + 2 * Ly::RAWT)[(is_v ? kTcTile : 0) + row]
+                 : 0.f;
         fence_proxy_async_smem();
         mbar_arrive(&conv_full[st]);
         mbar_arrive(&raw_empty[rs]);
@@ -420,7 +433,7 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
 #pragma unroll
       for (int c = 0; c < kTcTile; ++c) {
         x[c] = __uint_as_float(sr[c >> 5][c & 31]) * a.scale_log2;
-        if constexpr (I8) x[c] *= ksc[c];
+        if constexpr (ROW_SC) x[c] *= ksc[c];
       }
       if (valid < kTcTile || (CAUSAL && t0 + kTcTile - 1 > a.min_pos)) {  // CTA-uniform
         const int lim = CAUSAL ? min(valid, my_pos - t0 + 1) : valid;
@@ -467,7 +480,7 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
         const float p0 = ex2_approx(x[c] - m), p1 = ex2_approx(x[c + 1] - m);
         l0 += p0;
         l1 += p1;
-        if constexpr (I8)
+        if constexpr (ROW_SC)
           pk[c / 2] = Mma<T>::pack(p0 * ksc[kTcTile + c], p1 * ksc[kTcTile + c + 1]);
         else
           pk[c / 2] = Mma<T>::pack(p0, p1);
@@ -533,10 +546,11 @@ __device__ __forceinline__ void tc05_attention_cta(uint8_t* smem, const Tc05Args
 // prefix's block ids from row 0 of the block tables), and writes the rows'
 // partials (normalised output, maximum in natural-log units, sum) to its
 // slot for pa_reduce.
-template <typename T, int D>
-__global__ void __launch_bounds__(PrefixTcLayout<D, false, 1>::THREADS, 1)
+template <typename T, int D, int KC>
+__global__ void __launch_bounds__(PrefixTcLayout<D, KC != kKc16, 1>::THREADS, 1)
     prefix_attention_kernel(const __grid_constant__ PrefixParams p) {
-  constexpr int NT = PrefixTcLayout<D, false, 1>::THREADS, ROWS = PrefixTcLayout<D, false, 1>::ROWS;
+  using Ly = PrefixTcLayout<D, KC != kKc16, 1>;
+  constexpr int NT = Ly::THREADS, ROWS = Ly::ROWS;
   static_assert(ROWS == kPrefixCtaRows, "the host's plan counts rows per CTA");
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -589,6 +603,7 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, false, 1>::THREADS, 1)
     const long long row = row_of(rr);
     if (row < 0) return;
     float* dst = p.tmp_out + ((size_t)row * p.num_slots + slot) * D + c0;
+    if (KC == kKcE4) inv *= p.v_scale;
 #pragma unroll
     for (int e = 0; e < 32; e += 4)
       *reinterpret_cast<float4*>(dst + e) =
@@ -613,7 +628,11 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, false, 1>::THREADS, 1)
   a.min_pos = 0;
   a.scale_log2 = p.scale_log2;
   a.err = p.err;
-  tc05_attention_cta<T, D, false, false, 1>(smem, a, q_row, page_block, row_pos, sink,
+  a.k_codes = p.k_cache;
+  a.v_codes = p.v_cache;
+  a.k_scales = p.k_scales;
+  a.v_scales = p.v_scales;
+  tc05_attention_cta<T, D, false, KC, 1>(smem, a, q_row, page_block, row_pos, sink,
                                             [&](int lane) { check(lane, 32); });
 }
 
@@ -624,12 +643,12 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, false, 1>::THREADS, 1)
 // one past its last row's position (kv_end) and masks key t for a row at
 // position pos when t > pos. Every row sees position 0, so its running
 // maximum is finite from the first tile on. Rows past the chunk's take the
-// tile's last position (finite values that are never stored). I8: the cache
-// holds INT8 codes and row scales.
-template <typename QT, int D, bool I8>
-__global__ void __launch_bounds__(PrefixTcLayout<D, I8, I8 ? 1 : 2>::THREADS, 1)
+// tile's last position (finite values that are never stored). KC: the
+// cache's kind (16-bit elements, INT8 codes and row scales, or E4M3 codes).
+template <typename QT, int D, int KC>
+__global__ void __launch_bounds__(PrefixTcLayout<D, KC != kKc16, KC != kKc16 ? 1 : 2>::THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
-  using Ly = PrefixTcLayout<D, I8, I8 ? 1 : 2>;
+  using Ly = PrefixTcLayout<D, KC != kKc16, KC != kKc16 ? 1 : 2>;
   constexpr int NT = Ly::THREADS, ROWS = Ly::ROWS;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -681,6 +700,7 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, I8, I8 ? 1 : 2>::THREADS, 1)
     const int r = r_first + rr;
     if (r >= rows_total) return;
     QT* dst = out + ((size_t)(q0 + r / G) * Hq + g * G + r % G) * D + c0;
+    if (KC == kKcE4) inv *= p.v_scale;
 #pragma unroll
     for (int e = 0; e < 32; e += 8) {
       uint4 v;
@@ -708,8 +728,8 @@ __global__ void __launch_bounds__(PrefixTcLayout<D, I8, I8 ? 1 : 2>::THREADS, 1)
   a.min_pos = pos0 + r_first / G;
   a.scale_log2 = p.scale_log2;
   a.err = p.err;
-  tc05_attention_cta<QT, D, true, I8, I8 ? 1 : 2>(smem, a, q_row, page_block, row_pos, sink,
-                                                   [](int) {});
+  tc05_attention_cta<QT, D, true, KC, KC != kKc16 ? 1 : 2>(smem, a, q_row, page_block, row_pos,
+                                                           sink, [](int) {});
 }
 
 __global__ void copy_blocks_kernel(uint8_t* k_cache, uint8_t* v_cache, const int32_t* pairs,
@@ -727,10 +747,10 @@ __global__ void copy_blocks_kernel(uint8_t* k_cache, uint8_t* v_cache, const int
   for (size_t i = threadIdx.x; i < block_bytes / 16; i += blockDim.x) d[i] = s[i];
 }
 
-template <typename T, int D>
+template <typename T, int D, int KC>
 cudaError_t launch_prefix(const PrefixParams& p, cudaStream_t st) {
-  using Ly = PrefixTcLayout<D, false, 1>;
-  auto kern = prefix_attention_kernel<T, D>;
+  using Ly = PrefixTcLayout<D, KC != kKc16, 1>;
+  auto kern = prefix_attention_kernel<T, D, KC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((p.num_seqs * p.group + Ly::ROWS - 1) / Ly::ROWS, p.num_prefix_splits,
@@ -738,10 +758,10 @@ cudaError_t launch_prefix(const PrefixParams& p, cudaStream_t st) {
   return launch_pdl(kern, grid, dim3(Ly::THREADS), Ly::SMEM, st, p);
 }
 
-template <typename QT, int D, bool I8>
+template <typename QT, int D, int KC>
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t st) {
-  using Ly = PrefixTcLayout<D, I8, I8 ? 1 : 2>;
-  auto kern = prefill_tc_kernel<QT, D, I8>;
+  using Ly = PrefixTcLayout<D, KC != kKc16, KC != kKc16 ? 1 : 2>;
+  auto kern = prefill_tc_kernel<QT, D, KC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
   if (e != cudaSuccess) return e;
   const long long tiles = ((long long)p.max_q_len * p.group + Ly::ROWS - 1) / Ly::ROWS;
@@ -751,41 +771,40 @@ cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_prefix_attention(const PrefixParams& p, int dtype, cudaStream_t st) {
-  if (dtype == PA_BF16) {
-    if (p.head_dim == 64) return launch_prefix<__nv_bfloat16, 64>(p, st);
-    if (p.head_dim == 128) return launch_prefix<__nv_bfloat16, 128>(p, st);
-  } else if (dtype == PA_F16) {
-    if (p.head_dim == 64) return launch_prefix<__half, 64>(p, st);
-    if (p.head_dim == 128) return launch_prefix<__half, 128>(p, st);
-  }
-  return cudaErrorInvalidValue;
+// kind: the cache's (0 = the query's 16-bit type, 1 = INT8 codes and row
+// scales, 2 = FP8 E4M3 codes); head dims 64 and 128, queries bf16 or f16.
+#define PA_TC05_DISPATCH(LAUNCH, P)                                      \
+  do {                                                                   \
+    const int d_ = (P).head_dim;                                         \
+    if (d_ != 64 && d_ != 128) return cudaErrorInvalidValue;             \
+    if (dtype != PA_BF16 && dtype != PA_F16) return cudaErrorInvalidValue; \
+    if (kind < 0 || kind > 2) return cudaErrorInvalidValue;              \
+    const int i_ = (dtype == PA_BF16 ? 0 : 6) + (d_ == 64 ? 0 : 3) + kind; \
+    switch (i_) {                                                        \
+      case 0: return LAUNCH<__nv_bfloat16, 64, kKc16>(P, st);            \
+      case 1: return LAUNCH<__nv_bfloat16, 64, kKcI8>(P, st);            \
+      case 2: return LAUNCH<__nv_bfloat16, 64, kKcE4>(P, st);            \
+      case 3: return LAUNCH<__nv_bfloat16, 128, kKc16>(P, st);           \
+      case 4: return LAUNCH<__nv_bfloat16, 128, kKcI8>(P, st);           \
+      case 5: return LAUNCH<__nv_bfloat16, 128, kKcE4>(P, st);           \
+      case 6: return LAUNCH<__half, 64, kKc16>(P, st);                   \
+      case 7: return LAUNCH<__half, 64, kKcI8>(P, st);                   \
+      case 8: return LAUNCH<__half, 64, kKcE4>(P, st);                   \
+      case 9: return LAUNCH<__half, 128, kKc16>(P, st);                  \
+      case 10: return LAUNCH<__half, 128, kKcI8>(P, st);                 \
+      default: return LAUNCH<__half, 128, kKcE4>(P, st);                 \
+    }                                                                    \
+  } while (0)
+
+cudaError_t launch_prefix_attention(const PrefixParams& p, int dtype, int kind, cudaStream_t st) {
+  PA_TC05_DISPATCH(launch_prefix, p);
 }
 
-cudaError_t launch_prefill_attention(const PrefillParams& p, int dtype, bool int8,
+cudaError_t launch_prefill_attention(const PrefillParams& p, int dtype, int kind,
                                      cudaStream_t st) {
-#define PA_PREFILL_D(QT_, I8_)                                       \
-  switch (p.head_dim) {                                              \
-    case 64: return launch_prefill<QT_, 64, I8_>(p, st);             \
-    case 128: return launch_prefill<QT_, 128, I8_>(p, st);           \
-    default: return cudaErrorInvalidValue;                           \
-  }
-  if (dtype == PA_BF16) {
-    if (int8) {
-      PA_PREFILL_D(__nv_bfloat16, true)
-    } else {
-      PA_PREFILL_D(__nv_bfloat16, false)
-    }
-  } else if (dtype == PA_F16) {
-    if (int8) {
-      PA_PREFILL_D(__half, true)
-    } else {
-      PA_PREFILL_D(__half, false)
-    }
-  }
-#undef PA_PREFILL_D
-  return cudaErrorInvalidValue;
+  PA_TC05_DISPATCH(launch_prefill, p);
 }
+#undef PA_TC05_DISPATCH
 
 cudaError_t launch_copy_blocks(uint8_t* k_cache, uint8_t* v_cache, const int32_t* block_pairs,
                                int num_pairs, int num_blocks, size_t block_bytes, unsigned* err,

@@ -30,16 +30,19 @@ struct PrefixParams {
   float* tmp_out;
   float* max_logits;
   float* exp_sums;
-  const void* query;            // [S][Hq][D], same element type as the cache
+  const void* query;            // [S][Hq][D] (a 16-bit cache holds the same type)
   const uint8_t* k_cache;       // [NB][Hkv][bs][D]
   const uint8_t* v_cache;
+  const float* k_scales;        // INT8 caches: row scales [NB][Hkv][bs] (else unused)
+  const float* v_scales;
   const int32_t* block_tables;  // [S][MB]; the first prefix_pages entries of every row agree
   const int32_t* context_lens;  // [S]; every context covers the prefix
   unsigned* err;                // device error word
   int num_seqs, num_heads, num_kv_heads, group, head_dim, block_size, num_blocks;
   int max_blocks_per_seq, prefix_pages, prefix_tokens;
   int num_slots, slot0, num_prefix_splits, tokens_per_split;
-  float scale_log2;  // scale * log2(e)
+  float scale_log2;  // scale * log2(e) (* k_scale for an FP8 cache)
+  float v_scale;     // FP8 caches: multiplies the output (else unused)
 };
 
 // Rows of one tensor-core query tile (the M of one MMA), rows of query heads
@@ -48,9 +51,12 @@ constexpr int kPrefixTcRows = 128;
 constexpr int kPrefixCtaRows = 128;
 constexpr int kPrefixTile = 64;
 
-// dtype: 1 = bf16, 2 = f16 (pa_dtype values). Returns cudaErrorInvalidValue
-// for other element types or head dimensions (64 and 128 are built).
-cudaError_t launch_prefix_attention(const PrefixParams& p, int dtype, cudaStream_t stream);
+// dtype: the query's, 1 = bf16, 2 = f16 (pa_dtype values); kind: the
+// cache's, 0 = the query's type, 1 = INT8 codes with row scales, 2 = FP8 E4M3
+// codes. Returns cudaErrorInvalidValue for other types, kinds or head
+// dimensions (64 and 128 are built).
+cudaError_t launch_prefix_attention(const PrefixParams& p, int dtype, int kind,
+                                    cudaStream_t stream);
 
 // Causal multi-query (prefill) attention over the paged cache ("PagedAttention
 // in mistral.rs": a prefill phase next to the paged decode, and speculative
@@ -77,12 +83,12 @@ struct PrefillParams {
   unsigned* err;
   int num_seqs, num_heads, num_kv_heads, group, head_dim, block_size, num_blocks;
   int num_tokens, max_blocks_per_seq, max_q_len;
-  float scale_log2;  // scale * log2(e)
+  float scale_log2;  // scale * log2(e) (* k_scale for an FP8 cache)
+  float v_scale;     // FP8 caches: multiplies the output (else unused)
 };
 
-// dtype: 1 = bf16, 2 = f16 (the query's; the cache's too unless int8, an
-// INT8 cache with row scales). Head dims 64 and 128 are built.
-cudaError_t launch_prefill_attention(const PrefillParams& p, int dtype, bool int8,
+// dtype and kind as launch_prefix_attention's.
+cudaError_t launch_prefill_attention(const PrefillParams& p, int dtype, int kind,
                                      cudaStream_t stream);
 
 // Copies whole blocks (all kv heads, K and V) src -> dst for each pair of

@@ -64,12 +64,17 @@ def lib() -> ctypes.CDLL:
             "pa_decode_workspace_clear": [P, Z, P],
             "pa_decode_cascade_workspace_size": [I, I, I, I, I, I],
             "pa_decode_cascade": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, Z, P],
+            "pa_decode_cascade_fp8": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, F, F, I, I, P, Z,
+                                      P],
+            "pa_decode_cascade_int8": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, Z,
+                                       P],
             "pa_copy_blocks": [P, P, P, I, I, I, I, I, I, P],
             "pa_block_budget": [I, ctypes.c_double, Z, I, I, I, I, I, I],
             "pa_reshape_and_cache_int8": [P, P, P, P, P, P, P, I, I, I, I, I, I, P],
             "pa_decode_int8": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, Z, P],
             "pa_prefill": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P],
             "pa_prefill_int8": [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P],
+            "pa_prefill_fp8": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, F, F, I, P],
             "pa_decode_static_scratch": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F,
                                          F, P],
             "pa_get_device_error": [P, P],
@@ -326,6 +331,34 @@ def prefill_int8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
            "pa_prefill_int8")
 
 
+def prefill_fp8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+                v_cache: torch.Tensor, block_tables: torch.Tensor, cu_q: torch.Tensor,
+                context_lens: torch.Tensor, num_kv_heads: int, max_q_len: int, scale: float,
+                k_scale: float, v_scale: float, stream=None):
+    """pa_prefill_fp8: pa_prefill over an FP8 E4M3 cache (uint8 codes) with
+    per-tensor scales."""
+    _on_device(out=out, query=query, k_cache=k_cache, v_cache=v_cache,
+               block_tables=block_tables, cu_q=cu_q, context_lens=context_lens)
+    _need(query.dim() == 3, "query: expected [num_tokens, num_heads, head_dim]")
+    _shape("out", out, query.shape)
+    _dtype("out", out, query.dtype)
+    _check_caches(k_cache, v_cache, num_kv_heads, query.shape[2], torch.uint8)
+    _need(block_tables.dim() == 2, "block_tables: expected [num_seqs, max_blocks_per_seq]")
+    _dtype("block_tables", block_tables, torch.int32)
+    S = block_tables.shape[0]
+    _shape("cu_q", cu_q, (S + 1,))
+    _dtype("cu_q", cu_q, torch.int32)
+    _shape("context_lens", context_lens, (S,))
+    _dtype("context_lens", context_lens, torch.int32)
+    T, Hq, D = query.shape
+    NB, _, bs, _ = k_cache.shape
+    S, MB = block_tables.shape
+    _check(lib().pa_prefill_fp8(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(block_tables), _ptr(cu_q), _ptr(context_lens), T, S, Hq,
+                                num_kv_heads, D, bs, NB, MB, max_q_len, scale, k_scale, v_scale,
+                                _DTYPE[query.dtype], _stream(stream)), "pa_prefill_fp8")
+
+
 def decode_plan(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
                 block_size: int, max_blocks_per_seq: int, window: int = 0) -> Tuple[int, int]:
     """pa_decode_plan: (num_splits, pages_per_split)."""
@@ -416,6 +449,53 @@ def decode_cascade(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor
                                    bs, NB, MB, scale, _DTYPE[query.dtype], prefix_pages,
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)), "pa_decode_cascade")
+
+
+def decode_cascade_fp8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+                       v_cache: torch.Tensor, block_tables: torch.Tensor,
+                       context_lens: torch.Tensor, num_kv_heads: int, scale: float,
+                       k_scale: float, v_scale: float, prefix_pages: int,
+                       workspace: torch.Tensor, stream=None):
+    """pa_decode_cascade_fp8: pa_decode_cascade over an FP8 E4M3 cache (uint8
+    codes) with per-tensor scales."""
+    _on_device(out=out, query=query, k_cache=k_cache, v_cache=v_cache,
+               block_tables=block_tables, context_lens=context_lens, workspace=workspace)
+    _check_decode_args(out, query, k_cache, v_cache, block_tables, context_lens, num_kv_heads,
+                       torch.uint8)
+    S, Hq, D = query.shape
+    NB, _, bs, _ = k_cache.shape
+    MB = block_tables.shape[1]
+    _check(lib().pa_decode_cascade_fp8(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(block_tables), _ptr(context_lens), S, Hq,
+                                       num_kv_heads, D, bs, NB, MB, scale, k_scale, v_scale,
+                                       _DTYPE[query.dtype], prefix_pages, _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream)), "pa_decode_cascade_fp8")
+
+
+def decode_cascade_int8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+                        v_cache: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor,
+                        block_tables: torch.Tensor, context_lens: torch.Tensor,
+                        num_kv_heads: int, scale: float, prefix_pages: int,
+                        workspace: torch.Tensor, stream=None):
+    """pa_decode_cascade_int8: pa_decode_cascade over an INT8 cache with per-row
+    scales."""
+    _on_device(out=out, query=query, k_cache=k_cache, v_cache=v_cache, k_scales=k_scales,
+               v_scales=v_scales, block_tables=block_tables, context_lens=context_lens,
+               workspace=workspace)
+    _check_decode_args(out, query, k_cache, v_cache, block_tables, context_lens, num_kv_heads,
+                       torch.int8)
+    _check_scales(k_scales, v_scales, k_cache)
+    S, Hq, D = query.shape
+    NB, _, bs, _ = k_cache.shape
+    MB = block_tables.shape[1]
+    _check(lib().pa_decode_cascade_int8(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(k_scales), _ptr(v_scales), _ptr(block_tables),
+                                        _ptr(context_lens), S, Hq, num_kv_heads, D, bs, NB, MB,
+                                        scale, _DTYPE[query.dtype], prefix_pages,
+                                        _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream(stream)), "pa_decode_cascade_int8")
 
 
 def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_pairs: torch.Tensor,

@@ -94,3 +94,17 @@ def bits(t: torch.Tensor) -> torch.Tensor:
 
 def device_errors() -> int:
     return pa.get_device_error()
+
+
+def gpu_int8_caches(case):
+    """INT8 caches and row scales on the GPU (pa_slot_mapping +
+    pa_reshape_and_cache_int8), written in the same order as the oracle's."""
+    kc, vc = wl.empty_caches(case, device=DEV)
+    ks, vs = wl.empty_scales(case, device=DEV)
+    steps = [(case.pre_seq[a:b], case.pre_pos[a:b], case.pre_key[a:b], case.pre_value[a:b])
+             for a, b in case.pre_chunks if b > a]
+    steps.append((None, case.new_pos, case.new_key, case.new_value))
+    for seq, pos, key, val in steps:
+        sm = gpu_slot_mapping(case, seq, pos)
+        pa.reshape_and_cache_int8(to_dev(key), to_dev(val), kc, vc, ks, vs, sm)
+    return kc, vc, ks, vs

@@ -31,7 +31,8 @@ def test_header_declares_the_boundary():
                  "pa_decode_partials", "pa_decode_plan", "pa_decode_workspace_size",
                  "pa_decode_cascade", "pa_decode_cascade_workspace_size", "pa_copy_blocks",
                  "pa_block_budget", "pa_reshape_and_cache_int8", "pa_decode_int8",
-                 "pa_prefill",
+                 "pa_prefill", "pa_prefill_int8", "pa_prefill_fp8", "pa_decode_cascade_fp8",
+                 "pa_decode_cascade_int8",
                  "pa_get_device_error", "pa_status_string", "pa_version"):
         assert want in names
 
@@ -172,6 +173,35 @@ def test_cascade_and_copy_blocks_reject_bad_arguments_on_host(L):
     assert call(pp=0) == -3 and call(pp=9) == -3
     assert call(wsb=1024) == -7
     assert call(ws=P + 4) == -10
+
+    # the 8-bit caches: the same checks, with the FP8 scales and INT8 row scales
+    def fp8(**kw):
+        a = dict(out=P, q=P, k=P, v=P, bt=P, cl=P, S=4, Hq=8, Hkv=2, D=128, bs=32, NB=40, MB=8,
+                 scale=0.1, ks=1.0, vs=1.0, qd=1, pp=3, ws=P, wsb=1 << 30)
+        a.update(kw)
+        return L.pa_decode_cascade_fp8(a["out"], a["q"], a["k"], a["v"], a["bt"], a["cl"],
+                                       a["S"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"],
+                                       a["MB"], a["scale"], a["ks"], a["vs"], a["qd"], a["pp"],
+                                       a["ws"], a["wsb"], None)
+
+    assert fp8(S=0, q=None) == 0
+    assert fp8(ws=None) == -1 and fp8(qd=0) == -2 and fp8(D=96) == -4 and fp8(pp=9) == -3
+    assert fp8(ks=0.0) == -11 and fp8(vs=float("nan")) == -11
+    assert fp8(wsb=1024) == -7
+
+    def int8(**kw):
+        a = dict(out=P, q=P, k=P, v=P, ksc=P, vsc=P, bt=P, cl=P, S=4, Hq=8, Hkv=2, D=64, bs=16,
+                 NB=40, MB=8, scale=0.1, qd=2, pp=3, ws=P, wsb=1 << 30)
+        a.update(kw)
+        return L.pa_decode_cascade_int8(a["out"], a["q"], a["k"], a["v"], a["ksc"], a["vsc"],
+                                        a["bt"], a["cl"], a["S"], a["Hq"], a["Hkv"], a["D"],
+                                        a["bs"], a["NB"], a["MB"], a["scale"], a["qd"], a["pp"],
+                                        a["ws"], a["wsb"], None)
+
+    assert int8(S=0, q=None) == 0
+    assert int8(ksc=None) == -1 and int8(ws=None) == -1
+    assert int8(qd=0) == -2 and int8(D=96) == -4 and int8(pp=0) == -3
+    assert int8(ksc=P + 4) == -10 and int8(wsb=64) == -7
     f = L.pa_copy_blocks
     assert f(P, P, P, 0, 2, 64, 32, 10, 2, None) == 0
     assert f(P, None, P, 1, 2, 64, 32, 10, 2, None) == -1
@@ -280,6 +310,37 @@ def test_prefill_rejects_bad_arguments_on_host(L):
     assert call(D=96) == -4 and call(bs=8) == -5
     assert call(mq=0) == -3 and call(mq=41) == -3
     assert call(out=P + 2) == -10 and call(k=P + 8) == -10
+
+
+def test_8bit_prefill_rejects_bad_arguments_on_host(L):
+    """pa_prefill_fp8 and pa_prefill_int8 share pa_prefill's checks, plus the
+    FP8 scales (finite, positive) and the INT8 row scales (present, aligned)."""
+    def fp8(**kw):
+        a = dict(out=P, q=P, k=P, v=P, bt=P, cu=P, cl=P, T=40, S=4, Hq=8, Hkv=2, D=128, bs=32,
+                 NB=10, MB=8, mq=16, scale=0.1, ks=0.5, vs=2.0, qd=1)
+        a.update(kw)
+        return L.pa_prefill_fp8(a["out"], a["q"], a["k"], a["v"], a["bt"], a["cu"], a["cl"],
+                                a["T"], a["S"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"],
+                                a["MB"], a["mq"], a["scale"], a["ks"], a["vs"], a["qd"], None)
+
+    assert fp8(T=0, q=None) == 0
+    assert fp8(cu=None) == -1 and fp8(qd=0) == -2 and fp8(D=96) == -4 and fp8(bs=8) == -5
+    assert fp8(ks=0.0) == -11 and fp8(vs=-1.0) == -11 and fp8(ks=float("inf")) == -11
+    assert fp8(ks=float("nan")) == -11
+    assert fp8(k=P + 8) == -10
+
+    def int8(**kw):
+        a = dict(out=P, q=P, k=P, v=P, ksc=P, vsc=P, bt=P, cu=P, cl=P, T=40, S=4, Hq=8, Hkv=2,
+                 D=64, bs=16, NB=10, MB=8, mq=16, scale=0.1, qd=2)
+        a.update(kw)
+        return L.pa_prefill_int8(a["out"], a["q"], a["k"], a["v"], a["ksc"], a["vsc"], a["bt"],
+                                 a["cu"], a["cl"], a["T"], a["S"], a["Hq"], a["Hkv"], a["D"],
+                                 a["bs"], a["NB"], a["MB"], a["mq"], a["scale"], a["qd"], None)
+
+    assert int8(S=0, q=None) == 0
+    assert int8(ksc=None) == -1 and int8(vsc=None) == -1
+    assert int8(qd=0) == -2 and int8(D=96) == -4
+    assert int8(vsc=P + 4) == -10
 
 
 def test_int8_widening_identity_holds_for_every_code():

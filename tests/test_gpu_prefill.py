@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from _gpu import DEV, device_errors, gpu_caches, to_dev
+from _gpu import DEV, device_errors, gpu_caches, gpu_int8_caches, to_dev
 from _helpers import oracle_caches
 from paged_kv_cache_context_gb300 import build, pa
 from paged_kv_cache_context_gb300 import workloads as wl
@@ -140,21 +140,6 @@ def test_prefill_device_checks():
 
 
 # ------------------------------------------------------------ INT8 cache
-def gpu_int8_caches(case):
-    """INT8 caches and row scales on the GPU (pa_slot_mapping +
-    pa_reshape_and_cache_int8), written in the same order as the oracle's."""
-    from _gpu import gpu_slot_mapping
-    kc, vc = wl.empty_caches(case, device=DEV)
-    ks, vs = wl.empty_scales(case, device=DEV)
-    steps = [(case.pre_seq[a:b], case.pre_pos[a:b], case.pre_key[a:b], case.pre_value[a:b])
-             for a, b in case.pre_chunks if b > a]
-    steps.append((None, case.new_pos, case.new_key, case.new_value))
-    for seq, pos, key, val in steps:
-        sm = gpu_slot_mapping(case, seq, pos)
-        pa.reshape_and_cache_int8(to_dev(key), to_dev(val), kc, vc, ks, vs, sm)
-    return kc, vc, ks, vs
-
-
 @pytest.mark.parametrize("D,Hq,Hkv,bs,qd,per_seq", [
     (128, 32, 8, 32, torch.bfloat16, 16),    # G 4
     (128, 16, 2, 16, torch.float16, 100),    # G 8, bs 16, several row tiles
@@ -204,6 +189,62 @@ def test_prefill_int8_flags_a_bad_block_and_keeps_the_rest():
     out = torch.full(tuple(query.shape), float("nan"), dtype=torch.bfloat16, device=DEV)
     pa.prefill_int8(out, to_dev(query), kg, vg, ksg, vsg, to_dev(bt), to_dev(cu),
                     to_dev(case.context_lens), 2, max_q, case.scale)
+    torch.cuda.synchronize()
+    assert device_errors() & 2
+    g = out.float().cpu().double().numpy()
+    assert np.isfinite(g).all()
+    assert np.abs(g[0:24] - ref[0:24]).max() <= TOL
+
+
+# ------------------------------------------------------------ FP8 cache
+@pytest.mark.parametrize("D,Hq,Hkv,bs,qd,per_seq", [
+    (128, 32, 8, 32, torch.bfloat16, 16),    # G 4
+    (128, 16, 2, 16, torch.float16, 100),    # G 8, bs 16, several row tiles
+    (64, 16, 16, 64, torch.bfloat16, 7),     # G 1, bs 64, D 64
+    (64, 12, 4, 32, torch.float16, 300),     # G 3; short contexts taken whole
+    (128, 8, 1, 32, torch.bfloat16, 1),      # one query token
+])
+def test_prefill_fp8_matches_oracle(D, Hq, Hkv, bs, qd, per_seq):
+    """pa_prefill_fp8 against the oracle's prefill over the same E4M3 codes
+    and per-tensor scales ("PagedAttention in mistral.rs", KV Cache
+    Quantization); the caches are written by pa_reshape_and_cache and equal
+    the oracle's byte for byte."""
+    case = wl.make_case(f"pfe_{D}_{Hq}_{Hkv}_{bs}", 160 + D + Hq + bs, 9, Hq, Hkv, D, bs,
+                        len_range=(1, 500), q_dtype=qd, kv_dtype="fp8_e4m3", extra_blocks=3)
+    kg, vg = gpu_caches(case)
+    ko, vo = oracle_caches(case)
+    assert torch.equal(kg.cpu(), ko) and torch.equal(vg.cpu(), vo)
+    query, q_seq, q_pos, cu, max_q = chunk(case, per_seq, 161 + D + per_seq)
+    out = torch.full(tuple(query.shape), float("nan"), dtype=qd, device=DEV)
+    pa.prefill_fp8(out, to_dev(query), kg, vg, to_dev(case.block_tables), to_dev(cu),
+                   to_dev(case.context_lens), Hkv, max_q, case.scale, case.k_scale, case.v_scale)
+    torch.cuda.synchronize()
+    assert device_errors() == 0
+    ref, bad = oracle.prefill(query, q_seq, q_pos, ko, vo, case.block_tables, Hkv, bs,
+                              case.scale, "fp8_e4m3", case.k_scale, case.v_scale)
+    assert bad == 0
+    g = out.float().cpu().double().numpy()
+    assert np.isfinite(g).all()
+    err = np.abs(g - ref).max()
+    assert err <= TOL, f"max abs error {err:.3g}"
+
+
+def test_prefill_fp8_flags_a_bad_block_and_keeps_the_rest():
+    """A block id outside the pool in one sequence's table reads as zeros
+    (flagged); the other sequences keep the oracle's answer."""
+    case = wl.make_case("pfe_bad", 170, 4, 8, 2, 64, lens=[40, 70, 9, 100],
+                        q_dtype=torch.bfloat16, kv_dtype="fp8_e4m3", extra_blocks=2)
+    kg, vg = gpu_caches(case)
+    ko, vo = oracle_caches(case)
+    query, q_seq, q_pos, cu, max_q = chunk(case, 8, 171)
+    ref, _ = oracle.prefill(query, q_seq, q_pos, ko, vo, case.block_tables, 2,
+                            case.block_size, case.scale, "fp8_e4m3", case.k_scale, case.v_scale)
+    device_errors()
+    bt = case.block_tables.clone()
+    bt[3, 0] = case.num_blocks + 5
+    out = torch.full(tuple(query.shape), float("nan"), dtype=torch.bfloat16, device=DEV)
+    pa.prefill_fp8(out, to_dev(query), kg, vg, to_dev(bt), to_dev(cu), to_dev(case.context_lens),
+                   2, max_q, case.scale, case.k_scale, case.v_scale)
     torch.cuda.synchronize()
     assert device_errors() & 2
     g = out.float().cpu().double().numpy()
