@@ -619,8 +619,16 @@ def run_prefill(args, rank, local_rank, world):
     S, Hq, Hkv, D, bs = (case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim,
                          case.block_size)
     int8 = args.prefill_int8
+    fp8 = args.prefill_fp8 and not int8
     if int8:
         case = dataclasses.replace(case, kv_dtype="int8")
+    if fp8:
+        # per-tensor scales amax / 448 over every row written, in fp32
+        def amax(chunks):
+            return max(float(t.float().abs().max()) for t in chunks if t.numel())
+        ksc = amax([case.pre_key, case.new_key]) / 448.0
+        vsc = amax([case.pre_value, case.new_value]) / 448.0
+        case = dataclasses.replace(case, kv_dtype="fp8_e4m3", k_scale=ksc, v_scale=vsc)
     bt = case.block_tables.to(dev)
     cl = case.context_lens.to(dev)
     kc, vc = wl.empty_caches(case, device=str(dev))
@@ -634,7 +642,8 @@ def run_prefill(args, rank, local_rank, world):
             pa.reshape_and_cache_int8(key.to(dev).contiguous(), val.to(dev).contiguous(), kc, vc,
                                       ks, vs, sm)
         else:
-            pa.reshape_and_cache(key.to(dev).contiguous(), val.to(dev).contiguous(), kc, vc, sm)
+            pa.reshape_and_cache(key.to(dev).contiguous(), val.to(dev).contiguous(), kc, vc, sm,
+                                 case.kv_dtype, case.k_scale, case.v_scale)
     reps = [(kc, vc, ks, vs)] + [(kc.clone(), vc.clone(),
                                   None if ks is None else ks.clone(),
                                   None if vs is None else vs.clone())
@@ -649,7 +658,7 @@ def run_prefill(args, rank, local_rank, world):
     cud = cu.to(dev)
     out = torch.empty(T, Hq, D, dtype=case.q_dtype, device=dev)
     flops = 4.0 * D * Hq * float((q_pos.to(torch.int64) + 1).sum())
-    elem = 1 if int8 else torch.finfo(case.q_dtype).bits // 8
+    elem = 1 if int8 or fp8 else torch.finfo(case.q_dtype).bits // 8
     kv_bytes = sum(-(-int(n) // bs) for n in case.context_lens.tolist()) * bs * Hkv * 2 * \
         (D * elem + (4 if int8 else 0))
 
@@ -658,6 +667,9 @@ def run_prefill(args, rank, local_rank, world):
         if int8:
             pa.prefill_int8(out, q_, k_, v_, ks_, vs_, bt_, cu_, cl_, Hkv, max_q, case.scale,
                             stream=stream)
+        elif fp8:
+            pa.prefill_fp8(out, q_, k_, v_, bt_, cu_, cl_, Hkv, max_q, case.scale, case.k_scale,
+                           case.v_scale, stream=stream)
         else:
             pa.prefill(out, q_, k_, v_, bt_, cu_, cl_, Hkv, max_q, case.scale, stream=stream)
 
@@ -734,7 +746,8 @@ def run_prefill(args, rank, local_rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "impl": "ours",
         "config": {"workload": args.workload, "path": "prefill",
-                   "cache_dtype": "int8" if int8 else str(case.q_dtype).replace("torch.", ""),
+                   "cache_dtype": case.kv_dtype if int8 or fp8
+                   else str(case.q_dtype).replace("torch.", ""),
                    "num_seqs": S,
                    "num_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "block_size": bs,
                    "query_tokens": T, "max_q_len": max_q, "flops_per_step": flops,
@@ -744,9 +757,10 @@ def run_prefill(args, rank, local_rank, world):
                      "peak_kind": peak_kind, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tf, 4),
                      "traffic": measured_traffic(f"{args.workload}/prefill" +
-                                                 ("_int8" if int8 else "")),
+                                                 ("_int8" if int8 else "_fp8" if fp8 else "")),
                      "kernel": "prefill_tc_kernel (tcgen05 kind::f16, TMEM accumulators" +
-                               (", INT8 codes widened to f16 in shared memory)" if int8 else ")"),
+                               (", INT8 codes widened to f16 in shared memory)" if int8 else
+                                ", E4M3 codes widened to f16 in shared memory)" if fp8 else ")"),
                      "kernel_us_mean": round(per * 1e6, 2)},
         "e2e": {"value": round(flops_all / e2e_t / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
@@ -765,8 +779,8 @@ def run_prefill(args, rank, local_rank, world):
         reps_o = 0
         while time.perf_counter() - tq < 10.0 and reps_o < 50:
             oracle.prefill(query[pick], q_seq[pick], q_pos[pick], ko, vo, case.block_tables, Hkv,
-                           bs, case.scale, "int8" if int8 else "auto", k_scales=kso,
-                           v_scales=vso)
+                           bs, case.scale, case.kv_dtype, case.k_scale, case.v_scale,
+                           k_scales=kso, v_scales=vso)
             reps_o += 1
         t_o = (time.perf_counter() - tq) / reps_o
         f_o = 4.0 * D * Hq * float((q_pos[pick].to(torch.int64) + 1).sum())
@@ -826,6 +840,9 @@ def main(argv=None):
                     help="leave out the oracle timing (for profiler runs of the same line)")
     ap.add_argument("--prefill-tokens", type=int, default=512,
                     help="--path prefill: query tokens per sequence (its last positions)")
+    ap.add_argument("--prefill-fp8", action="store_true",
+                    help="--path prefill over an FP8 E4M3 cache with per-tensor scales "
+                         "(pa_prefill_fp8)")
     ap.add_argument("--prefill-int8", action="store_true",
                     help="with --path prefill: the cache held as INT8 codes with row scales "
                          "(pa_prefill_int8)")
