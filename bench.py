@@ -274,6 +274,19 @@ def run_ours(args, rank, local_rank, world):
         if case.kv_dtype != "auto" or case.q_dtype == torch.float32:
             raise SystemExit("--path int8 needs a workload with a bf16/f16 native cache")
         case = dataclasses.replace(case, kv_dtype="int8")
+    if args.path == "cascade" and args.cascade_kv != "auto":
+        if case.kv_dtype != "auto" or case.q_dtype == torch.float32:
+            raise SystemExit("--cascade-kv needs a workload with a bf16/f16 native cache")
+        if args.cascade_kv == "int8":
+            case = dataclasses.replace(case, kv_dtype="int8")
+        else:
+            # per-tensor scales amax / 448 over every row written, in fp32
+            def amax(ts):
+                return max(float(t.float().abs().max()) for t in ts if t.numel())
+            case = dataclasses.replace(case, kv_dtype="fp8_e4m3",
+                                       k_scale=amax([case.pre_key, case.new_key]) / 448.0,
+                                       v_scale=amax([case.pre_value, case.new_value]) / 448.0)
+    int8_cache = case.kv_dtype == "int8"  # rows written with per-row scales
     S, Hq, Hkv, D, bs = (case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim,
                          case.block_size)
     MB, NB = case.max_blocks_per_seq, case.num_blocks
@@ -283,13 +296,13 @@ def run_ours(args, rank, local_rank, world):
 
     # caches: prefill rows written by the library itself
     kc, vc = wl.empty_caches(case, device=str(dev))
-    ks, vs = wl.empty_scales(case, device=str(dev)) if int8 else (None, None)
+    ks, vs = wl.empty_scales(case, device=str(dev)) if int8_cache else (None, None)
     for a, b in case.pre_chunks:
         if b > a:
             sm = torch.empty(b - a, dtype=torch.int64, device=dev)
             pa.slot_mapping(sm, bt, case.pre_seq[a:b].to(dev), case.pre_pos[a:b].to(dev), bs,
                             case.window)
-            if int8:
+            if int8_cache:
                 pa.reshape_and_cache_int8(case.pre_key[a:b].contiguous(),
                                           case.pre_value[a:b].contiguous(), kc, vc, ks, vs, sm)
             else:
@@ -329,8 +342,14 @@ def run_ours(args, rank, local_rank, world):
     f_write, f_clear, f_dec = (L.pa_reshape_and_cache, L.pa_decode_workspace_clear,
                                L.pa_decode_balanced)
     clear_args = (ptr(ws), Z(ws_bytes), sp)
-    if not int8 and (f_clear(*clear_args) or f_dec(*dec_args[0])):
+    if not int8_cache and (f_clear(*clear_args) or f_dec(*dec_args[0])):
         raise RuntimeError("pa_decode_balanced failed")
+    if int8_cache:
+        # pa_reshape_and_cache_int8: codes and row scales
+        write_args = [(ptr(new_k), ptr(new_v), ptr(k_), ptr(v_), ptr(ks_), ptr(vs_),
+                       ptr(new_sm), I(S), I(Hkv), I(D), I(bs), I(NB),
+                       I(pa._DTYPE[new_k.dtype]), sp) for (k_, v_, ks_, vs_) in reps]
+        f_write = L.pa_reshape_and_cache_int8
     launches_per_step = 3  # cache write, counter clear, decode
     prefix_pages = case.shared_prefix_tokens // bs
     if args.path == "cascade":
@@ -339,11 +358,24 @@ def run_ours(args, rank, local_rank, world):
             raise SystemExit("--path cascade needs a workload with a shared prefix")
         ws_bytes = pa.decode_cascade_workspace_size(S, Hq, Hkv, D, bs, prefix_pages)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-        dec_args = [(ptr(out), ptr(q), ptr(k_), ptr(v_), ptr(bt), ptr(cl), I(S), I(Hq), I(Hkv),
-                     I(D), I(bs), I(NB), I(MB), F(case.scale), I(qd), I(prefix_pages), ptr(ws),
-                     Z(ws_bytes), sp) for (k_, v_, _, _) in reps]
-        f_dec = L.pa_decode_cascade
-        if f_dec(*dec_args[0]):
+        if case.kv_dtype == "fp8_e4m3":
+            dec_args = [(ptr(out), ptr(q), ptr(k_), ptr(v_), ptr(bt), ptr(cl), I(S), I(Hq),
+                         I(Hkv), I(D), I(bs), I(NB), I(MB), F(case.scale), F(case.k_scale),
+                         F(case.v_scale), I(qd), I(prefix_pages), ptr(ws), Z(ws_bytes), sp)
+                        for (k_, v_, _, _) in reps]
+            f_dec = L.pa_decode_cascade_fp8
+        elif int8_cache:
+            dec_args = [(ptr(out), ptr(q), ptr(k_), ptr(v_), ptr(ks_), ptr(vs_), ptr(bt),
+                         ptr(cl), I(S), I(Hq), I(Hkv), I(D), I(bs), I(NB), I(MB), F(case.scale),
+                         I(qd), I(prefix_pages), ptr(ws), Z(ws_bytes), sp)
+                        for (k_, v_, ks_, vs_) in reps]
+            f_dec = L.pa_decode_cascade_int8
+        else:
+            dec_args = [(ptr(out), ptr(q), ptr(k_), ptr(v_), ptr(bt), ptr(cl), I(S), I(Hq),
+                         I(Hkv), I(D), I(bs), I(NB), I(MB), F(case.scale), I(qd),
+                         I(prefix_pages), ptr(ws), Z(ws_bytes), sp) for (k_, v_, _, _) in reps]
+            f_dec = L.pa_decode_cascade
+        if f_write(*write_args[0]) or f_dec(*dec_args[0]):
             raise RuntimeError("pa_decode_cascade failed")
         launches_per_step = 4  # cache write, prefix attention, suffix decode, reduce
     if int8:
@@ -413,8 +445,9 @@ def run_ours(args, rank, local_rank, world):
         # suffix
         nslots = ws_bytes // (4 * S * Hq * (D + 2))
         elem = torch.finfo(case.q_dtype).bits // 8
+        row_b = D * (1 if case.kv_dtype != "auto" else elem) + (4 if int8_cache else 0)
         unique_kv = (case.shared_prefix_tokens + sum(
-            case.attended(s) - case.shared_prefix_tokens for s in range(S))) * Hkv * D * 2 * elem
+            case.attended(s) - case.shared_prefix_tokens for s in range(S))) * Hkv * 2 * row_b
         sb["kernel"] = (unique_kv + S * Hq * D * 2 * elem + 2 * S * Hq * nslots * (D + 2) * 4 +
                         S * MB * 4 + S * 4)
     elapsed_max = all_reduce(elapsed, "max", dev)
@@ -426,7 +459,7 @@ def run_ours(args, rank, local_rank, world):
 
     # ---- the cache write at prefill scale: every context token of the batch
     write_prefill = None
-    if args.path != "int8" and case.pre_key.shape[0] > 0:
+    if not int8_cache and case.pre_key.shape[0] > 0:
         write_prefill = prefill_scale_write(case, pa, dev, stream, bt, reps)
 
     # ---- e2e: the public pa_decode call with host buffers
@@ -444,7 +477,8 @@ def run_ours(args, rank, local_rank, world):
                    "window": case.window, "cache_dtype": case.kv_dtype if case.kv_dtype != "auto"
                    else str(case.q_dtype).replace("torch.", ""),
                    "storage_dtype": str(case.q_dtype).replace("torch.", ""),
-                   "decode_path": args.path, "decode_ctas": num_ctas.value if not int8 else None,
+                   "decode_path": args.path,
+                   "decode_ctas": num_ctas.value if args.path == "balanced" else None,
                    "workspace_bytes": ws_bytes,
                    "kv_bytes_per_step": sb["kv"], "bytes_per_step": sb["total"],
                    "l2": f"{args.replicas} rotating cache replicas of "
@@ -457,8 +491,10 @@ def run_ours(args, rank, local_rank, world):
                      "traffic": (measured_traffic(args.workload) if args.path == "balanced"
                                  else measured_traffic(f"{args.workload}/{args.path}")
                                  if args.path == "int8" else None),
-                     "kernel": {"cascade": "pa_decode_cascade: prefix attention + suffix "
-                                           "decode + reduce",
+                     "kernel": {"cascade": {"auto": "pa_decode_cascade",
+                                            "fp8_e4m3": "pa_decode_cascade_fp8",
+                                            "int8": "pa_decode_cascade_int8"}[case.kv_dtype] +
+                                           ": prefix attention + suffix decode + reduce",
                                 "int8": "pa_decode_int8: counter clear + paged_decode_kernel "
                                         "(balanced mode, INT8 rows and row scales)",
                                 "balanced": "paged_decode_kernel (balanced mode)"}[args.path],
@@ -541,9 +577,19 @@ def run_e2e(args, case, pa, L, dev, stream, reps, new_sm, bt, cl, q, new_k, new_
                            Hkv, case.scale, case.window, ws)
             out_h.copy_(out, non_blocking=True)
             return
-        pa.reshape_and_cache(dev_bufs["k"], dev_bufs["v"], k_, v_, dev_bufs["sm"],
-                             case.kv_dtype, case.k_scale, case.v_scale)
-        if args.path == "cascade":
+        if case.kv_dtype == "int8":
+            pa.reshape_and_cache_int8(dev_bufs["k"], dev_bufs["v"], k_, v_, ks_, vs_,
+                                      dev_bufs["sm"])
+        else:
+            pa.reshape_and_cache(dev_bufs["k"], dev_bufs["v"], k_, v_, dev_bufs["sm"],
+                                 case.kv_dtype, case.k_scale, case.v_scale)
+        if args.path == "cascade" and case.kv_dtype == "fp8_e4m3":
+            pa.decode_cascade_fp8(out, dev_bufs["q"], k_, v_, dev_bufs["bt"], dev_bufs["cl"],
+                                  Hkv, case.scale, case.k_scale, case.v_scale, prefix_pages, ws)
+        elif args.path == "cascade" and case.kv_dtype == "int8":
+            pa.decode_cascade_int8(out, dev_bufs["q"], k_, v_, ks_, vs_, dev_bufs["bt"],
+                                   dev_bufs["cl"], Hkv, case.scale, prefix_pages, ws)
+        elif args.path == "cascade":
             pa.decode_cascade(out, dev_bufs["q"], k_, v_, dev_bufs["bt"], dev_bufs["cl"], Hkv,
                               case.scale, prefix_pages, ws)
         else:
@@ -840,6 +886,10 @@ def main(argv=None):
                     help="leave out the oracle timing (for profiler runs of the same line)")
     ap.add_argument("--prefill-tokens", type=int, default=512,
                     help="--path prefill: query tokens per sequence (its last positions)")
+    ap.add_argument("--cascade-kv", choices=("auto", "fp8_e4m3", "int8"), default="auto",
+                    help="with --path cascade: the cache held as FP8 E4M3 codes with per-tensor "
+                         "scales (pa_decode_cascade_fp8) or INT8 codes with row scales "
+                         "(pa_decode_cascade_int8)")
     ap.add_argument("--prefill-fp8", action="store_true",
                     help="--path prefill over an FP8 E4M3 cache with per-tensor scales "
                          "(pa_prefill_fp8)")
