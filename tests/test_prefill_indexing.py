@@ -1,6 +1,7 @@
 """The paged prefill kernel's index arithmetic, restated on the CPU.
 
-The kernel runs one CTA per (128-row query tile, kv head, sequence); its rows
+The kernel runs one CTA per (query tile, kv head, sequence), the tile 256
+rows (two 128-row MMA tiles) over a 16-bit cache and 128 over an 8-bit one; its rows
 are the (token, head-in-group) pairs r = i * G + j of one sequence's chunk,
 token i sitting at position n - q_len + i. It streams keys of positions
 [0, kv_end) in 64-token tiles, with kv_end one past the position of the
@@ -14,10 +15,10 @@ import random
 
 import pytest
 
-ROWS, TILE = 128, 64
+TILE = 64
 
 
-def kernel_accesses(q_lens, ctx, G, Hkv, Hq, bs, MB, NB, D, tables):
+def kernel_accesses(q_lens, ctx, G, Hkv, Hq, bs, MB, NB, D, tables, ROWS=256):
     """Per CTA of the grid: the query / output rows it touches, the cache
     element offsets it reads and the (token, head, key) triples it attends,
     following the kernel's formulas."""
@@ -61,8 +62,9 @@ def kernel_accesses(q_lens, ctx, G, Hkv, Hq, bs, MB, NB, D, tables):
     return T, rows_touched, reads, pairs
 
 
+@pytest.mark.parametrize("rows", [256, 128])
 @pytest.mark.parametrize("seed", range(4))
-def test_accesses_in_bounds_and_attention_is_causal(seed):
+def test_accesses_in_bounds_and_attention_is_causal(seed, rows):
     rng = random.Random(seed)
     for _ in range(25):
         S = rng.randint(1, 5)
@@ -78,9 +80,10 @@ def test_accesses_in_bounds_and_attention_is_causal(seed):
         pool = list(range(NB))
         rng.shuffle(pool)
         tables = [pool[s * MB:(s + 1) * MB] for s in range(S)]
-        T, rows, reads, pairs = kernel_accesses(q_lens, ctx, G, Hkv, Hq, bs, MB, NB, D, tables)
+        T, touched, reads, pairs = kernel_accesses(q_lens, ctx, G, Hkv, Hq, bs, MB, NB, D,
+                                                   tables, rows)
         # every output row written once, inside [T][Hq]
-        assert sorted(rows) == list(range(T * Hq))
+        assert sorted(touched) == list(range(T * Hq))
         cache_bytes = NB * Hkv * bs * D * 2
         assert all(0 <= a and b <= cache_bytes for a, b in reads)
         # exactly the causal pairs: token i of sequence s (position n - q_len + i)
