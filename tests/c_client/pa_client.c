@@ -43,5 +43,17 @@ int main(void)
            (int)pa_decode_int8(p, p, (const int8_t*)p, (const int8_t*)p, (const float*)p,
                                (const float*)p, (const int32_t*)p, (const int32_t*)p, 4, 8, 2,
                                128, 32, 10, 8, 0.1f, 0, PA_F32, NULL, 0, NULL));
+    printf("prefill_fp8_scale %d\n",
+           (int)pa_prefill_fp8(p, p, (const uint8_t*)p, (const uint8_t*)p, (const int32_t*)p,
+                               (const int32_t*)p, (const int32_t*)p, 40, 4, 8, 2, 128, 32, 10, 8,
+                               16, 0.1f, 0.f, 1.f, PA_BF16, NULL));
+    printf("cascade_fp8_head_dim %d\n",
+           (int)pa_decode_cascade_fp8(p, p, (const uint8_t*)p, (const uint8_t*)p,
+                                      (const int32_t*)p, (const int32_t*)p, 4, 8, 2, 96, 32, 40,
+                                      8, 0.1f, 1.f, 1.f, PA_BF16, 3, p, (size_t)1 << 30, NULL));
+    printf("cascade_int8_null_scales %d\n",
+           (int)pa_decode_cascade_int8(p, p, (const int8_t*)p, (const int8_t*)p, NULL, NULL,
+                                       (const int32_t*)p, (const int32_t*)p, 4, 8, 2, 64, 16, 40,
+                                       8, 0.1f, PA_F16, 3, p, (size_t)1 << 30, NULL));
     return 0;
 }

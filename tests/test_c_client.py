@@ -35,3 +35,5 @@ def test_c_program_links_and_calls_the_abi(tmp_path):
     assert got["decode_empty"] == "0"
     assert got["decode_head_dim"] == "-4" and got["decode_group"] == "-3"
     assert got["write_null"] == "-1" and got["int8_f32_query"] == "-2"
+    assert got["prefill_fp8_scale"] == "-11"
+    assert got["cascade_fp8_head_dim"] == "-4" and got["cascade_int8_null_scales"] == "-1"
