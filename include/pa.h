@@ -395,12 +395,14 @@ pa_status pa_decode_balanced(void* out, const void* query,
  * the same prefix blocks ("PagedAttention in mistral.rs", opening section:
  * prefix caching keeps a prefix's KV state in the paged cache and reuses
  * it). Same result as pa_decode with window 0, computed in three launches:
- *   1. each sequence's own pages after the prefix (pages prefix_pages ..),
- *      one CTA per (sequence, kv head), into partial slot 0;
- *   2. the shared prefix (pages 0 .. prefix_pages - 1 of row 0 of
+ *   1. the shared prefix (pages 0 .. prefix_pages - 1 of row 0 of
  *      block_tables) for all S * G query heads of each kv head at once, on
  *      the tensor cores in 128-row tiles, cut into up to (prefix tokens /
- *      64) token ranges, into slots 1 .. ;
+ *      64) token ranges, into partial slots 1 .. ;
+ *   2. each sequence's own pages after the prefix (pages prefix_pages ..),
+ *      one CTA per (sequence, kv head), into slot 0; this launch starts
+ *      beside the first on the SMs it leaves free and waits for it at its
+ *      end;
  *   3. pa_reduce of the slots into `out`.
  * The prefix K/V is read once per kv head for the whole batch instead of
  * once per sequence.
