@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from _helpers import (attended_rows, oracle_caches, oracle_decode, oracle_int8_caches,
-                      torch_int8_dequant)
+                      torch_dequant, torch_int8_dequant)
 from paged_kv_cache_context_gb300 import workloads as wl
 
 
@@ -31,6 +31,8 @@ def dense_causal(case, query, q_seq, q_pos):
         K, V = key[:p + 1].float(), val[:p + 1].float()
         if case.kv_dtype == "int8":
             K, V = torch_int8_dequant(K), torch_int8_dequant(V)
+        if case.kv_dtype == "fp8_e4m3":
+            K, V = torch_dequant(K, case.k_scale), torch_dequant(V, case.v_scale)
         for h in range(case.num_heads):
             q = query[t, h].float().double()
             logits = (K[:, h // G].double() @ q) * sc
@@ -62,6 +64,21 @@ def test_prefill_over_an_int8_cache():
     query, q_seq, q_pos = wl.prefill_queries(case, 20, seed=93)
     out, bad = oracle.prefill(query, q_seq, q_pos, kc, vc, case.block_tables, 2, 32, case.scale,
                               "int8", k_scales=ks, v_scales=vs)
+    assert bad == 0
+    ref = dense_causal(case, query, q_seq, q_pos)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12 * max(1.0, np.abs(ref).max()))
+
+
+def test_prefill_over_an_fp8_cache():
+    """An FP8 E4M3 cache with per-tensor scales: the dense reference takes the
+    rows through PyTorch's E4M3 cast (a library routine) and back times the
+    scale in fp32."""
+    case = wl.make_case("pf_e4", 94, 3, 8, 2, 64, lens=[3, 40, 70], kv_dtype="fp8_e4m3",
+                        kv_src_dtype=torch.float32)
+    kc, vc = oracle_caches(case)
+    query, q_seq, q_pos = wl.prefill_queries(case, 20, seed=95)
+    out, bad = oracle.prefill(query, q_seq, q_pos, kc, vc, case.block_tables, 2, 32, case.scale,
+                              "fp8_e4m3", case.k_scale, case.v_scale)
     assert bad == 0
     ref = dense_causal(case, query, q_seq, q_pos)
     np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12 * max(1.0, np.abs(ref).max()))
